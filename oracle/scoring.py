@@ -1,0 +1,144 @@
+"""Label scores, probabilities and the three label-scoring methods -- oracle
+(test infrastructure), float64.
+
+"To Classify, Try a Trie Tree":
+  sec. 3.2  score(m) = prod_{k=1}^{d_m} P(x_k | prompt, x_1..x_{k-1})
+            P^(m)    = score(m) / sum_{m'} score(m')
+            prefix label: score(refund) = P(refund) * (1 - P(request | refund));
+            read for several continuations as (1 - sum over all children c of
+            P(c | label)), and -inf (probability 0) once that sum reaches 1.
+  sec. 3.3  letters: the M letter probabilities at ANSWER:, rescaled to sum to 1.
+  sec. 3.1  trie_decode: at a branching node pick the most likely child,
+            follow forced tokens, stop once one label is left.
+Ties (a reading; the pages are silent): argmax takes the lowest label index,
+trie_decode the lowest child token id.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import model as M
+from .trie import children_of, label_path
+
+NEG_INF = -np.inf
+PREFIX_SATURATION = 1.0 - 1e-12
+
+
+def logscores_from_table(trie: dict, logp) -> np.ndarray:
+    """log score(m) for every label, given logp(node, child_token) = log P(child
+    token | context ending at node). Model-free: planted tables use it too."""
+    Mn = trie["num_labels"]
+    out = np.empty(Mn)
+    tok = trie["token"]
+    for m in range(Mn):
+        path = label_path(trie, m)
+        d = int(trie["label_decide_depth"][m])
+        s = 0.0
+        for k in range(1, d + 1):
+            s += logp(path[k - 1], int(tok[path[k]]))
+        end = path[-1]
+        ch = children_of(trie, end)
+        if len(ch):
+            cont = sum(np.exp(logp(end, int(tok[c]))) for c in ch)
+            s = s + np.log1p(-cont) if cont < PREFIX_SATURATION else NEG_INF
+        out[m] = s
+    return out
+
+
+def normalise(logscore: np.ndarray) -> tuple:
+    """(P^, argmax): P^(m) = score(m) / sum score; argmax = lowest index of the max."""
+    finite = logscore[np.isfinite(logscore)]
+    if len(finite) == 0:
+        return np.full(len(logscore), np.nan), 0
+    mx = finite.max()
+    w = np.where(np.isfinite(logscore), np.exp(logscore - mx), 0.0)
+    prob = w / w.sum()
+    return prob, int(np.argmax(logscore))
+
+
+def eval_logprob_rows(L: M.Layer, doc_k: np.ndarray, doc_v: np.ndarray, trie: dict, nodes=None) -> dict:
+    """log-prob of every child token at each node (default: the evaluated set
+    P), each node attending to the document and to its own path."""
+    tok = trie["token"]
+    rows = {}
+    for e in (trie["eval_nodes"] if nodes is None else nodes):
+        e = int(e)
+        path = [e]
+        while path[-1] != 0:
+            path.append(int(trie["parent"][path[-1]]))
+        path = path[::-1]
+        z = M.path_state(L, doc_k, doc_v, [int(tok[u]) for u in path])
+        lp = M.head_logprobs(L, z)
+        rows[e] = {int(tok[c]): float(lp[tok[c]]) for c in children_of(trie, e)}
+    return rows
+
+
+def trie_tree(L: M.Layer, doc_k: np.ndarray, doc_v: np.ndarray, trie: dict) -> dict:
+    """trie_tree for one document (doc_k, doc_v float64 [l, H_kv, 128])."""
+    rows = eval_logprob_rows(L, doc_k, doc_v, trie)
+    ls = logscores_from_table(trie, lambda u, t: rows[u][t])
+    prob, am = normalise(ls)
+    return {"logscore": ls, "prob": prob, "argmax": am, "rows": rows}
+
+
+def label_logscore_flat(L: M.Layer, doc_k, doc_v, root_token: int, label: list, decide_depth: int,
+                        continuation_children: list | None = None) -> float:
+    """Scores one label as its own flat causal sequence [root, x_1 .. x_t]
+    (the "simple" per-label request of sec. 3.2), summing its first
+    decide_depth token log-probs; continuation_children (prefix labels) adds
+    log(1 - sum_c P(c | label))."""
+    seq = [int(root_token)] + [int(t) for t in label]
+    lp = M.sequence_logprobs(L, doc_k, doc_v, seq)
+    s = sum(lp[k - 1, seq[k]] for k in range(1, decide_depth + 1))
+    if continuation_children:
+        cont = sum(np.exp(lp[len(label), c]) for c in continuation_children)
+        s = s + np.log1p(-cont) if cont < PREFIX_SATURATION else NEG_INF
+    return float(s)
+
+
+def letters(L: M.Layer, doc_k, doc_v, letter_tokens: list, root_token: int) -> dict:
+    """letters (sec. 3.3): logits of the M letter rows at ANSWER:, softmax over them."""
+    z = M.path_state(L, doc_k, doc_v, [int(root_token)])
+    W = M.bf16_to_f64(L.lm_bits[np.asarray(letter_tokens)])
+    logits = W @ z
+    lp = logits - M.logsumexp(logits)
+    prob = np.exp(lp)
+    return {"logprob": lp, "prob": prob, "argmax": int(np.argmax(lp)), "logits": logits}
+
+
+def _unique_label(trie: dict, u: int) -> int:
+    lo, hi = u, u + int(trie["subtree_size"][u])
+    for m, e in enumerate(trie["label_end_node"]):
+        if lo <= e < hi:
+            return m
+    raise AssertionError("subtree holds no label")
+
+
+def trie_decode(L: M.Layer, doc_k, doc_v, trie: dict, child_logits=None) -> dict:
+    """Greedy trie_decode (sec. 3.1) for one document. child_logits(u) may
+    supply {child_token: logit} at node u (planted tables); by default the
+    layer computes them. Returns the label and the nodes where logits were
+    computed, in order."""
+    tok = trie["token"]
+    u = 0
+    touched = []
+    while True:
+        while trie["subtree_labels"][u] > 1 and len(children_of(trie, u)) == 1:
+            u = int(children_of(trie, u)[0])
+        if trie["subtree_labels"][u] == 1:
+            return {"label": _unique_label(trie, u), "touched": touched}
+        if child_logits is None:
+            path = [u]
+            while path[-1] != 0:
+                path.append(int(trie["parent"][path[-1]]))
+            z = M.path_state(L, doc_k, doc_v, [int(tok[p]) for p in path[::-1]])
+            W = L.lm_head()
+            cl = {int(tok[c]): float(W[tok[c]].astype(np.float64) @ z) for c in children_of(trie, u)}
+        else:
+            cl = child_logits(u)
+        touched.append(u)
+        best = None
+        for c in children_of(trie, u):  # ascending token id: first max wins ties
+            if best is None or cl[int(tok[c])] > cl[int(tok[best])]:
+                best = int(c)
+        u = best
