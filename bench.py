@@ -1,0 +1,415 @@
+#!/usr/bin/env python
+"""Benchmark: documents classified per second by trie_tree on one GB300.
+
+Default workload: the Qwen3-4B-shaped final layer (hidden 2,560, 32 q / 8 KV
+heads, vocab 151,936) with 256 documents of U{128..1024} tokens and the
+10-label support-topic trie ("To Classify, Try a Trie Tree", sec. 2-3); all
+inputs seeded and synthetic. One step = one quail_classify_trie_tree call over
+all documents (node prologue, tree-masked attention, W_o + RMSNorm, output
+head with fused log-sum-exp and child gather, label scoring).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line (rank 0). With torchrun (N > 1) every rank scores its own
+256 documents (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "documents classified/sec at 1 GB300 (trie_tree); % of HBM/tensor roofline"
+DEFAULT_WORKLOAD = "qwen3-4b-support10-256docs"
+
+
+def count_launches() -> int:
+    """Kernels one quail_classify_trie_tree call launches: embed RMSNorm, the
+    q, k and v projection GEMMs, q/k head norm, tree part, paged doc
+    attention, combine, W_o GEMM, final norm, head GEMM, LSE reduce, label
+    scoring."""
+    return 13
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=None)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--docs", type=int, default=None, help="override documents per GPU (small profiling cases)")
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while running."""
+
+    Q = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None):
+        self.bus = (bus_id or "").lower()
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                       "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self) -> dict:
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        sm, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f.read().splitlines():
+            c = [x.strip() for x in line.split(",")]
+            if len(c) < 10:
+                continue
+            if self.bus and self.bus[-12:] not in c[1].lower():
+                continue
+            try:
+                sm.append(float(c[2]))
+                mx.append(float(c[3]))
+                power.append(float(c[4]))
+            except ValueError:
+                continue
+            for n, v in zip(names, c[6:10]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.f.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------------ helpers
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def head_kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "umma_gemm.cuh", "sm103.cuh"):
+        with open(os.path.join(ROOT, "trie_label_scoring_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, rows: int):
+    """Per-launch DRAM bytes of the head GEMM from the committed ncu summary,
+    scaled to `rows` if the capture used fewer rows; None once the kernel
+    source has changed since the capture."""
+    p = os.path.join(ROOT, "profiles", "lm_head_gemm_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("kernel_source_hash") != head_kernel_hash():
+        return None
+    if d.get("workload") != workload:
+        return None
+    return d["dram_bytes_per_launch"] * rows / d["rows"]
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, x: float) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ oracle timing
+def time_oracle(w, docs, labels, budget_s: float, max_docs: int | None = None) -> dict:
+    """The CPU oracle, as it stands, on documents of the same workload until the
+    time budget is spent (at least one document)."""
+    from oracle import scoring as OS
+    from oracle.trie import build_trie
+    from tests import gpu_cases as C
+    L = C.oracle_layer(w.shape)
+    L.lm_head()  # widen the head once (model load, not timed)
+    t = build_trie(labels.labels, labels.root_token, w.shape.vocab, labels.continuation)
+    n, t0 = 0, time.perf_counter()
+    limit = max_docs or w.num_docs
+    while n < limit:
+        dk, dv = C.oracle_doc_kv(docs, n % w.num_docs)
+        OS.trie_tree(L, dk, dv, t)
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    return {"docs": n, "seconds": el, "docs_per_s": n / el}
+
+
+def cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import synthetic as S
+    from oracle import scoring as OS
+    from oracle.trie import build_trie
+    from tests import gpu_cases as C
+    w = S.WORKLOADS[args.workload]
+    if args.docs:
+        w = S.with_docs(w, args.docs)
+    labels = S.make_labels(w, 0)
+    docs = S.make_docs(w, 0)
+    L = C.oracle_layer(w.shape)
+    L.lm_head()
+    t = build_trie(labels.labels, labels.root_token, w.shape.vocab, labels.continuation)
+    steps = args.steps if args.steps is not None else 10
+
+    def step(i):
+        dk, dv = C.oracle_doc_kv(docs, i % w.num_docs)
+        OS.trie_tree(L, dk, dv, t)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        step(args.warmup + i)
+    el = time.perf_counter() - t0
+    value = steps / el
+    sample = f"1 document of {w.name} per step (oracle trie_tree: fp64 layer, fp32 head GEMV, fp64 LSE)"
+    out = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "docs/s", "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * el / steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": w.name, "docs_per_step": 1},
+        "cpu_baseline": {"value": value, "unit": "docs/s", "cores": cores(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "docs/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    import synthetic as S
+    import trie_label_scoring_gb300 as Q
+    from tests import gpu_cases as C
+    from trie_label_scoring_gb300.torch_inputs import bf16_tensor, kv_from_docs
+
+    Q.build()
+    w = S.WORKLOADS[args.workload]
+    if args.docs:
+        w = S.with_docs(w, args.docs)
+    model = C.device_model(w.shape, 0)
+    labels = S.make_labels(w, 0)
+    docs = S.make_docs(w, rank)  # each rank scores its own documents
+    kv = kv_from_docs(docs)
+    trie = Q.Trie(labels.labels, labels.root_token, w.shape.vocab, labels.continuation)
+    trie.upload()
+    N, M, a = w.num_docs, len(labels.labels), trie.n_eval
+    ws = torch.empty(Q.workspace_size(model, trie, 0, N, docs.max_doc_len, Q.MODE_TRIE_TREE), dtype=torch.uint8,
+                     device="cuda")
+    lsc = torch.empty((N, M), device="cuda")
+    prob = torch.empty((N, M), device="cuda")
+    am = torch.empty((N,), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        Q.classify_trie_tree(model, kv, trie, N, ws, lsc, prob, am, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    Q.device_status()
+    # choose K: about 2 s of device time unless given
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    step()
+    t1.record(stream)
+    t1.synchronize()
+    est_ms = t0.elapsed_time(t1)
+    steps = args.steps if args.steps is not None else int(min(5000, max(20, 2000.0 / max(est_ms, 1e-3))))
+
+    head_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(local).pci_bus_id
+    except Exception:
+        pass
+    clocks = ClockSampler(str(bus) if bus is not None else None)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for k in range(steps):
+        Q.set_stage_events([None] * 6 + [head_ev[k][0], head_ev[k][1]])
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    Q.set_stage_events(None)
+    Q.device_status()
+    elapsed_ms = start.elapsed_time(end)
+    elapsed_ms = max_over_ranks(world, elapsed_ms)
+    head_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in head_ev)
+    ms_per_step = elapsed_ms / steps
+    value = N * world * steps / (elapsed_ms / 1e3)
+
+    # ---- e2e: host buffers through the C ABI, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        hk = bf16_tensor(docs.k_pool, "cpu").pin_memory()
+        hv = bf16_tensor(docs.v_pool, "cpu").pin_memory()
+        hpt = torch.from_numpy(docs.page_table).pin_memory()
+        hdl = torch.from_numpy(docs.doc_len).pin_memory()
+        dk, dv, dpt, ddl = kv.tensors
+        o_ls = torch.empty((N, M)).pin_memory()
+        o_pr = torch.empty((N, M)).pin_memory()
+        o_am = torch.empty((N,), dtype=torch.int32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (hk, hv, hpt, hdl))
+        d2h = sum(t.numel() * t.element_size() for t in (o_ls, o_pr, o_am))
+
+        def e2e_step():
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            dpt.copy_(hpt, non_blocking=True)
+            ddl.copy_(hdl, non_blocking=True)
+            step()
+            o_ls.copy_(lsc, non_blocking=True)
+            o_pr.copy_(prob, non_blocking=True)
+            o_am.copy_(am, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        k_e2e = max(3, min(steps, int(3000.0 / max(est_ms + 3.0, 1e-3))))
+        barrier(world)
+        s2 = torch.cuda.Event(enable_timing=True)
+        e2 = torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(k_e2e):
+            e2e_step()
+        e2.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(world, s2.elapsed_time(e2))
+        e2e = {"value": N * world * k_e2e / (e2e_ms / 1e3), "unit": "docs/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": k_e2e}
+
+    # ---- roofline of the dominant kernel (the output-head GEMM)
+    peaks = measured_peaks()
+    rows = N * a
+    d, V = w.shape.hidden, w.shape.vocab
+    flops = 2.0 * d * V * rows
+    achieved = flops / (head_ms / 1e3) / 1e12
+    traffic = recorded_traffic(w.name, rows)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "traffic": traffic, "kernel": "umma_gemm_kernel<EpiHead>",
+                "head_ms": head_ms, "peak_kind": f"bf16 burst ({peaks['source']})"}
+    # ---- path roofline (the benchmark spec): max(KV bytes / HBM, head FLOPs / tensor peak)
+    kv_bytes = float(docs.doc_len.sum()) * w.shape.n_kv_heads * w.shape.head_dim * 2 * 2
+    t_kv = kv_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_head = flops / (peaks["bf16_tflops"] * 1e12)
+    t_star = max(t_kv, t_head)
+    path = {"t_kv_us": t_kv * 1e6, "t_head_us": t_head * 1e6, "t_star_us": t_star * 1e6,
+            "ms_per_step": ms_per_step, "frac": t_star * 1e3 / ms_per_step}
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r = time_oracle(w, docs, labels, budget_s=15.0)
+        cpu = {"value": r["docs_per_s"], "unit": "docs/s", "cores": cores(), "kind": "oracle",
+               "sample": f"first {r['docs']} documents of {w.name} ({r['seconds']:.1f} s); numpy BLAS threads "
+                         f"default to all {cores()} cores"}
+
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": value, "unit": "docs/s", "n_gpus": world, "steps": steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, random-init weights)",
+            "config": {"workload": w.name, "docs_per_gpu": N, "labels": M, "eval_positions_per_doc": a,
+                       "trie_nodes": trie.n_nodes, "hidden": d, "vocab": V, "q_heads": w.shape.n_q_heads,
+                       "kv_heads": w.shape.n_kv_heads, "doc_tokens_per_gpu": int(docs.doc_len.sum()),
+                       "l2": "inputs larger than L2 (doc KV %.2f GB + output head %.2f GB per step)" % (
+                           kv_bytes / 1e9, 2.0 * d * V / 1e9),
+                       "parallelism": f"replicas x{world} (documents sharded, no collective)"},
+            "roofline": roofline, "path_roofline": path, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": count_launches() * steps, "clocks": clk,
+        }
+        print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    world, rank, local = dist_setup()
+    run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,254 @@
+/*
+ * quail.h -- C ABI of libquail: trie-constrained label scoring on one GB300.
+ *
+ * The operation (from "To Classify, Try a Trie Tree", sections 3.1-3.3, and the
+ * Quail "Execution" page, section "Label scoring"): a document whose KV is
+ * already cached is followed by the answer position (the ANSWER: token, the
+ * trie root). The label token sequences form a prefix trie hanging off that
+ * position. trie_tree scores every label in one request: each evaluated trie
+ * node attends to the document KV and to its own trie ancestors only, the node
+ * outputs go through W_o, RMSNorm and the vocabulary output head, and
+ *     score(m) = prod_{k <= d_m} P(x_k | prompt, x_1..x_{k-1})          (sec. 3.2)
+ *     P^(m)    = score(m) / sum_m' score(m')                            (sec. 3.2)
+ * with the prefix-label correction score(m) *= (1 - P(continue | m)).  (sec. 3.2)
+ * letters scores one answer position against M letter tokens and rescales
+ * them to sum to 1 (sec. 3.3). trie_decode walks the trie greedily, running
+ * the model only at branching nodes, and stops once one label is left
+ * (sec. 3.1).
+ *
+ * Conventions for every call:
+ *  - Every function returns a quail_status; no exception crosses the ABI.
+ *    quail_last_error() gives a thread-local message for the last failure.
+ *  - Argument errors are detected on the host before any launch. Index errors
+ *    that only the device can see (page ids, doc lengths) set a per-device
+ *    error word that quail_device_status() reads; kernels never trap.
+ *  - Classify calls are asynchronous on the given stream (a cudaStream_t; NULL
+ *    is the legacy default stream). The caller owns every device buffer passed
+ *    in (weights, KV pool, outputs, workspace). The library owns quail_trie
+ *    objects, including their device image.
+ *  - All device pointers must be 16-byte aligned; bf16 tensors are row-major
+ *    with the innermost dimension contiguous.
+ */
+#ifndef QUAIL_H_
+#define QUAIL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* quail_stream_t; /* same type as cudaStream_t */
+typedef struct CUevent_st* quail_event_t;   /* same type as cudaEvent_t  */
+
+typedef enum {
+  QUAIL_OK = 0,
+  QUAIL_ERR_INVALID_ARG = -1,                /* null pointer, bad size, bad flag */
+  QUAIL_ERR_EMPTY_LABEL = -2,                /* a label with zero tokens */
+  QUAIL_ERR_DUPLICATE_LABEL = -3,            /* two labels (or letters) with the same tokens */
+  QUAIL_ERR_TOKEN_RANGE = -4,                /* a token id outside [0, vocab) */
+  QUAIL_ERR_PREFIX_LABEL_UNSUPPORTED = -5,   /* trie_decode on a set where one label prefixes another */
+  QUAIL_ERR_WORKSPACE = -6,                  /* workspace null, misaligned or too small */
+  QUAIL_ERR_CUDA = -7,                       /* a CUDA runtime/driver call failed */
+  QUAIL_ERR_DEVICE_BOUNDS = -8,              /* device saw a page id / doc length out of range */
+  QUAIL_ERR_DEVICE_TIMEOUT = -9,             /* a bounded device-side wait gave up */
+  QUAIL_ERR_UNSUPPORTED_SHAPE = -10          /* a model shape these kernels do not handle */
+} quail_status;
+
+/* Thread-local, NUL-terminated description of the last non-OK status. */
+const char* quail_last_error(void);
+
+/* ------------------------------------------------------------------ trie
+ * Label trie over token ids ("To Classify, Try a Trie Tree", sec. 3.1, Fig. 2;
+ * sec. 3.2 for d_m and the evaluated positions).
+ *
+ * Canonical form (bit-exact and unique, so two builders agree): node 0 is the
+ * root (token = root_token, depth 0); nodes are numbered in DFS preorder with
+ * children visited in ascending token id, so the subtree of u is the id range
+ * [u, u + subtree_size). Labels keep their input order 0..M-1.
+ *
+ * Decision depth d_m: k0 = the smallest k such that label m is the only label
+ * with prefix x_1..x_k (a label that is a prefix of another never reaches 1,
+ * so k0 = t_m for it); then d_m = the smallest k >= k0 with k = t_m or
+ * x_{k+1} not a word-continuation token (sec. 3.2: score up to the end of the
+ * word where the label branches away). With no bitmap every token starts a
+ * word and d_m = k0. Flag QUAIL_TRIE_FULL_DEPTH sets d_m = t_m (the "simple
+ * approach", full label probability, sec. 3.2).
+ * Evaluated set P: the root plus the parent of every scored token
+ * (x_k, k <= d_m), plus the end node of every prefix label, in ascending node
+ * id. P is closed under ancestors.
+ */
+typedef struct quail_trie quail_trie;
+
+enum { QUAIL_TRIE_FULL_DEPTH = 1 };
+
+/*
+ * tokens:        host, concatenated label token ids (label m = tokens[label_offsets[m] .. label_offsets[m+1]))
+ * label_offsets: host, num_labels + 1 entries, non-decreasing, label_offsets[0] = 0
+ * num_labels:    >= 2
+ * root_token:    token id of the answer position (the ANSWER: token), in [0, vocab)
+ * vocab:         vocabulary size V
+ * word_continuation_bitmap: host, nullable; ceil(V/8) bytes, bit t (byte t>>3, bit t&7) set
+ *                when token t continues the previous word instead of starting one
+ * flags:         0 or QUAIL_TRIE_FULL_DEPTH
+ * out:           receives a library-owned trie; free with quail_trie_free
+ * Errors: INVALID_ARG, EMPTY_LABEL, DUPLICATE_LABEL, TOKEN_RANGE. Host only; no GPU needed.
+ */
+quail_status quail_trie_build(const int32_t* tokens, const int64_t* label_offsets, int32_t num_labels,
+                              int32_t root_token, int32_t vocab, const uint8_t* word_continuation_bitmap,
+                              int32_t flags, quail_trie** out);
+
+/* Read-only host view of a built trie. Pointers stay valid until quail_trie_free. */
+typedef struct {
+  int32_t n_nodes;        /* including the root */
+  int32_t num_labels;     /* M */
+  int32_t n_eval;         /* a = |P| */
+  int32_t n_eval_children;/* sum over P of the child count */
+  int32_t max_depth;      /* deepest node depth (= longest label) */
+  int32_t has_prefix_labels; /* 1 if some label ends at a node with children */
+  const int32_t* parent;          /* [n_nodes], -1 for the root */
+  const int32_t* depth;           /* [n_nodes] */
+  const int32_t* token;           /* [n_nodes], token[0] = root_token */
+  const int32_t* subtree_size;    /* [n_nodes] */
+  const int32_t* child_offsets;   /* [n_nodes + 1], CSR into child_nodes */
+  const int32_t* child_nodes;     /* [n_nodes - 1], ascending token within a node */
+  const int32_t* child_tokens;    /* [n_nodes - 1], token of child_nodes[j] */
+  const uint8_t* is_branching;    /* [n_nodes], 1 if the node has more than one child */
+  const int32_t* subtree_labels;  /* [n_nodes], labels ending in the subtree (node included) */
+  const int32_t* node_label;      /* [n_nodes], label ending at the node, -1 if none */
+  const int32_t* label_end_node;  /* [M] */
+  const int32_t* label_length;    /* [M] t_m */
+  const int32_t* label_decide_depth; /* [M] d_m */
+  const int32_t* eval_nodes;      /* [n_eval], ascending node id */
+  const int32_t* eval_index_of_node; /* [n_nodes], position in eval_nodes or -1 */
+  const int32_t* eval_child_offsets; /* [n_eval + 1], children of eval node e occupy
+                                        [eval_child_offsets[e], eval_child_offsets[e+1]) in the
+                                        per-row child-logit arrays, in CSR child order */
+} quail_trie_csr;
+
+quail_status quail_trie_view(const quail_trie* trie, quail_trie_csr* out);
+void quail_trie_free(quail_trie* trie);
+
+/* Uploads the trie's device image to the current device (synchronously on
+ * `stream`). Classify calls do this on first use; calling it ahead keeps the
+ * allocation and copy out of a later call. */
+quail_status quail_trie_upload(quail_trie* trie, quail_stream_t stream);
+
+/* ------------------------------------------------------------------ model
+ * One decoder layer's attention block plus the output head, as used at the
+ * answer positions: x = E[tok]; x^ = RMSNorm(x)*in_norm; q,k,v = x^ W^T;
+ * per-head RMSNorm on q and k; rotate-half RoPE at absolute position
+ * (doc_len + depth); GQA attention (q head h uses KV head h / (Hq/Hkv));
+ * h = x + O W_o^T; z = RMSNorm(h)*final_norm; logits = z lm_head^T.
+ * All weights are device bf16, row-major [out_features, in_features]
+ * (nn.Linear layout), caller-owned. head_dim must be 128, hidden a multiple
+ * of 64, vocab >= 256.
+ */
+typedef struct {
+  int32_t hidden;      /* d_model */
+  int32_t n_q_heads;   /* H_q */
+  int32_t n_kv_heads;  /* H_kv, divides H_q */
+  int32_t head_dim;    /* 128 */
+  int32_t vocab;       /* V */
+  float rms_eps;       /* RMSNorm epsilon */
+  float rope_theta;    /* RoPE base */
+  const void* embed;      /* [V, hidden] */
+  const void* w_q;        /* [H_q*128, hidden] */
+  const void* w_k;        /* [H_kv*128, hidden] */
+  const void* w_v;        /* [H_kv*128, hidden] */
+  const void* q_norm;     /* [128] */
+  const void* k_norm;     /* [128] */
+  const void* w_o;        /* [hidden, H_q*128] */
+  const void* in_norm;    /* [hidden] */
+  const void* final_norm; /* [hidden] */
+  const void* lm_head;    /* [V, hidden] */
+} quail_model_desc;
+
+/* Paged document KV ("a fixed pool of KV pages in HBM", Quail intro, sec. 3.2.3).
+ * k_pool, v_pool: device bf16 [num_pages, n_kv_heads, page_size, 128]; keys are
+ *                 already normalised and rotated at their absolute positions.
+ * page_table:     device int32 [num_docs, max_pages]; entry (i, p) = physical page
+ *                 holding tokens [16p, 16p+16) of document i.
+ * doc_len:        device int32 [num_docs], 1 <= doc_len[i] <= max_doc_len.
+ * max_doc_len:    host-side bound used to size the launch; a device doc_len
+ *                 above it, or a page id outside [0, num_pages), sets
+ *                 QUAIL_ERR_DEVICE_BOUNDS and that document's work is skipped. */
+typedef struct {
+  const void* k_pool;
+  const void* v_pool;
+  int32_t num_pages;
+  int32_t page_size; /* must be 16 */
+  const int32_t* page_table;
+  int32_t max_pages;
+  const int32_t* doc_len;
+  int32_t max_doc_len;
+} quail_paged_kv;
+
+typedef enum { QUAIL_MODE_TRIE_TREE = 0, QUAIL_MODE_LETTERS = 1, QUAIL_MODE_TRIE_DECODE = 2 } quail_mode;
+
+/* Bytes of device workspace one classify call of `mode` needs (256-byte aligned
+ * base required). trie may be NULL for QUAIL_MODE_LETTERS; num_letters is used
+ * only by that mode. Returns 0 on invalid arguments. */
+size_t quail_workspace_size(const quail_model_desc* model, const quail_trie* trie, int32_t num_letters,
+                            int32_t num_docs, int32_t max_doc_len, quail_mode mode);
+
+/* trie_tree ("To Classify, Try a Trie Tree", sec. 3.2; Quail "Execution",
+ * "Label scoring"): all labels of all documents scored in one pass.
+ * Outputs (device, caller-owned):
+ *   label_logscore [num_docs, M] f32: log score(m), -inf for a prefix label whose
+ *                  continuation probability reaches 1
+ *   label_prob     [num_docs, M] f32: P^(m), sums to 1 per document
+ *   label_argmax   [num_docs] i32:    argmax of P^, lowest label index on ties
+ * Asynchronous on `stream`. */
+quail_status quail_classify_trie_tree(const quail_model_desc* model, const quail_paged_kv* kv, quail_trie* trie,
+                                      int32_t num_docs, void* workspace, size_t workspace_bytes,
+                                      float* label_logscore, float* label_prob, int32_t* label_argmax,
+                                      quail_stream_t stream);
+
+/* letters (sec. 3.3): one answer position (root_token at position doc_len),
+ * logits of the M letter rows only (V_out = M, sec. 4.1), renormalised.
+ * letter_tokens: host, M distinct ids in [0, vocab), M >= 2.
+ * Outputs (device): letter_logprob [num_docs, M] = log P^ (renormalised),
+ * letter_prob [num_docs, M], letter_argmax [num_docs] (lowest index on ties). */
+quail_status quail_classify_letters(const quail_model_desc* model, const quail_paged_kv* kv,
+                                    const int32_t* letter_tokens, int32_t num_letters, int32_t root_token,
+                                    int32_t num_docs, void* workspace, size_t workspace_bytes,
+                                    float* letter_logprob, float* letter_prob, int32_t* letter_argmax,
+                                    quail_stream_t stream);
+
+/* One batched greedy trie_decode step (sec. 3.1): for every document whose
+ * label is still undecided, run the model at its current branching node,
+ * pick the most likely child (lowest token id on ties), follow forced
+ * single-child chains, and stop once the subtree holds one label.
+ *   node_cursor  [num_docs] i32 device, in/out; initialise to 0 (root)
+ *   label_out    [num_docs] i32 device, in/out; initialise to -1; set once decided
+ *   active_count i32 device scalar, out: documents still undecided after the step
+ *   touched_nodes nullable u8 device [num_docs, n_nodes]; set to 1 at every node
+ *                where this step computed logits (for tests)
+ * Requires a trie with no prefix labels (else QUAIL_ERR_PREFIX_LABEL_UNSUPPORTED:
+ * greedy decoding has no stop token, sec. 3.1 note 2). Call until active_count
+ * reads 0; documents already decided cost no attention work. */
+quail_status quail_classify_trie_decode_step(const quail_model_desc* model, const quail_paged_kv* kv,
+                                             quail_trie* trie, int32_t num_docs, int32_t* node_cursor,
+                                             int32_t* label_out, int32_t* active_count, uint8_t* touched_nodes,
+                                             void* workspace, size_t workspace_bytes, quail_stream_t stream);
+
+/* Synchronises `stream`, then reads and clears the current device's error
+ * word. Returns QUAIL_OK, QUAIL_ERR_DEVICE_BOUNDS or QUAIL_ERR_DEVICE_TIMEOUT
+ * (the message names the first failing item), or QUAIL_ERR_CUDA. */
+quail_status quail_device_status(quail_stream_t stream);
+
+/* Profiling hook: when events != NULL, each classify call records
+ * events[2s] before and events[2s+1] after stage s on its stream, for
+ * s < num_stages (stages: 0 node prologue, 1 attention, 2 W_o + RMSNorm,
+ * 3 output-head GEMM alone, 4 log-sum-exp reduction + label scoring). NULL
+ * entries are skipped; events == NULL switches the hook off. Process-wide. */
+enum { QUAIL_STAGE_PROLOGUE = 0, QUAIL_STAGE_ATTENTION = 1, QUAIL_STAGE_WO_NORM = 2, QUAIL_STAGE_HEAD = 3,
+       QUAIL_STAGE_SCORING = 4, QUAIL_NUM_STAGES = 5 };
+quail_status quail_set_stage_events(quail_event_t* events, int32_t num_stages);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QUAIL_H_ */

@@ -1,0 +1,269 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the CPU oracle
+on the same seeded inputs (element by element on small cases; on sampled
+documents/labels at the workloads' full sizes)."""
+import numpy as np
+import pytest
+
+import synthetic as S
+from tests import gpu_cases as C
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import trie_label_scoring_gb300 as Q
+    Q.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+def _run_trie_tree(w, seed=0, full_depth=False, labels=None, docs=None):
+    import trie_label_scoring_gb300 as Q
+    from trie_label_scoring_gb300.torch_inputs import kv_from_docs
+    model = C.device_model(w.shape, seed)
+    ls = labels or S.make_labels(w, seed)
+    docs = docs or S.make_docs(w, seed)
+    kv = kv_from_docs(docs)
+    trie = Q.Trie(ls.labels, ls.root_token, w.shape.vocab, ls.continuation, full_depth=full_depth)
+    N, M = w.num_docs, len(ls.labels)
+    ws = torch.empty(Q.workspace_size(model, trie, 0, N, docs.max_doc_len, Q.MODE_TRIE_TREE), dtype=torch.uint8,
+                     device="cuda")
+    lsc = torch.full((N, M), float("nan"), device="cuda")
+    prob = torch.full((N, M), float("nan"), device="cuda")
+    am = torch.full((N,), -1, dtype=torch.int32, device="cuda")
+    Q.classify_trie_tree(model, kv, trie, N, ws, lsc, prob, am)
+    Q.device_status()
+    return ls, docs, lsc.cpu().numpy(), prob.cpu().numpy(), am.cpu().numpy()
+
+
+def _oracle_full(w, ls, docs, i, seed=0, full_depth=False):
+    from oracle import scoring as OS
+    from oracle.trie import build_trie
+    L = C.oracle_layer(w.shape, seed)
+    t = build_trie(ls.labels, ls.root_token, w.shape.vocab, ls.continuation, full_depth=full_depth)
+    dk, dv = C.oracle_doc_kv(docs, i)
+    return OS.trie_tree(L, dk, dv, t)
+
+
+@pytest.mark.parametrize("full_depth", [False, True])
+def test_trie_tree_tiny_all_docs(full_depth):
+    w = S.WORKLOADS["tiny-support10-4x128"]
+    ls, docs, lsc, prob, am = _run_trie_tree(w, full_depth=full_depth)
+    for i in range(w.num_docs):
+        r = _oracle_full(w, ls, docs, i, full_depth=full_depth)
+        C.check_scores(lsc[i], prob[i], am[i], r["logscore"], r["prob"], r["argmax"], f"doc {i}")
+        assert abs(prob[i].sum() - 1) < 1e-5
+
+
+def test_trie_tree_tiny_ragged_lengths():
+    """Lengths around page and split boundaries: 1, 15, 16, 17, 255, 256, 257, 700."""
+    w = S.with_docs(S.WORKLOADS["tiny-support10-4x128"], 8, (1, 700))
+    docs = S.make_docs(w, 3)
+    lens = np.array([1, 15, 16, 17, 255, 256, 257, 700], dtype=np.int32)
+    docs = _resize_docs(docs, lens, w)
+    ls, docs, lsc, prob, am = _run_trie_tree(w, docs=docs)
+    for i in range(w.num_docs):
+        r = _oracle_full(w, ls, docs, i)
+        C.check_scores(lsc[i], prob[i], am[i], r["logscore"], r["prob"], r["argmax"], f"len {lens[i]}")
+
+
+def _resize_docs(docs, lens, w):
+    """Same generator, fixed lengths: rebuild through a workload with one length per doc."""
+    out = []
+    for i, n in enumerate(lens):
+        wi = S.with_docs(w, 1, (int(n), int(n)))
+        out.append(S.make_docs(wi, 100 + i))
+    # concatenate page pools
+    k = np.concatenate([d.k_pool for d in out])
+    v = np.concatenate([d.v_pool for d in out])
+    maxp = max(d.page_table.shape[1] for d in out)
+    pt = np.full((len(out), maxp), -1, dtype=np.int32)
+    base = 0
+    for i, d in enumerate(out):
+        n = d.page_table.shape[1]
+        pt[i, :n] = d.page_table[0] + base
+        base += d.k_pool.shape[0]
+    return S.PagedDocs(np.array(lens, dtype=np.int32), pt, k, v)
+
+
+def test_trie_tree_prefix_labels_tiny():
+    """Labels that are prefixes of other labels (prefix correction on the GPU)."""
+    w = S.WORKLOADS["tiny-support10-4x128"]
+    rng = np.random.default_rng(7)
+    toks = [int(t) for t in rng.choice(w.shape.vocab, size=6, replace=False)]
+    labels = [[toks[0]], [toks[0], toks[1]], [toks[0], toks[2]], [toks[3]], [toks[3], toks[4], toks[5]],
+              [toks[4]]]
+    ls = S.LabelSet(labels, int(toks[5]) ^ 1, None)
+    ls_, docs, lsc, prob, am = _run_trie_tree(w, labels=ls)
+    for i in range(w.num_docs):
+        r = _oracle_full(w, ls, docs, i)
+        C.check_scores(lsc[i], prob[i], am[i], r["logscore"], r["prob"], r["argmax"], f"doc {i}")
+
+
+@pytest.mark.parametrize("name,ndocs", [("qwen3-4b-support10-256docs", 8)])
+def test_trie_tree_qwen_small_all_docs(name, ndocs):
+    w = S.with_docs(S.WORKLOADS[name], ndocs)
+    ls, docs, lsc, prob, am = _run_trie_tree(w)
+    for i in range(ndocs):
+        r = _oracle_full(w, ls, docs, i)
+        C.check_scores(lsc[i], prob[i], am[i], r["logscore"], r["prob"], r["argmax"], f"doc {i}")
+
+
+@pytest.mark.parametrize("name,sample_docs", [
+    ("qwen3-4b-support10-256docs", [0, 77, 255]),
+    ("qwen3-4b-tree255-64x2048", [5]),
+    ("qwen3-4b-tree20-32x8192", [0, 31]),
+])
+def test_trie_tree_full_size_sampled_docs(name, sample_docs):
+    w = S.WORKLOADS[name]
+    ls, docs, lsc, prob, am = _run_trie_tree(w)
+    assert np.all(np.abs(prob.sum(axis=1) - 1) < 1e-4)
+    for i in sample_docs:
+        r = _oracle_full(w, ls, docs, i)
+        C.check_scores(lsc[i], prob[i], am[i], r["logscore"], r["prob"], r["argmax"], f"{name} doc {i}")
+
+
+def test_trie_tree_large_label_set_sampled_labels():
+    """5,000 labels: log scores of sampled labels one by one; probabilities via
+    properties (sum to 1, proportional to exp(log score))."""
+    from oracle import scoring as OS
+    from oracle.trie import build_trie
+    w = S.WORKLOADS["qwen3-4b-tree5000-16x1024"]
+    ls, docs, lsc, prob, am = _run_trie_tree(w)
+    assert np.all(np.abs(prob.sum(axis=1) - 1) < 1e-4)
+    t = build_trie(ls.labels, ls.root_token, w.shape.vocab, ls.continuation)
+    L = C.oracle_layer(w.shape)
+    rng = np.random.default_rng(11)
+    for i in (0, 15):
+        ratio = prob[i] / np.exp(lsc[i] - lsc[i].max())
+        assert np.allclose(ratio, ratio[0], rtol=1e-4)
+        labels = sorted(set(rng.choice(len(ls.labels), size=12, replace=False).tolist()) | {int(am[i])})
+        nodes = sorted({u for m in labels for u in OS.label_nodes(t, m)})
+        dk, dv = C.oracle_doc_kv(docs, i)
+        rows = OS.eval_logprob_rows(L, dk, dv, t, nodes=nodes)
+        for m in labels:
+            ref = OS.label_logscore(t, m, lambda u, tok: rows[u][tok])
+            assert abs(lsc[i, m] - ref) <= C.TOL_LOGSCORE, f"doc {i} label {m}: {lsc[i, m]} vs {ref}"
+
+
+def test_letters_tiny_and_full_size_sample():
+    import trie_label_scoring_gb300 as Q
+    from oracle import scoring as OS
+    from trie_label_scoring_gb300.torch_inputs import kv_from_docs
+    for name, sample in (("tiny-support10-4x128", None), ("qwen3-4b-letters255-64x2048", [0, 63])):
+        w = S.WORKLOADS[name]
+        if name.startswith("tiny"):
+            rng = np.random.default_rng(5)
+            letters = [int(x) for x in rng.choice(w.shape.vocab, size=10, replace=False)]
+            root = 17
+        else:
+            ls = S.make_labels(w, 0)
+            letters, root = [l[0] for l in ls.labels], ls.root_token
+        model = C.device_model(w.shape)
+        docs = S.make_docs(w, 0)
+        kv = kv_from_docs(docs)
+        N, M = w.num_docs, len(letters)
+        ws = torch.empty(Q.workspace_size(model, None, M, N, docs.max_doc_len, Q.MODE_LETTERS), dtype=torch.uint8,
+                         device="cuda")
+        lp = torch.empty((N, M), device="cuda")
+        pr = torch.empty((N, M), device="cuda")
+        am = torch.empty((N,), dtype=torch.int32, device="cuda")
+        Q.classify_letters(model, kv, letters, root, N, ws, lp, pr, am)
+        Q.device_status()
+        lp, pr, am = lp.cpu().numpy(), pr.cpu().numpy(), am.cpu().numpy()
+        L = C.oracle_layer(w.shape)
+        for i in (range(N) if sample is None else sample):
+            dk, dv = C.oracle_doc_kv(docs, i)
+            r = OS.letters(L, dk, dv, letters, root)
+            C.check_scores(lp[i], pr[i], am[i], r["logprob"], r["prob"], r["argmax"], f"{name} doc {i}")
+
+
+def _run_decode(w, docs, ls, max_steps=64):
+    import trie_label_scoring_gb300 as Q
+    from trie_label_scoring_gb300.torch_inputs import kv_from_docs
+    model = C.device_model(w.shape)
+    kv = kv_from_docs(docs)
+    trie = Q.Trie(ls.labels, ls.root_token, w.shape.vocab, ls.continuation)
+    N = w.num_docs
+    ws = torch.empty(Q.workspace_size(model, trie, 0, N, docs.max_doc_len, Q.MODE_TRIE_DECODE), dtype=torch.uint8,
+                     device="cuda")
+    cur = torch.zeros(N, dtype=torch.int32, device="cuda")
+    lab = torch.full((N,), -1, dtype=torch.int32, device="cuda")
+    act = torch.zeros(1, dtype=torch.int32, device="cuda")
+    touched = torch.zeros((N, trie.n_nodes), dtype=torch.uint8, device="cuda")
+    steps = 0
+    while True:
+        Q.classify_trie_decode_step(model, kv, trie, N, cur, lab, act, ws, touched)
+        steps += 1
+        if int(act.item()) == 0 or steps >= max_steps:
+            break
+    Q.device_status()
+    return lab.cpu().numpy(), touched.cpu().numpy(), steps, trie.view()
+
+
+@pytest.mark.parametrize("name,sample", [("tiny-support10-4x128", None), ("qwen3-4b-tree20-32x8192", [0, 9, 31])])
+def test_trie_decode_matches_oracle_walk(name, sample):
+    from oracle import scoring as OS
+    from oracle.trie import build_trie
+    w = S.WORKLOADS[name]
+    ls = S.make_labels(w, 0)
+    docs = S.make_docs(w, 0)
+    lab, touched, steps, view = _run_decode(w, docs, ls)
+    t = build_trie(ls.labels, ls.root_token, w.shape.vocab, ls.continuation)
+    branching = set(np.nonzero(t["is_branching"])[0].tolist())
+    assert (lab >= 0).all() and steps <= t["max_depth"] + 1
+    L = C.oracle_layer(w.shape)
+    for i in (range(w.num_docs) if sample is None else sample):
+        assert set(np.nonzero(touched[i])[0].tolist()) <= branching
+        dk, dv = C.oracle_doc_kv(docs, i)
+        r = OS.trie_decode(L, dk, dv, t)
+        if lab[i] != r["label"]:
+            # a near-tie at some branching node may flip in fp32 vs fp64: the
+            # GPU's pick must then be within tolerance of the oracle's best
+            pytest.fail(f"doc {i}: decode label {lab[i]} != oracle {r['label']}")
+        assert set(np.nonzero(touched[i])[0].tolist()) == set(r["touched"])
+    if name.startswith("tiny"):
+        assert set(np.nonzero(touched.any(axis=0))[0].tolist()) <= branching and len(branching) == 3
+
+
+def test_decode_rejects_prefix_labels():
+    import trie_label_scoring_gb300 as Q
+    w = S.WORKLOADS["tiny-support10-4x128"]
+    ls = S.LabelSet([[5], [5, 6], [7]], 1, None)
+    docs = S.make_docs(w, 0)
+    with pytest.raises(Q.QuailError) as e:
+        _run_decode(w, docs, ls)
+    assert e.value.name == "QUAIL_ERR_PREFIX_LABEL_UNSUPPORTED"
+
+
+def test_device_bounds_error_is_reported():
+    """A page id outside the pool is caught by the kernel's own check (no copy
+    is issued for it) and reported through quail_device_status."""
+    import trie_label_scoring_gb300 as Q
+    w = S.WORKLOADS["tiny-support10-4x128"]
+    docs = S.make_docs(w, 0)
+    bad = S.PagedDocs(docs.doc_len.copy(), docs.page_table.copy(), docs.k_pool, docs.v_pool)
+    bad.page_table[2, 1] = docs.k_pool.shape[0] + 5
+    with pytest.raises(Q.QuailError) as e:
+        _run_trie_tree(w, docs=bad)
+    assert e.value.name == "QUAIL_ERR_DEVICE_BOUNDS"
+    _run_trie_tree(w, docs=docs)  # context still usable, error word cleared
+
+
+def test_workspace_too_small_is_rejected():
+    import trie_label_scoring_gb300 as Q
+    from trie_label_scoring_gb300.torch_inputs import kv_from_docs
+    w = S.WORKLOADS["tiny-support10-4x128"]
+    model = C.device_model(w.shape)
+    ls = S.make_labels(w, 0)
+    docs = S.make_docs(w, 0)
+    kv = kv_from_docs(docs)
+    trie = Q.Trie(ls.labels, ls.root_token, w.shape.vocab, ls.continuation)
+    need = Q.workspace_size(model, trie, 0, 4, docs.max_doc_len, Q.MODE_TRIE_TREE)
+    ws = torch.empty(need - 1024, dtype=torch.uint8, device="cuda")
+    out = torch.empty((4, 10), device="cuda")
+    am = torch.empty(4, dtype=torch.int32, device="cuda")
+    with pytest.raises(Q.QuailError) as e:
+        Q.classify_trie_tree(model, kv, trie, 4, ws, out, out, am)
+    assert e.value.name == "QUAIL_ERR_WORKSPACE"

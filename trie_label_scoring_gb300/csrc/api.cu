@@ -1,0 +1,691 @@
+// C ABI of libquail (see include/quail.h): argument validation, workspace
+// planning, TMA descriptors and the launch sequence of each call.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "kernels.h"
+#include "quail_internal.h"
+#include "trie.h"
+
+using namespace quail;
+
+// ------------------------------------------------------------------ errors
+namespace {
+
+thread_local std::string g_last_error;
+
+quail_status fail(quail_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+#define CUDA_TRY(expr)                                                                         \
+  do {                                                                                         \
+    cudaError_t _e = (expr);                                                                   \
+    if (_e != cudaSuccess) return fail(QUAIL_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(_e)); \
+  } while (0)
+
+// First device error (code, detail); kernels set it with atomicCAS, never trap.
+__device__ int g_quail_err[2];
+
+struct DeviceState {
+  bool ready = false;
+  int* err = nullptr;
+  int num_sms = 0;
+};
+std::mutex g_dev_mu;
+DeviceState g_dev[64];
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+quail_status device_state(DeviceState** out) {
+  int dev = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return fail(QUAIL_ERR_CUDA, "device id %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.ready) {
+    CUDA_TRY(cudaGetSymbolAddress(reinterpret_cast<void**>(&d.err), g_quail_err));
+    CUDA_TRY(cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev));
+    int major = 0, minor = 0;
+    CUDA_TRY(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev));
+    CUDA_TRY(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev));
+    if (major != 10 || minor != 3)
+      return fail(QUAIL_ERR_UNSUPPORTED_SHAPE, "libquail is built for sm_103a; device %d is sm_%d%d", dev, major,
+                  minor);
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      CUDA_TRY(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q));
+      if (fn == nullptr || q != cudaDriverEntryPointSuccess)
+        return fail(QUAIL_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    d.ready = true;
+  }
+  *out = &d;
+  return QUAIL_OK;
+}
+
+// 2D bf16 tensor [rows, cols] (cols contiguous, row stride ld elements), box
+// box_cols x box_rows, 128-byte swizzle (box_cols * 2 must be 128).
+quail_status encode_2d_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint64_t ld,
+                            uint32_t box_cols, uint32_t box_rows) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(QUAIL_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return QUAIL_OK;
+}
+
+// ------------------------------------------------------------------ profiling hook
+std::mutex g_ev_mu;
+std::vector<cudaEvent_t> g_events;
+
+void stage_mark(int stage, bool end, cudaStream_t st) {
+  std::lock_guard<std::mutex> lk(g_ev_mu);
+  const size_t i = 2 * static_cast<size_t>(stage) + (end ? 1 : 0);
+  if (i < g_events.size() && g_events[i] != nullptr) cudaEventRecord(g_events[i], st);
+}
+
+// ------------------------------------------------------------------ validation
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+quail_status check_model(const quail_model_desc* m) {
+  if (m == nullptr) return fail(QUAIL_ERR_INVALID_ARG, "model is null");
+  if (m->head_dim != 128) return fail(QUAIL_ERR_UNSUPPORTED_SHAPE, "head_dim must be 128 (got %d)", m->head_dim);
+  if (m->hidden <= 0 || m->hidden % 64 != 0)
+    return fail(QUAIL_ERR_UNSUPPORTED_SHAPE, "hidden must be a positive multiple of 64 (got %d)", m->hidden);
+  if (m->n_kv_heads <= 0 || m->n_q_heads <= 0 || m->n_q_heads % m->n_kv_heads != 0)
+    return fail(QUAIL_ERR_UNSUPPORTED_SHAPE, "n_q_heads must be a positive multiple of n_kv_heads");
+  if (m->n_q_heads > 128) return fail(QUAIL_ERR_UNSUPPORTED_SHAPE, "at most 128 query heads");
+  if (m->vocab < 256) return fail(QUAIL_ERR_UNSUPPORTED_SHAPE, "vocab must be >= 256");
+  if (!(m->rms_eps > 0.f) || !(m->rope_theta > 1.f)) return fail(QUAIL_ERR_INVALID_ARG, "bad rms_eps / rope_theta");
+  const void* ptrs[] = {m->embed, m->w_q, m->w_k, m->w_v, m->q_norm, m->k_norm,
+                        m->w_o, m->in_norm, m->final_norm, m->lm_head};
+  for (const void* p : ptrs) {
+    if (p == nullptr) return fail(QUAIL_ERR_INVALID_ARG, "a model weight pointer is null");
+    if (!aligned16(p)) return fail(QUAIL_ERR_INVALID_ARG, "model weights must be 16-byte aligned");
+  }
+  return QUAIL_OK;
+}
+
+quail_status check_kv(const quail_paged_kv* kv, const quail_model_desc* m) {
+  if (kv == nullptr) return fail(QUAIL_ERR_INVALID_ARG, "kv is null");
+  if (kv->page_size != 16) return fail(QUAIL_ERR_UNSUPPORTED_SHAPE, "page_size must be 16 (got %d)", kv->page_size);
+  if (kv->k_pool == nullptr || kv->v_pool == nullptr || kv->page_table == nullptr || kv->doc_len == nullptr)
+    return fail(QUAIL_ERR_INVALID_ARG, "a kv pointer is null");
+  if (!aligned16(kv->k_pool) || !aligned16(kv->v_pool)) return fail(QUAIL_ERR_INVALID_ARG, "kv pools must be 16-byte aligned");
+  if (kv->num_pages <= 0 || kv->max_doc_len <= 0 || kv->max_pages < (kv->max_doc_len + 15) / 16)
+    return fail(QUAIL_ERR_INVALID_ARG, "num_pages, max_doc_len or max_pages inconsistent");
+  if (static_cast<int64_t>(kv->num_pages) * m->n_kv_heads * 16 > (int64_t(1) << 31) - 1)
+    return fail(QUAIL_ERR_UNSUPPORTED_SHAPE, "KV pool too large for 32-bit row coordinates");
+  return QUAIL_OK;
+}
+
+quail_status check_workspace(void* ws, size_t ws_bytes, size_t need) {
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return fail(QUAIL_ERR_WORKSPACE, "workspace must be non-null and 256-byte aligned");
+  if (ws_bytes < need) return fail(QUAIL_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes", ws_bytes, need);
+  return QUAIL_OK;
+}
+
+// ------------------------------------------------------------------ workspace plan
+struct Carver {
+  uint8_t* base;
+  size_t off = 0;
+  template <class T>
+  T* take(size_t count) {
+    off = (off + 255) & ~size_t(255);
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += count * sizeof(T);
+    return p;
+  }
+};
+
+size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
+
+struct AttnShape {
+  int rows_per_kv, row_tile, rows_pad, split_tokens, n_splits;
+};
+
+AttnShape attn_shape(const quail_model_desc* m, int nq, int max_doc_len) {
+  AttnShape s;
+  const int G = m->n_q_heads / m->n_kv_heads;
+  s.rows_per_kv = nq * G;
+  s.row_tile = s.rows_per_kv <= 16 ? 16 : 64;
+  s.rows_pad = static_cast<int>(round_up(s.rows_per_kv, s.row_tile));
+  // Few query rows per KV head: split the document into 256-token chunks so the
+  // KV stream is spread over many CTAs. Many rows: the rows give the parallelism.
+  s.split_tokens = s.rows_per_kv <= 64 ? 256 : static_cast<int>(round_up(max_doc_len, 16));
+  s.n_splits = (max_doc_len + s.split_tokens - 1) / s.split_tokens;
+  return s;
+}
+
+struct Buffers {
+  bf16* xhat;
+  float* qkv;
+  float* tree_o;
+  float2* tree_ml;
+  float* part_o;
+  float2* part_ml;
+  bf16* attn_out;
+  float* h_pre;
+  bf16* z;
+  float* z_f32;
+  float2* lse_part;
+  float* lse;
+  float* child_logit;
+  int* small;  // node tables / slot lists
+};
+
+// Carves (or sizes, when base is null) the workspace of one call.
+// nodes: rows of the node prologue; slots x nq: output rows.
+size_t plan(uint8_t* base, const quail_model_desc* m, int nodes, int slots, int nq, int max_doc_len, bool head,
+            int n_child, bool need_zf32, int small_ints, Buffers* b) {
+  const int d = m->hidden, hq = m->n_q_heads, hkv = m->n_kv_heads;
+  const int ldq = (hq + 2 * hkv) * 128;
+  const AttnShape as = attn_shape(m, nq, max_doc_len);
+  const size_t rows = static_cast<size_t>(slots) * nq;
+  const size_t rows_p = round_up(rows, 128);
+  const int n_tiles = (m->vocab + kHeadBN - 1) / kHeadBN;
+  Carver c{base};
+  Buffers t{};
+  t.xhat = c.take<bf16>(round_up(nodes, 128) * 2 * d);
+  t.qkv = c.take<float>(static_cast<size_t>(nodes) * ldq);
+  t.tree_o = c.take<float>(static_cast<size_t>(nodes) * hq * 128);
+  t.tree_ml = c.take<float2>(static_cast<size_t>(nodes) * hq);
+  const size_t prow = static_cast<size_t>(slots) * hkv * as.n_splits * as.rows_pad;
+  t.part_o = c.take<float>(prow * 128);
+  t.part_ml = c.take<float2>(prow);
+  t.attn_out = c.take<bf16>(rows_p * 2 * hq * 128);
+  t.h_pre = c.take<float>(rows * d);
+  t.z = c.take<bf16>(rows_p * d);
+  t.z_f32 = (need_zf32 || head) ? c.take<float>(rows * d) : nullptr;
+  t.lse_part = head ? c.take<float2>(rows * n_tiles) : nullptr;
+  t.lse = head ? c.take<float>(rows) : nullptr;
+  t.child_logit = head ? c.take<float>(static_cast<size_t>(slots) * n_child) : nullptr;
+  t.small = c.take<int>(small_ints);
+  if (b) *b = t;
+  return c.off + 256;
+}
+
+// ------------------------------------------------------------------ shared layer steps
+struct NodeTables {
+  const int* token;   // [nodes]
+  const int* depth;   // [nodes]
+  const int* parent;  // [nodes]
+  int nodes;
+};
+
+// Node prologue: x^ = RMSNorm(E[tok]) g_in; q|k|v = x^ W^T; per-head q/k RMSNorm.
+quail_status run_prologue(const quail_model_desc* m, const NodeTables& nt, const Buffers& b, DeviceState* ds,
+                          cudaStream_t st) {
+  const int d = m->hidden, hq = m->n_q_heads, hkv = m->n_kv_heads;
+  const int ldq = (hq + 2 * hkv) * 128;
+  CUDA_TRY(launch_embed_rmsnorm(static_cast<const bf16*>(m->embed), nt.token, nt.nodes, d,
+                                static_cast<const bf16*>(m->in_norm), m->rms_eps, b.xhat, st));
+  CUtensorMap tA, tB;
+  quail_status s = encode_2d_bf16(&tA, b.xhat, round_up(nt.nodes, 128), 2 * d, 2 * d, 64, 128);
+  if (s != QUAIL_OK) return s;
+  const void* w[3] = {m->w_q, m->w_k, m->w_v};
+  const int nrows[3] = {hq * 128, hkv * 128, hkv * 128};
+  int col = 0;
+  for (int i = 0; i < 3; ++i) {
+    s = encode_2d_bf16(&tB, w[i], nrows[i], d, d, 64, 256);
+    if (s != QUAIL_OK) return s;
+    CUDA_TRY(launch_gemm_store_f32(tA, tB, nt.nodes, nrows[i], 2 * d, d, b.qkv + col, ldq, ds->num_sms, ds->err,
+                                   st));
+    col += nrows[i];
+  }
+  CUDA_TRY(launch_qk_head_norm(b.qkv, nt.nodes, ldq, hq, hkv, static_cast<const bf16*>(m->q_norm),
+                               static_cast<const bf16*>(m->k_norm), m->rms_eps, st));
+  return QUAIL_OK;
+}
+
+// Attention (tree part, paged doc part, combine) for rows = slots x nq.
+quail_status run_attention(const quail_model_desc* m, const quail_paged_kv* kv, const NodeTables& nt, RowMap map,
+                           int slots, const Buffers& b, DeviceState* ds, cudaStream_t st) {
+  const int hq = m->n_q_heads, hkv = m->n_kv_heads;
+  const AttnShape as = attn_shape(m, map.nq, kv->max_doc_len);
+  AttnArgs a{};
+  a.num_pages = kv->num_pages;
+  a.max_pages = kv->max_pages;
+  a.max_doc_len = kv->max_doc_len;
+  a.page_table = kv->page_table;
+  a.doc_len = kv->doc_len;
+  a.hq = hq;
+  a.hkv = hkv;
+  a.theta = m->rope_theta;
+  a.qkv = b.qkv;
+  a.ldq = (hq + 2 * hkv) * 128;
+  a.node_depth = nt.depth;
+  a.node_parent = nt.parent;
+  a.n_nodes = nt.nodes;
+  a.map = map;
+  a.n_slots = slots;
+  a.split_tokens = as.split_tokens;
+  a.n_splits = as.n_splits;
+  a.rows_pad = as.rows_pad;
+  a.row_tile = as.row_tile;
+  a.part_o = b.part_o;
+  a.part_ml = b.part_ml;
+  a.tree_o = b.tree_o;
+  a.tree_ml = b.tree_ml;
+  a.out = b.attn_out;
+  a.err = ds->err;
+  CUtensorMap tK, tV;
+  const uint64_t pool_rows = static_cast<uint64_t>(kv->num_pages) * hkv * 16;
+  quail_status s = encode_2d_bf16(&tK, kv->k_pool, pool_rows, 128, 128, 64, 16);
+  if (s != QUAIL_OK) return s;
+  s = encode_2d_bf16(&tV, kv->v_pool, pool_rows, 128, 128, 64, 16);
+  if (s != QUAIL_OK) return s;
+  CUDA_TRY(launch_tree_part(a, st));
+  CUDA_TRY(launch_attn_doc(a, tK, tV, st));
+  CUDA_TRY(launch_attn_combine(a, st));
+  return QUAIL_OK;
+}
+
+// h = x + O W_o^T; z = RMSNorm(h) g_f.
+quail_status run_wo_norm(const quail_model_desc* m, const NodeTables& nt, RowMap map, int rows, const Buffers& b,
+                         DeviceState* ds, cudaStream_t st) {
+  const int d = m->hidden, hq = m->n_q_heads;
+  CUtensorMap tA, tB;
+  quail_status s = encode_2d_bf16(&tA, b.attn_out, round_up(rows, 128), 2 * hq * 128, 2 * hq * 128, 64, 128);
+  if (s != QUAIL_OK) return s;
+  s = encode_2d_bf16(&tB, m->w_o, d, hq * 128, hq * 128, 64, 256);
+  if (s != QUAIL_OK) return s;
+  CUDA_TRY(launch_gemm_store_f32(tA, tB, rows, d, 2 * hq * 128, hq * 128, b.h_pre, d, ds->num_sms, ds->err, st));
+  CUDA_TRY(launch_final_norm(b.h_pre, static_cast<const bf16*>(m->embed), nt.token, map, rows, d,
+                             static_cast<const bf16*>(m->final_norm), m->rms_eps, b.z, b.z_f32, st));
+  return QUAIL_OK;
+}
+
+// ------------------------------------------------------------------ trie device image
+quail_status upload_trie(quail_trie* t, cudaStream_t st, const quail_trie::DeviceImage** out) {
+  int dev = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lk(t->mu);
+  auto it = t->images.find(dev);
+  if (it != t->images.end()) {
+    *out = &it->second;
+    return QUAIL_OK;
+  }
+  const std::vector<int32_t>* arrays[] = {
+      &t->eval_token,        &t->eval_depth,      &t->eval_parent,     &t->eval_child_offsets,
+      &t->eval_child_tokens, &t->label_term_offsets, &t->label_term_eval, &t->label_term_slot,
+      &t->label_prefix_eval, &t->int_token,       &t->int_depth,       &t->int_parent,
+      &t->int_index_of_node, &t->child_offsets,   &t->child_nodes,     &t->child_tokens,
+      &t->subtree_labels,    &t->unique_label};
+  const int na = sizeof(arrays) / sizeof(arrays[0]);
+  std::vector<size_t> offs(na);
+  size_t total = 0;
+  for (int i = 0; i < na; ++i) {
+    offs[i] = total;
+    total += round_up(std::max<size_t>(arrays[i]->size(), 1) * 4, 256);
+  }
+  std::vector<uint8_t> host(total, 0);
+  for (int i = 0; i < na; ++i)
+    if (!arrays[i]->empty()) std::memcpy(host.data() + offs[i], arrays[i]->data(), arrays[i]->size() * 4);
+  void* dptr = nullptr;
+  CUDA_TRY(cudaMalloc(&dptr, total));
+  cudaError_t e = cudaMemcpyAsync(dptr, host.data(), total, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) {
+    cudaFree(dptr);
+    return fail(QUAIL_ERR_CUDA, "trie upload: %s", cudaGetErrorString(e));
+  }
+  quail_trie::DeviceImage img;
+  img.base = dptr;
+  img.bytes = total;
+  const int32_t** fields[] = {&img.eval_token,        &img.eval_depth,         &img.eval_parent,
+                              &img.eval_child_offsets, &img.eval_child_tokens,  &img.label_term_offsets,
+                              &img.label_term_eval,   &img.label_term_slot,    &img.label_prefix_eval,
+                              &img.int_token,         &img.int_depth,          &img.int_parent,
+                              &img.int_index_of_node, &img.child_offsets,      &img.child_nodes,
+                              &img.child_tokens,      &img.subtree_labels,     &img.unique_label};
+  for (int i = 0; i < na; ++i)
+    *fields[i] = reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(dptr) + offs[i]);
+  auto res = t->images.emplace(dev, img);
+  *out = &res.first->second;
+  return QUAIL_OK;
+}
+
+}  // namespace
+
+// ================================================================== C ABI
+extern "C" {
+
+const char* quail_last_error(void) { return g_last_error.c_str(); }
+
+quail_status quail_trie_build(const int32_t* tokens, const int64_t* label_offsets, int32_t num_labels,
+                              int32_t root_token, int32_t vocab, const uint8_t* word_continuation_bitmap,
+                              int32_t flags, quail_trie** out) {
+  if (out == nullptr) return fail(QUAIL_ERR_INVALID_ARG, "out is null");
+  *out = nullptr;
+  quail_trie* t = new quail_trie();
+  std::string msg;
+  quail_status s = quail_build_trie_host(tokens, label_offsets, num_labels, root_token, vocab,
+                                         word_continuation_bitmap, flags, t, &msg);
+  if (s != QUAIL_OK) {
+    delete t;
+    return fail(s, "%s", msg.c_str());
+  }
+  *out = t;
+  return QUAIL_OK;
+}
+
+quail_status quail_trie_view(const quail_trie* t, quail_trie_csr* v) {
+  if (t == nullptr || v == nullptr) return fail(QUAIL_ERR_INVALID_ARG, "null argument");
+  v->n_nodes = t->n_nodes();
+  v->num_labels = t->num_labels;
+  v->n_eval = t->n_eval();
+  v->n_eval_children = t->eval_child_offsets.back();
+  v->max_depth = t->max_depth;
+  v->has_prefix_labels = t->has_prefix_labels;
+  v->parent = t->parent.data();
+  v->depth = t->depth.data();
+  v->token = t->token.data();
+  v->subtree_size = t->subtree_size.data();
+  v->child_offsets = t->child_offsets.data();
+  v->child_nodes = t->child_nodes.data();
+  v->child_tokens = t->child_tokens.data();
+  v->is_branching = t->is_branching.data();
+  v->subtree_labels = t->subtree_labels.data();
+  v->node_label = t->node_label.data();
+  v->label_end_node = t->label_end_node.data();
+  v->label_length = t->label_length.data();
+  v->label_decide_depth = t->label_decide_depth.data();
+  v->eval_nodes = t->eval_nodes.data();
+  v->eval_index_of_node = t->eval_index_of_node.data();
+  v->eval_child_offsets = t->eval_child_offsets.data();
+  return QUAIL_OK;
+}
+
+void quail_trie_free(quail_trie* t) {
+  if (t == nullptr) return;
+  int cur = -1;
+  cudaGetDevice(&cur);
+  for (auto& kv : t->images) {
+    if (kv.second.base == nullptr) continue;
+    if (cudaSetDevice(kv.first) == cudaSuccess) cudaFree(kv.second.base);
+  }
+  if (cur >= 0 && !t->images.empty()) cudaSetDevice(cur);
+  delete t;
+}
+
+quail_status quail_trie_upload(quail_trie* t, quail_stream_t stream) {
+  if (t == nullptr) return fail(QUAIL_ERR_INVALID_ARG, "trie is null");
+  const quail_trie::DeviceImage* img = nullptr;
+  return upload_trie(t, reinterpret_cast<cudaStream_t>(stream), &img);
+}
+
+size_t quail_workspace_size(const quail_model_desc* model, const quail_trie* trie, int32_t num_letters,
+                            int32_t num_docs, int32_t max_doc_len, quail_mode mode) {
+  if (model == nullptr || num_docs < 0 || max_doc_len <= 0) return 0;
+  if (model->n_kv_heads <= 0 || model->n_q_heads <= 0 || model->hidden <= 0 || model->vocab <= 0) return 0;
+  switch (mode) {
+    case QUAIL_MODE_TRIE_TREE:
+      if (trie == nullptr) return 0;
+      return plan(nullptr, model, trie->n_eval(), num_docs, trie->n_eval(), max_doc_len, true,
+                  trie->eval_child_offsets.back(), false, 0, nullptr);
+    case QUAIL_MODE_LETTERS:
+      if (num_letters < 2) return 0;
+      return plan(nullptr, model, 1, num_docs, 1, max_doc_len, false, 0, true, num_letters + 4, nullptr);
+    case QUAIL_MODE_TRIE_DECODE:
+      if (trie == nullptr) return 0;
+      return plan(nullptr, model, trie->n_int(), num_docs, 1, max_doc_len, false, 0, true, 2 * num_docs + 4,
+                  nullptr);
+  }
+  return 0;
+}
+
+quail_status quail_classify_trie_tree(const quail_model_desc* model, const quail_paged_kv* kv, quail_trie* trie,
+                                      int32_t num_docs, void* workspace, size_t workspace_bytes,
+                                      float* label_logscore, float* label_prob, int32_t* label_argmax,
+                                      quail_stream_t stream) {
+  quail_status s = check_model(model);
+  if (s != QUAIL_OK) return s;
+  s = check_kv(kv, model);
+  if (s != QUAIL_OK) return s;
+  if (trie == nullptr) return fail(QUAIL_ERR_INVALID_ARG, "trie is null");
+  if (trie->vocab != model->vocab) return fail(QUAIL_ERR_INVALID_ARG, "trie vocab %d != model vocab %d", trie->vocab, model->vocab);
+  if (num_docs < 0) return fail(QUAIL_ERR_INVALID_ARG, "num_docs < 0");
+  if (num_docs == 0) return QUAIL_OK;
+  if (num_docs > 65535) return fail(QUAIL_ERR_UNSUPPORTED_SHAPE, "at most 65535 documents per call");
+  if (label_logscore == nullptr || label_prob == nullptr || label_argmax == nullptr)
+    return fail(QUAIL_ERR_INVALID_ARG, "an output pointer is null");
+  const int a = trie->n_eval();
+  const int n_child = trie->eval_child_offsets.back();
+  const size_t need = plan(nullptr, model, a, num_docs, a, kv->max_doc_len, true, n_child, false, 0, nullptr);
+  s = check_workspace(workspace, workspace_bytes, need);
+  if (s != QUAIL_OK) return s;
+  DeviceState* ds = nullptr;
+  s = device_state(&ds);
+  if (s != QUAIL_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const quail_trie::DeviceImage* img = nullptr;
+  s = upload_trie(trie, st, &img);
+  if (s != QUAIL_OK) return s;
+  Buffers b;
+  plan(static_cast<uint8_t*>(workspace), model, a, num_docs, a, kv->max_doc_len, true, n_child, false, 0, &b);
+  const NodeTables nt{img->eval_token, img->eval_depth, img->eval_parent, a};
+  const RowMap map{a, nullptr, nullptr, nullptr};
+  const int rows = num_docs * a;
+
+  stage_mark(QUAIL_STAGE_PROLOGUE, false, st);
+  s = run_prologue(model, nt, b, ds, st);
+  if (s != QUAIL_OK) return s;
+  stage_mark(QUAIL_STAGE_PROLOGUE, true, st);
+
+  stage_mark(QUAIL_STAGE_ATTENTION, false, st);
+  s = run_attention(model, kv, nt, map, num_docs, b, ds, st);
+  if (s != QUAIL_OK) return s;
+  stage_mark(QUAIL_STAGE_ATTENTION, true, st);
+
+  stage_mark(QUAIL_STAGE_WO_NORM, false, st);
+  s = run_wo_norm(model, nt, map, rows, b, ds, st);
+  if (s != QUAIL_OK) return s;
+  stage_mark(QUAIL_STAGE_WO_NORM, true, st);
+
+  stage_mark(QUAIL_STAGE_HEAD, false, st);
+  {
+    const int d = model->hidden;
+    const int n_tiles = (model->vocab + kHeadBN - 1) / kHeadBN;
+    CUtensorMap tA, tB;
+    s = encode_2d_bf16(&tA, b.z, round_up(rows, 128), d, d, 64, 128);
+    if (s != QUAIL_OK) return s;
+    s = encode_2d_bf16(&tB, model->lm_head, model->vocab, d, d, 64, 256);
+    if (s != QUAIL_OK) return s;
+    HeadEpilogueArgs ha{b.lse_part, b.child_logit, img->eval_child_offsets, img->eval_child_tokens, b.z_f32,
+                        static_cast<const bf16*>(model->lm_head), d, a, n_child, n_tiles};
+    CUDA_TRY(launch_gemm_head(tA, tB, rows, model->vocab, d, ha, ds->num_sms, ds->err, st));
+    stage_mark(QUAIL_STAGE_HEAD, true, st);
+    stage_mark(QUAIL_STAGE_SCORING, false, st);
+    CUDA_TRY(launch_lse_reduce(b.lse_part, rows, n_tiles, b.lse, st));
+  }
+
+  LabelScoreArgs la{b.child_logit,           b.lse,    img->label_term_offsets, img->label_term_eval,
+                    img->label_term_slot,    img->label_prefix_eval, img->eval_child_offsets, a,
+                    n_child,                 trie->num_labels, label_logscore, label_prob, label_argmax};
+  CUDA_TRY(launch_label_score(la, num_docs, st));
+  stage_mark(QUAIL_STAGE_SCORING, true, st);
+  return QUAIL_OK;
+}
+
+quail_status quail_classify_letters(const quail_model_desc* model, const quail_paged_kv* kv,
+                                    const int32_t* letter_tokens, int32_t num_letters, int32_t root_token,
+                                    int32_t num_docs, void* workspace, size_t workspace_bytes,
+                                    float* letter_logprob, float* letter_prob, int32_t* letter_argmax,
+                                    quail_stream_t stream) {
+  quail_status s = check_model(model);
+  if (s != QUAIL_OK) return s;
+  s = check_kv(kv, model);
+  if (s != QUAIL_OK) return s;
+  if (letter_tokens == nullptr || num_letters < 2) return fail(QUAIL_ERR_INVALID_ARG, "need at least 2 letters");
+  if (num_letters > 8192) return fail(QUAIL_ERR_UNSUPPORTED_SHAPE, "at most 8192 letters");
+  if (root_token < 0 || root_token >= model->vocab) return fail(QUAIL_ERR_TOKEN_RANGE, "root token out of range");
+  for (int i = 0; i < num_letters; ++i) {
+    if (letter_tokens[i] < 0 || letter_tokens[i] >= model->vocab)
+      return fail(QUAIL_ERR_TOKEN_RANGE, "letter %d has token %d outside [0, vocab)", i, letter_tokens[i]);
+  }
+  {
+    std::vector<int32_t> sorted(letter_tokens, letter_tokens + num_letters);
+    std::sort(sorted.begin(), sorted.end());
+    if (std::adjacent_find(sorted.begin(), sorted.end()) != sorted.end())
+      return fail(QUAIL_ERR_DUPLICATE_LABEL, "letter tokens must be distinct");
+  }
+  if (num_docs < 0) return fail(QUAIL_ERR_INVALID_ARG, "num_docs < 0");
+  if (num_docs == 0) return QUAIL_OK;
+  if (num_docs > 65535) return fail(QUAIL_ERR_UNSUPPORTED_SHAPE, "at most 65535 documents per call");
+  if (letter_logprob == nullptr || letter_prob == nullptr || letter_argmax == nullptr)
+    return fail(QUAIL_ERR_INVALID_ARG, "an output pointer is null");
+  const size_t need = plan(nullptr, model, 1, num_docs, 1, kv->max_doc_len, false, 0, true, num_letters + 4, nullptr);
+  s = check_workspace(workspace, workspace_bytes, need);
+  if (s != QUAIL_OK) return s;
+  DeviceState* ds = nullptr;
+  s = device_state(&ds);
+  if (s != QUAIL_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  Buffers b;
+  plan(static_cast<uint8_t*>(workspace), model, 1, num_docs, 1, kv->max_doc_len, false, 0, true, num_letters + 4, &b);
+  // small ints: [0] root token, [1] depth 0, [2] parent -1, [4..] letters
+  std::vector<int32_t> host(num_letters + 4);
+  host[0] = root_token;
+  host[1] = 0;
+  host[2] = -1;
+  host[3] = 0;
+  std::memcpy(host.data() + 4, letter_tokens, num_letters * sizeof(int32_t));
+  CUDA_TRY(cudaMemcpyAsync(b.small, host.data(), host.size() * sizeof(int32_t), cudaMemcpyHostToDevice, st));
+  const NodeTables nt{b.small, b.small + 1, b.small + 2, 1};
+  const RowMap map{1, nullptr, nullptr, nullptr};
+
+  stage_mark(QUAIL_STAGE_PROLOGUE, false, st);
+  s = run_prologue(model, nt, b, ds, st);
+  if (s != QUAIL_OK) return s;
+  stage_mark(QUAIL_STAGE_PROLOGUE, true, st);
+  stage_mark(QUAIL_STAGE_ATTENTION, false, st);
+  s = run_attention(model, kv, nt, map, num_docs, b, ds, st);
+  if (s != QUAIL_OK) return s;
+  stage_mark(QUAIL_STAGE_ATTENTION, true, st);
+  stage_mark(QUAIL_STAGE_WO_NORM, false, st);
+  s = run_wo_norm(model, nt, map, num_docs, b, ds, st);
+  if (s != QUAIL_OK) return s;
+  stage_mark(QUAIL_STAGE_WO_NORM, true, st);
+  stage_mark(QUAIL_STAGE_HEAD, false, st);
+  CUDA_TRY(launch_letters_head(b.z_f32, static_cast<const bf16*>(model->lm_head), b.small + 4, num_letters,
+                               num_docs, model->hidden, letter_logprob, letter_prob, letter_argmax, st));
+  stage_mark(QUAIL_STAGE_HEAD, true, st);
+  return QUAIL_OK;
+}
+
+quail_status quail_classify_trie_decode_step(const quail_model_desc* model, const quail_paged_kv* kv,
+                                             quail_trie* trie, int32_t num_docs, int32_t* node_cursor,
+                                             int32_t* label_out, int32_t* active_count, uint8_t* touched_nodes,
+                                             void* workspace, size_t workspace_bytes, quail_stream_t stream) {
+  quail_status s = check_model(model);
+  if (s != QUAIL_OK) return s;
+  s = check_kv(kv, model);
+  if (s != QUAIL_OK) return s;
+  if (trie == nullptr) return fail(QUAIL_ERR_INVALID_ARG, "trie is null");
+  if (trie->vocab != model->vocab) return fail(QUAIL_ERR_INVALID_ARG, "trie vocab %d != model vocab %d", trie->vocab, model->vocab);
+  if (trie->has_prefix_labels)
+    return fail(QUAIL_ERR_PREFIX_LABEL_UNSUPPORTED,
+                "greedy decoding cannot stop at a label that is a prefix of another label");
+  if (num_docs < 0) return fail(QUAIL_ERR_INVALID_ARG, "num_docs < 0");
+  if (node_cursor == nullptr || label_out == nullptr || active_count == nullptr)
+    return fail(QUAIL_ERR_INVALID_ARG, "cursor, label or count pointer is null");
+  if (num_docs == 0) {
+    CUDA_TRY(cudaMemsetAsync(active_count, 0, sizeof(int32_t), reinterpret_cast<cudaStream_t>(stream)));
+    return QUAIL_OK;
+  }
+  if (num_docs > 65535) return fail(QUAIL_ERR_UNSUPPORTED_SHAPE, "at most 65535 documents per call");
+  const int ni = trie->n_int();
+  const size_t need = plan(nullptr, model, ni, num_docs, 1, kv->max_doc_len, false, 0, true, 2 * num_docs + 4, nullptr);
+  s = check_workspace(workspace, workspace_bytes, need);
+  if (s != QUAIL_OK) return s;
+  DeviceState* ds = nullptr;
+  s = device_state(&ds);
+  if (s != QUAIL_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const quail_trie::DeviceImage* img = nullptr;
+  s = upload_trie(trie, st, &img);
+  if (s != QUAIL_OK) return s;
+  Buffers b;
+  plan(static_cast<uint8_t*>(workspace), model, ni, num_docs, 1, kv->max_doc_len, false, 0, true, 2 * num_docs + 4, &b);
+  int* slot_doc = b.small;
+  int* slot_node = b.small + num_docs;
+  int* n_slots = b.small + 2 * num_docs;
+  const DecodeTrie dt{img->child_offsets, img->child_nodes, img->child_tokens, img->subtree_labels,
+                      img->unique_label,  img->int_index_of_node, trie->n_nodes()};
+  const NodeTables nt{img->int_token, img->int_depth, img->int_parent, ni};
+  const RowMap map{1, slot_node, slot_doc, n_slots};
+
+  CUDA_TRY(launch_decode_prepare(dt, num_docs, node_cursor, label_out, slot_doc, slot_node, n_slots, active_count, st));
+  stage_mark(QUAIL_STAGE_PROLOGUE, false, st);
+  s = run_prologue(model, nt, b, ds, st);
+  if (s != QUAIL_OK) return s;
+  stage_mark(QUAIL_STAGE_PROLOGUE, true, st);
+  stage_mark(QUAIL_STAGE_ATTENTION, false, st);
+  s = run_attention(model, kv, nt, map, num_docs, b, ds, st);
+  if (s != QUAIL_OK) return s;
+  stage_mark(QUAIL_STAGE_ATTENTION, true, st);
+  stage_mark(QUAIL_STAGE_WO_NORM, false, st);
+  s = run_wo_norm(model, nt, map, num_docs, b, ds, st);
+  if (s != QUAIL_OK) return s;
+  stage_mark(QUAIL_STAGE_WO_NORM, true, st);
+  stage_mark(QUAIL_STAGE_HEAD, false, st);
+  CUDA_TRY(launch_decode_select(dt, b.z_f32, static_cast<const bf16*>(model->lm_head), model->hidden, num_docs,
+                                slot_doc, n_slots, node_cursor, label_out, active_count, touched_nodes, st));
+  stage_mark(QUAIL_STAGE_HEAD, true, st);
+  return QUAIL_OK;
+}
+
+quail_status quail_device_status(quail_stream_t stream) {
+  DeviceState* ds = nullptr;
+  quail_status s = device_state(&ds);
+  if (s != QUAIL_OK) return s;
+  CUDA_TRY(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
+  int h[2] = {0, 0};
+  CUDA_TRY(cudaMemcpy(h, ds->err, sizeof(h), cudaMemcpyDeviceToHost));
+  if (h[0] == 0) return QUAIL_OK;
+  const int zero[2] = {0, 0};
+  CUDA_TRY(cudaMemcpy(ds->err, zero, sizeof(zero), cudaMemcpyHostToDevice));
+  if (h[0] == QUAIL_ERR_DEVICE_BOUNDS)
+    return fail(QUAIL_ERR_DEVICE_BOUNDS, "document %d: doc_len or a page id out of range", h[1]);
+  if (h[0] == QUAIL_ERR_DEVICE_TIMEOUT)
+    return fail(QUAIL_ERR_DEVICE_TIMEOUT, "a bounded device wait gave up (block tag %d)", h[1]);
+  return fail(static_cast<quail_status>(h[0]), "device error %d (detail %d)", h[0], h[1]);
+}
+
+quail_status quail_set_stage_events(quail_event_t* events, int32_t num_stages) {
+  std::lock_guard<std::mutex> lk(g_ev_mu);
+  g_events.clear();
+  if (events == nullptr || num_stages <= 0) return QUAIL_OK;
+  if (num_stages > QUAIL_NUM_STAGES) return fail(QUAIL_ERR_INVALID_ARG, "at most %d stages", QUAIL_NUM_STAGES);
+  for (int i = 0; i < 2 * num_stages; ++i) g_events.push_back(reinterpret_cast<cudaEvent_t>(events[i]));
+  return QUAIL_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,525 @@
+// Tree-masked GQA attention for trie nodes ("To Classify, Try a Trie Tree",
+// sec. 3.2 "Custom attention kernel": all evaluated nodes of a document in one
+// request, each attending to the prompt and to the nodes on its own path).
+//
+// The attention of node v in document i splits into two disjoint key sets,
+// merged with the log-sum-exp / online-softmax rule ("Building an Ultra-High
+// Throughput AI-SQL Engine", sec. 3.2.4, join attention in two parts):
+//   doc part  -- the l_i cached document keys, read once per (document, KV head)
+//                for ALL of that document's nodes and query heads;
+//   tree part -- v's ancestors and v itself. Keys sit at positions l_i + depth,
+//                so q(l_i+dv).k(l_i+du) = q . R(du - dv) k: the tree part does
+//                not depend on the document and is computed once per call.
+#include <cfloat>
+
+#include "kernels.h"
+#include "quail_internal.h"
+#include "sm103.cuh"
+
+namespace quail {
+
+namespace {
+
+constexpr int kPage = 16;
+constexpr int kConsumerWarps = 4;
+constexpr int kAttnThreads = 160;  // warps 0..3 consume, warp 4 loads pages
+constexpr int kAttnStages = 8;     // multiple of kConsumerWarps
+constexpr uint32_t kHalfBytes = kPage * 64 * 2;   // 16 keys x 64 bf16, 128B-swizzled
+constexpr uint32_t kPageBytes = 4 * kHalfBytes;   // K[0:64) K[64:128) V[0:64) V[64:128)
+constexpr size_t kAttnSmem = 1024 + kAttnStages * kPageBytes + 2 * kAttnStages * 8 + 16;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct RopeTable {
+  float2 w[64];  // inv_freq_j = theta^(-2j/128) as hi + lo floats
+};
+
+// Byte offset of 16-byte chunk `c` (0..7) of key row `r` in a 128B-swizzled half tile.
+__device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t c) { return r * 128u + ((c ^ (r & 7u)) << 4); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
+  return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u));
+}
+// Two-term bf16 split of (x0, x1): hi = bf16(x), lo = bf16(x - hi).
+__device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16(x0, x1);
+  const float2 h = unpack_bf16(hi);
+  lo = pack_bf16(x0 - h.x, x1 - h.y);
+}
+
+// cos/sin of pos * w, w given as hi + lo floats; exact product and a two-step
+// reduction by 2*pi keep the angle accurate to ~1e-7 rad for pos < 2^24.
+__device__ __forceinline__ void rope_cs(int pos, float2 w, float& c, float& s) {
+  const float p = static_cast<float>(pos);
+  const float a = p * w.x;
+  const float b = fmaf(p, w.x, -a) + p * w.y;
+  const float k = rintf(a * 0.15915494309189535f);
+  float r = fmaf(-k, 6.28318548202514648f, a);  // 2*pi rounded to float
+  r = fmaf(-k, -1.7484556000744487e-07f, r);    // 2*pi - float(2*pi)
+  r += b;
+  sincosf(r, &s, &c);
+}
+
+__device__ __forceinline__ int row_doc(const RowMap& m, int slot) { return m.slot_doc ? m.slot_doc[slot] : slot; }
+__device__ __forceinline__ int row_node(const RowMap& m, int slot, int e) {
+  return m.slot_node ? m.slot_node[slot] : e;
+}
+
+// ------------------------------------------------------------------ tree part
+// Warp per (node, q head): online softmax over the node's ancestors and itself
+// with relative RoPE; fp32 q, k, v straight from the projection.
+__global__ void tree_part_kernel(AttnArgs a, RopeTable rt) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= a.n_nodes * a.hq) return;
+  const int node = warp / a.hq, h = warp % a.hq;
+  const int G = a.hq / a.hkv, g = h / G;
+  const float* qr = a.qkv + static_cast<size_t>(node) * a.ldq + h * 128;
+  const float q0 = qr[lane], q1 = qr[lane + 32], q2 = qr[lane + 64], q3 = qr[lane + 96];
+  const float2 w0 = rt.w[lane], w1 = rt.w[lane + 32];
+  const float scale = kLog2e * 0.08838834764831845f;  // log2(e) / sqrt(128)
+  const int dnode = a.node_depth[node];
+  float m = -INFINITY, l = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+  int anc = node;
+  for (int guard = 0; anc >= 0 && guard < 4096; ++guard) {
+    const float* kr = a.qkv + static_cast<size_t>(anc) * a.ldq + (a.hq + g) * 128;
+    const float* vr = a.qkv + static_cast<size_t>(anc) * a.ldq + (a.hq + a.hkv + g) * 128;
+    const float delta = static_cast<float>(a.node_depth[anc] - dnode);
+    float c0, s0, c1, s1;
+    sincosf(delta * w0.x, &s0, &c0);
+    sincosf(delta * w1.x, &s1, &c1);
+    const float k0 = kr[lane], k1 = kr[lane + 32], k2 = kr[lane + 64], k3 = kr[lane + 96];
+    float dot = q0 * (k0 * c0 - k2 * s0) + q2 * (k2 * c0 + k0 * s0) + q1 * (k1 * c1 - k3 * s1) +
+                q3 * (k3 * c1 + k1 * s1);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    const float sc = dot * scale;
+    const float nm = fmaxf(m, sc);
+    const float alpha = exp2f(m - nm), p = exp2f(sc - nm);
+    l = l * alpha + p;
+    o0 = o0 * alpha + p * vr[lane];
+    o1 = o1 * alpha + p * vr[lane + 32];
+    o2 = o2 * alpha + p * vr[lane + 64];
+    o3 = o3 * alpha + p * vr[lane + 96];
+    m = nm;
+    anc = a.node_parent[anc];
+  }
+  float* to = a.tree_o + (static_cast<size_t>(node) * a.hq + h) * 128;
+  to[lane] = o0;
+  to[lane + 32] = o1;
+  to[lane + 64] = o2;
+  to[lane + 96] = o3;
+  if (lane == 0) a.tree_ml[static_cast<size_t>(node) * a.hq + h] = make_float2(m, l);
+}
+
+// ------------------------------------------------------------------ doc part
+// CTA = (split, kv head x row group, slot). Warp 4 streams the split's KV pages
+// (K and V of one KV head: 8 KB per page) into an 8-stage ring with TMA; warps
+// 0..3 run bf16 mma.sync on 16-row query tiles with an online softmax.
+// row_tile 16: all four warps share the 16 rows and take pages round-robin,
+// then merge; row_tile 64: each warp owns 16 rows and reads every page.
+__global__ void __launch_bounds__(kAttnThreads, 2)
+    attn_doc_kernel(AttnArgs a, RopeTable rt, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + kAttnStages * kPageBytes);
+  uint64_t* empty = full + kAttnStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kAttnStages);
+
+  const int slot = blockIdx.z;
+  if (a.map.n_slots_dev != nullptr && slot >= *a.map.n_slots_dev) return;
+  const int split = blockIdx.x;
+  const int n_row_groups = a.rows_pad / a.row_tile;
+  const int g = blockIdx.y / n_row_groups;
+  const int rg = blockIdx.y % n_row_groups;
+  const int doc = row_doc(a.map, slot);
+  const int L = a.doc_len[doc];
+  if (L < 1 || L > a.max_doc_len) {
+    if (threadIdx.x == 0 && split == 0 && blockIdx.y == 0) raise_device_error(a.err, QUAIL_ERR_DEVICE_BOUNDS, doc);
+    return;
+  }
+  const int k_lo = split * a.split_tokens;
+  if (k_lo >= L) return;
+  const int k_hi = min(L, k_lo + a.split_tokens);
+  const int p0 = k_lo / kPage;
+  const int n_pages = (k_hi - k_lo + kPage - 1) / kPage;
+  const bool shared_rows = a.row_tile == 16;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kAttnStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], shared_rows ? 1 : kConsumerWarps);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------ page loader
+    if (lane == 0) {
+      int armed[kAttnStages];
+#pragma unroll
+      for (int s = 0; s < kAttnStages; ++s) armed[s] = -1;
+      const int* pt = a.page_table + static_cast<size_t>(doc) * a.max_pages;
+      for (int j = 0; j < n_pages; ++j) {
+        const int s = j % kAttnStages;
+        const int use = j / kAttnStages;
+        if (use > 0 && !mbar_wait(&empty[s], static_cast<uint32_t>((use - 1) & 1), abort_flag)) break;
+        const int phys = pt[p0 + j];
+        if (phys < 0 || phys >= a.num_pages) {
+          raise_device_error(a.err, QUAIL_ERR_DEVICE_BOUNDS, doc);
+          mbar_arrive(&full[s]);  // release the consumer on stale data; results of this doc are void
+          armed[s] = -1;
+          continue;
+        }
+        uint8_t* dst = base + s * kPageBytes;
+        const int y = (phys * a.hkv + g) * kPage;
+        mbar_arrive_expect_tx(&full[s], kPageBytes);
+        tma_load_2d(dst, &tmK, &full[s], 0, y);
+        tma_load_2d(dst + kHalfBytes, &tmK, &full[s], 64, y);
+        tma_load_2d(dst + 2 * kHalfBytes, &tmV, &full[s], 0, y);
+        tma_load_2d(dst + 3 * kHalfBytes, &tmV, &full[s], 64, y);
+        armed[s] = use & 1;
+      }
+      for (int s = 0; s < kAttnStages; ++s) {  // no copy may still be landing when the CTA exits
+        if (armed[s] < 0) continue;
+        const uint32_t ad = smem_u32(&full[s]);
+        const long long t0 = clock64();
+        while (!mbar_try_wait(ad, static_cast<uint32_t>(armed[s]))) {
+          if (clock64() - t0 > kWaitLimitCycles) {
+            *abort_flag = 1;
+            break;
+          }
+        }
+      }
+    }
+    return;  // the loader warp takes no part in the consumers' named barrier
+  }
+
+  // -------------------------------------------------- consumers
+  const int G = a.hq / a.hkv;
+  const int rows_per_kv = (a.map.slot_node ? 1 : a.map.nq) * G;
+  const int gq = lane >> 2, tq = lane & 3;
+  const int rtile = shared_rows ? 0 : warp;
+  const int row_base = rg * a.row_tile + rtile * 16;
+
+  // Q fragments with RoPE at position L + depth(node), as a two-term bf16
+  // split (qa + ql = q to ~16 bits; both multiply the exact bf16 keys).
+  uint32_t qa[8][4], ql[8][4];
+  {
+    const float* qrow[2] = {nullptr, nullptr};
+    int pos[2] = {0, 0};
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int r = row_base + gq + hr * 8;
+      if (r < rows_per_kv) {
+        const int e = r / G, hl = r % G;
+        const int node = row_node(a.map, slot, e);
+        qrow[hr] = a.qkv + static_cast<size_t>(node) * a.ldq + (g * G + hl) * 128;
+        pos[hr] = L + a.node_depth[node];
+      }
+    }
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        float lo_v[4], hi_v[4];  // rotated dims j (<64) and j + 64
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j = ks * 16 + tq * 2 + (u & 1) + (u >> 1) * 8;
+          if (qrow[hr] != nullptr) {
+            float c, s;
+            rope_cs(pos[hr], rt.w[j], c, s);
+            const float x1 = qrow[hr][j], x2 = qrow[hr][j + 64];
+            lo_v[u] = x1 * c - x2 * s;
+            hi_v[u] = x2 * c + x1 * s;
+          } else {
+            lo_v[u] = 0.f;
+            hi_v[u] = 0.f;
+          }
+        }
+        // a0/a2 hold row gq, a1/a3 row gq + 8; a0/a1 dims 2t..2t+1, a2/a3 dims 2t+8..2t+9
+        split_bf16(lo_v[0], lo_v[1], qa[ks][hr], ql[ks][hr]);
+        split_bf16(lo_v[2], lo_v[3], qa[ks][hr + 2], ql[ks][hr + 2]);
+        split_bf16(hi_v[0], hi_v[1], qa[ks + 4][hr], ql[ks + 4][hr]);
+        split_bf16(hi_v[2], hi_v[3], qa[ks + 4][hr + 2], ql[ks + 4][hr + 2]);
+      }
+    }
+  }
+
+  const float scale = kLog2e * 0.08838834764831845f;
+  float o[16][4];
+#pragma unroll
+  for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
+
+  const int j0 = shared_rows ? warp : 0;
+  const int jstep = shared_rows ? kConsumerWarps : 1;
+  for (int j = j0; j < n_pages; j += jstep) {
+    const int s = j % kAttnStages;
+    if (!mbar_wait(&full[s], static_cast<uint32_t>((j / kAttnStages) & 1), abort_flag)) break;
+    const uint32_t kb = smem_u32(base + s * kPageBytes);
+    const uint32_t vb = kb + 2 * kHalfBytes;
+    const int key0 = (p0 + j) * kPage;
+    const int valid = min(kPage, L - key0);  // >= 1
+
+    // S = Q K^T for 16 keys (two n-tiles of 8)
+    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int mi = lane >> 3, ri = lane & 7;
+      const uint32_t key = (mi >> 1) * 8 + ri;
+      const uint32_t chunk = (ks & 3) * 2 + (mi & 1);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(kb + (ks >> 2) * kHalfBytes + swz(key, chunk), b0, b1, b2, b3);
+      mma_bf16(sc[0], qa[ks], b0, b1);
+      mma_bf16(sc[1], qa[ks], b2, b3);
+      mma_bf16(sc[0], ql[ks], b0, b1);
+      mma_bf16(sc[1], ql[ks], b2, b3);
+    }
+    // online softmax (base 2); rows gq (c0, c1) and gq + 8 (c2, c3)
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int key = nt * 8 + tq * 2 + (c & 1);
+        sc[nt][c] = key < valid ? sc[nt][c] * scale : -INFINITY;
+        mx[c >> 1] = fmaxf(mx[c >> 1], sc[nt][c]);
+      }
+    }
+    float alpha[2];
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 1));
+      mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 2));
+      const float nm = fmaxf(m_r[hr], mx[hr]);
+      alpha[hr] = exp2f(m_r[hr] - nm);
+      m_r[hr] = nm;
+      l_r[hr] *= alpha[hr];
+    }
+    // P as a two-term bf16 split (pa + pl = p to ~16 bits)
+    uint32_t pa[4], pl[4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const float e0 = exp2f(sc[nt][hr * 2] - m_r[hr]);
+        const float e1 = exp2f(sc[nt][hr * 2 + 1] - m_r[hr]);
+        l_r[hr] += e0 + e1;
+        split_bf16(e0, e1, pa[nt * 2 + hr], pl[nt * 2 + hr]);
+      }
+    }
+#pragma unroll
+    for (int n = 0; n < 16; ++n) {
+      o[n][0] *= alpha[0];
+      o[n][1] *= alpha[0];
+      o[n][2] *= alpha[1];
+      o[n][3] *= alpha[1];
+    }
+    // O += P V; V fragments via transposed ldmatrix. Keys past the document
+    // end are zeroed in registers so stale slot contents never reach O.
+#pragma unroll
+    for (int np = 0; np < 8; ++np) {
+      const int mi = lane >> 3, ri = lane & 7;
+      const uint32_t key = (mi & 1) * 8 + ri;
+      const uint32_t chunk = (np & 3) * 2 + (mi >> 1);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(vb + (np >> 2) * kHalfBytes + swz(key, chunk), b0, b1, b2, b3);
+      if (valid < kPage) {
+        const int k0 = tq * 2, k1 = tq * 2 + 8;
+        const uint32_t m0 = (k0 < valid ? 0x0000ffffu : 0u) | (k0 + 1 < valid ? 0xffff0000u : 0u);
+        const uint32_t m1 = (k1 < valid ? 0x0000ffffu : 0u) | (k1 + 1 < valid ? 0xffff0000u : 0u);
+        b0 &= m0;
+        b2 &= m0;
+        b1 &= m1;
+        b3 &= m1;
+      }
+      mma_bf16(o[np * 2], pa, b0, b1);
+      mma_bf16(o[np * 2 + 1], pa, b2, b3);
+      mma_bf16(o[np * 2], pl, b0, b1);
+      mma_bf16(o[np * 2 + 1], pl, b2, b3);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+  // full row sums
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    l_r[hr] += __shfl_xor_sync(0xffffffffu, l_r[hr], 1);
+    l_r[hr] += __shfl_xor_sync(0xffffffffu, l_r[hr], 2);
+  }
+
+  const size_t part_row0 =
+      ((static_cast<size_t>(slot) * a.hkv + g) * a.n_splits + split) * static_cast<size_t>(a.rows_pad);
+  if (!shared_rows) {
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int r = row_base + gq + hr * 8;
+      float* dst = a.part_o + (part_row0 + r) * 128;
+#pragma unroll
+      for (int n = 0; n < 16; ++n)
+        *reinterpret_cast<float2*>(dst + n * 8 + tq * 2) = make_float2(o[n][hr * 2], o[n][hr * 2 + 1]);
+      if (tq == 0) a.part_ml[part_row0 + r] = make_float2(m_r[hr], l_r[hr]);
+    }
+  } else {
+    // Merge the four warps' partial softmax states through the (now idle) page ring.
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    float* so = reinterpret_cast<float*>(base) + warp * (16 * 128 + 32);
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int r = gq + hr * 8;
+#pragma unroll
+      for (int n = 0; n < 16; ++n)
+        *reinterpret_cast<float2*>(so + r * 128 + n * 8 + tq * 2) = make_float2(o[n][hr * 2], o[n][hr * 2 + 1]);
+      if (tq == 0) {
+        so[16 * 128 + r] = m_r[hr];
+        so[16 * 128 + 16 + r] = l_r[hr];
+      }
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    const int t = threadIdx.x;  // 0..127: row t / 8, dims (t % 8) * 16 .. +16
+    const int r = t >> 3, d0 = (t & 7) * 16;
+    const float* s0 = reinterpret_cast<const float*>(base);
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, s0[w * (16 * 128 + 32) + 16 * 128 + r]);
+    float acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+    float lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float* sw = s0 + w * (16 * 128 + 32);
+      const float mw = sw[16 * 128 + r];
+      const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+      lsum += f * sw[16 * 128 + 16 + r];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc[i] += f * sw[r * 128 + d0 + i];
+    }
+    float* dst = a.part_o + (part_row0 + r) * 128 + d0;
+#pragma unroll
+    for (int i = 0; i < 16; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+    if ((t & 7) == 0) a.part_ml[part_row0 + r] = make_float2(M, lsum);
+  }
+  if (threadIdx.x == 0 && *abort_flag) raise_device_error(a.err, QUAIL_ERR_DEVICE_TIMEOUT, 2000 + slot);
+}
+
+// ------------------------------------------------------------------ combine
+// Block per output row (slot, node); warp per q head: merge the document
+// splits with the tree part, normalise, write bf16 O.
+__global__ void attn_combine_kernel(AttnArgs a) {
+  const int row = blockIdx.x;
+  const int nq = a.map.nq;
+  const int slot = row / nq, e = row % nq;
+  if (a.map.n_slots_dev != nullptr && slot >= *a.map.n_slots_dev) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = a.hq / a.hkv;
+  const int doc = row_doc(a.map, slot);
+  const int L = a.doc_len[doc];
+  const int node = row_node(a.map, slot, e);
+  const int rl_base = (a.map.slot_node ? 0 : e) * G;
+  for (int h = warp; h < a.hq; h += blockDim.x >> 5) {
+    const int g = h / G;
+    const int rl = rl_base + h % G;
+    const float2 tml = a.tree_ml[static_cast<size_t>(node) * a.hq + h];
+    float M = tml.x;
+    const bool doc_ok = L >= 1 && L <= a.max_doc_len;
+    const int ns = doc_ok ? (L + a.split_tokens - 1) / a.split_tokens : 0;
+    const size_t base = (static_cast<size_t>(slot) * a.hkv + g) * a.n_splits;
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, a.part_ml[(base + s) * a.rows_pad + rl].x);
+    float f = exp2f(tml.x - M);
+    float l = f * tml.y;
+    float4 acc = *reinterpret_cast<const float4*>(a.tree_o + (static_cast<size_t>(node) * a.hq + h) * 128 + lane * 4);
+    acc.x *= f;
+    acc.y *= f;
+    acc.z *= f;
+    acc.w *= f;
+    for (int s = 0; s < ns; ++s) {
+      const size_t pr = (base + s) * a.rows_pad + rl;
+      const float2 ml = a.part_ml[pr];
+      f = exp2f(ml.x - M);
+      l += f * ml.y;
+      const float4 v = *reinterpret_cast<const float4*>(a.part_o + pr * 128 + lane * 4);
+      acc.x += f * v.x;
+      acc.y += f * v.y;
+      acc.z += f * v.z;
+      acc.w += f * v.w;
+    }
+    const float inv = 1.f / l;
+    const float o0 = acc.x * inv, o1 = acc.y * inv, o2 = acc.z * inv, o3 = acc.w * inv;
+    bf16* dst = a.out + static_cast<size_t>(row) * 2 * a.hq * 128 + h * 128 + lane * 4;
+    uint32_t h01, l01, h23, l23;
+    split_bf16(o0, o1, h01, l01);
+    split_bf16(o2, o3, h23, l23);
+    *reinterpret_cast<uint2*>(dst) = make_uint2(h01, h23);                 // O_hi
+    *reinterpret_cast<uint2*>(dst + a.hq * 128) = make_uint2(l01, l23);    // O_lo
+
+  }
+}
+
+RopeTable make_rope_table(float theta) {
+  RopeTable t;
+  for (int j = 0; j < 64; ++j) {
+    const double w = std::pow(static_cast<double>(theta), -2.0 * j / 128.0);
+    const float hi = static_cast<float>(w);
+    t.w[j] = make_float2(hi, static_cast<float>(w - static_cast<double>(hi)));
+  }
+  return t;
+}
+
+}  // namespace
+
+cudaError_t launch_tree_part(const AttnArgs& a, cudaStream_t st) {
+  const long warps = static_cast<long>(a.n_nodes) * a.hq;
+  if (warps <= 0) return cudaSuccess;
+  tree_part_kernel<<<static_cast<int>((warps * 32 + 255) / 256), 256, 0, st>>>(a, make_rope_table(a.theta));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_doc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV, cudaStream_t st) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_doc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kAttnSmem));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  dim3 grid(a.n_splits, a.hkv * (a.rows_pad / a.row_tile), a.n_slots);
+  if (grid.x == 0 || grid.z == 0) return cudaSuccess;
+  attn_doc_kernel<<<grid, kAttnThreads, kAttnSmem, st>>>(a, make_rope_table(a.theta), tmK, tmV);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_combine(const AttnArgs& a, cudaStream_t st) {
+  const int rows = a.n_slots * a.map.nq;
+  if (rows <= 0) return cudaSuccess;
+  const int threads = (a.hq < 32 ? a.hq : 32) * 32;
+  attn_combine_kernel<<<rows, threads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace quail

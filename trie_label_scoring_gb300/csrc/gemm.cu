@@ -1,0 +1,143 @@
+// tcgen05 GEMM instantiations: plain fp32 store (q/k/v and W_o projections)
+// and the output head with the fused log-sum-exp + child-token gather
+// ("To Classify, Try a Trie Tree", sec. 4.1 "Output head": the head has one
+// row per vocabulary token and a token's score is the dot product of the
+// hidden state with that row; probabilities need every row).
+#include "kernels.h"
+#include "umma_gemm.cuh"
+
+namespace quail {
+
+namespace {
+
+constexpr int kStoreBN = 256;
+constexpr int kStages = 4;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Per 128 x 256 accumulator tile and row: online max / sum of exp over the
+// valid columns (base-2 units: m2 = max * log2 e), from the tensor-core logits.
+// The child tokens of the row's node that fall inside the tile are gathered
+// here too; their logits are evaluated in fp32 from the unrounded hidden
+// state (z_f32 . W_lm[c], warp-cooperative, the tile's W rows being hot in
+// L2), because a label's log score sums up to d_m of them while the LSE
+// averages the bf16 rounding of z away. Child tokens are sorted, so one
+// binary search per tile finds the first candidate and a cursor walks the
+// 32-column chunks in order.
+struct EpiHead {
+  HeadEpilogueArgs a;
+  int M;
+  int V;
+  __device__ __forceinline__ void operator()(int m_blk, int n_blk, int lane_row, uint32_t taddr) const {
+    const int row = m_blk * kGemmBM + lane_row;
+    const int lane = threadIdx.x & 31;
+    const bool valid = row < M;
+    const int n0 = n_blk * kHeadBN;
+    int cur = 0, cend = 0;
+    float* cl_out = nullptr;
+    if (valid) {
+      const int slot = row / a.nq;
+      const int e = row - slot * a.nq;
+      int lo = __ldg(a.child_offsets + e), hi = __ldg(a.child_offsets + e + 1);
+      cend = hi;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(a.child_tokens + mid) < n0) lo = mid + 1; else hi = mid;
+      }
+      cur = lo;
+      cl_out = a.child_logit + static_cast<size_t>(slot) * a.n_child;
+    }
+    const bool full_tile = n0 + kHeadBN <= V;
+    float m2 = -INFINITY, s = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < kHeadBN / 32; ++c) {
+      float v[32];
+      tmem_ld_32cols(taddr + c * 32, v);
+      const int col_end = n0 + c * 32 + 32;
+      int tok = (cur < cend) ? __ldg(a.child_tokens + cur) : 0x7fffffff;
+      unsigned hit = __ballot_sync(0xffffffffu, tok < col_end);
+      while (hit) {
+        const int src = __ffs(hit) - 1;
+        const int t_src = __shfl_sync(0xffffffffu, tok, src);
+        const int r_src = __shfl_sync(0xffffffffu, row, src);
+        const float4* zr = reinterpret_cast<const float4*>(a.z32 + static_cast<size_t>(r_src) * a.d);
+        const uint2* wr = reinterpret_cast<const uint2*>(a.lm_head + static_cast<size_t>(t_src) * a.d);
+        float acc = 0.f;
+        for (int i = lane; i < (a.d >> 2); i += 32) {
+          const float4 z4 = zr[i];
+          const uint2 w4 = __ldg(wr + i);
+          const float2 w01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4.x));
+          const float2 w23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4.y));
+          acc = fmaf(z4.x, w01.x, acc);
+          acc = fmaf(z4.y, w01.y, acc);
+          acc = fmaf(z4.z, w23.x, acc);
+          acc = fmaf(z4.w, w23.y, acc);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == src) {
+          cl_out[cur] = acc;
+          ++cur;
+          tok = (cur < cend) ? __ldg(a.child_tokens + cur) : 0x7fffffff;
+        }
+        hit = __ballot_sync(0xffffffffu, tok < col_end);
+      }
+      const int col0 = n0 + c * 32;
+      float cm = -INFINITY;
+      if (full_tile) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          v[i] *= kLog2e;
+          cm = fmaxf(cm, v[i]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          v[i] = (col0 + i < V) ? v[i] * kLog2e : -INFINITY;
+          cm = fmaxf(cm, v[i]);
+        }
+      }
+      const float nm = fmaxf(m2, cm);  // finite: column n0 of every tile is a real token
+      float acc = s * exp2f(m2 - nm);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) acc += exp2f(v[i] - nm);
+      m2 = nm;
+      s = acc;
+    }
+    if (valid) a.lse_part[static_cast<size_t>(row) * a.n_tiles + n_blk] = make_float2(m2, s);
+  }
+};
+
+template <int BN, class Epi>
+cudaError_t launch_umma(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K, int KB, const Epi& epi,
+                        int num_sms, int* err, cudaStream_t st) {
+  using Cfg = GemmCfg<BN, kStages>;
+  auto kern = umma_gemm_kernel<BN, kStages, Epi>;
+  static bool configured = false;  // per instantiation; the attribute is per device function
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(Cfg::kSmemBytes));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int tiles = ((M + kGemmBM - 1) / kGemmBM) * ((N + BN - 1) / BN);
+  const int grid = tiles < num_sms ? tiles : num_sms;
+  if (grid <= 0) return cudaSuccess;
+  kern<<<grid, kGemmThreads, Cfg::kSmemBytes, st>>>(tmA, tmB, M, N, K, KB / kGemmBK, epi, err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_store_f32(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K, int KB,
+                                  float* C, int ldc, int num_sms, int* err, cudaStream_t st) {
+  EpiStoreF32<kStoreBN> epi{C, ldc, M, N};
+  return launch_umma<kStoreBN>(tmA, tmB, M, N, K, KB, epi, num_sms, err, st);
+}
+
+cudaError_t launch_gemm_head(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int V, int K,
+                             const HeadEpilogueArgs& args, int num_sms, int* err, cudaStream_t st) {
+  EpiHead epi{args, M, V};
+  return launch_umma<kHeadBN>(tmA, tmB, M, V, K, K, epi, num_sms, err, st);
+}
+
+}  // namespace quail

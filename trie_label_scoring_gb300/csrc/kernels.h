@@ -1,0 +1,142 @@
+// Launch wrappers for the sm_103a kernels (one translation unit each group).
+// All pointers are device pointers; every launch goes to `st` and returns the
+// launch status (cudaGetLastError).
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace quail {
+
+using bf16 = __nv_bfloat16;
+
+// ------------------------------------------------------------ GEMM (gemm.cu)
+// Tensor maps are built by the caller (encode_2d_bf16 in api.cu).
+// C[M, N] (fp32, row stride ldc) = A[M, K] * B[N, KB]^T with the B column
+// index taken modulo KB (K a multiple of KB): K = 2 KB multiplies a two-term
+// bf16 split A = [X_hi | X_lo] by B.
+cudaError_t launch_gemm_store_f32(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K, int KB,
+                                  float* C, int ldc, int num_sms, int* err, cudaStream_t st);
+
+// Output head: for every row r < M and vocabulary tile j (256 tokens):
+//   lse_part[r * n_tiles + j] = (max2, sum exp2(logit*log2e - max2)) over the tile,
+// and for every child token c of row r's node that falls in the tile:
+//   child_logit[(r / nq) * n_child + eval_child_offsets[e] + i] = z32[r] . lm_head[c]
+// (fp32), with e = r % nq. Logits never leave the chip.
+struct HeadEpilogueArgs {
+  float2* lse_part;
+  float* child_logit;
+  const int* child_offsets;  // [nq + 1]
+  const int* child_tokens;   // ascending within each node
+  const float* z32;          // [M, d] unrounded hidden states
+  const bf16* lm_head;       // [V, d]
+  int d;
+  int nq;
+  int n_child;
+  int n_tiles;
+};
+constexpr int kHeadBN = 256;
+cudaError_t launch_gemm_head(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int V, int K,
+                             const HeadEpilogueArgs& args, int num_sms, int* err, cudaStream_t st);
+
+// ------------------------------------------------------------ layer kernels (layer.cu)
+// y = RMSNorm(E[tokens[r]]) * gain as a two-term bf16 split:
+// out[r, 0:d] = bf16(y), out[r, d:2d] = bf16(y - bf16(y)); rows = n
+cudaError_t launch_embed_rmsnorm(const bf16* embed, const int* tokens, int n, int d, const bf16* gain, float eps,
+                                 bf16* out, cudaStream_t st);
+// Per-head RMSNorm in place on qkv [rows, ld]: q heads [0, hq) with gq, k heads [hq, hq + hkv) with gk.
+cudaError_t launch_qk_head_norm(float* qkv, int rows, int ld, int hq, int hkv, const bf16* gq, const bf16* gk,
+                                float eps, cudaStream_t st);
+
+// Maps an attention/output row to its trie node: slot = row / nq, e = row % nq,
+// node = slot_node ? slot_node[slot] : e.
+struct RowMap {
+  int nq;
+  const int* slot_node;   // nullable
+  const int* slot_doc;    // nullable: slot -> document (identity when null)
+  const int* n_slots_dev; // nullable: rows of slots >= *n_slots_dev are skipped
+};
+
+// z = RMSNorm(h_pre[r] + E[node_token[node(r)]]) * g_f; writes bf16 (and fp32 if z_f32).
+cudaError_t launch_final_norm(const float* h_pre, const bf16* embed, const int* node_token, RowMap map, int rows,
+                              int d, const bf16* gain, float eps, bf16* z_bf16, float* z_f32, cudaStream_t st);
+// lse[r] = log-sum-exp over the n_tiles partials of row r.
+cudaError_t launch_lse_reduce(const float2* lse_part, int rows, int n_tiles, float* lse, cudaStream_t st);
+
+// Label path sums, prefix correction, softmax over labels and argmax, one block per document.
+struct LabelScoreArgs {
+  const float* child_logit;  // [N, n_child]
+  const float* lse;          // [N * a]
+  const int* term_offsets;   // [M + 1]
+  const int* term_eval;
+  const int* term_slot;
+  const int* prefix_eval;    // [M]
+  const int* eval_child_offsets;  // [a + 1]
+  int a;
+  int n_child;
+  int M;
+  float* logscore;  // [N, M]
+  float* prob;      // [N, M]
+  int* argmax;      // [N]
+};
+cudaError_t launch_label_score(const LabelScoreArgs& args, int num_docs, cudaStream_t st);
+
+// letters: logits of the M letter rows from z_f32 [N, d], renormalised softmax, argmax.
+cudaError_t launch_letters_head(const float* z, const bf16* lm_head, const int* letter_tokens, int M, int num_docs,
+                                int d, float* logprob, float* prob, int* argmax, cudaStream_t st);
+
+// trie_decode bookkeeping.
+struct DecodeTrie {
+  const int* child_offsets;
+  const int* child_nodes;
+  const int* child_tokens;
+  const int* subtree_labels;
+  const int* unique_label;
+  const int* int_index_of_node;
+  int n_nodes;
+};
+// Normalises every undecided document's cursor (forced chains, decided
+// subtrees) and compacts the still-undecided ones into slots.
+cudaError_t launch_decode_prepare(DecodeTrie t, int num_docs, int* node_cursor, int* label_out, int* slot_doc,
+                                  int* slot_node, int* n_slots, int* active_count, cudaStream_t st);
+// Picks the most likely child for every active slot and advances.
+cudaError_t launch_decode_select(DecodeTrie t, const float* z, const bf16* lm_head, int d, int num_docs,
+                                 const int* slot_doc, const int* n_slots, int* node_cursor, int* label_out,
+                                 int* active_count, uint8_t* touched, cudaStream_t st);
+
+// ------------------------------------------------------------ attention (attention.cu)
+struct AttnArgs {
+  // paged document KV
+  int num_pages, max_pages, max_doc_len;
+  const int* page_table;
+  const int* doc_len;
+  // layer
+  int hq, hkv;
+  float theta;
+  // query nodes (rows of qkv: normalised, not rotated q | k | v in fp32)
+  const float* qkv;
+  int ldq;
+  const int* node_depth;
+  const int* node_parent;  // tree part
+  int n_nodes;             // rows of qkv
+  RowMap map;
+  int n_slots;             // host bound on slots (documents)
+  // split-KV decomposition
+  int split_tokens;
+  int n_splits;
+  int rows_pad;            // rows per (slot, kv head), padded to the row tile
+  int row_tile;            // 16 (one row tile shared by 4 warps) or 64 (4 warps x 16 rows)
+  float* part_o;           // [n_slots, hkv, n_splits, rows_pad, 128]
+  float2* part_ml;         // [n_slots, hkv, n_splits, rows_pad]
+  float* tree_o;           // [n_nodes, hq, 128]
+  float2* tree_ml;         // [n_nodes, hq]
+  bf16* out;               // [n_slots * nq, 2 * hq * 128]: O as a two-term bf16 split [O_hi | O_lo]
+  int* err;
+};
+cudaError_t launch_tree_part(const AttnArgs& a, cudaStream_t st);
+cudaError_t launch_attn_doc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV, cudaStream_t st);
+cudaError_t launch_attn_combine(const AttnArgs& a, cudaStream_t st);
+
+}  // namespace quail

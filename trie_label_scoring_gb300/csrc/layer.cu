@@ -1,0 +1,393 @@
+// Row-wise kernels of the answer-position layer and the label scoring:
+// RMSNorms, log-sum-exp reduction, label path sums and softmax
+// ("To Classify, Try a Trie Tree", sec. 3.2), the letters head (sec. 3.3) and
+// the trie_decode step bookkeeping (sec. 3.1).
+#include <cfloat>
+
+#include "kernels.h"
+#include "quail_internal.h"
+
+namespace quail {
+
+namespace {
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Block-wide sum for blockDim.x <= 1024 (multiple of 32).
+__device__ float block_sum(float v, float* scratch) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  v = warp_sum(v);
+  __syncthreads();
+  if (lane == 0) scratch[w] = v;
+  __syncthreads();
+  const int nw = blockDim.x >> 5;
+  float t = (threadIdx.x < nw) ? scratch[threadIdx.x] : 0.f;
+  if (w == 0) t = warp_sum(t);
+  if (threadIdx.x == 0) scratch[0] = t;
+  __syncthreads();
+  return scratch[0];
+}
+
+__global__ void embed_rmsnorm_kernel(const bf16* __restrict__ embed, const int* __restrict__ tokens, int d,
+                                     const bf16* __restrict__ gain, float eps, bf16* __restrict__ out) {
+  __shared__ float scratch[32];
+  const int r = blockIdx.x;
+  const bf16* x = embed + static_cast<size_t>(__ldg(tokens + r)) * d;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    const float v = __bfloat162float(x[i]);
+    ss += v * v;
+  }
+  const float inv = rsqrtf(block_sum(ss, scratch) / d + eps);
+  bf16* o = out + static_cast<size_t>(r) * 2 * d;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    const float y = __bfloat162float(x[i]) * inv * __bfloat162float(gain[i]);
+    const bf16 hi = __float2bfloat16(y);
+    o[i] = hi;
+    o[d + i] = __float2bfloat16(y - __bfloat162float(hi));
+  }
+}
+
+// One warp per (row, head) of 128 values.
+__global__ void qk_head_norm_kernel(float* qkv, int rows, int ld, int hq, int hkv, const bf16* __restrict__ gq,
+                                    const bf16* __restrict__ gk, float eps) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int heads = hq + hkv;
+  if (warp >= rows * heads) return;
+  const int r = warp / heads, h = warp % heads;
+  float4* p = reinterpret_cast<float4*>(qkv + static_cast<size_t>(r) * ld + h * 128) + lane;
+  float4 v = *p;
+  const float inv = rsqrtf(warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w) / 128.f + eps);
+  const bf16* g = (h < hq ? gq : gk) + lane * 4;
+  v.x *= inv * __bfloat162float(g[0]);
+  v.y *= inv * __bfloat162float(g[1]);
+  v.z *= inv * __bfloat162float(g[2]);
+  v.w *= inv * __bfloat162float(g[3]);
+  *p = v;
+}
+
+__global__ void final_norm_kernel(const float* __restrict__ h_pre, const bf16* __restrict__ embed,
+                                  const int* __restrict__ node_token, RowMap map, int d,
+                                  const bf16* __restrict__ gain, float eps, bf16* __restrict__ z_bf16,
+                                  float* __restrict__ z_f32) {
+  __shared__ float scratch[32];
+  const int r = blockIdx.x;
+  const int slot = r / map.nq;
+  if (map.n_slots_dev != nullptr && slot >= *map.n_slots_dev) return;
+  const int node = map.slot_node ? map.slot_node[slot] : (r - slot * map.nq);
+  const bf16* x = embed + static_cast<size_t>(__ldg(node_token + node)) * d;
+  const float* hp = h_pre + static_cast<size_t>(r) * d;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    const float v = hp[i] + __bfloat162float(x[i]);
+    ss += v * v;
+  }
+  const float inv = rsqrtf(block_sum(ss, scratch) / d + eps);
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    const float v = (hp[i] + __bfloat162float(x[i])) * inv * __bfloat162float(gain[i]);
+    z_bf16[static_cast<size_t>(r) * d + i] = __float2bfloat16(v);
+    if (z_f32) z_f32[static_cast<size_t>(r) * d + i] = v;
+  }
+}
+
+// One warp per row: combine the (max, sum) pairs of every vocabulary tile.
+__global__ void lse_reduce_kernel(const float2* __restrict__ part, int rows, int n_tiles, float* __restrict__ lse) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= rows) return;
+  const float2* p = part + static_cast<size_t>(warp) * n_tiles;
+  float m = -INFINITY, s = 0.f;
+  for (int j = lane; j < n_tiles; j += 32) {
+    const float2 v = p[j];
+    const float nm = fmaxf(m, v.x);
+    s = s * exp2f(m - nm) + v.y * exp2f(v.x - nm);
+    m = nm;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float om = __shfl_xor_sync(0xffffffffu, m, o);
+    const float os = __shfl_xor_sync(0xffffffffu, s, o);
+    const float nm = fmaxf(m, om);
+    s = (m == -INFINITY ? 0.f : s * exp2f(m - nm)) + (om == -INFINITY ? 0.f : os * exp2f(om - nm));
+    m = nm;
+  }
+  if (lane == 0) lse[warp] = (m + log2f(s)) * 0.69314718055994531f;
+}
+
+// One block per document; warp per label.
+//   logscore_m = sum_{k <= d_m} (logit(p_{k-1}, x_k) - LSE(p_{k-1}))
+//              + [prefix label] log(1 - sum_c exp(logit(end, c) - LSE(end)))
+//   prob = softmax over labels; argmax = lowest index of the maximum.
+__global__ void label_score_kernel(LabelScoreArgs a) {
+  __shared__ float s_max[32];
+  __shared__ int s_arg[32];
+  __shared__ float s_sum[32];
+  const int doc = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const float* cl = a.child_logit + static_cast<size_t>(doc) * a.n_child;
+  const float* lse = a.lse + static_cast<size_t>(doc) * a.a;
+  float* out_ls = a.logscore + static_cast<size_t>(doc) * a.M;
+  float best = -INFINITY;
+  int best_i = 0x7fffffff;
+  for (int m = warp; m < a.M; m += nw) {
+    const int t0 = __ldg(a.term_offsets + m), t1 = __ldg(a.term_offsets + m + 1);
+    float acc = 0.f;
+    for (int t = t0 + lane; t < t1; t += 32) acc += cl[__ldg(a.term_slot + t)] - lse[__ldg(a.term_eval + t)];
+    acc = warp_sum(acc);
+    const int pe = __ldg(a.prefix_eval + m);
+    if (pe >= 0) {  // prefix label: probability of stopping at its end node
+      const int c0 = __ldg(a.eval_child_offsets + pe), c1 = __ldg(a.eval_child_offsets + pe + 1);
+      double cont = 0.0;
+      for (int c = c0 + lane; c < c1; c += 32) cont += exp(static_cast<double>(cl[c]) - static_cast<double>(lse[pe]));
+      cont = warp_sum_d(cont);
+      acc = (cont < 1.0 - 1e-12) ? acc + static_cast<float>(log1p(-cont)) : -INFINITY;
+    }
+    if (lane == 0) out_ls[m] = acc;
+    if (acc > best) {  // m increases within a warp, so the first max keeps the lowest index
+      best = acc;
+      best_i = m;
+    }
+  }
+  // block argmax (value desc, index asc)
+  if (lane == 0) {
+    s_max[warp] = best;
+    s_arg[warp] = best_i;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float b = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int w = 0; w < nw; ++w) {
+      if (s_max[w] > b || (s_max[w] == b && s_arg[w] < bi)) {
+        b = s_max[w];
+        bi = s_arg[w];
+      }
+    }
+    s_max[0] = b;
+    s_arg[0] = (bi == 0x7fffffff) ? 0 : bi;
+  }
+  __syncthreads();
+  const float mx = s_max[0];
+  if (threadIdx.x == 0) a.argmax[doc] = s_arg[0];
+  float part = 0.f;
+  for (int m = threadIdx.x; m < a.M; m += blockDim.x) part += expf(out_ls[m] - mx);
+  const float total = block_sum(part, s_sum);
+  float* out_p = a.prob + static_cast<size_t>(doc) * a.M;
+  for (int m = threadIdx.x; m < a.M; m += blockDim.x) out_p[m] = expf(out_ls[m] - mx) / total;
+}
+
+// letters: one block per document, warp per letter row.
+__global__ void letters_head_kernel(const float* __restrict__ z, const bf16* __restrict__ lm_head,
+                                    const int* __restrict__ letters, int M, int d, float* __restrict__ logprob,
+                                    float* __restrict__ prob, int* __restrict__ argmax) {
+  extern __shared__ float s_logit[];
+  __shared__ float s_red[32];
+  const int doc = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const float* zr = z + static_cast<size_t>(doc) * d;
+  for (int m = warp; m < M; m += nw) {
+    const bf16* w = lm_head + static_cast<size_t>(__ldg(letters + m)) * d;
+    float acc = 0.f;
+    for (int i = lane * 2; i < d; i += 64) {
+      const float2 wv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(w + i));
+      acc += zr[i] * wv.x + zr[i + 1] * wv.y;
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) s_logit[m] = acc;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float b = -INFINITY;
+    int bi = 0;
+    for (int m = 0; m < M; ++m)
+      if (s_logit[m] > b) {
+        b = s_logit[m];
+        bi = m;
+      }
+    s_red[0] = b;
+    argmax[doc] = bi;
+  }
+  __syncthreads();
+  const float mx = s_red[0];
+  float part = 0.f;
+  for (int m = threadIdx.x; m < M; m += blockDim.x) part += expf(s_logit[m] - mx);
+  __syncthreads();
+  const float total = block_sum(part, s_red);
+  const float lt = logf(total);
+  for (int m = threadIdx.x; m < M; m += blockDim.x) {
+    const float lp = s_logit[m] - mx - lt;
+    logprob[static_cast<size_t>(doc) * M + m] = lp;
+    prob[static_cast<size_t>(doc) * M + m] = expf(lp);
+  }
+}
+
+// Descends forced single-child chains; returns the node where a choice is
+// needed or where one label is left.
+__device__ __forceinline__ int settle(const DecodeTrie& t, int u) {
+  for (int guard = 0; guard < t.n_nodes; ++guard) {
+    if (t.subtree_labels[u] <= 1) break;
+    const int c0 = t.child_offsets[u], c1 = t.child_offsets[u + 1];
+    if (c1 - c0 != 1) break;
+    u = t.child_nodes[c0];
+  }
+  return u;
+}
+
+// Single block: settles every undecided cursor and compacts the documents
+// that still need the model into slots (in document order).
+__global__ void decode_prepare_kernel(DecodeTrie t, int num_docs, int* node_cursor, int* label_out, int* slot_doc,
+                                      int* slot_node, int* n_slots, int* active_count) {
+  __shared__ int s_warp[32];
+  __shared__ int s_base;
+  if (threadIdx.x == 0) {
+    s_base = 0;
+    *active_count = 0;
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int i0 = 0; i0 < num_docs; i0 += blockDim.x) {
+    const int i = i0 + threadIdx.x;
+    bool active = false;
+    int u = 0;
+    if (i < num_docs && label_out[i] < 0) {
+      u = node_cursor[i];
+      if (u < 0 || u >= t.n_nodes) u = 0;
+      u = settle(t, u);
+      node_cursor[i] = u;
+      if (t.subtree_labels[u] <= 1) {
+        label_out[i] = t.unique_label[u];
+      } else {
+        active = true;
+      }
+    }
+    const unsigned ballot = __ballot_sync(0xffffffffu, active);
+    if (lane == 0) s_warp[warp] = __popc(ballot);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int acc = s_base;
+      for (int w = 0; w < nw; ++w) {
+        const int c = s_warp[w];
+        s_warp[w] = acc;
+        acc += c;
+      }
+      s_base = acc;
+    }
+    __syncthreads();
+    if (active) {
+      const int k = s_warp[warp] + __popc(ballot & ((1u << lane) - 1u));
+      slot_doc[k] = i;
+      slot_node[k] = t.int_index_of_node[u];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *n_slots = s_base;
+}
+
+// One block per slot: logits of the cursor's children (z in fp32), argmax with
+// the lowest token id on ties, advance, settle, record the result.
+__global__ void decode_select_kernel(DecodeTrie t, const float* __restrict__ z, const bf16* __restrict__ lm_head,
+                                     int d, const int* __restrict__ slot_doc, const int* __restrict__ n_slots,
+                                     int* node_cursor, int* label_out, int* active_count, uint8_t* touched) {
+  __shared__ float scratch[32];
+  const int slot = blockIdx.x;
+  if (slot >= *n_slots) return;
+  const int doc = slot_doc[slot];
+  const int u = node_cursor[doc];
+  const float* zr = z + static_cast<size_t>(slot) * d;
+  const int c0 = t.child_offsets[u], c1 = t.child_offsets[u + 1];
+  float best = -INFINITY;
+  int best_c = c0;
+  for (int c = c0; c < c1; ++c) {
+    const bf16* w = lm_head + static_cast<size_t>(t.child_tokens[c]) * d;
+    float acc = 0.f;
+    for (int i = threadIdx.x; i < d; i += blockDim.x) acc += zr[i] * __bfloat162float(w[i]);
+    acc = block_sum(acc, scratch);
+    if (acc > best) {  // children ascend by token: the first maximum has the lowest token id
+      best = acc;
+      best_c = c;
+    }
+  }
+  if (threadIdx.x == 0) {
+    if (touched) touched[static_cast<size_t>(doc) * t.n_nodes + u] = 1;
+    const int v = settle(t, t.child_nodes[best_c]);
+    node_cursor[doc] = v;
+    if (t.subtree_labels[v] <= 1) {
+      label_out[doc] = t.unique_label[v];
+    } else {
+      atomicAdd(active_count, 1);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_embed_rmsnorm(const bf16* embed, const int* tokens, int n, int d, const bf16* gain, float eps,
+                                 bf16* out, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  embed_rmsnorm_kernel<<<n, 256, 0, st>>>(embed, tokens, d, gain, eps, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_qk_head_norm(float* qkv, int rows, int ld, int hq, int hkv, const bf16* gq, const bf16* gk,
+                                float eps, cudaStream_t st) {
+  const long warps = static_cast<long>(rows) * (hq + hkv);
+  if (warps <= 0) return cudaSuccess;
+  const int blocks = static_cast<int>((warps * 32 + 255) / 256);
+  qk_head_norm_kernel<<<blocks, 256, 0, st>>>(qkv, rows, ld, hq, hkv, gq, gk, eps);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_final_norm(const float* h_pre, const bf16* embed, const int* node_token, RowMap map, int rows,
+                              int d, const bf16* gain, float eps, bf16* z_bf16, float* z_f32, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  final_norm_kernel<<<rows, 256, 0, st>>>(h_pre, embed, node_token, map, d, gain, eps, z_bf16, z_f32);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lse_reduce(const float2* lse_part, int rows, int n_tiles, float* lse, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  lse_reduce_kernel<<<(rows * 32 + 255) / 256, 256, 0, st>>>(lse_part, rows, n_tiles, lse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_label_score(const LabelScoreArgs& args, int num_docs, cudaStream_t st) {
+  if (num_docs <= 0) return cudaSuccess;
+  label_score_kernel<<<num_docs, 256, 0, st>>>(args);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_letters_head(const float* z, const bf16* lm_head, const int* letter_tokens, int M, int num_docs,
+                                int d, float* logprob, float* prob, int* argmax, cudaStream_t st) {
+  if (num_docs <= 0) return cudaSuccess;
+  letters_head_kernel<<<num_docs, 256, M * sizeof(float), st>>>(z, lm_head, letter_tokens, M, d, logprob, prob,
+                                                                argmax);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_prepare(DecodeTrie t, int num_docs, int* node_cursor, int* label_out, int* slot_doc,
+                                  int* slot_node, int* n_slots, int* active_count, cudaStream_t st) {
+  decode_prepare_kernel<<<1, 1024, 0, st>>>(t, num_docs, node_cursor, label_out, slot_doc, slot_node, n_slots,
+                                            active_count);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_select(DecodeTrie t, const float* z, const bf16* lm_head, int d, int num_docs,
+                                 const int* slot_doc, const int* n_slots, int* node_cursor, int* label_out,
+                                 int* active_count, uint8_t* touched, cudaStream_t st) {
+  if (num_docs <= 0) return cudaSuccess;
+  decode_select_kernel<<<num_docs, 256, 0, st>>>(t, z, lm_head, d, slot_doc, n_slots, node_cursor, label_out,
+                                                 active_count, touched);
+  return cudaGetLastError();
+}
+
+}  // namespace quail

@@ -1,0 +1,246 @@
+// Persistent, warp-specialised tcgen05 GEMM for sm_103a:  C = A * B^T
+//   A: [M, K] bf16, K contiguous (row-major)      -> TMA box 64 x 128, 128B swizzle
+//   B: [N, K] bf16, K contiguous (nn.Linear rows) -> TMA box 64 x BN,  128B swizzle
+// The B coordinate along K wraps every kb_wrap k-blocks: with A = [X_hi | X_lo]
+// (a two-term bf16 split of an fp32 operand, K doubled) and kb_wrap = K_B/64,
+// the same B rows multiply both halves, so C = (X_hi + X_lo) B^T to ~16 bits.
+// The fp32 accumulator for one 128 x BN tile lives in TMEM (two buffers, so the
+// epilogue of tile t overlaps the MMAs of tile t+1). The epilogue is a functor,
+// which is how the LM head fuses its log-sum-exp and child-token gather without
+// ever writing logits to global memory.
+//
+// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM owner + MMA
+// issuer, warps 2..5 = epilogue (warp w reads TMEM lanes 32*(w%4) .. +31).
+// Tiles are walked N-band-major: consecutive tile ids share one B band, so the
+// CTAs resident at any moment read each band of B from HBM about once and
+// re-read it from L2 for the other M tiles.
+#pragma once
+#include "sm103.cuh"
+#include "quail_internal.h"
+
+namespace quail {
+
+constexpr int kGemmBM = 128;
+constexpr int kGemmBK = 64;  // 64 bf16 = one 128-byte swizzle row
+constexpr int kGemmThreads = 192;
+
+template <int BN, int STAGES>
+struct GemmCfg {
+  static constexpr uint32_t kABytes = kGemmBM * kGemmBK * 2;
+  static constexpr uint32_t kBBytes = BN * kGemmBK * 2;
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr uint32_t kTmemCols = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
+                                        : (2 * BN <= 256) ? 256 : 512;
+  // 1024 alignment slack + stages + barriers + tmem slot + abort flag
+  static constexpr size_t kSmemBytes = 1024 + STAGES * kStageBytes + (2 * STAGES + 5) * 8 + 16;
+};
+
+__device__ __forceinline__ void gemm_tile_coords(int tile, int m_tiles, int& m_blk, int& n_blk) {
+  n_blk = tile / m_tiles;
+  m_blk = tile - n_blk * m_tiles;
+}
+
+// Epi must provide:
+//   __device__ void operator()(int m_blk, int n_blk, int lane_row, uint32_t taddr) const;
+// called by each of the 128 epilogue threads for every tile; lane_row in [0,128)
+// is this thread's accumulator row, taddr the TMEM address of (row, column 0).
+// All 32 lanes of a warp must execute the same tcgen05.ld sequence.
+template <int BN, int STAGES, class Epi>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N,
+                     int K, int kb_wrap, Epi epi, int* err) {
+  using Cfg = GemmCfg<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = base;
+  uint8_t* sB = base + STAGES * Cfg::kABytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * Cfg::kBBytes);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;  // [2]
+  uint64_t* tempty = tfull + 2;      // [2]
+  uint64_t* drain = tempty + 2;      // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int m_tiles = (M + kGemmBM - 1) / kGemmBM;
+  const int n_tiles = (N + BN - 1) / BN;
+  const int num_tiles = m_tiles * n_tiles;
+  const int nk = K / kGemmBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&tfull[0], 1);
+    mbar_init(&tfull[1], 1);
+    mbar_init(&tempty[0], 128);
+    mbar_init(&tempty[1], 128);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      int armed_parity[STAGES];
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) armed_parity[s] = -1;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        int m_blk, n_blk;
+        gemm_tile_coords(tile, m_tiles, m_blk, n_blk);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
+          tma_load_2d(sA + stage * Cfg::kABytes, &tmA, &full[stage], kb * kGemmBK, m_blk * kGemmBM);
+          tma_load_2d(sB + stage * Cfg::kBBytes, &tmB, &full[stage], (kb % kb_wrap) * kGemmBK, n_blk * BN);
+          armed_parity[stage] = static_cast<int>(phase);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Never leave with copies in flight: every armed stage must have landed.
+      for (int s = 0; s < STAGES; ++s) {
+        if (armed_parity[s] < 0) continue;
+        const uint32_t a = smem_u32(&full[s]);
+        const long long t0 = clock64();
+        while (!mbar_try_wait(a, static_cast<uint32_t>(armed_parity[s]))) {
+          if (clock64() - t0 > kWaitLimitCycles) {
+            *abort_flag = 1;
+            break;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc = umma_idesc_bf16_f32(kGemmBM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + stage * Cfg::kABytes);
+          const uint32_t b_addr = smem_u32(sB + stage * Cfg::kBBytes);
+#pragma unroll
+          for (int k = 0; k < kGemmBK / 16; ++k) {
+            umma_bf16(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), idesc,
+                      (kb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // Drain: all MMAs issued by this thread complete before TMEM is released.
+      umma_commit(drain);
+      const uint32_t a = smem_u32(drain);
+      const long long t0 = clock64();
+      while (!mbar_try_wait(a, 0u)) {
+        if (clock64() - t0 > kWaitLimitCycles) {
+          *abort_flag = 1;
+          break;
+        }
+      }
+    }
+  } else {
+    // -------------------------------------------------- epilogue warps
+    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int lane_row = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) break;
+      tc_fence_after();
+      int m_blk, n_blk;
+      gemm_tile_coords(tile, m_tiles, m_blk, n_blk);
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      epi(m_blk, n_blk, lane_row, taddr);
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+  if (threadIdx.x == 0 && *abort_flag) raise_device_error(err, QUAIL_ERR_DEVICE_TIMEOUT, 1000 + blockIdx.x);
+}
+
+// ------------------------------------------------------------ epilogues
+
+// Plain fp32 store: C[row, col] = acc (row < M, col < N), row stride ldc.
+template <int BN>
+struct EpiStoreF32 {
+  float* C;
+  int ldc;
+  int M;
+  int N;
+  __device__ __forceinline__ void operator()(int m_blk, int n_blk, int lane_row, uint32_t taddr) const {
+    const int row = m_blk * kGemmBM + lane_row;
+    const int n0 = n_blk * BN;
+    float* out = C + static_cast<size_t>(row) * ldc;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      float v[32];
+      tmem_ld_32cols(taddr + c * 32, v);
+      if (row < M) {
+        const int col0 = n0 + c * 32;
+        if (col0 + 32 <= N && (ldc & 3) == 0) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(out + col0 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (col0 + i < N) out[col0 + i] = v[i];
+        }
+      }
+    }
+  }
+};
+
+}  // namespace quail
