@@ -24,25 +24,36 @@ NEG_INF = -np.inf
 PREFIX_SATURATION = 1.0 - 1e-12
 
 
-def logscores_from_table(trie: dict, logp) -> np.ndarray:
-    """log score(m) for every label, given logp(node, child_token) = log P(child
-    token | context ending at node). Model-free: planted tables use it too."""
-    Mn = trie["num_labels"]
-    out = np.empty(Mn)
+def label_logscore(trie: dict, m: int, logp) -> float:
+    """log score(m) given logp(node, child_token) = log P(child token | context
+    ending at node): the first d_m token log-probs of the label's path, plus
+    log(1 - sum over the end node's children) for a prefix label."""
     tok = trie["token"]
-    for m in range(Mn):
-        path = label_path(trie, m)
-        d = int(trie["label_decide_depth"][m])
-        s = 0.0
-        for k in range(1, d + 1):
-            s += logp(path[k - 1], int(tok[path[k]]))
-        end = path[-1]
-        ch = children_of(trie, end)
-        if len(ch):
-            cont = sum(np.exp(logp(end, int(tok[c]))) for c in ch)
-            s = s + np.log1p(-cont) if cont < PREFIX_SATURATION else NEG_INF
-        out[m] = s
-    return out
+    path = label_path(trie, m)
+    d = int(trie["label_decide_depth"][m])
+    s = 0.0
+    for k in range(1, d + 1):
+        s += logp(path[k - 1], int(tok[path[k]]))
+    end = path[-1]
+    ch = children_of(trie, end)
+    if len(ch):
+        cont = sum(np.exp(logp(end, int(tok[c]))) for c in ch)
+        s = s + np.log1p(-cont) if cont < PREFIX_SATURATION else NEG_INF
+    return s
+
+
+def logscores_from_table(trie: dict, logp) -> np.ndarray:
+    """log score(m) for every label (model-free: planted tables use it too)."""
+    return np.array([label_logscore(trie, m, logp) for m in range(trie["num_labels"])], dtype=np.float64)
+
+
+def label_nodes(trie: dict, m: int) -> list:
+    """Nodes whose next-token distribution label m's score reads."""
+    path = label_path(trie, m)
+    nodes = path[: int(trie["label_decide_depth"][m])]
+    if len(children_of(trie, path[-1])):
+        nodes.append(path[-1])
+    return nodes
 
 
 def normalise(logscore: np.ndarray) -> tuple:
