@@ -286,6 +286,9 @@ def run_ours(args, world, rank, local):
     steps = args.steps if args.steps is not None else int(min(5000, max(20, 2000.0 / max(est_ms, 1e-3))))
 
     head_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for e0, e1 in head_ev:  # torch creates the CUDA event on first record; the library re-records it
+        e0.record(stream)
+        e1.record(stream)
     bus = None
     try:
         bus = torch.cuda.get_device_properties(local).pci_bus_id
