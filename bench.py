@@ -285,10 +285,12 @@ def run_ours(args, world, rank, local):
     est_ms = t0.elapsed_time(t1)
     steps = args.steps if args.steps is not None else int(min(5000, max(20, 2000.0 / max(est_ms, 1e-3))))
 
-    head_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    for e0, e1 in head_ev:  # torch creates the CUDA event on first record; the library re-records it
-        e0.record(stream)
-        e1.record(stream)
+    # stage events for every step (10 per step: begin/end of the 5 stages); the
+    # head GEMM's pair (stage 3) gives the roofline kernel's own duration
+    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(10)] for _ in range(steps)]
+    for evs in stage_ev:  # torch creates the CUDA event on first record; the library re-records it
+        for e in evs:
+            e.record(stream)
     bus = None
     try:
         bus = torch.cuda.get_device_properties(local).pci_bus_id
@@ -303,7 +305,7 @@ def run_ours(args, world, rank, local):
     end = torch.cuda.Event(enable_timing=True)
     start.record(stream)
     for k in range(steps):
-        Q.set_stage_events([None] * 6 + [head_ev[k][0], head_ev[k][1]])
+        Q.set_stage_events(stage_ev[k])
         step()
     end.record(stream)
     torch.cuda.synchronize()
@@ -313,7 +315,9 @@ def run_ours(args, world, rank, local):
     Q.device_status()
     elapsed_ms = start.elapsed_time(end)
     elapsed_ms = max_over_ranks(world, elapsed_ms)
-    head_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in head_ev)
+    stages_ms = {name: statistics.mean(ev[2 * i].elapsed_time(ev[2 * i + 1]) for ev in stage_ev)
+                 for i, name in enumerate(Q.STAGES)}
+    head_ms = stages_ms["head"]
     ms_per_step = elapsed_ms / steps
     value = N * world * steps / (elapsed_ms / 1e3)
 
@@ -394,7 +398,7 @@ def run_ours(args, world, rank, local):
                        "l2": "inputs larger than L2 (doc KV %.2f GB + output head %.2f GB per step)" % (
                            kv_bytes / 1e9, 2.0 * d * V / 1e9),
                        "parallelism": f"replicas x{world} (documents sharded, no collective)"},
-            "roofline": roofline, "path_roofline": path, "cpu_baseline": cpu, "e2e": e2e,
+            "roofline": roofline, "path_roofline": path, "stages_ms": stages_ms, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": count_launches() * steps, "clocks": clk,
         }
         print(json.dumps(out), flush=True)

@@ -13,6 +13,7 @@
 #include <vector>
 
 #include "kernels.h"
+#include "umma_gemm.cuh"
 #include "quail_internal.h"
 #include "trie.h"
 
@@ -121,6 +122,7 @@ quail_status check_model(const quail_model_desc* m) {
     return fail(QUAIL_ERR_UNSUPPORTED_SHAPE, "n_q_heads must be a positive multiple of n_kv_heads");
   if (m->n_q_heads > 128) return fail(QUAIL_ERR_UNSUPPORTED_SHAPE, "at most 128 query heads");
   if (m->vocab < 256) return fail(QUAIL_ERR_UNSUPPORTED_SHAPE, "vocab must be >= 256");
+  if (m->hidden > 12288) return fail(QUAIL_ERR_UNSUPPORTED_SHAPE, "hidden must be <= 12288");
   if (!(m->rms_eps > 0.f) || !(m->rope_theta > 1.f)) return fail(QUAIL_ERR_INVALID_ARG, "bad rms_eps / rope_theta");
   const void* ptrs[] = {m->embed, m->w_q, m->w_k, m->w_v, m->q_norm, m->k_norm,
                         m->w_o, m->in_norm, m->final_norm, m->lm_head};
@@ -176,22 +178,49 @@ AttnShape attn_shape(const quail_model_desc* m, int nq, int max_doc_len) {
   s.rows_per_kv = nq * G;
   s.row_tile = s.rows_per_kv <= 16 ? 16 : 64;
   s.rows_pad = static_cast<int>(round_up(s.rows_per_kv, s.row_tile));
-  // Few query rows per KV head: split the document into 256-token chunks so the
-  // KV stream is spread over many CTAs. Many rows: the rows give the parallelism.
-  s.split_tokens = s.rows_per_kv <= 64 ? 256 : static_cast<int>(round_up(max_doc_len, 16));
+  // Few query rows per KV head: split the document into 512-token chunks so the
+  // KV stream is spread over many CTAs. Many rows: the rows give the
+  // parallelism, and splits only bound the page list a CTA holds (2,048 tokens).
+  s.split_tokens = s.rows_per_kv <= 64 ? 512 : static_cast<int>(std::min<size_t>(round_up(max_doc_len, 16), 2048));
   s.n_splits = (max_doc_len + s.split_tokens - 1) / s.split_tokens;
   return s;
 }
 
+// SM count used to balance split-K; the workspace size and the call use the
+// same device, so they agree.
+int planning_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+    return n;
+  cudaGetLastError();
+  return 152;
+}
+
+struct GemmPlan {
+  int ks_qkv, ks_wo;
+};
+
+GemmPlan gemm_plan(const quail_model_desc* m, int nodes, size_t rows, int sms) {
+  const int ldq = (m->n_q_heads + 2 * m->n_kv_heads) * 128;
+  GemmPlan g;
+  g.ks_qkv = choose_k_splits(static_cast<int>(round_up(nodes, 128) / 128 * round_up(ldq, 256) / 256),
+                             m->hidden / 64, sms);
+  g.ks_wo = choose_k_splits(static_cast<int>(round_up(rows, 128) / 128 * round_up(m->hidden, 256) / 256),
+                            m->n_q_heads * 128 / 64, sms);
+  return g;
+}
+
 struct Buffers {
+  GemmPlan gp;
   bf16* xhat;
+  float* qkv_part;
   float* qkv;
   float* tree_o;
   float2* tree_ml;
   float* part_o;
   float2* part_ml;
   bf16* attn_out;
-  float* h_pre;
+  float* h_part;
   bf16* z;
   float* z_f32;
   float2* lse_part;
@@ -212,7 +241,9 @@ size_t plan(uint8_t* base, const quail_model_desc* m, int nodes, int slots, int 
   const int n_tiles = (m->vocab + kHeadBN - 1) / kHeadBN;
   Carver c{base};
   Buffers t{};
+  t.gp = gemm_plan(m, nodes, rows, planning_sms());
   t.xhat = c.take<bf16>(round_up(nodes, 128) * 2 * d);
+  t.qkv_part = c.take<float>(static_cast<size_t>(t.gp.ks_qkv) * nodes * ldq);
   t.qkv = c.take<float>(static_cast<size_t>(nodes) * ldq);
   t.tree_o = c.take<float>(static_cast<size_t>(nodes) * hq * 128);
   t.tree_ml = c.take<float2>(static_cast<size_t>(nodes) * hq);
@@ -220,7 +251,7 @@ size_t plan(uint8_t* base, const quail_model_desc* m, int nodes, int slots, int 
   t.part_o = c.take<float>(prow * 128);
   t.part_ml = c.take<float2>(prow);
   t.attn_out = c.take<bf16>(rows_p * 2 * hq * 128);
-  t.h_pre = c.take<float>(rows * d);
+  t.h_part = c.take<float>(static_cast<size_t>(t.gp.ks_wo) * rows * d);
   t.z = c.take<bf16>(rows_p * d);
   t.z_f32 = (need_zf32 || head) ? c.take<float>(rows * d) : nullptr;
   t.lse_part = head ? c.take<float2>(rows * n_tiles) : nullptr;
@@ -239,28 +270,45 @@ struct NodeTables {
   int nodes;
 };
 
-// Node prologue: x^ = RMSNorm(E[tok]) g_in; q|k|v = x^ W^T; per-head q/k RMSNorm.
+// Node prologue: x^ = RMSNorm(E[tok]) g_in (two-term bf16 split);
+// q|k|v = x^ W^T in one launch when the three weight blocks align to 256 rows;
+// per-head q/k RMSNorm while summing the k-split slabs.
 quail_status run_prologue(const quail_model_desc* m, const NodeTables& nt, const Buffers& b, DeviceState* ds,
                           cudaStream_t st) {
   const int d = m->hidden, hq = m->n_q_heads, hkv = m->n_kv_heads;
   const int ldq = (hq + 2 * hkv) * 128;
   CUDA_TRY(launch_embed_rmsnorm(static_cast<const bf16*>(m->embed), nt.token, nt.nodes, d,
                                 static_cast<const bf16*>(m->in_norm), m->rms_eps, b.xhat, st));
-  CUtensorMap tA, tB;
+  CUtensorMap tA;
   quail_status s = encode_2d_bf16(&tA, b.xhat, round_up(nt.nodes, 128), 2 * d, 2 * d, 64, 128);
   if (s != QUAIL_OK) return s;
   const void* w[3] = {m->w_q, m->w_k, m->w_v};
   const int nrows[3] = {hq * 128, hkv * 128, hkv * 128};
+  const size_t slab = static_cast<size_t>(nt.nodes) * ldq;
+  const bool aligned = (hq * 128) % 256 == 0 && (hkv * 128) % 256 == 0;
+  BSet bs{};
   int col = 0;
   for (int i = 0; i < 3; ++i) {
-    s = encode_2d_bf16(&tB, w[i], nrows[i], d, d, 64, 256);
+    const int slot = aligned ? i : 0;
+    s = encode_2d_bf16(&bs.map[slot], w[i], nrows[i], d, d, 64, 256);
     if (s != QUAIL_OK) return s;
-    CUDA_TRY(launch_gemm_store_f32(tA, tB, nt.nodes, nrows[i], 2 * d, d, b.qkv + col, ldq, ds->num_sms, ds->err,
-                                   st));
+    bs.n_begin[slot] = aligned ? col : 0;
+    bs.n_begin[slot + 1] = aligned ? col + nrows[i] : nrows[i];
+    if (!aligned) {
+      bs.count = 1;
+      CUDA_TRY(launch_gemm_proj(tA, bs, nt.nodes, nrows[i], d, b.gp.ks_qkv, b.qkv_part + col, slab, ldq, ds->num_sms,
+                                ds->err, st));
+    }
     col += nrows[i];
   }
-  CUDA_TRY(launch_qk_head_norm(b.qkv, nt.nodes, ldq, hq, hkv, static_cast<const bf16*>(m->q_norm),
-                               static_cast<const bf16*>(m->k_norm), m->rms_eps, st));
+  if (aligned) {
+    bs.count = 3;
+    CUDA_TRY(launch_gemm_proj(tA, bs, nt.nodes, ldq, d, b.gp.ks_qkv, b.qkv_part, slab, ldq, ds->num_sms, ds->err,
+                              st));
+  }
+  CUDA_TRY(launch_qk_head_norm(b.qkv_part, b.gp.ks_qkv, slab, b.qkv, nt.nodes, ldq, hq, hkv,
+                               static_cast<const bf16*>(m->q_norm), static_cast<const bf16*>(m->k_norm), m->rms_eps,
+                               st));
   return QUAIL_OK;
 }
 
@@ -307,17 +355,22 @@ quail_status run_attention(const quail_model_desc* m, const quail_paged_kv* kv, 
   return QUAIL_OK;
 }
 
-// h = x + O W_o^T; z = RMSNorm(h) g_f.
+// h = x + O W_o^T (O as a two-term bf16 split); z = RMSNorm(h) g_f.
 quail_status run_wo_norm(const quail_model_desc* m, const NodeTables& nt, RowMap map, int rows, const Buffers& b,
                          DeviceState* ds, cudaStream_t st) {
   const int d = m->hidden, hq = m->n_q_heads;
-  CUtensorMap tA, tB;
+  CUtensorMap tA;
   quail_status s = encode_2d_bf16(&tA, b.attn_out, round_up(rows, 128), 2 * hq * 128, 2 * hq * 128, 64, 128);
   if (s != QUAIL_OK) return s;
-  s = encode_2d_bf16(&tB, m->w_o, d, hq * 128, hq * 128, 64, 256);
+  BSet bs{};
+  s = encode_2d_bf16(&bs.map[0], m->w_o, d, hq * 128, hq * 128, 64, 256);
   if (s != QUAIL_OK) return s;
-  CUDA_TRY(launch_gemm_store_f32(tA, tB, rows, d, 2 * hq * 128, hq * 128, b.h_pre, d, ds->num_sms, ds->err, st));
-  CUDA_TRY(launch_final_norm(b.h_pre, static_cast<const bf16*>(m->embed), nt.token, map, rows, d,
+  bs.n_begin[0] = 0;
+  bs.n_begin[1] = d;
+  bs.count = 1;
+  const size_t slab = static_cast<size_t>(rows) * d;
+  CUDA_TRY(launch_gemm_proj(tA, bs, rows, d, hq * 128, b.gp.ks_wo, b.h_part, slab, d, ds->num_sms, ds->err, st));
+  CUDA_TRY(launch_final_norm(b.h_part, b.gp.ks_wo, slab, static_cast<const bf16*>(m->embed), nt.token, map, rows, d,
                              static_cast<const bf16*>(m->final_norm), m->rms_eps, b.z, b.z_f32, st));
   return QUAIL_OK;
 }

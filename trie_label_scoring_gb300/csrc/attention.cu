@@ -26,7 +26,8 @@ constexpr int kAttnThreads = 160;  // warps 0..3 consume, warp 4 loads pages
 constexpr int kAttnStages = 8;     // multiple of kConsumerWarps
 constexpr uint32_t kHalfBytes = kPage * 64 * 2;   // 16 keys x 64 bf16, 128B-swizzled
 constexpr uint32_t kPageBytes = 4 * kHalfBytes;   // K[0:64) K[64:128) V[0:64) V[64:128)
-constexpr size_t kAttnSmem = 1024 + kAttnStages * kPageBytes + 2 * kAttnStages * 8 + 16;
+constexpr int kMaxSplitPages = 128;  // split_tokens <= 2048
+constexpr size_t kAttnSmem = 1024 + kAttnStages * kPageBytes + 2 * kAttnStages * 8 + 16 + kMaxSplitPages * 4;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct RopeTable {
@@ -146,6 +147,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   uint64_t* full = reinterpret_cast<uint64_t*>(base + kAttnStages * kPageBytes);
   uint64_t* empty = full + kAttnStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kAttnStages);
+  int* s_pages = reinterpret_cast<int*>(empty + kAttnStages) + 4;  // physical page of each split page
 
   const int slot = blockIdx.z;
   if (a.map.n_slots_dev != nullptr && slot >= *a.map.n_slots_dev) return;
@@ -179,16 +181,20 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------ page loader
+    // All page ids of the split in one coalesced read, so no TMA issue waits
+    // on a dependent global load.
+    const int* pt = a.page_table + static_cast<size_t>(doc) * a.max_pages;
+    for (int j = lane; j < n_pages; j += 32) s_pages[j] = pt[p0 + j];
+    __syncwarp();
     if (lane == 0) {
       int armed[kAttnStages];
 #pragma unroll
       for (int s = 0; s < kAttnStages; ++s) armed[s] = -1;
-      const int* pt = a.page_table + static_cast<size_t>(doc) * a.max_pages;
       for (int j = 0; j < n_pages; ++j) {
         const int s = j % kAttnStages;
         const int use = j / kAttnStages;
         if (use > 0 && !mbar_wait(&empty[s], static_cast<uint32_t>((use - 1) & 1), abort_flag)) break;
-        const int phys = pt[p0 + j];
+        const int phys = s_pages[j];
         if (phys < 0 || phys >= a.num_pages) {
           raise_device_error(a.err, QUAIL_ERR_DEVICE_BOUNDS, doc);
           mbar_arrive(&full[s]);  // release the consumer on stale data; results of this doc are void

@@ -10,8 +10,9 @@ namespace quail {
 
 namespace {
 
-constexpr int kStoreBN = 256;
-constexpr int kStages = 4;
+constexpr int kProjBN = 256;
+constexpr int kProjStages = 3;  // 64 KB per stage (A_hi, A_lo, B)
+constexpr int kHeadStages = 4;  // 48 KB per stage
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Per 128 x 256 accumulator tile and row: online max / sum of exp over the
@@ -27,7 +28,8 @@ struct EpiHead {
   HeadEpilogueArgs a;
   int M;
   int V;
-  __device__ __forceinline__ void operator()(int m_blk, int n_blk, int lane_row, uint32_t taddr) const {
+  __device__ __forceinline__ void operator()(int m_blk, int n_blk, int /*ks*/, int lane_row,
+                                             uint32_t taddr) const {
     const int row = m_blk * kGemmBM + lane_row;
     const int lane = threadIdx.x & 31;
     const bool valid = row < M;
@@ -107,37 +109,61 @@ struct EpiHead {
   }
 };
 
-template <int BN, class Epi>
-cudaError_t launch_umma(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K, int KB, const Epi& epi,
+template <int BN, int STAGES, bool SPLIT_A, class Epi>
+cudaError_t launch_umma(const CUtensorMap& tmA, const BSet& bset, int M, int N, int nk, int k_splits, const Epi& epi,
                         int num_sms, int* err, cudaStream_t st) {
-  using Cfg = GemmCfg<BN, kStages>;
-  auto kern = umma_gemm_kernel<BN, kStages, Epi>;
-  static bool configured = false;  // per instantiation; the attribute is per device function
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(Cfg::kSmemBytes));
+  using Cfg = GemmCfg<BN, STAGES, SPLIT_A>;
+  auto kern = umma_gemm_kernel<BN, STAGES, SPLIT_A, Epi>;
+  static int configured_device = -1;  // the attribute is set per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(Cfg::kSmemBytes));
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured_device = dev;
   }
-  const int tiles = ((M + kGemmBM - 1) / kGemmBM) * ((N + BN - 1) / BN);
-  const int grid = tiles < num_sms ? tiles : num_sms;
+  const int units = ((M + kGemmBM - 1) / kGemmBM) * ((N + BN - 1) / BN) * k_splits;
+  const int grid = units < num_sms ? units : num_sms;
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, kGemmThreads, Cfg::kSmemBytes, st>>>(tmA, tmB, M, N, K, KB / kGemmBK, epi, err);
+  kern<<<grid, kGemmThreads, Cfg::kSmemBytes, st>>>(tmA, bset, M, N, nk, k_splits, epi, err);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_gemm_store_f32(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K, int KB,
-                                  float* C, int ldc, int num_sms, int* err, cudaStream_t st) {
-  EpiStoreF32<kStoreBN> epi{C, ldc, M, N};
-  return launch_umma<kStoreBN>(tmA, tmB, M, N, K, KB, epi, num_sms, err, st);
+int choose_k_splits(int tiles, int nk, int num_sms) {
+  // Largest SM efficiency units / (waves * SMs), preferring fewer splits; at
+  // least 4 k-blocks per unit.
+  int best = 1;
+  double best_eff = 0.0;
+  for (int ks = 1; ks <= 8 && nk / ks >= 4; ++ks) {
+    const long units = static_cast<long>(tiles) * ks;
+    const long waves = (units + num_sms - 1) / num_sms;
+    const double eff = static_cast<double>(units) / static_cast<double>(waves * num_sms);
+    if (eff > best_eff + 0.05) {
+      best_eff = eff;
+      best = ks;
+    }
+  }
+  return best;
+}
+
+cudaError_t launch_gemm_proj(const CUtensorMap& tmA, const BSet& bset, int M, int N, int K, int k_splits, float* C,
+                             size_t slab, int ldc, int num_sms, int* err, cudaStream_t st) {
+  EpiStoreF32<kProjBN> epi{C, slab, ldc, M, N};
+  return launch_umma<kProjBN, kProjStages, true>(tmA, bset, M, N, K / kGemmBK, k_splits, epi, num_sms, err, st);
 }
 
 cudaError_t launch_gemm_head(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int V, int K,
                              const HeadEpilogueArgs& args, int num_sms, int* err, cudaStream_t st) {
   EpiHead epi{args, M, V};
-  return launch_umma<kHeadBN>(tmA, tmB, M, V, K, K, epi, num_sms, err, st);
+  BSet b{};
+  b.map[0] = tmB;
+  b.n_begin[0] = 0;
+  b.n_begin[1] = V;
+  b.count = 1;
+  return launch_umma<kHeadBN, kHeadStages, false>(tmA, b, M, V, K / kGemmBK, 1, epi, num_sms, err, st);
 }
 
 }  // namespace quail

@@ -14,11 +14,15 @@ using bf16 = __nv_bfloat16;
 
 // ------------------------------------------------------------ GEMM (gemm.cu)
 // Tensor maps are built by the caller (encode_2d_bf16 in api.cu).
-// C[M, N] (fp32, row stride ldc) = A[M, K] * B[N, KB]^T with the B column
-// index taken modulo KB (K a multiple of KB): K = 2 KB multiplies a two-term
-// bf16 split A = [X_hi | X_lo] by B.
-cudaError_t launch_gemm_store_f32(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K, int KB,
-                                  float* C, int ldc, int num_sms, int* err, cudaStream_t st);
+// Projection GEMM with a two-term bf16 split A = [X_hi | X_lo] ([M, 2K]) and up
+// to three B tensors side by side along N (BSet, each [N_i, K], segment starts
+// multiples of 256): partial tiles of k-split s go to C + s * slab
+// ([M, ldc] fp32 each); the consumer sums the k_splits slabs.
+struct BSet;
+cudaError_t launch_gemm_proj(const CUtensorMap& tmA, const BSet& bset, int M, int N, int K, int k_splits, float* C,
+                             size_t slab, int ldc, int num_sms, int* err, cudaStream_t st);
+// k-splits that balance `tiles` work tiles of nk k-blocks over num_sms SMs.
+int choose_k_splits(int tiles, int nk, int num_sms);
 
 // Output head: for every row r < M and vocabulary tile j (256 tokens):
 //   lse_part[r * n_tiles + j] = (max2, sum exp2(logit*log2e - max2)) over the tile,
@@ -46,9 +50,11 @@ cudaError_t launch_gemm_head(const CUtensorMap& tmA, const CUtensorMap& tmB, int
 // out[r, 0:d] = bf16(y), out[r, d:2d] = bf16(y - bf16(y)); rows = n
 cudaError_t launch_embed_rmsnorm(const bf16* embed, const int* tokens, int n, int d, const bf16* gain, float eps,
                                  bf16* out, cudaStream_t st);
-// Per-head RMSNorm in place on qkv [rows, ld]: q heads [0, hq) with gq, k heads [hq, hq + hkv) with gk.
-cudaError_t launch_qk_head_norm(float* qkv, int rows, int ld, int hq, int hkv, const bf16* gq, const bf16* gk,
-                                float eps, cudaStream_t st);
+// qkv[r] = sum over the k_splits slabs of part (slab stride `slab`), then
+// per-head RMSNorm of the q heads [0, hq) with gq and k heads [hq, hq + hkv)
+// with gk; v heads copied. qkv and each slab are [rows, ld].
+cudaError_t launch_qk_head_norm(const float* part, int k_splits, size_t slab, float* qkv, int rows, int ld, int hq,
+                                int hkv, const bf16* gq, const bf16* gk, float eps, cudaStream_t st);
 
 // Maps an attention/output row to its trie node: slot = row / nq, e = row % nq,
 // node = slot_node ? slot_node[slot] : e.
@@ -59,9 +65,11 @@ struct RowMap {
   const int* n_slots_dev; // nullable: rows of slots >= *n_slots_dev are skipped
 };
 
-// z = RMSNorm(h_pre[r] + E[node_token[node(r)]]) * g_f; writes bf16 (and fp32 if z_f32).
-cudaError_t launch_final_norm(const float* h_pre, const bf16* embed, const int* node_token, RowMap map, int rows,
-                              int d, const bf16* gain, float eps, bf16* z_bf16, float* z_f32, cudaStream_t st);
+// z = RMSNorm(sum_s h_part[s][r] + E[node_token[node(r)]]) * g_f over the
+// k_splits slabs of h_part; writes bf16 (and fp32 if z_f32).
+cudaError_t launch_final_norm(const float* h_part, int k_splits, size_t slab, const bf16* embed,
+                              const int* node_token, RowMap map, int rows, int d, const bf16* gain, float eps,
+                              bf16* z_bf16, float* z_f32, cudaStream_t st);
 // lse[r] = log-sum-exp over the n_tiles partials of row r.
 cudaError_t launch_lse_reduce(const float2* lse_part, int rows, int n_tiles, float* lse, cudaStream_t st);
 

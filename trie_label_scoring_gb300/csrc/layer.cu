@@ -57,44 +57,58 @@ __global__ void embed_rmsnorm_kernel(const bf16* __restrict__ embed, const int* 
   }
 }
 
-// One warp per (row, head) of 128 values.
-__global__ void qk_head_norm_kernel(float* qkv, int rows, int ld, int hq, int hkv, const bf16* __restrict__ gq,
+// One warp per (row, head) of 128 values: sum the k-split slabs, then the
+// per-head RMSNorm for q and k heads (v heads are only summed).
+__global__ void qk_head_norm_kernel(const float* __restrict__ part, int k_splits, size_t slab, float* qkv, int rows,
+                                    int ld, int hq, int hkv, const bf16* __restrict__ gq,
                                     const bf16* __restrict__ gk, float eps) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  const int heads = hq + hkv;
+  const int heads = hq + 2 * hkv;
   if (warp >= rows * heads) return;
   const int r = warp / heads, h = warp % heads;
-  float4* p = reinterpret_cast<float4*>(qkv + static_cast<size_t>(r) * ld + h * 128) + lane;
-  float4 v = *p;
-  const float inv = rsqrtf(warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w) / 128.f + eps);
-  const bf16* g = (h < hq ? gq : gk) + lane * 4;
-  v.x *= inv * __bfloat162float(g[0]);
-  v.y *= inv * __bfloat162float(g[1]);
-  v.z *= inv * __bfloat162float(g[2]);
-  v.w *= inv * __bfloat162float(g[3]);
-  *p = v;
+  const size_t off = static_cast<size_t>(r) * ld + h * 128 + lane * 4;
+  float4 v = *reinterpret_cast<const float4*>(part + off);
+  for (int s = 1; s < k_splits; ++s) {
+    const float4 w = *reinterpret_cast<const float4*>(part + s * slab + off);
+    v.x += w.x;
+    v.y += w.y;
+    v.z += w.z;
+    v.w += w.w;
+  }
+  if (h < hq + hkv) {
+    const float inv = rsqrtf(warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w) / 128.f + eps);
+    const bf16* g = (h < hq ? gq : gk) + lane * 4;
+    v.x *= inv * __bfloat162float(g[0]);
+    v.y *= inv * __bfloat162float(g[1]);
+    v.z *= inv * __bfloat162float(g[2]);
+    v.w *= inv * __bfloat162float(g[3]);
+  }
+  *reinterpret_cast<float4*>(qkv + off) = v;
 }
 
-__global__ void final_norm_kernel(const float* __restrict__ h_pre, const bf16* __restrict__ embed,
-                                  const int* __restrict__ node_token, RowMap map, int d,
-                                  const bf16* __restrict__ gain, float eps, bf16* __restrict__ z_bf16,
+__global__ void final_norm_kernel(const float* __restrict__ h_part, int k_splits, size_t slab,
+                                  const bf16* __restrict__ embed, const int* __restrict__ node_token, RowMap map,
+                                  int d, const bf16* __restrict__ gain, float eps, bf16* __restrict__ z_bf16,
                                   float* __restrict__ z_f32) {
+  extern __shared__ float s_h[];  // [d]
   __shared__ float scratch[32];
   const int r = blockIdx.x;
   const int slot = r / map.nq;
   if (map.n_slots_dev != nullptr && slot >= *map.n_slots_dev) return;
   const int node = map.slot_node ? map.slot_node[slot] : (r - slot * map.nq);
   const bf16* x = embed + static_cast<size_t>(__ldg(node_token + node)) * d;
-  const float* hp = h_pre + static_cast<size_t>(r) * d;
+  const float* hp = h_part + static_cast<size_t>(r) * d;
   float ss = 0.f;
   for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    const float v = hp[i] + __bfloat162float(x[i]);
+    float v = __bfloat162float(x[i]);
+    for (int s = 0; s < k_splits; ++s) v += hp[s * slab + i];
+    s_h[i] = v;
     ss += v * v;
   }
   const float inv = rsqrtf(block_sum(ss, scratch) / d + eps);
   for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    const float v = (hp[i] + __bfloat162float(x[i])) * inv * __bfloat162float(gain[i]);
+    const float v = s_h[i] * inv * __bfloat162float(gain[i]);
     z_bf16[static_cast<size_t>(r) * d + i] = __float2bfloat16(v);
     if (z_f32) z_f32[static_cast<size_t>(r) * d + i] = v;
   }
@@ -338,19 +352,21 @@ cudaError_t launch_embed_rmsnorm(const bf16* embed, const int* tokens, int n, in
   return cudaGetLastError();
 }
 
-cudaError_t launch_qk_head_norm(float* qkv, int rows, int ld, int hq, int hkv, const bf16* gq, const bf16* gk,
-                                float eps, cudaStream_t st) {
-  const long warps = static_cast<long>(rows) * (hq + hkv);
+cudaError_t launch_qk_head_norm(const float* part, int k_splits, size_t slab, float* qkv, int rows, int ld, int hq,
+                                int hkv, const bf16* gq, const bf16* gk, float eps, cudaStream_t st) {
+  const long warps = static_cast<long>(rows) * (hq + 2 * hkv);
   if (warps <= 0) return cudaSuccess;
   const int blocks = static_cast<int>((warps * 32 + 255) / 256);
-  qk_head_norm_kernel<<<blocks, 256, 0, st>>>(qkv, rows, ld, hq, hkv, gq, gk, eps);
+  qk_head_norm_kernel<<<blocks, 256, 0, st>>>(part, k_splits, slab, qkv, rows, ld, hq, hkv, gq, gk, eps);
   return cudaGetLastError();
 }
 
-cudaError_t launch_final_norm(const float* h_pre, const bf16* embed, const int* node_token, RowMap map, int rows,
-                              int d, const bf16* gain, float eps, bf16* z_bf16, float* z_f32, cudaStream_t st) {
+cudaError_t launch_final_norm(const float* h_part, int k_splits, size_t slab, const bf16* embed,
+                              const int* node_token, RowMap map, int rows, int d, const bf16* gain, float eps,
+                              bf16* z_bf16, float* z_f32, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
-  final_norm_kernel<<<rows, 256, 0, st>>>(h_pre, embed, node_token, map, d, gain, eps, z_bf16, z_f32);
+  final_norm_kernel<<<rows, 256, d * sizeof(float), st>>>(h_part, k_splits, slab, embed, node_token, map, d, gain,
+                                                         eps, z_bf16, z_f32);
   return cudaGetLastError();
 }
 

@@ -1,19 +1,27 @@
 // Persistent, warp-specialised tcgen05 GEMM for sm_103a:  C = A * B^T
 //   A: [M, K] bf16, K contiguous (row-major)      -> TMA box 64 x 128, 128B swizzle
 //   B: [N, K] bf16, K contiguous (nn.Linear rows) -> TMA box 64 x BN,  128B swizzle
-// The B coordinate along K wraps every kb_wrap k-blocks: with A = [X_hi | X_lo]
-// (a two-term bf16 split of an fp32 operand, K doubled) and kb_wrap = K_B/64,
-// the same B rows multiply both halves, so C = (X_hi + X_lo) B^T to ~16 bits.
 // The fp32 accumulator for one 128 x BN tile lives in TMEM (two buffers, so the
 // epilogue of tile t overlaps the MMAs of tile t+1). The epilogue is a functor,
 // which is how the LM head fuses its log-sum-exp and child-token gather without
 // ever writing logits to global memory.
 //
+// Options:
+//  * SPLIT_A: A = [X_hi | X_lo] (a two-term bf16 split of an fp32 operand,
+//    2K columns). Each pipeline stage holds the k-block of X_hi, of X_lo and of
+//    B; both A halves multiply the same B tile into one accumulator, so
+//    C = (X_hi + X_lo) B^T to ~16 bits while B is read once.
+//  * Up to three B tensors side by side along N (BSet), each starting at a
+//    multiple of BN: q, k and v projections in one launch.
+//  * Split-K over CTAs: work unit = (tile, k-split); the epilogue receives the
+//    split index and writes its partial tile to its own slab (no atomics); the
+//    next kernel sums the slabs.
+//
 // Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM owner + MMA
 // issuer, warps 2..5 = epilogue (warp w reads TMEM lanes 32*(w%4) .. +31).
-// Tiles are walked N-band-major: consecutive tile ids share one B band, so the
-// CTAs resident at any moment read each band of B from HBM about once and
-// re-read it from L2 for the other M tiles.
+// Units are walked N-band-major: consecutive ids share one B band, so the CTAs
+// resident at any moment read each band of B from HBM about once and re-read it
+// from L2 for the other M tiles.
 #pragma once
 #include "sm103.cuh"
 #include "quail_internal.h"
@@ -24,37 +32,54 @@ constexpr int kGemmBM = 128;
 constexpr int kGemmBK = 64;  // 64 bf16 = one 128-byte swizzle row
 constexpr int kGemmThreads = 192;
 
-template <int BN, int STAGES>
+// Up to three B operands covering output columns [n_begin[i], n_begin[i+1]).
+struct BSet {
+  CUtensorMap map[3];
+  int n_begin[4];
+  int count;
+};
+
+template <int BN, int STAGES, bool SPLIT_A>
 struct GemmCfg {
   static constexpr uint32_t kABytes = kGemmBM * kGemmBK * 2;
   static constexpr uint32_t kBBytes = BN * kGemmBK * 2;
-  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr uint32_t kStageBytes = (SPLIT_A ? 2 : 1) * kABytes + kBBytes;
   static constexpr uint32_t kTmemCols = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
                                         : (2 * BN <= 256) ? 256 : 512;
   // 1024 alignment slack + stages + barriers + tmem slot + abort flag
   static constexpr size_t kSmemBytes = 1024 + STAGES * kStageBytes + (2 * STAGES + 5) * 8 + 16;
 };
 
-__device__ __forceinline__ void gemm_tile_coords(int tile, int m_tiles, int& m_blk, int& n_blk) {
-  n_blk = tile / m_tiles;
-  m_blk = tile - n_blk * m_tiles;
+struct GemmUnit {
+  int m_blk, n_blk, ks, kb0, kb1;
+};
+
+// unit -> (tile, k-split); tile -> (n band, m tile), N-band-major.
+__device__ __forceinline__ GemmUnit gemm_unit(int u, int m_tiles, int k_splits, int nk) {
+  GemmUnit g;
+  g.ks = u % k_splits;
+  const int tile = u / k_splits;
+  g.n_blk = tile / m_tiles;
+  g.m_blk = tile - g.n_blk * m_tiles;
+  g.kb0 = g.ks * nk / k_splits;
+  g.kb1 = (g.ks + 1) * nk / k_splits;
+  return g;
 }
 
 // Epi must provide:
-//   __device__ void operator()(int m_blk, int n_blk, int lane_row, uint32_t taddr) const;
-// called by each of the 128 epilogue threads for every tile; lane_row in [0,128)
+//   __device__ void operator()(int m_blk, int n_blk, int ks, int lane_row, uint32_t taddr) const;
+// called by each of the 128 epilogue threads for every unit; lane_row in [0,128)
 // is this thread's accumulator row, taddr the TMEM address of (row, column 0).
 // All 32 lanes of a warp must execute the same tcgen05.ld sequence.
-template <int BN, int STAGES, class Epi>
+// nk = k-blocks of B's K extent (A has nk k-blocks, or 2*nk with SPLIT_A).
+template <int BN, int STAGES, bool SPLIT_A, class Epi>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N,
-                     int K, int kb_wrap, Epi epi, int* err) {
-  using Cfg = GemmCfg<BN, STAGES>;
+    umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ BSet bset, int M, int N,
+                     int nk, int k_splits, Epi epi, int* err) {
+  using Cfg = GemmCfg<BN, STAGES, SPLIT_A>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = base;
-  uint8_t* sB = base + STAGES * Cfg::kABytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * Cfg::kBBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + STAGES * Cfg::kStageBytes);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;  // [2]
   uint64_t* tempty = tfull + 2;      // [2]
@@ -66,8 +91,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int lane = threadIdx.x & 31;
   const int m_tiles = (M + kGemmBM - 1) / kGemmBM;
   const int n_tiles = (N + BN - 1) / BN;
-  const int num_tiles = m_tiles * n_tiles;
-  const int nk = K / kGemmBK;
+  const int num_units = m_tiles * n_tiles * k_splits;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -82,7 +106,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
+    for (int i = 0; i < bset.count; ++i) tma_prefetch_desc(&bset.map[i]);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, Cfg::kTmemCols);
@@ -102,17 +126,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        int m_blk, n_blk;
-        gemm_tile_coords(tile, m_tiles, m_blk, n_blk);
-        for (int kb = 0; kb < nk; ++kb) {
+      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+        const GemmUnit g = gemm_unit(u, m_tiles, k_splits, nk);
+        const int n0 = g.n_blk * BN;
+        int bi = 0;
+        while (bi + 1 < bset.count && n0 >= bset.n_begin[bi + 1]) ++bi;
+        const CUtensorMap* tmB = &bset.map[bi];
+        const int nb = n0 - bset.n_begin[bi];
+        for (int kb = g.kb0; kb < g.kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
+          uint8_t* st = base + stage * Cfg::kStageBytes;
           mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
-          tma_load_2d(sA + stage * Cfg::kABytes, &tmA, &full[stage], kb * kGemmBK, m_blk * kGemmBM);
-          tma_load_2d(sB + stage * Cfg::kBBytes, &tmB, &full[stage], (kb % kb_wrap) * kGemmBK, n_blk * BN);
+          tma_load_2d(st, &tmA, &full[stage], kb * kGemmBK, g.m_blk * kGemmBM);
+          if (SPLIT_A) tma_load_2d(st + Cfg::kABytes, &tmA, &full[stage], (nk + kb) * kGemmBK, g.m_blk * kGemmBM);
+          tma_load_2d(st + (SPLIT_A ? 2 : 1) * Cfg::kABytes, tmB, &full[stage], kb * kGemmBK, nb);
           armed_parity[stage] = static_cast<int>(phase);
           if (++stage == STAGES) {
             stage = 0;
@@ -142,22 +172,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+        const GemmUnit g = gemm_unit(u, m_tiles, k_splits, nk);
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < nk; ++kb) {
+        for (int kb = g.kb0; kb < g.kb1; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(sA + stage * Cfg::kABytes);
-          const uint32_t b_addr = smem_u32(sB + stage * Cfg::kBBytes);
+          const uint32_t st = smem_u32(base + stage * Cfg::kStageBytes);
+          const uint32_t b_addr = st + (SPLIT_A ? 2 : 1) * Cfg::kABytes;
 #pragma unroll
-          for (int k = 0; k < kGemmBK / 16; ++k) {
-            umma_bf16(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), idesc,
-                      (kb | k) != 0 ? 1u : 0u);
+          for (int half = 0; half < (SPLIT_A ? 2 : 1); ++half) {
+            const uint32_t a_addr = st + half * Cfg::kABytes;
+#pragma unroll
+            for (int k = 0; k < kGemmBK / 16; ++k) {
+              umma_bf16(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), idesc,
+                        (kb > g.kb0 || half > 0 || k > 0) ? 1u : 0u);
+            }
           }
           umma_commit(&empty[stage]);
           if (++stage == STAGES) {
@@ -187,13 +222,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int lane_row = quarter * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
       if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) break;
       tc_fence_after();
-      int m_blk, n_blk;
-      gemm_tile_coords(tile, m_tiles, m_blk, n_blk);
+      const GemmUnit g = gemm_unit(u, m_tiles, k_splits, nk);
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      epi(m_blk, n_blk, lane_row, taddr);
+      epi(g.m_blk, g.n_blk, g.ks, lane_row, taddr);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
       acc ^= 1;
@@ -212,17 +246,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 // ------------------------------------------------------------ epilogues
 
-// Plain fp32 store: C[row, col] = acc (row < M, col < N), row stride ldc.
+// fp32 store of the partial tile of k-split ks:
+//   C[ks * slab + row * ldc + col] = acc   (row < M, col < N)
 template <int BN>
 struct EpiStoreF32 {
   float* C;
+  size_t slab;
   int ldc;
   int M;
   int N;
-  __device__ __forceinline__ void operator()(int m_blk, int n_blk, int lane_row, uint32_t taddr) const {
+  __device__ __forceinline__ void operator()(int m_blk, int n_blk, int ks, int lane_row, uint32_t taddr) const {
     const int row = m_blk * kGemmBM + lane_row;
     const int n0 = n_blk * BN;
-    float* out = C + static_cast<size_t>(row) * ldc;
+    float* out = C + ks * slab + static_cast<size_t>(row) * ldc;
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       float v[32];
