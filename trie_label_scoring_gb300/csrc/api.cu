@@ -172,16 +172,19 @@ struct AttnShape {
   int rows_per_kv, row_tile, rows_pad, split_tokens, n_splits;
 };
 
-AttnShape attn_shape(const quail_model_desc* m, int nq, int max_doc_len) {
+AttnShape attn_shape(const quail_model_desc* m, int nq, int slots, int max_doc_len, int sms) {
   AttnShape s;
   const int G = m->n_q_heads / m->n_kv_heads;
   s.rows_per_kv = nq * G;
   s.row_tile = s.rows_per_kv <= 16 ? 16 : 64;
   s.rows_pad = static_cast<int>(round_up(s.rows_per_kv, s.row_tile));
-  // Few query rows per KV head: split the document into 512-token chunks so the
-  // KV stream is spread over many CTAs. Many rows: the rows give the
-  // parallelism, and splits only bound the page list a CTA holds (2,048 tokens).
-  s.split_tokens = s.rows_per_kv <= 64 ? 512 : static_cast<int>(std::min<size_t>(round_up(max_doc_len, 16), 2048));
+  // One split per document when (document, KV head, row group) work items
+  // already fill the GPU several times over: the epilogue then merges the tree
+  // part directly. Otherwise 512-token splits spread long documents over more
+  // CTAs and a combine kernel merges them. A split holds at most 256 pages.
+  const long items = static_cast<long>(slots) * m->n_kv_heads * (s.rows_pad / s.row_tile);
+  const int whole = static_cast<int>(round_up(max_doc_len, 16));
+  s.split_tokens = (items >= 6L * sms) ? std::min(whole, 4096) : std::min(whole, 512);
   s.n_splits = (max_doc_len + s.split_tokens - 1) / s.split_tokens;
   return s;
 }
@@ -235,7 +238,7 @@ size_t plan(uint8_t* base, const quail_model_desc* m, int nodes, int slots, int 
             int n_child, bool need_zf32, int small_ints, Buffers* b) {
   const int d = m->hidden, hq = m->n_q_heads, hkv = m->n_kv_heads;
   const int ldq = (hq + 2 * hkv) * 128;
-  const AttnShape as = attn_shape(m, nq, max_doc_len);
+  const AttnShape as = attn_shape(m, nq, slots, max_doc_len, planning_sms());
   const size_t rows = static_cast<size_t>(slots) * nq;
   const size_t rows_p = round_up(rows, 128);
   const int n_tiles = (m->vocab + kHeadBN - 1) / kHeadBN;
@@ -247,7 +250,7 @@ size_t plan(uint8_t* base, const quail_model_desc* m, int nodes, int slots, int 
   t.qkv = c.take<float>(static_cast<size_t>(nodes) * ldq);
   t.tree_o = c.take<float>(static_cast<size_t>(nodes) * hq * 128);
   t.tree_ml = c.take<float2>(static_cast<size_t>(nodes) * hq);
-  const size_t prow = static_cast<size_t>(slots) * hkv * as.n_splits * as.rows_pad;
+  const size_t prow = as.n_splits > 1 ? static_cast<size_t>(slots) * hkv * as.n_splits * as.rows_pad : 0;
   t.part_o = c.take<float>(prow * 128);
   t.part_ml = c.take<float2>(prow);
   t.attn_out = c.take<bf16>(rows_p * 2 * hq * 128);
@@ -316,7 +319,7 @@ quail_status run_prologue(const quail_model_desc* m, const NodeTables& nt, const
 quail_status run_attention(const quail_model_desc* m, const quail_paged_kv* kv, const NodeTables& nt, RowMap map,
                            int slots, const Buffers& b, DeviceState* ds, cudaStream_t st) {
   const int hq = m->n_q_heads, hkv = m->n_kv_heads;
-  const AttnShape as = attn_shape(m, map.nq, kv->max_doc_len);
+  const AttnShape as = attn_shape(m, map.nq, slots, kv->max_doc_len, ds->num_sms);
   AttnArgs a{};
   a.num_pages = kv->num_pages;
   a.max_pages = kv->max_pages;
@@ -351,7 +354,7 @@ quail_status run_attention(const quail_model_desc* m, const quail_paged_kv* kv, 
   if (s != QUAIL_OK) return s;
   CUDA_TRY(launch_tree_part(a, st));
   CUDA_TRY(launch_attn_doc(a, tK, tV, st));
-  CUDA_TRY(launch_attn_combine(a, st));
+  if (as.n_splits > 1) CUDA_TRY(launch_attn_combine(a, st));
   return QUAIL_OK;
 }
 

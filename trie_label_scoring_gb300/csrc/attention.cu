@@ -26,8 +26,7 @@ constexpr int kAttnThreads = 160;  // warps 0..3 consume, warp 4 loads pages
 constexpr int kAttnStages = 8;     // multiple of kConsumerWarps
 constexpr uint32_t kHalfBytes = kPage * 64 * 2;   // 16 keys x 64 bf16, 128B-swizzled
 constexpr uint32_t kPageBytes = 4 * kHalfBytes;   // K[0:64) K[64:128) V[0:64) V[64:128)
-constexpr int kMaxSplitPages = 128;  // split_tokens <= 2048
-constexpr size_t kAttnSmem = 1024 + kAttnStages * kPageBytes + 2 * kAttnStages * 8 + 16 + kMaxSplitPages * 4;
+
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct RopeTable {
@@ -139,12 +138,42 @@ __global__ void tree_part_kernel(AttnArgs a, RopeTable rt) {
 // 0..3 run bf16 mma.sync on 16-row query tiles with an online softmax.
 // row_tile 16: all four warps share the 16 rows and take pages round-robin,
 // then merge; row_tile 64: each warp owns 16 rows and reads every page.
-__global__ void __launch_bounds__(kAttnThreads, 2)
+// The q fragments (RoPE at l_i + depth, two-term bf16 split) are built once
+// per CTA in shared memory in mma fragment order. With one split per
+// document the epilogue merges the tree part and writes O itself; otherwise
+// it writes (O, max, sum) partials for attn_combine_kernel.
+constexpr uint32_t kQTileBytes = 8 * 2 * 32 * 16;  // ks x {hi, lo} x lane x uint4
+constexpr int kMaxSplitPagesV2 = 256;              // split_tokens <= 4096
+
+__host__ __device__ constexpr size_t attn_smem_bytes(int q_tiles) {
+  return 1024 + kAttnStages * kPageBytes + q_tiles * kQTileBytes + 2 * kAttnStages * 8 + 16 + kMaxSplitPagesV2 * 4;
+}
+
+__device__ __forceinline__ void mma_pair(float (&d0)[4], float (&d1)[4], const uint4& a, uint32_t b0, uint32_t b1,
+                                         uint32_t b2, uint32_t b3) {
+  const uint32_t av[4] = {a.x, a.y, a.z, a.w};
+  mma_bf16(d0, av, b0, b1);
+  mma_bf16(d1, av, b2, b3);
+}
+
+// Writes o (fp32) as the two-term bf16 split [hi | lo] of output row `orow`.
+__device__ __forceinline__ void store_o_split(bf16* out, int hq, size_t orow, int col, float x0, float x1) {
+  uint32_t hi, lo;
+  split_bf16(x0, x1, hi, lo);
+  bf16* dst = out + orow * 2 * hq * 128 + col;
+  *reinterpret_cast<uint32_t*>(dst) = hi;
+  *reinterpret_cast<uint32_t*>(dst + hq * 128) = lo;
+}
+
+__global__ void __launch_bounds__(kAttnThreads, 3)
     attn_doc_kernel(AttnArgs a, RopeTable rt, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV) {
   extern __shared__ uint8_t smem_raw[];
+  const bool shared_rows = a.row_tile == 16;
+  const int q_tiles = shared_rows ? 1 : kConsumerWarps;
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(base + kAttnStages * kPageBytes);
+  uint8_t* s_q = base + kAttnStages * kPageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(s_q + q_tiles * kQTileBytes);
   uint64_t* empty = full + kAttnStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kAttnStages);
   int* s_pages = reinterpret_cast<int*>(empty + kAttnStages) + 4;  // physical page of each split page
@@ -166,8 +195,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   const int k_hi = min(L, k_lo + a.split_tokens);
   const int p0 = k_lo / kPage;
   const int n_pages = (k_hi - k_lo + kPage - 1) / kPage;
-  const bool shared_rows = a.row_tile == 16;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = a.hq / a.hkv;
+  const int nq_rows = (a.map.slot_node ? 1 : a.map.nq);
+  const int rows_per_kv = nq_rows * G;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kAttnStages; ++s) {
@@ -226,55 +257,49 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   }
 
   // -------------------------------------------------- consumers
-  const int G = a.hq / a.hkv;
-  const int rows_per_kv = (a.map.slot_node ? 1 : a.map.nq) * G;
+  const int t = threadIdx.x;  // 0..127
   const int gq = lane >> 2, tq = lane & 3;
-  const int rtile = shared_rows ? 0 : warp;
-  const int row_base = rg * a.row_tile + rtile * 16;
 
-  // Q fragments with RoPE at position L + depth(node), as a two-term bf16
-  // split (qa + ql = q to ~16 bits; both multiply the exact bf16 keys).
-  uint32_t qa[8][4], ql[8][4];
+  // q fragments: item = (tile, row, pair j) -> rotated dims j and j + 64, split
+  // into hi/lo bf16 and scattered to their (ks, lane, register, half) slots.
   {
-    const float* qrow[2] = {nullptr, nullptr};
-    int pos[2] = {0, 0};
-#pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-      const int r = row_base + gq + hr * 8;
-      if (r < rows_per_kv) {
-        const int e = r / G, hl = r % G;
+    uint16_t* sq16 = reinterpret_cast<uint16_t*>(s_q);
+    const int items = q_tiles * 16 * 64;
+    for (int it = t; it < items; it += kConsumerWarps * 32) {
+      const int qt = it / (16 * 64);
+      const int r = (it / 64) % 16;
+      const int j = it % 64;
+      const int rr = rg * a.row_tile + qt * 16 + r;  // row within (slot, kv head)
+      float y0 = 0.f, y1 = 0.f;
+      if (rr < rows_per_kv) {
+        const int e = rr / G, hl = rr % G;
         const int node = row_node(a.map, slot, e);
-        qrow[hr] = a.qkv + static_cast<size_t>(node) * a.ldq + (g * G + hl) * 128;
-        pos[hr] = L + a.node_depth[node];
+        const float* q = a.qkv + static_cast<size_t>(node) * a.ldq + (g * G + hl) * 128;
+        float c, sn;
+        rope_cs(L + a.node_depth[node], rt.w[j], c, sn);
+        const float x1 = q[j], x2 = q[j + 64];
+        y0 = x1 * c - x2 * sn;
+        y1 = x2 * c + x1 * sn;
       }
-    }
+      const int col = j % 16;
+      const int reg = (r >= 8 ? 1 : 0) + (col >= 8 ? 2 : 0);
+      const int ln = (r % 8) * 4 + (col % 8) / 2;
+      const int half = col & 1;
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-#pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        float lo_v[4], hi_v[4];  // rotated dims j (<64) and j + 64
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int j = ks * 16 + tq * 2 + (u & 1) + (u >> 1) * 8;
-          if (qrow[hr] != nullptr) {
-            float c, s;
-            rope_cs(pos[hr], rt.w[j], c, s);
-            const float x1 = qrow[hr][j], x2 = qrow[hr][j + 64];
-            lo_v[u] = x1 * c - x2 * s;
-            hi_v[u] = x2 * c + x1 * s;
-          } else {
-            lo_v[u] = 0.f;
-            hi_v[u] = 0.f;
-          }
-        }
-        // a0/a2 hold row gq, a1/a3 row gq + 8; a0/a1 dims 2t..2t+1, a2/a3 dims 2t+8..2t+9
-        split_bf16(lo_v[0], lo_v[1], qa[ks][hr], ql[ks][hr]);
-        split_bf16(lo_v[2], lo_v[3], qa[ks][hr + 2], ql[ks][hr + 2]);
-        split_bf16(hi_v[0], hi_v[1], qa[ks + 4][hr], ql[ks + 4][hr]);
-        split_bf16(hi_v[2], hi_v[3], qa[ks + 4][hr + 2], ql[ks + 4][hr + 2]);
+      for (int w = 0; w < 2; ++w) {  // dims j (ks = j / 16) and j + 64 (ks + 4)
+        const float y = w ? y1 : y0;
+        const int ks = j / 16 + 4 * w;
+        const __nv_bfloat16 hb = __float2bfloat16(y);
+        const __nv_bfloat16 lb = __float2bfloat16(y - __bfloat162float(hb));
+        const int idx = (((qt * 8 + ks) * 2 + 0) * 32 + ln) * 8 + reg * 2 + half;  // in bf16 units
+        sq16[idx] = *reinterpret_cast<const uint16_t*>(&hb);
+        sq16[idx + 32 * 8] = *reinterpret_cast<const uint16_t*>(&lb);
       }
     }
   }
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+  const int qtile = shared_rows ? 0 : warp;
+  const uint4* qf = reinterpret_cast<const uint4*>(s_q + qtile * kQTileBytes) + lane;  // [ks][hi/lo][lane]
 
   const float scale = kLog2e * 0.08838834764831845f;
   float o[16][4];
@@ -292,8 +317,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     const int key0 = (p0 + j) * kPage;
     const int valid = min(kPage, L - key0);  // >= 1
 
-    // S = Q K^T for 16 keys (two n-tiles of 8)
-    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // S = (q_hi + q_lo) K^T for 16 keys; four independent accumulator chains
+    float sh[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    float sl[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
       const int mi = lane >> 3, ri = lane & 7;
@@ -301,19 +327,20 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       const uint32_t chunk = (ks & 3) * 2 + (mi & 1);
       uint32_t b0, b1, b2, b3;
       ldsm_x4(kb + (ks >> 2) * kHalfBytes + swz(key, chunk), b0, b1, b2, b3);
-      mma_bf16(sc[0], qa[ks], b0, b1);
-      mma_bf16(sc[1], qa[ks], b2, b3);
-      mma_bf16(sc[0], ql[ks], b0, b1);
-      mma_bf16(sc[1], ql[ks], b2, b3);
+      const uint4 qh = qf[(ks * 2 + 0) * 32];
+      const uint4 ql = qf[(ks * 2 + 1) * 32];
+      mma_pair(sh[0], sh[1], qh, b0, b1, b2, b3);
+      mma_pair(sl[0], sl[1], ql, b0, b1, b2, b3);
     }
     // online softmax (base 2); rows gq (c0, c1) and gq + 8 (c2, c3)
+    float sc[2][4];
     float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int key = nt * 8 + tq * 2 + (c & 1);
-        sc[nt][c] = key < valid ? sc[nt][c] * scale : -INFINITY;
+        sc[nt][c] = key < valid ? (sh[nt][c] + sl[nt][c]) * scale : -INFINITY;
         mx[c >> 1] = fmaxf(mx[c >> 1], sc[nt][c]);
       }
     }
@@ -379,17 +406,37 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     l_r[hr] += __shfl_xor_sync(0xffffffffu, l_r[hr], 2);
   }
 
+  const bool fused = a.n_splits == 1;
   const size_t part_row0 =
       ((static_cast<size_t>(slot) * a.hkv + g) * a.n_splits + split) * static_cast<size_t>(a.rows_pad);
   if (!shared_rows) {
+    const int row_base = rg * a.row_tile + warp * 16;
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
       const int r = row_base + gq + hr * 8;
-      float* dst = a.part_o + (part_row0 + r) * 128;
+      if (!fused) {
+        float* dst = a.part_o + (part_row0 + r) * 128;
 #pragma unroll
-      for (int n = 0; n < 16; ++n)
-        *reinterpret_cast<float2*>(dst + n * 8 + tq * 2) = make_float2(o[n][hr * 2], o[n][hr * 2 + 1]);
-      if (tq == 0) a.part_ml[part_row0 + r] = make_float2(m_r[hr], l_r[hr]);
+        for (int n = 0; n < 16; ++n)
+          *reinterpret_cast<float2*>(dst + n * 8 + tq * 2) = make_float2(o[n][hr * 2], o[n][hr * 2 + 1]);
+        if (tq == 0) a.part_ml[part_row0 + r] = make_float2(m_r[hr], l_r[hr]);
+      } else if (r < rows_per_kv) {
+        const int e = r / G, h = g * G + r % G;
+        const int node = row_node(a.map, slot, e);
+        const float2 tml = a.tree_ml[static_cast<size_t>(node) * a.hq + h];
+        const float M = fmaxf(m_r[hr], tml.x);
+        const float f1 = exp2f(m_r[hr] - M), f2 = exp2f(tml.x - M);
+        const float inv = 1.f / (f1 * l_r[hr] + f2 * tml.y);
+        const float* to = a.tree_o + (static_cast<size_t>(node) * a.hq + h) * 128;
+        const size_t orow = static_cast<size_t>(slot) * a.map.nq + e;
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+          const int col = n * 8 + tq * 2;
+          const float2 tv = *reinterpret_cast<const float2*>(to + col);
+          store_o_split(a.out, a.hq, orow, h * 128 + col, (f1 * o[n][hr * 2] + f2 * tv.x) * inv,
+                        (f1 * o[n][hr * 2 + 1] + f2 * tv.y) * inv);
+        }
+      }
     }
   } else {
     // Merge the four warps' partial softmax states through the (now idle) page ring.
@@ -407,8 +454,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       }
     }
     asm volatile("bar.sync 1, 128;" ::: "memory");
-    const int t = threadIdx.x;  // 0..127: row t / 8, dims (t % 8) * 16 .. +16
-    const int r = t >> 3, d0 = (t & 7) * 16;
+    const int r = t >> 3, d0 = (t & 7) * 16;  // row r, dims d0 .. d0 + 16
     const float* s0 = reinterpret_cast<const float*>(base);
     float M = -INFINITY;
 #pragma unroll
@@ -426,10 +472,26 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
 #pragma unroll
       for (int i = 0; i < 16; ++i) acc[i] += f * sw[r * 128 + d0 + i];
     }
-    float* dst = a.part_o + (part_row0 + r) * 128 + d0;
+    if (!fused) {
+      float* dst = a.part_o + (part_row0 + r) * 128 + d0;
 #pragma unroll
-    for (int i = 0; i < 16; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
-    if ((t & 7) == 0) a.part_ml[part_row0 + r] = make_float2(M, lsum);
+      for (int i = 0; i < 16; i += 4)
+        *reinterpret_cast<float4*>(dst + i) = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+      if ((t & 7) == 0) a.part_ml[part_row0 + r] = make_float2(M, lsum);
+    } else if (r < rows_per_kv) {
+      const int e = r / G, h = g * G + r % G;
+      const int node = row_node(a.map, slot, e);
+      const float2 tml = a.tree_ml[static_cast<size_t>(node) * a.hq + h];
+      const float M2 = fmaxf(M, tml.x);
+      const float f1 = exp2f(M - M2), f2 = exp2f(tml.x - M2);
+      const float inv = 1.f / (f1 * lsum + f2 * tml.y);
+      const float* to = a.tree_o + (static_cast<size_t>(node) * a.hq + h) * 128 + d0;
+      const size_t orow = static_cast<size_t>(slot) * a.map.nq + e;
+#pragma unroll
+      for (int i = 0; i < 16; i += 2)
+        store_o_split(a.out, a.hq, orow, h * 128 + d0 + i, (f1 * acc[i] + f2 * to[i]) * inv,
+                      (f1 * acc[i + 1] + f2 * to[i + 1]) * inv);
+    }
   }
   if (threadIdx.x == 0 && *abort_flag) raise_device_error(a.err, QUAIL_ERR_DEVICE_TIMEOUT, 2000 + slot);
 }
@@ -507,16 +569,22 @@ cudaError_t launch_tree_part(const AttnArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_attn_doc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV, cudaStream_t st) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_doc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kAttnSmem));
+  static int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(attn_doc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(attn_smem_bytes(kConsumerWarps)));
     if (e != cudaSuccess) return e;
-    configured = true;
+    e = cudaFuncSetAttribute(attn_doc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
   }
   dim3 grid(a.n_splits, a.hkv * (a.rows_pad / a.row_tile), a.n_slots);
   if (grid.x == 0 || grid.z == 0) return cudaSuccess;
-  attn_doc_kernel<<<grid, kAttnThreads, kAttnSmem, st>>>(a, make_rope_table(a.theta), tmK, tmV);
+  const size_t smem = attn_smem_bytes(a.row_tile == 16 ? 1 : kConsumerWarps);
+  attn_doc_kernel<<<grid, kAttnThreads, smem, st>>>(a, make_rope_table(a.theta), tmK, tmV);
   return cudaGetLastError();
 }
 
