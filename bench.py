@@ -33,11 +33,11 @@ DEFAULT_WORKLOAD = "qwen3-4b-support10-256docs"
 
 
 def count_launches() -> int:
-    """Kernels one quail_classify_trie_tree call launches: embed RMSNorm, the
-    q, k and v projection GEMMs, q/k head norm, tree part, paged doc
-    attention, combine, W_o GEMM, final norm, head GEMM, LSE reduce, label
-    scoring."""
-    return 13
+    """Kernels one quail_classify_trie_tree call launches on this workload:
+    embed RMSNorm, the q|k|v projection GEMM, q/k head norm, tree part, paged
+    doc attention (which merges the tree part itself: one split per
+    document), W_o GEMM, final norm, head GEMM, LSE reduce + label scoring."""
+    return 9
 
 
 def parse():

@@ -578,13 +578,23 @@ quail_status quail_classify_trie_tree(const quail_model_desc* model, const quail
                         static_cast<const bf16*>(model->lm_head), d, a, n_child, n_tiles};
     CUDA_TRY(launch_gemm_head(tA, tB, rows, model->vocab, d, ha, ds->num_sms, ds->err, st));
     stage_mark(QUAIL_STAGE_HEAD, true, st);
-    stage_mark(QUAIL_STAGE_SCORING, false, st);
-    CUDA_TRY(launch_lse_reduce(b.lse_part, rows, n_tiles, b.lse, st));
   }
-
-  LabelScoreArgs la{b.child_logit,           b.lse,    img->label_term_offsets, img->label_term_eval,
-                    img->label_term_slot,    img->label_prefix_eval, img->eval_child_offsets, a,
-                    n_child,                 trie->num_labels, label_logscore, label_prob, label_argmax};
+  stage_mark(QUAIL_STAGE_SCORING, false, st);
+  LabelScoreArgs la{b.child_logit,
+                    b.lse_part,
+                    (model->vocab + kHeadBN - 1) / kHeadBN,
+                    b.lse,
+                    img->label_term_offsets,
+                    img->label_term_eval,
+                    img->label_term_slot,
+                    img->label_prefix_eval,
+                    img->eval_child_offsets,
+                    a,
+                    n_child,
+                    trie->num_labels,
+                    label_logscore,
+                    label_prob,
+                    label_argmax};
   CUDA_TRY(launch_label_score(la, num_docs, st));
   stage_mark(QUAIL_STAGE_SCORING, true, st);
   return QUAIL_OK;

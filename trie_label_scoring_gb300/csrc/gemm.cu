@@ -133,15 +133,18 @@ cudaError_t launch_umma(const CUtensorMap& tmA, const BSet& bset, int M, int N, 
 }  // namespace
 
 int choose_k_splits(int tiles, int nk, int num_sms) {
-  // Largest SM efficiency units / (waves * SMs), preferring fewer splits; at
-  // least 4 k-blocks per unit.
+  // The smallest split count whose units fill the SMs to >= 75% over whole
+  // waves (fewer splits = fewer partial slabs); else the best one found. Each
+  // unit keeps at least 4 k-blocks. Measured at the W_o shape, more splits
+  // add slab traffic without speeding up the operand stream.
   int best = 1;
   double best_eff = 0.0;
   for (int ks = 1; ks <= 8 && nk / ks >= 4; ++ks) {
     const long units = static_cast<long>(tiles) * ks;
     const long waves = (units + num_sms - 1) / num_sms;
     const double eff = static_cast<double>(units) / static_cast<double>(waves * num_sms);
-    if (eff > best_eff + 0.05) {
+    if (eff >= 0.75) return ks;
+    if (eff > best_eff) {
       best_eff = eff;
       best = ks;
     }

@@ -73,10 +73,14 @@ cudaError_t launch_final_norm(const float* h_part, int k_splits, size_t slab, co
 // lse[r] = log-sum-exp over the n_tiles partials of row r.
 cudaError_t launch_lse_reduce(const float2* lse_part, int rows, int n_tiles, float* lse, cudaStream_t st);
 
-// Label path sums, prefix correction, softmax over labels and argmax, one block per document.
+// Label path sums, prefix correction, softmax over labels and argmax, one block
+// per document; the block first reduces its a rows' log-sum-exp from the
+// head's tile partials (and stores them in lse).
 struct LabelScoreArgs {
   const float* child_logit;  // [N, n_child]
-  const float* lse;          // [N * a]
+  const float2* lse_part;    // [N * a, n_tiles]
+  int n_tiles;
+  float* lse;                // [N * a], written
   const int* term_offsets;   // [M + 1]
   const int* term_eval;
   const int* term_slot;

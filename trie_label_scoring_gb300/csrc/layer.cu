@@ -37,23 +37,51 @@ __device__ float block_sum(float v, float* scratch) {
   return scratch[0];
 }
 
-__global__ void embed_rmsnorm_kernel(const bf16* __restrict__ embed, const int* __restrict__ tokens, int d,
-                                     const bf16* __restrict__ gain, float eps, bf16* __restrict__ out) {
+constexpr int kNormThreads = 256;
+constexpr int kNormMaxVec = 12;  // float4 / 8-bf16 vectors per thread: d <= 4 * 256 * 12 = 12288
+
+__device__ __forceinline__ float4 bf16x4_to_float4(uint2 u) {
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ uint32_t f2_to_bf16x2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Block per row; the row stays in registers between the two passes; 8-byte
+// vector accesses. Output: [hi | lo] two-term bf16 split of RMSNorm(x) * gain.
+__global__ void __launch_bounds__(kNormThreads) embed_rmsnorm_kernel(const bf16* __restrict__ embed,
+                                                                     const int* __restrict__ tokens, int d,
+                                                                     const bf16* __restrict__ gain, float eps,
+                                                                     bf16* __restrict__ out) {
   __shared__ float scratch[32];
   const int r = blockIdx.x;
-  const bf16* x = embed + static_cast<size_t>(__ldg(tokens + r)) * d;
+  const uint2* x = reinterpret_cast<const uint2*>(embed + static_cast<size_t>(__ldg(tokens + r)) * d);
+  const int nv = d >> 2;
+  float4 v[kNormMaxVec];
   float ss = 0.f;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    const float v = __bfloat162float(x[i]);
-    ss += v * v;
+#pragma unroll
+  for (int i = 0; i < kNormMaxVec; ++i) {
+    const int c = threadIdx.x + i * kNormThreads;
+    v[i] = c < nv ? bf16x4_to_float4(__ldg(x + c)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
   }
   const float inv = rsqrtf(block_sum(ss, scratch) / d + eps);
-  bf16* o = out + static_cast<size_t>(r) * 2 * d;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    const float y = __bfloat162float(x[i]) * inv * __bfloat162float(gain[i]);
-    const bf16 hi = __float2bfloat16(y);
-    o[i] = hi;
-    o[d + i] = __float2bfloat16(y - __bfloat162float(hi));
+  const uint2* gv = reinterpret_cast<const uint2*>(gain);
+  uint2* ohi = reinterpret_cast<uint2*>(out + static_cast<size_t>(r) * 2 * d);
+  uint2* olo = reinterpret_cast<uint2*>(out + static_cast<size_t>(r) * 2 * d + d);
+#pragma unroll
+  for (int i = 0; i < kNormMaxVec; ++i) {
+    const int c = threadIdx.x + i * kNormThreads;
+    if (c >= nv) break;
+    const float4 g = bf16x4_to_float4(__ldg(gv + c));
+    const float y0 = v[i].x * inv * g.x, y1 = v[i].y * inv * g.y, y2 = v[i].z * inv * g.z, y3 = v[i].w * inv * g.w;
+    const uint2 hi = make_uint2(f2_to_bf16x2(y0, y1), f2_to_bf16x2(y2, y3));
+    const float4 h = bf16x4_to_float4(hi);
+    ohi[c] = hi;
+    olo[c] = make_uint2(f2_to_bf16x2(y0 - h.x, y1 - h.y), f2_to_bf16x2(y2 - h.z, y3 - h.w));
   }
 }
 
@@ -87,54 +115,75 @@ __global__ void qk_head_norm_kernel(const float* __restrict__ part, int k_splits
   *reinterpret_cast<float4*>(qkv + off) = v;
 }
 
-__global__ void final_norm_kernel(const float* __restrict__ h_part, int k_splits, size_t slab,
-                                  const bf16* __restrict__ embed, const int* __restrict__ node_token, RowMap map,
-                                  int d, const bf16* __restrict__ gain, float eps, bf16* __restrict__ z_bf16,
-                                  float* __restrict__ z_f32) {
-  extern __shared__ float s_h[];  // [d]
+// Block per row: h = x + sum of the k-split slabs, kept in registers; z in bf16
+// (and fp32 when z_f32 is given). float4 / 8-byte vector accesses.
+__global__ void __launch_bounds__(kNormThreads) final_norm_kernel(const float* __restrict__ h_part, int k_splits,
+                                                                  size_t slab, const bf16* __restrict__ embed,
+                                                                  const int* __restrict__ node_token, RowMap map,
+                                                                  int d, const bf16* __restrict__ gain, float eps,
+                                                                  bf16* __restrict__ z_bf16,
+                                                                  float* __restrict__ z_f32) {
   __shared__ float scratch[32];
   const int r = blockIdx.x;
   const int slot = r / map.nq;
   if (map.n_slots_dev != nullptr && slot >= *map.n_slots_dev) return;
   const int node = map.slot_node ? map.slot_node[slot] : (r - slot * map.nq);
-  const bf16* x = embed + static_cast<size_t>(__ldg(node_token + node)) * d;
-  const float* hp = h_part + static_cast<size_t>(r) * d;
+  const uint2* x = reinterpret_cast<const uint2*>(embed + static_cast<size_t>(__ldg(node_token + node)) * d);
+  const float4* hp = reinterpret_cast<const float4*>(h_part + static_cast<size_t>(r) * d);
+  const size_t slab4 = slab >> 2;
+  const int nv = d >> 2;
+  float4 v[kNormMaxVec];
   float ss = 0.f;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    float v = __bfloat162float(x[i]);
-    for (int s = 0; s < k_splits; ++s) v += hp[s * slab + i];
-    s_h[i] = v;
-    ss += v * v;
+#pragma unroll
+  for (int i = 0; i < kNormMaxVec; ++i) {
+    const int c = threadIdx.x + i * kNormThreads;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c < nv) {
+      a = bf16x4_to_float4(__ldg(x + c));
+      for (int s = 0; s < k_splits; ++s) {
+        const float4 p = hp[s * slab4 + c];
+        a.x += p.x;
+        a.y += p.y;
+        a.z += p.z;
+        a.w += p.w;
+      }
+    }
+    v[i] = a;
+    ss += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w;
   }
   const float inv = rsqrtf(block_sum(ss, scratch) / d + eps);
-  for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    const float v = s_h[i] * inv * __bfloat162float(gain[i]);
-    z_bf16[static_cast<size_t>(r) * d + i] = __float2bfloat16(v);
-    if (z_f32) z_f32[static_cast<size_t>(r) * d + i] = v;
+  const uint2* gv = reinterpret_cast<const uint2*>(gain);
+  uint2* zb = reinterpret_cast<uint2*>(z_bf16 + static_cast<size_t>(r) * d);
+  float4* zf = z_f32 ? reinterpret_cast<float4*>(z_f32 + static_cast<size_t>(r) * d) : nullptr;
+#pragma unroll
+  for (int i = 0; i < kNormMaxVec; ++i) {
+    const int c = threadIdx.x + i * kNormThreads;
+    if (c >= nv) break;
+    const float4 g = bf16x4_to_float4(__ldg(gv + c));
+    const float4 y = make_float4(v[i].x * inv * g.x, v[i].y * inv * g.y, v[i].z * inv * g.z, v[i].w * inv * g.w);
+    zb[c] = make_uint2(f2_to_bf16x2(y.x, y.y), f2_to_bf16x2(y.z, y.w));
+    if (zf) zf[c] = y;
   }
 }
 
-// One warp per row: combine the (max, sum) pairs of every vocabulary tile.
+// One warp per row: max over the tile partials, then the rescaled sum.
 __global__ void lse_reduce_kernel(const float2* __restrict__ part, int rows, int n_tiles, float* __restrict__ lse) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= rows) return;
   const float2* p = part + static_cast<size_t>(warp) * n_tiles;
-  float m = -INFINITY, s = 0.f;
+  float m = -INFINITY;
+#pragma unroll 4
+  for (int j = lane; j < n_tiles; j += 32) m = fmaxf(m, p[j].x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float s = 0.f;
+#pragma unroll 4
   for (int j = lane; j < n_tiles; j += 32) {
     const float2 v = p[j];
-    const float nm = fmaxf(m, v.x);
-    s = s * exp2f(m - nm) + v.y * exp2f(v.x - nm);
-    m = nm;
+    s += v.y * exp2f(v.x - m);
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float om = __shfl_xor_sync(0xffffffffu, m, o);
-    const float os = __shfl_xor_sync(0xffffffffu, s, o);
-    const float nm = fmaxf(m, om);
-    s = (m == -INFINITY ? 0.f : s * exp2f(m - nm)) + (om == -INFINITY ? 0.f : os * exp2f(om - nm));
-    m = nm;
-  }
+  s = warp_sum(s);
   if (lane == 0) lse[warp] = (m + log2f(s)) * 0.69314718055994531f;
 }
 
@@ -149,7 +198,25 @@ __global__ void label_score_kernel(LabelScoreArgs a) {
   const int doc = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const float* cl = a.child_logit + static_cast<size_t>(doc) * a.n_child;
-  const float* lse = a.lse + static_cast<size_t>(doc) * a.a;
+  float* lse = a.lse + static_cast<size_t>(doc) * a.a;
+  // log-sum-exp of this document's a rows from the head's tile partials (warp per row)
+  for (int e = warp; e < a.a; e += nw) {
+    const float2* p = a.lse_part + (static_cast<size_t>(doc) * a.a + e) * a.n_tiles;
+    float m = -INFINITY;
+#pragma unroll 4
+    for (int j = lane; j < a.n_tiles; j += 32) m = fmaxf(m, p[j].x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float sm = 0.f;
+#pragma unroll 4
+    for (int j = lane; j < a.n_tiles; j += 32) {
+      const float2 v = p[j];
+      sm += v.y * exp2f(v.x - m);
+    }
+    sm = warp_sum(sm);
+    if (lane == 0) lse[e] = (m + log2f(sm)) * 0.69314718055994531f;
+  }
+  __syncthreads();
   float* out_ls = a.logscore + static_cast<size_t>(doc) * a.M;
   float best = -INFINITY;
   int best_i = 0x7fffffff;
@@ -348,7 +415,7 @@ __global__ void decode_select_kernel(DecodeTrie t, const float* __restrict__ z, 
 cudaError_t launch_embed_rmsnorm(const bf16* embed, const int* tokens, int n, int d, const bf16* gain, float eps,
                                  bf16* out, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
-  embed_rmsnorm_kernel<<<n, 256, 0, st>>>(embed, tokens, d, gain, eps, out);
+  embed_rmsnorm_kernel<<<n, kNormThreads, 0, st>>>(embed, tokens, d, gain, eps, out);
   return cudaGetLastError();
 }
 
@@ -365,8 +432,8 @@ cudaError_t launch_final_norm(const float* h_part, int k_splits, size_t slab, co
                               const int* node_token, RowMap map, int rows, int d, const bf16* gain, float eps,
                               bf16* z_bf16, float* z_f32, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
-  final_norm_kernel<<<rows, 256, d * sizeof(float), st>>>(h_part, k_splits, slab, embed, node_token, map, d, gain,
-                                                         eps, z_bf16, z_f32);
+  final_norm_kernel<<<rows, kNormThreads, 0, st>>>(h_part, k_splits, slab, embed, node_token, map, d, gain, eps,
+                                                  z_bf16, z_f32);
   return cudaGetLastError();
 }
 

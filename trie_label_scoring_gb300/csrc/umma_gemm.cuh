@@ -54,11 +54,13 @@ struct GemmUnit {
   int m_blk, n_blk, ks, kb0, kb1;
 };
 
-// unit -> (tile, k-split); tile -> (n band, m tile), N-band-major.
-__device__ __forceinline__ GemmUnit gemm_unit(int u, int m_tiles, int k_splits, int nk) {
+// unit -> (k-split, tile) with the k-split slowest, so the CTAs resident at
+// one time share B bands and A rows in L2; tile -> (n band, m tile), N-band-major.
+__device__ __forceinline__ GemmUnit gemm_unit(int u, int m_tiles, int n_tiles, int k_splits, int nk) {
   GemmUnit g;
-  g.ks = u % k_splits;
-  const int tile = u / k_splits;
+  const int tiles = m_tiles * n_tiles;
+  g.ks = u / tiles;
+  const int tile = u - g.ks * tiles;
   g.n_blk = tile / m_tiles;
   g.m_blk = tile - g.n_blk * m_tiles;
   g.kb0 = g.ks * nk / k_splits;
@@ -127,7 +129,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-        const GemmUnit g = gemm_unit(u, m_tiles, k_splits, nk);
+        const GemmUnit g = gemm_unit(u, m_tiles, n_tiles, k_splits, nk);
         const int n0 = g.n_blk * BN;
         int bi = 0;
         while (bi + 1 < bset.count && n0 >= bset.n_begin[bi + 1]) ++bi;
@@ -173,7 +175,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-        const GemmUnit g = gemm_unit(u, m_tiles, k_splits, nk);
+        const GemmUnit g = gemm_unit(u, m_tiles, n_tiles, k_splits, nk);
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -225,7 +227,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
       if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) break;
       tc_fence_after();
-      const GemmUnit g = gemm_unit(u, m_tiles, k_splits, nk);
+      const GemmUnit g = gemm_unit(u, m_tiles, n_tiles, k_splits, nk);
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
       epi(g.m_blk, g.n_blk, g.ks, lane_row, taddr);
       tc_fence_before();
