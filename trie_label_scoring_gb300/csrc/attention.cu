@@ -344,15 +344,31 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
         mx[c >> 1] = fmaxf(mx[c >> 1], sc[nt][c]);
       }
     }
-    float alpha[2];
+    // Lazy rescale: the reference max m_r only moves when a row max exceeds it
+    // by more than 8 (base 2), so p <= 256 stays far from fp32 overflow and the
+    // O rescale (64 multiplies) is skipped on almost every page. Exact: O, l
+    // and m_r always describe sum_j exp2(s_j - m_r) (v_j, 1).
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
       mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 1));
       mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 2));
-      const float nm = fmaxf(m_r[hr], mx[hr]);
-      alpha[hr] = exp2f(m_r[hr] - nm);
-      m_r[hr] = nm;
-      l_r[hr] *= alpha[hr];
+    }
+    if (__any_sync(0xffffffffu, mx[0] > m_r[0] + 8.f || mx[1] > m_r[1] + 8.f)) {
+      float alpha[2];
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const float nm = fmaxf(m_r[hr], mx[hr]);
+        alpha[hr] = exp2f(m_r[hr] - nm);
+        m_r[hr] = nm;
+        l_r[hr] *= alpha[hr];
+      }
+#pragma unroll
+      for (int n = 0; n < 16; ++n) {
+        o[n][0] *= alpha[0];
+        o[n][1] *= alpha[0];
+        o[n][2] *= alpha[1];
+        o[n][3] *= alpha[1];
+      }
     }
     // P as a two-term bf16 split (pa + pl = p to ~16 bits)
     uint32_t pa[4], pl[4];
@@ -365,13 +381,6 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
         l_r[hr] += e0 + e1;
         split_bf16(e0, e1, pa[nt * 2 + hr], pl[nt * 2 + hr]);
       }
-    }
-#pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      o[n][0] *= alpha[0];
-      o[n][1] *= alpha[0];
-      o[n][2] *= alpha[1];
-      o[n][3] *= alpha[1];
     }
     // O += P V; V fragments via transposed ldmatrix. Keys past the document
     // end are zeroed in registers so stale slot contents never reach O.
