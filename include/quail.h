@@ -234,6 +234,32 @@ quail_status quail_classify_trie_decode_step(const quail_model_desc* model, cons
                                              int32_t* label_out, int32_t* active_count, uint8_t* touched_nodes,
                                              void* workspace, size_t workspace_bytes, quail_stream_t stream);
 
+/* trie_tree for callers that cannot allocate device memory: an engine that has
+ * already claimed nearly all of the GPU's memory for its own pools (a KV-cache
+ * manager that reserves HBM at start-up), or a code path where cudaMalloc is
+ * not allowed because it would synchronise the device in the middle of
+ * latency-critical work. The pages this library follows have no counterpart of
+ * this call; it exists for such integrations only.
+ *
+ * Same arguments, kernels and outputs as quail_classify_trie_tree, without the
+ * workspace: the trie tables and every intermediate live in one fixed device
+ * array of QUAIL_NOALLOC_SCRATCH_BYTES (64 MiB) that the library holds on every
+ * GPU it is loaded on, until the process exits. The call allocates nothing
+ * (no cudaMalloc, no cudaFree, no allocating library routine) and does not
+ * need quail_trie_upload. If the call would need more scratch than the array
+ * holds (about 230 documents of up to 1,024 tokens at the Qwen3-4B shape with
+ * the 10-label trie), it returns QUAIL_ERR_WORKSPACE before launching anything.
+ * Its first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture. Every call shares the array: calls whose work overlaps on the GPU
+ * (two streams, or two threads) race and corrupt each other's results, so
+ * serialise them. The array keeps the previous call's contents; nothing in it
+ * needs to start at zero. */
+#define QUAIL_NOALLOC_SCRATCH_BYTES (64ull << 20)
+quail_status quail_classify_trie_tree_noalloc(const quail_model_desc* model, const quail_paged_kv* kv,
+                                              const quail_trie* trie, int32_t num_docs, float* label_logscore,
+                                              float* label_prob, int32_t* label_argmax, quail_stream_t stream);
+
 /* Synchronises `stream`, then reads and clears the current device's error
  * word. Returns QUAIL_OK, QUAIL_ERR_DEVICE_BOUNDS or QUAIL_ERR_DEVICE_TIMEOUT
  * (the message names the first failing item), or QUAIL_ERR_CUDA. */

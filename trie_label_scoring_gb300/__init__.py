@@ -12,6 +12,7 @@ Entry points (same names as the C ABI, without the quail_ prefix):
   classify_trie_tree(...)        -> quail_classify_trie_tree
   classify_letters(...)          -> quail_classify_letters
   classify_trie_decode_step(...) -> quail_classify_trie_decode_step
+  classify_trie_tree_noalloc(...) -> quail_classify_trie_tree_noalloc
   device_status(...)             -> quail_device_status
   set_stage_events(...)          -> quail_set_stage_events
 """
@@ -94,6 +95,9 @@ _SIGNATURES = {
                                                        ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
                                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                        ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "quail_classify_trie_tree_noalloc": (ctypes.c_int, [ctypes.POINTER(ModelDesc), ctypes.POINTER(PagedKV),
+                                                        ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "quail_device_status": (ctypes.c_int, [ctypes.c_void_p]),
     "quail_set_stage_events": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
 }
@@ -256,6 +260,14 @@ def classify_trie_decode_step(model: Model, kv: KV, trie: Trie, num_docs: int, n
         ctypes.byref(model.desc), ctypes.byref(kv.desc), trie.handle, int(num_docs), _ptr(node_cursor),
         _ptr(label_out), _ptr(active_count), _ptr(touched_nodes), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def classify_trie_tree_noalloc(model: Model, kv: KV, trie: Trie, num_docs: int, label_logscore, label_prob,
+                               label_argmax, stream=None) -> None:
+    """trie_tree in the library's fixed device scratch: no workspace, no device allocation."""
+    _check(lib().quail_classify_trie_tree_noalloc(
+        ctypes.byref(model.desc), ctypes.byref(kv.desc), trie.handle, int(num_docs), _ptr(label_logscore),
+        _ptr(label_prob), _ptr(label_argmax), _stream(stream)))
 
 
 def device_status(stream=None) -> None:

@@ -428,6 +428,61 @@ quail_status upload_trie(quail_trie* t, cudaStream_t st, const quail_trie::Devic
   return QUAIL_OK;
 }
 
+// ------------------------------------------------------------------ fixed scratch
+// Scratch for quail_classify_trie_tree_noalloc: one fixed device array that the
+// library holds on every device it is loaded on, so that entry point never
+// allocates. Host code only uses its address from cudaGetSymbolAddress.
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(QUAIL_NOALLOC_SCRATCH_BYTES);
+__device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+uint8_t* g_noalloc_ptr[64] = {};
+
+// Device address of the fixed scratch on the current device (looked up once per device).
+quail_status noalloc_scratch(uint8_t** out) {
+  int dev = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return fail(QUAIL_ERR_CUDA, "device id %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr)
+      return fail(QUAIL_ERR_CUDA, "cudaGetSymbolAddress(fixed scratch): %s", cudaGetErrorString(e));
+    g_noalloc_ptr[dev] = static_cast<uint8_t*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return QUAIL_OK;
+}
+
+// The trie tables the trie_tree kernels read, in one block of `bytes` bytes.
+size_t trie_tree_image_bytes(const quail_trie* t) {
+  const std::vector<int32_t>* arrays[] = {&t->eval_token,         &t->eval_depth,         &t->eval_parent,
+                                          &t->eval_child_offsets, &t->eval_child_tokens,  &t->label_term_offsets,
+                                          &t->label_term_eval,    &t->label_term_slot,    &t->label_prefix_eval};
+  size_t total = 0;
+  for (const auto* a : arrays) total += round_up(std::max<size_t>(a->size(), 1) * 4, 256);
+  return total;
+}
+
+// Copies those tables into dst (device) on `st` and points img at them.
+quail_status copy_trie_tree_image(const quail_trie* t, uint8_t* dst, cudaStream_t st, quail_trie::DeviceImage* img) {
+  const std::vector<int32_t>* arrays[] = {&t->eval_token,         &t->eval_depth,         &t->eval_parent,
+                                          &t->eval_child_offsets, &t->eval_child_tokens,  &t->label_term_offsets,
+                                          &t->label_term_eval,    &t->label_term_slot,    &t->label_prefix_eval};
+  const int32_t** fields[] = {&img->eval_token,         &img->eval_depth,        &img->eval_parent,
+                              &img->eval_child_offsets, &img->eval_child_tokens, &img->label_term_offsets,
+                              &img->label_term_eval,    &img->label_term_slot,   &img->label_prefix_eval};
+  size_t off = 0;
+  for (int i = 0; i < 9; ++i) {
+    if (!arrays[i]->empty())
+      CUDA_TRY(cudaMemcpyAsync(dst + off, arrays[i]->data(), arrays[i]->size() * 4, cudaMemcpyHostToDevice, st));
+    *fields[i] = reinterpret_cast<const int32_t*>(dst + off);
+    off += round_up(std::max<size_t>(arrays[i]->size(), 1) * 4, 256);
+  }
+  return QUAIL_OK;
+}
+
 }  // namespace
 
 // ================================================================== C ABI
@@ -751,6 +806,74 @@ quail_status quail_set_stage_events(quail_event_t* events, int32_t num_stages) {
   if (events == nullptr || num_stages <= 0) return QUAIL_OK;
   if (num_stages > QUAIL_NUM_STAGES) return fail(QUAIL_ERR_INVALID_ARG, "at most %d stages", QUAIL_NUM_STAGES);
   for (int i = 0; i < 2 * num_stages; ++i) g_events.push_back(reinterpret_cast<cudaEvent_t>(events[i]));
+  return QUAIL_OK;
+}
+
+
+// trie_tree without any device allocation: the same kernels as
+// quail_classify_trie_tree, with the trie tables and every intermediate placed
+// in the library's fixed scratch array instead of a caller workspace and a
+// library-allocated trie image. For callers that must not allocate device
+// memory (see quail.h).
+quail_status quail_classify_trie_tree_noalloc(const quail_model_desc* model, const quail_paged_kv* kv,
+                                              const quail_trie* trie, int32_t num_docs, float* label_logscore,
+                                              float* label_prob, int32_t* label_argmax, quail_stream_t stream) {
+  quail_status s = check_model(model);
+  if (s != QUAIL_OK) return s;
+  s = check_kv(kv, model);
+  if (s != QUAIL_OK) return s;
+  if (trie == nullptr) return fail(QUAIL_ERR_INVALID_ARG, "trie is null");
+  if (trie->vocab != model->vocab) return fail(QUAIL_ERR_INVALID_ARG, "trie vocab %d != model vocab %d", trie->vocab, model->vocab);
+  if (num_docs < 0) return fail(QUAIL_ERR_INVALID_ARG, "num_docs < 0");
+  if (num_docs == 0) return QUAIL_OK;
+  if (num_docs > 65535) return fail(QUAIL_ERR_UNSUPPORTED_SHAPE, "at most 65535 documents per call");
+  if (label_logscore == nullptr || label_prob == nullptr || label_argmax == nullptr)
+    return fail(QUAIL_ERR_INVALID_ARG, "an output pointer is null");
+  const int a = trie->n_eval();
+  const int n_child = trie->eval_child_offsets.back();
+  const size_t image = trie_tree_image_bytes(trie);
+  const size_t need = image + plan(nullptr, model, a, num_docs, a, kv->max_doc_len, true, n_child, false, 0, nullptr);
+  if (need > kNoAllocScratchBytes)
+    return fail(QUAIL_ERR_WORKSPACE,
+                "this call needs %zu bytes of scratch but the fixed scratch holds %zu: pass fewer documents "
+                "or use quail_classify_trie_tree with a caller-allocated workspace",
+                need, kNoAllocScratchBytes);
+  DeviceState* ds = nullptr;
+  s = device_state(&ds);
+  if (s != QUAIL_OK) return s;
+  uint8_t* scratch = nullptr;
+  s = noalloc_scratch(&scratch);
+  if (s != QUAIL_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  quail_trie::DeviceImage img{};
+  s = copy_trie_tree_image(trie, scratch, st, &img);
+  if (s != QUAIL_OK) return s;
+  Buffers b;
+  plan(scratch + image, model, a, num_docs, a, kv->max_doc_len, true, n_child, false, 0, &b);
+  const NodeTables nt{img.eval_token, img.eval_depth, img.eval_parent, a};
+  const RowMap map{a, nullptr, nullptr, nullptr};
+  const int rows = num_docs * a;
+  s = run_prologue(model, nt, b, ds, st);
+  if (s != QUAIL_OK) return s;
+  s = run_attention(model, kv, nt, map, num_docs, b, ds, st);
+  if (s != QUAIL_OK) return s;
+  s = run_wo_norm(model, nt, map, rows, b, ds, st);
+  if (s != QUAIL_OK) return s;
+  const int d = model->hidden;
+  const int n_tiles = (model->vocab + kHeadBN - 1) / kHeadBN;
+  CUtensorMap tA, tB;
+  s = encode_2d_bf16(&tA, b.z, round_up(rows, 128), d, d, 64, 128);
+  if (s != QUAIL_OK) return s;
+  s = encode_2d_bf16(&tB, model->lm_head, model->vocab, d, d, 64, 256);
+  if (s != QUAIL_OK) return s;
+  HeadEpilogueArgs ha{b.lse_part, b.child_logit, img.eval_child_offsets, img.eval_child_tokens, b.z_f32,
+                      static_cast<const bf16*>(model->lm_head), d, a, n_child, n_tiles};
+  CUDA_TRY(launch_gemm_head(tA, tB, rows, model->vocab, d, ha, ds->num_sms, ds->err, st));
+  LabelScoreArgs la{b.child_logit,       b.lse_part,          n_tiles,        b.lse,
+                    img.label_term_offsets, img.label_term_eval, img.label_term_slot, img.label_prefix_eval,
+                    img.eval_child_offsets, a,                  n_child,        trie->num_labels,
+                    label_logscore,      label_prob,          label_argmax};
+  CUDA_TRY(launch_label_score(la, num_docs, st));
   return QUAIL_OK;
 }
 
