@@ -170,21 +170,40 @@ size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
 
 struct AttnShape {
   int rows_per_kv, row_tile, rows_pad, split_tokens, n_splits;
+  bool tc;  // tcgen05 kernel (128-row tiles) instead of the mma.sync one
 };
 
 AttnShape attn_shape(const quail_model_desc* m, int nq, int slots, int max_doc_len, int sms) {
   AttnShape s;
   const int G = m->n_q_heads / m->n_kv_heads;
   s.rows_per_kv = nq * G;
-  s.row_tile = s.rows_per_kv <= 16 ? 16 : 64;
-  s.rows_pad = static_cast<int>(round_up(s.rows_per_kv, s.row_tile));
-  // One split per document when (document, KV head, row group) work items
-  // already fill the GPU several times over: the epilogue then merges the tree
-  // part directly. Otherwise 512-token splits spread long documents over more
-  // CTAs and a combine kernel merges them. A split holds at most 256 pages.
-  const long items = static_cast<long>(slots) * m->n_kv_heads * (s.rows_pad / s.row_tile);
   const int whole = static_cast<int>(round_up(max_doc_len, 16));
-  s.split_tokens = (items >= 6L * sms) ? std::min(whole, 4096) : std::min(whole, 512);
+  if (s.rows_per_kv <= 16) {
+    // A few query rows per KV head (the support-topic shape): mma.sync kernel,
+    // four warps share 16 rows. One split per document when the (document,
+    // KV head) items already fill the GPU several times over (the epilogue then
+    // merges the tree part); else 512-token splits and the combine kernel.
+    s.tc = false;
+    s.row_tile = 16;
+    s.rows_pad = 16;
+    const long items = static_cast<long>(slots) * m->n_kv_heads;
+    s.split_tokens = (items >= 6L * sms) ? std::min(whole, 4096) : std::min(whole, 512);
+  } else {
+    // Many rows: tcgen05 kernel on 128-row tiles, one CTA per SM. Split the
+    // documents only as far as needed for about three CTAs per SM.
+    s.tc = true;
+    s.row_tile = 128;
+    s.rows_pad = static_cast<int>(round_up(s.rows_per_kv, 128));
+    const long items = static_cast<long>(slots) * m->n_kv_heads * (s.rows_pad / 128);
+    const long want = 3L * sms;
+    int split = std::min(whole, 4096);
+    if (items < want) {
+      const long parts = (want + items - 1) / items;
+      split = static_cast<int>(round_up((max_doc_len + parts - 1) / parts, 64));
+      split = std::max(256, std::min(split, 4096));
+    }
+    s.split_tokens = split;
+  }
   s.n_splits = (max_doc_len + s.split_tokens - 1) / s.split_tokens;
   return s;
 }
@@ -353,7 +372,11 @@ quail_status run_attention(const quail_model_desc* m, const quail_paged_kv* kv, 
   s = encode_2d_bf16(&tV, kv->v_pool, pool_rows, 128, 128, 64, 16);
   if (s != QUAIL_OK) return s;
   CUDA_TRY(launch_tree_part(a, st));
-  CUDA_TRY(launch_attn_doc(a, tK, tV, st));
+  if (as.tc) {
+    CUDA_TRY(launch_attn_doc_tc(a, tK, tV, st));
+  } else {
+    CUDA_TRY(launch_attn_doc(a, tK, tV, st));
+  }
   if (as.n_splits > 1) CUDA_TRY(launch_attn_combine(a, st));
   return QUAIL_OK;
 }

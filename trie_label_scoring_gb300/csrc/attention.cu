@@ -15,6 +15,7 @@
 #include "kernels.h"
 #include "quail_internal.h"
 #include "sm103.cuh"
+#include "attn_common.cuh"
 
 namespace quail {
 
@@ -26,12 +27,6 @@ constexpr int kAttnThreads = 160;  // warps 0..3 consume, warp 4 loads pages
 constexpr int kAttnStages = 8;     // multiple of kConsumerWarps
 constexpr uint32_t kHalfBytes = kPage * 64 * 2;   // 16 keys x 64 bf16, 128B-swizzled
 constexpr uint32_t kPageBytes = 4 * kHalfBytes;   // K[0:64) K[64:128) V[0:64) V[64:128)
-
-constexpr float kLog2e = 1.4426950408889634f;
-
-struct RopeTable {
-  float2 w[64];  // inv_freq_j = theta^(-2j/128) as hi + lo floats
-};
 
 // Byte offset of 16-byte chunk `c` (0..7) of key row `r` in a 128B-swizzled half tile.
 __device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t c) { return r * 128u + ((c ^ (r & 7u)) << 4); }
@@ -53,37 +48,6 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-__device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
-  return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u));
-}
-// Two-term bf16 split of (x0, x1): hi = bf16(x), lo = bf16(x - hi).
-__device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  hi = pack_bf16(x0, x1);
-  const float2 h = unpack_bf16(hi);
-  lo = pack_bf16(x0 - h.x, x1 - h.y);
-}
-
-// cos/sin of pos * w, w given as hi + lo floats; exact product and a two-step
-// reduction by 2*pi keep the angle accurate to ~1e-7 rad for pos < 2^24.
-__device__ __forceinline__ void rope_cs(int pos, float2 w, float& c, float& s) {
-  const float p = static_cast<float>(pos);
-  const float a = p * w.x;
-  const float b = fmaf(p, w.x, -a) + p * w.y;
-  const float k = rintf(a * 0.15915494309189535f);
-  float r = fmaf(-k, 6.28318548202514648f, a);  // 2*pi rounded to float
-  r = fmaf(-k, -1.7484556000744487e-07f, r);    // 2*pi - float(2*pi)
-  r += b;
-  sincosf(r, &s, &c);
-}
-
-__device__ __forceinline__ int row_doc(const RowMap& m, int slot) { return m.slot_doc ? m.slot_doc[slot] : slot; }
-__device__ __forceinline__ int row_node(const RowMap& m, int slot, int e) {
-  return m.slot_node ? m.slot_node[slot] : e;
-}
 
 // ------------------------------------------------------------------ tree part
 // Warp per (node, q head): online softmax over the node's ancestors and itself
@@ -97,7 +61,7 @@ __global__ void tree_part_kernel(AttnArgs a, RopeTable rt) {
   const float* qr = a.qkv + static_cast<size_t>(node) * a.ldq + h * 128;
   const float q0 = qr[lane], q1 = qr[lane + 32], q2 = qr[lane + 64], q3 = qr[lane + 96];
   const float2 w0 = rt.w[lane], w1 = rt.w[lane + 32];
-  const float scale = kLog2e * 0.08838834764831845f;  // log2(e) / sqrt(128)
+  const float scale = kAttnLog2e * 0.08838834764831845f;  // log2(e) / sqrt(128)
   const int dnode = a.node_depth[node];
   float m = -INFINITY, l = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
   int anc = node;
@@ -301,7 +265,7 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
   const int qtile = shared_rows ? 0 : warp;
   const uint4* qf = reinterpret_cast<const uint4*>(s_q + qtile * kQTileBytes) + lane;  // [ks][hi/lo][lane]
 
-  const float scale = kLog2e * 0.08838834764831845f;
+  const float scale = kAttnLog2e * 0.08838834764831845f;
   float o[16][4];
 #pragma unroll
   for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
@@ -311,7 +275,9 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
   const int jstep = shared_rows ? kConsumerWarps : 1;
   for (int j = j0; j < n_pages; j += jstep) {
     const int s = j % kAttnStages;
-    if (!mbar_wait(&full[s], static_cast<uint32_t>((j / kAttnStages) & 1), abort_flag)) break;
+    // warp-uniform wait: the shuffles and __any_sync below need every lane
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], static_cast<uint32_t>((j / kAttnStages) & 1), abort_flag)))
+      break;
     const uint32_t kb = smem_u32(base + s * kPageBytes);
     const uint32_t vb = kb + 2 * kHalfBytes;
     const int key0 = (p0 + j) * kPage;
@@ -558,15 +524,6 @@ __global__ void attn_combine_kernel(AttnArgs a) {
   }
 }
 
-RopeTable make_rope_table(float theta) {
-  RopeTable t;
-  for (int j = 0; j < 64; ++j) {
-    const double w = std::pow(static_cast<double>(theta), -2.0 * j / 128.0);
-    const float hi = static_cast<float>(w);
-    t.w[j] = make_float2(hi, static_cast<float>(w - static_cast<double>(hi)));
-  }
-  return t;
-}
 
 }  // namespace
 

@@ -150,5 +150,7 @@ struct AttnArgs {
 cudaError_t launch_tree_part(const AttnArgs& a, cudaStream_t st);
 cudaError_t launch_attn_doc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV, cudaStream_t st);
 cudaError_t launch_attn_combine(const AttnArgs& a, cudaStream_t st);
+// tcgen05 doc attention for 128-row query tiles (attention_tc.cu); row_tile must be 128.
+cudaError_t launch_attn_doc_tc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV, cudaStream_t st);
 
 }  // namespace quail
