@@ -190,7 +190,8 @@ AttnShape attn_shape(const quail_model_desc* m, int nq, int slots, int max_doc_l
     s.split_tokens = (items >= 6L * sms) ? std::min(whole, 4096) : std::min(whole, 512);
   } else {
     // Many rows: tcgen05 kernel on 128-row tiles, one CTA per SM. Split the
-    // documents only as far as needed for about three CTAs per SM.
+    // documents (in whole 128-key blocks) only as far as needed for about
+    // three waves of CTAs.
     s.tc = true;
     s.row_tile = 128;
     s.rows_pad = static_cast<int>(round_up(s.rows_per_kv, 128));
@@ -199,7 +200,7 @@ AttnShape attn_shape(const quail_model_desc* m, int nq, int slots, int max_doc_l
     int split = std::min(whole, 4096);
     if (items < want) {
       const long parts = (want + items - 1) / items;
-      split = static_cast<int>(round_up((max_doc_len + parts - 1) / parts, 64));
+      split = static_cast<int>(round_up((max_doc_len + parts - 1) / parts, 128));
       split = std::max(256, std::min(split, 4096));
     }
     s.split_tokens = split;

@@ -2,17 +2,26 @@
 // thousands of evaluated trie nodes x G query heads). Same math as
 // attn_doc_kernel in attention.cu ("To Classify, Try a Trie Tree", sec. 3.2:
 // every evaluated node attends to the document; the tree part and the merge
-// are shared), but a CTA owns a 128-row query tile and the two products run on
+// are shared), but a CTA owns a 128-row query tile and both products run on
 // the 5th-generation tensor cores with fp32 accumulators in TMEM:
-//   S   = Q_hi K^T + Q_lo K^T          (M 128 rows, N 64 keys, K 128 dims)
-//   O  += P_hi V   + P_lo V            (M 128 rows, N 128 dims, K 64 keys)
-// per block of 64 keys (4 pages). Q and P are two-term bf16 splits (as in the
-// mma.sync path); K comes from the TMA page ring as a K-major operand and V,
-// unchanged, as an MN-major one (dims contiguous).
+//   S_b  = Q_hi K^T + Q_lo K^T      (M 128 rows, N 128 keys, K 128 dims)
+//   O   += P_hi V   + P_lo V        (M 128 rows, N 128 dims, K 128 keys)
+// per block of 128 keys (8 pages). Q and P are two-term bf16 splits (as in
+// the mma.sync path) and both live in TMEM as the A operand: Q once per CTA,
+// P written by the softmax over the S block it was computed from. K and V come
+// from two TMA page rings (K-major K, MN-major V), so shared memory holds
+// nothing but keys and values.
 //
-// Roles (192 threads): warp 0 loads pages with TMA, warp 1 owns TMEM and issues
-// the MMAs, warps 2..5 (one thread per query row) build Q, run the softmax
-// (lazy reference max, as in attention.cu), write P, and finish the rows.
+// An M=128, K=16 MMA costs max(64, N/2) cycles on this part, so both products
+// use N = 128; per 128-key block the tensor pipe is busy 2 x 16 x 64 cycles.
+// MMAs are issued in pairs S(j) S(j+1) PV(j) PV(j+1): the softmax of block j
+// runs under S(j+1) and that of j+1 under PV(j), and S(j+2) (which reuses the
+// TMEM columns of P(j)) waits for PV(j) while PV(j+1) keeps the pipe busy.
+//
+// Roles (352 threads): warp 0 loads K pages, warp 1 owns TMEM and issues the
+// MMAs, warp 2 loads V pages, warps 3..10 (two warpgroups; each thread one
+// query row and half of every key block / of O's columns) build Q, run the
+// softmax (lazy reference max, as in attention.cu), write P and finish rows.
 #include "attn_common.cuh"
 #include "kernels.h"
 #include "quail_internal.h"
@@ -22,52 +31,118 @@ namespace quail {
 
 namespace {
 
-constexpr int kTcThreads = 192;
+constexpr int kTcSoftmaxWarps = 8;
+constexpr int kTcThreads = 32 * (3 + kTcSoftmaxWarps);
 constexpr int kTcRows = 128;
-constexpr int kTcBlkKeys = 64;                    // keys per block = 4 pages
-constexpr int kTcStages = 3;
-constexpr int kTcMaxPages = 256;                  // split_tokens <= 4096
-constexpr uint32_t kTcQPart = 2 * 128 * 128;      // 32 KB: 2 dim-halves x 128 rows x 128 B
-constexpr uint32_t kTcKVHalf = kTcBlkKeys * 128;  // 8 KB: 64 keys x 128 B
-constexpr uint32_t kTcStage = 4 * kTcKVHalf;      // K lo|hi, V lo|hi = 32 KB
-constexpr uint32_t kTcPPart = 128 * 128;          // 16 KB: 128 rows x 64 keys x 2 B
-constexpr uint32_t kOffKV = 2 * kTcQPart;
-constexpr uint32_t kOffP = kOffKV + kTcStages * kTcStage;
-constexpr uint32_t kOffBar = kOffP + 2 * kTcPPart;
-constexpr size_t kTcSmem = 1024 + kOffBar + 256 + kTcMaxPages * 4;
-constexpr uint32_t kTmemCols = 256;  // S double buffer (2 x 64) + O (128)
-constexpr uint32_t kTmemO = 128;
+constexpr int kTcBlkKeys = 128;                // keys per block = 8 pages
+constexpr int kTcBlkPages = kTcBlkKeys / 16;
+constexpr int kTcStages = 3;                   // per ring
+constexpr int kTcMaxPages = 256;               // split_tokens <= 4096
+constexpr uint32_t kTcHalf = kTcBlkKeys * 128;  // 16 KB: 128 keys x 64 dims (128 B rows, 128B swizzle)
+constexpr uint32_t kTcStage = 2 * kTcHalf;      // dims 0..63 | dims 64..127
+constexpr uint32_t kOffK = 0;
+constexpr uint32_t kOffV = kOffK + kTcStages * kTcStage;
+constexpr uint32_t kOffBar = kOffV + kTcStages * kTcStage;
+constexpr uint32_t kOffPages = kOffBar + 256;
+constexpr uint32_t kOffX = kOffPages + kTcMaxPages * 4;  // softmax exchange: 3 KB
+constexpr size_t kTcSmem = 1024 + kOffX + 3 * 1024;
+constexpr uint32_t kTmemCols = 512;  // S/P buffers 0..127, 128..255 | O 256..383 | Q hi 384..447, lo 448..511
+constexpr uint32_t kTmemO = 256;
+constexpr uint32_t kTmemQ = 384;  // column c of lane r: (q[r][2c], q[r][2c+1]) as bf16x2
 
-// 16-byte chunk c of row r in a 128B-swizzled region of 128-byte rows.
-__device__ __forceinline__ uint32_t sw_off(uint32_t r, uint32_t c) { return r * 128u + ((c ^ (r & 7u)) << 4); }
+struct TcBars {
+  uint64_t k_full[kTcStages], k_empty[kTcStages], v_full[kTcStages], v_empty[kTcStages];
+  uint64_t s_full[2];   // S_b complete (MMA commit)
+  uint64_t p_full[2];   // P_b written over S_b (256 softmax threads)
+  uint64_t pv_done[2];  // O += P_b V complete (MMA commit): P_b's columns and V's stage are free
+  uint64_t q_full, drain, xbar[2], lbar;
+  uint32_t tmem_slot;
+  int abort_flag;
+};
+static_assert(sizeof(TcBars) <= 256, "barrier block");
+static_assert(kTcSmem <= 227 * 1024, "shared memory");
+
+// D (+)= A * B^T with A in TMEM (M rows = lanes, K packed two bf16 per column)
+// and the B shared-memory descriptor given as its two 32-bit words.
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 bd;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 bd, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// One TMA page ring (K or V): block j's 8 pages into stage j % kTcStages, both
+// 64-dim halves, once the stage's previous block has been consumed.
+__device__ __forceinline__ void load_ring(uint8_t* ring, uint64_t* full, uint64_t* empty, const CUtensorMap* tm,
+                                          const int* s_pages, int n_pages, int n_blocks, const AttnArgs& a, int g,
+                                          int doc, volatile int* abort_flag) {
+  int armed[kTcStages];
+#pragma unroll
+  for (int s = 0; s < kTcStages; ++s) armed[s] = -1;
+  for (int blk = 0; blk < n_blocks; ++blk) {
+    const int s = blk % kTcStages;
+    const int use = blk / kTcStages;
+    if (use > 0 && !mbar_wait(&empty[s], static_cast<uint32_t>((use - 1) & 1), abort_flag)) break;
+    const int np = min(kTcBlkPages, n_pages - blk * kTcBlkPages);
+    int good = 0;
+    for (int q = 0; q < np; ++q) {
+      const int phys = s_pages[blk * kTcBlkPages + q];
+      good += (phys >= 0 && phys < a.num_pages) ? 1 : 0;
+    }
+    if (good < np) raise_device_error(a.err, QUAIL_ERR_DEVICE_BOUNDS, doc);
+    armed[s] = -1;
+    if (good == 0) {
+      mbar_arrive(&full[s]);  // release the consumer on stale data; results of this doc are void
+      continue;
+    }
+    uint8_t* st = ring + s * kTcStage;
+    mbar_arrive_expect_tx(&full[s], good * 2 * 2048);
+    for (int q = 0; q < np; ++q) {
+      const int phys = s_pages[blk * kTcBlkPages + q];
+      if (phys < 0 || phys >= a.num_pages) continue;
+      const int y = (phys * a.hkv + g) * 16;
+      tma_load_2d(st + q * 2048, tm, &full[s], 0, y);
+      tma_load_2d(st + kTcHalf + q * 2048, tm, &full[s], 64, y);
+    }
+    armed[s] = use & 1;
+  }
+  for (int s = 0; s < kTcStages; ++s) {  // no copy may still be landing when the CTA exits
+    if (armed[s] < 0) continue;
+    const uint32_t ad = smem_u32(&full[s]);
+    const long long t0 = clock64();
+    while (!mbar_try_wait(ad, static_cast<uint32_t>(armed[s]))) {
+      if (clock64() - t0 > kWaitLimitCycles) {
+        *abort_flag = 1;
+        break;
+      }
+    }
+  }
+}
 
 __global__ void __launch_bounds__(kTcThreads, 1)
     attn_doc_tc_kernel(AttnArgs a, RopeTable rt, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* kv_full = reinterpret_cast<uint64_t*>(base + kOffBar);
-  uint64_t* kv_empty = kv_full + kTcStages;
-  uint64_t* s_full = kv_empty + kTcStages;  // [2]
-  uint64_t* s_empty = s_full + 2;           // [2]
-  uint64_t* p_full = s_empty + 2;
-  uint64_t* p_empty = p_full + 1;
-  uint64_t* q_full = p_empty + 1;
-  uint64_t* drain = q_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* s_pages = reinterpret_cast<int*>(base + kOffBar + 256);
+  TcBars* bars = reinterpret_cast<TcBars*>(base + kOffBar);
+  volatile int* abort_flag = &bars->abort_flag;
+  int* s_pages = reinterpret_cast<int*>(base + kOffPages);
 
+  // grid: x = row tile (fastest, so the tiles that share a document's KV run
+  // together and re-read it from L2), y = split + n_splits * kv head, z = slot
   const int slot = blockIdx.z;
   if (a.map.n_slots_dev != nullptr && slot >= *a.map.n_slots_dev) return;
-  const int split = blockIdx.x;
-  const int row_tiles = a.rows_pad / kTcRows;
-  const int g = blockIdx.y / row_tiles;
-  const int rt_idx = blockIdx.y % row_tiles;
+  const int rt_idx = blockIdx.x;
+  const int split = blockIdx.y % a.n_splits;
+  const int g = blockIdx.y / a.n_splits;
   const int doc = row_doc(a.map, slot);
   const int L = a.doc_len[doc];
   if (L < 1 || L > a.max_doc_len) {
-    if (threadIdx.x == 0 && split == 0 && blockIdx.y == 0) raise_device_error(a.err, QUAIL_ERR_DEVICE_BOUNDS, doc);
+    if (threadIdx.x == 0 && split == 0 && blockIdx.x == 0 && g == 0) raise_device_error(a.err, QUAIL_ERR_DEVICE_BOUNDS, doc);
     return;
   }
   const int k_lo = split * a.split_tokens;
@@ -75,139 +150,126 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int k_hi = min(L, k_lo + a.split_tokens);
   const int p0 = k_lo / 16;
   const int n_pages = (k_hi - k_lo + 15) / 16;
-  const int n_blocks = (n_pages + 3) / 4;
+  const int n_blocks = (n_pages + kTcBlkPages - 1) / kTcBlkPages;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  {
+    const int* pt = a.page_table + static_cast<size_t>(doc) * a.max_pages;
+    for (int j = threadIdx.x; j < n_pages; j += kTcThreads) s_pages[j] = pt[p0 + j];
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTcStages; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&s_empty[b], 128);
+      mbar_init(&bars->s_full[b], 1);
+      mbar_init(&bars->p_full[b], 256);
+      mbar_init(&bars->pv_done[b], 1);
+      mbar_init(&bars->xbar[b], 256);
     }
-    mbar_init(p_full, 128);
-    mbar_init(p_empty, 1);
-    mbar_init(q_full, 128);
-    mbar_init(drain, 1);
+    mbar_init(&bars->q_full, 256);
+    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->lbar, 256);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_alloc(&bars->tmem_slot, kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t tmem_base = bars->tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------ page loader
-    const int* pt = a.page_table + static_cast<size_t>(doc) * a.max_pages;
-    for (int j = lane; j < n_pages; j += 32) s_pages[j] = pt[p0 + j];
-    __syncwarp();
+  if (warp == 0 || warp == 2) {
+    // ------------------------------------------------ page loaders (K: warp 0, V: warp 2)
     if (lane == 0) {
-      int armed[kTcStages];
-#pragma unroll
-      for (int s = 0; s < kTcStages; ++s) armed[s] = -1;
-      for (int blk = 0; blk < n_blocks; ++blk) {
-        const int s = blk % kTcStages;
-        const int use = blk / kTcStages;
-        if (use > 0 && !mbar_wait(&kv_empty[s], static_cast<uint32_t>((use - 1) & 1), abort_flag)) break;
-        const int np = min(4, n_pages - blk * 4);
-        int good = 0;
-        for (int q = 0; q < np; ++q) {
-          const int phys = s_pages[blk * 4 + q];
-          good += (phys >= 0 && phys < a.num_pages) ? 1 : 0;
-        }
-        if (good < np) raise_device_error(a.err, QUAIL_ERR_DEVICE_BOUNDS, doc);
-        armed[s] = -1;
-        if (good == 0) {
-          mbar_arrive(&kv_full[s]);  // release the consumer on stale data; results of this doc are void
-          continue;
-        }
-        uint8_t* st = base + kOffKV + s * kTcStage;
-        mbar_arrive_expect_tx(&kv_full[s], good * 4 * 2048);
-        for (int q = 0; q < np; ++q) {
-          const int phys = s_pages[blk * 4 + q];
-          if (phys < 0 || phys >= a.num_pages) continue;
-          const int y = (phys * a.hkv + g) * 16;
-          tma_load_2d(st + q * 2048, &tmK, &kv_full[s], 0, y);
-          tma_load_2d(st + kTcKVHalf + q * 2048, &tmK, &kv_full[s], 64, y);
-          tma_load_2d(st + 2 * kTcKVHalf + q * 2048, &tmV, &kv_full[s], 0, y);
-          tma_load_2d(st + 3 * kTcKVHalf + q * 2048, &tmV, &kv_full[s], 64, y);
-        }
-        armed[s] = use & 1;
-      }
-      for (int s = 0; s < kTcStages; ++s) {  // no copy may still be landing when the CTA exits
-        if (armed[s] < 0) continue;
-        const uint32_t ad = smem_u32(&kv_full[s]);
-        const long long t0 = clock64();
-        while (!mbar_try_wait(ad, static_cast<uint32_t>(armed[s]))) {
-          if (clock64() - t0 > kWaitLimitCycles) {
-            *abort_flag = 1;
-            break;
-          }
-        }
-      }
+      if (warp == 0)
+        load_ring(base + kOffK, bars->k_full, bars->k_empty, &tmK, s_pages, n_pages, n_blocks, a, g, doc, abort_flag);
+      else
+        load_ring(base + kOffV, bars->v_full, bars->v_empty, &tmV, s_pages, n_pages, n_blocks, a, g, doc, abort_flag);
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
+    // Issues S(j) as soon as K_j has landed and buffer j % 2 is free (PV(j - 2)
+    // done), and PV(j) as soon as the softmax has written P_j: whichever is
+    // ready first, so the tensor pipe never idles behind a fixed order while
+    // the softmax of the other buffer is still running.
     if (lane == 0) {
       constexpr uint32_t idesc_s = umma_idesc_bf16_f32(kTcRows, kTcBlkKeys);
       constexpr uint32_t idesc_pv = umma_idesc_bf16_f32_bmn(kTcRows, 128);
-      const uint32_t q_addr = smem_u32(base);
-      const uint32_t p_addr = smem_u32(base + kOffP);
-      // O += (P_hi + P_lo) V for block j, once the softmax has written P_j.
-      auto issue_pv = [&](int j) -> bool {
-        if (!mbar_wait(p_full, static_cast<uint32_t>(j & 1), abort_flag)) return false;
-        tc_fence_after();
-        const int s = j % kTcStages;
-        const uint32_t v_addr = smem_u32(base + kOffKV + s * kTcStage + 2 * kTcKVHalf);
+      // descriptors as two 32-bit words; stepping the start address (bits
+      // 0..13, in 16-byte units, addresses < 256 KB) is a 32-bit add
+      const uint64_t dk = smem_desc_sw128(smem_u32(base + kOffK));
+      const uint64_t dv = smem_desc_sw128_mn(smem_u32(base + kOffV), kTcHalf, 1024);
+      const uint32_t dk_lo = static_cast<uint32_t>(dk), dk_hi = static_cast<uint32_t>(dk >> 32);
+      const uint32_t dv_lo = static_cast<uint32_t>(dv), dv_hi = static_cast<uint32_t>(dv >> 32);
+      auto issue_s = [&](int j) {
+        const int s = j % kTcStages, b = j & 1;
+        const uint32_t k_lo = dk_lo + ((s * kTcStage) >> 4);
+        const uint32_t d = tmem_base + b * kTcBlkKeys, aq = tmem_base + kTmemQ;
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {  // 16 keys = one page per instruction
-            umma_bf16(tmem_base + kTmemO, smem_desc_sw128(p_addr + part * kTcPPart + kk * 32),
-                      smem_desc_sw128_mn(v_addr + kk * 2048, kTcKVHalf, 1024), idesc_pv,
-                      (j > 0 || part > 0 || kk > 0) ? 1u : 0u);
-          }
+          for (int ks = 0; ks < 8; ++ks)  // 16 dims per instruction; dims 0..63 in half 0
+            umma_ts(d, aq + part * 64 + ks * 8, k_lo + (((ks >> 2) * kTcHalf + (ks & 3) * 32) >> 4), dk_hi, idesc_s,
+                    (part | ks) != 0 ? 1u : 0u);
         }
-        umma_commit(p_empty);
-        umma_commit(&kv_empty[s]);
-        return true;
+        umma_commit(&bars->s_full[b]);
+        umma_commit(&bars->k_empty[s]);
       };
-      bool ok = mbar_wait(q_full, 0u, abort_flag);
-      if (ok) tc_fence_after();
-      for (int blk = 0; blk < n_blocks && ok; ++blk) {
-        const int s = blk % kTcStages;
-        const int sb = blk & 1;
-        if (!mbar_wait(&kv_full[s], static_cast<uint32_t>((blk / kTcStages) & 1), abort_flag) ||
-            (blk >= 2 && !mbar_wait(&s_empty[sb], static_cast<uint32_t>(((blk >> 1) - 1) & 1), abort_flag))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t k_addr = smem_u32(base + kOffKV + s * kTcStage);
+      // O += (P_hi + P_lo) V_j with P_j read from the columns of S_b: keys
+      // 64w..64w+63 were written by softmax warpgroup w, hi at +64w, lo at +64w+32.
+      auto issue_pv = [&](int j) {
+        const int s = j % kTcStages, b = j & 1;
+        const uint32_t v_lo = dv_lo + ((s * kTcStage) >> 4);
+        const uint32_t ap = tmem_base + b * kTcBlkKeys, d = tmem_base + kTmemO;
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {  // 16 dims per instruction; dims 0..63 in half 0
-            umma_bf16(tmem_base + sb * kTcBlkKeys,
-                      smem_desc_sw128(q_addr + part * kTcQPart + (ks >> 2) * 16384 + (ks & 3) * 32),
-                      smem_desc_sw128(k_addr + (ks >> 2) * kTcKVHalf + (ks & 3) * 32), idesc_s,
-                      (part | ks) != 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < 8; ++kk)  // 16 keys = one page per instruction
+            umma_ts(d, ap + (kk >> 2) * 64 + part * 32 + (kk & 3) * 8, v_lo + ((kk * 2048) >> 4), dv_hi, idesc_pv,
+                    (j > 0 || part > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(&s_full[sb]);
-        if (blk >= 1 && !issue_pv(blk - 1)) ok = false;
+        umma_commit(&bars->pv_done[b]);
+        umma_commit(&bars->v_empty[s]);
+      };
+      bool ok = mbar_wait(&bars->q_full, 0u, abort_flag);
+      if (ok) tc_fence_after();
+      int js = 0, jp = 0;  // next S, next PV
+      long long t_idle = clock64();
+      while (ok && jp < n_blocks) {
+        bool progressed = false;
+        if (jp < js && mbar_try_wait(smem_u32(&bars->p_full[jp & 1]), static_cast<uint32_t>((jp >> 1) & 1)) &&
+            mbar_try_wait(smem_u32(&bars->v_full[jp % kTcStages]), static_cast<uint32_t>((jp / kTcStages) & 1))) {
+          tc_fence_after();
+          issue_pv(jp++);
+          progressed = true;
+        }
+        if (js < n_blocks && js < jp + 2 &&
+            mbar_try_wait(smem_u32(&bars->k_full[js % kTcStages]), static_cast<uint32_t>((js / kTcStages) & 1)) &&
+            (js < 2 ||
+             mbar_try_wait(smem_u32(&bars->pv_done[js & 1]), static_cast<uint32_t>(((js - 2) >> 1) & 1)))) {
+          tc_fence_after();
+          issue_s(js++);
+          progressed = true;
+        }
+        if (progressed) {
+          t_idle = clock64();
+        } else if (*abort_flag) {
+          ok = false;
+        } else if (clock64() - t_idle > kWaitLimitCycles) {
+          *abort_flag = 1;
+          ok = false;
+        }
       }
-      if (ok && n_blocks >= 1) issue_pv(n_blocks - 1);
       // Drain: all MMAs issued by this thread complete before TMEM is released.
-      umma_commit(drain);
-      const uint32_t ad = smem_u32(drain);
+      umma_commit(&bars->drain);
+      const uint32_t ad = smem_u32(&bars->drain);
       const long long t0 = clock64();
       while (!mbar_try_wait(ad, 0u)) {
         if (clock64() - t0 > kWaitLimitCycles) {
@@ -217,10 +279,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
   } else {
-    // ------------------------------------------------ softmax warps: one thread per query row
+    // ------------------------------------------------ softmax warps
+    // Two warpgroups: wg 0 takes keys 0..63 of every block and O columns
+    // 0..63, wg 1 keys 64..127 and columns 64..127. Warp w reaches TMEM lanes
+    // 32 (w % 4) .. +31, so thread (wg, row) <-> TMEM lane row.
+    const int wg = (warp - 3) >> 2;
     const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;  // TMEM lane of this row
+    const int row = quarter * 32 + lane;
+    const int sthr = wg * 128 + row;  // 0..255
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+    float* xmax = reinterpret_cast<float*>(base + kOffX);  // [2 buffers][2 halves][128 rows]
+    float* xl = xmax + 512;                                // [2 halves][128 rows]
     const int G = a.hq / a.hkv;
     const int rows_per_kv = (a.map.slot_node ? 1 : a.map.nq) * G;
     const int rr = rt_idx * kTcRows + row;
@@ -231,129 +300,165 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       h = g * G + rr % G;
       node = row_node(a.map, slot, e);
     }
-    // Q row: RoPE at l_i + depth, two-term bf16 split, K-major 128B-swizzled.
+    // Q row into TMEM: RoPE at l_i + depth, two-term bf16 split; warpgroup 0
+    // builds dims 0..63, warpgroup 1 dims 64..127 (the two outputs of each
+    // rotate-half pair), column c of a half holding dims (2c, 2c + 1). The
+    // row is read with 16-byte loads, issued together per 32 dims.
     {
-      const float* q = row_ok ? a.qkv + static_cast<size_t>(node) * a.ldq + h * 128 : nullptr;
+      const float4* q4 =
+          row_ok ? reinterpret_cast<const float4*>(a.qkv + static_cast<size_t>(node) * a.ldq + h * 128) : nullptr;
       const int pos = row_ok ? L + a.node_depth[node] : 0;
-#pragma unroll 1
-      for (int c = 0; c < 8; ++c) {  // dims 8c..8c+7 (half 0) and 64+8c.. (half 1)
-        uint32_t h0[4], l0[4], h1[4], l1[4];
+      float hi[32], lo[32];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float y[4] = {0.f, 0.f, 0.f, 0.f};  // dims j, j+1 and j+64, j+65
-          if (row_ok) {
+      for (int half = 0; half < 2; ++half) {  // dims j = 32 half .. 32 half + 31 and j + 64
+        float4 x1[8], x2[8];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int j = c * 8 + 2 * i + u;
-              float cs, sn;
-              rope_cs(pos, rt.w[j], cs, sn);
-              const float x1 = q[j], x2 = q[j + 64];
-              y[u] = x1 * cs - x2 * sn;
-              y[2 + u] = x2 * cs + x1 * sn;
-            }
-          }
-          split_bf16(y[0], y[1], h0[i], l0[i]);
-          split_bf16(y[2], y[3], h1[i], l1[i]);
+        for (int i = 0; i < 8; ++i) {
+          x1[i] = row_ok ? q4[half * 8 + i] : make_float4(0.f, 0.f, 0.f, 0.f);
+          x2[i] = row_ok ? q4[16 + half * 8 + i] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        const uint32_t off = sw_off(row, c);
-        *reinterpret_cast<uint4*>(base + off) = make_uint4(h0[0], h0[1], h0[2], h0[3]);
-        *reinterpret_cast<uint4*>(base + 16384 + off) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
-        *reinterpret_cast<uint4*>(base + kTcQPart + off) = make_uint4(l0[0], l0[1], l0[2], l0[3]);
-        *reinterpret_cast<uint4*>(base + kTcQPart + 16384 + off) = make_uint4(l1[0], l1[1], l1[2], l1[3]);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float* p1 = reinterpret_cast<const float*>(x1) + 2 * c;
+          const float* p2 = reinterpret_cast<const float*>(x2) + 2 * c;
+          float y[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            float cs, sn;
+            rope_cs(pos, rt.w[half * 32 + 2 * c + u], cs, sn);
+            y[u] = wg == 0 ? p1[u] * cs - p2[u] * sn : p2[u] * cs + p1[u] * sn;
+          }
+          uint32_t hv, lv;
+          split_bf16(y[0], y[1], hv, lv);
+          hi[half * 16 + c] = __uint_as_float(hv);
+          lo[half * 16 + c] = __uint_as_float(lv);
+        }
       }
-      fence_proxy_async_smem();
-      mbar_arrive(q_full);
+      tmem_st_32cols(lane_addr + kTmemQ + wg * 32, hi);
+      tmem_st_32cols(lane_addr + kTmemQ + 64 + wg * 32, lo);
+      tc_fence_before();
+      mbar_arrive(&bars->q_full);
     }
     const float scale = kAttnLog2e * 0.08838834764831845f;  // log2(e) / sqrt(128)
-    float m_ref = -INFINITY, l_sum = 0.f;
+    float m_ref = -INFINITY, l_part = 0.f;
     bool ok = true;
 #pragma unroll 1
-    for (int blk = 0; blk < n_blocks; ++blk) {
-      const int sb = blk & 1;
-      const int s = blk % kTcStages;
-      // waits are made warp-uniform: the warp-collective tcgen05.ld / __any_sync
-      // below must never run with lanes that left the loop
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[sb], static_cast<uint32_t>((blk >> 1) & 1), abort_flag))) {
+    for (int j = 0; j < n_blocks; ++j) {
+      const int b = j & 1;
+      const uint32_t sp_col = b * kTcBlkKeys + wg * 64;  // this half's S columns, then its P columns
+      // waits are made warp-uniform: the warp-collective tcgen05.ld/st and
+      // __any_sync below must never run with lanes that left the loop
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[b], static_cast<uint32_t>((j >> 1) & 1), abort_flag))) {
         ok = false;
         break;
       }
       tc_fence_after();
       float s0[32], s1[32];
-      tmem_ld_32cols(lane_addr + sb * kTcBlkKeys, s0);
-      tmem_ld_32cols(lane_addr + sb * kTcBlkKeys + 32, s1);
-      tc_fence_before();
-      mbar_arrive(&s_empty[sb]);
-      const int valid = min(kTcBlkKeys, k_hi - (k_lo + blk * kTcBlkKeys));
-      float mx = -INFINITY;
+      tmem_ld_32cols(lane_addr + sp_col, s0);
+      tmem_ld_32cols(lane_addr + sp_col + 32, s1);
+      const int valid = min(kTcBlkKeys, k_hi - (k_lo + j * kTcBlkKeys)) - wg * 64;  // keys of this half
+      if (valid < 64) {  // last block only: keys past the document end
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        s0[i] = i < valid ? s0[i] * scale : -INFINITY;
-        s1[i] = i + 32 < valid ? s1[i] * scale : -INFINITY;
-        mx = fmaxf(mx, fmaxf(s0[i], s1[i]));
+        for (int i = 0; i < 32; ++i) {
+          s0[i] = i < valid ? s0[i] : -INFINITY;
+          s1[i] = i + 32 < valid ? s1[i] : -INFINITY;
+        }
       }
-      // PV of the previous block must be done before P is overwritten (and O rescaled).
-      if (blk >= 1 &&
-          !__all_sync(0xffffffffu, mbar_wait(p_empty, static_cast<uint32_t>((blk - 1) & 1), abort_flag))) {
+      float mraw = -INFINITY;  // max of the raw scores; the scale is positive
+#pragma unroll
+      for (int i = 0; i < 32; ++i) mraw = fmaxf(mraw, fmaxf(s0[i], s1[i]));
+      // row max over both halves (double-buffered exchange; bounded waits only,
+      // so an aborted peer cannot hang this CTA)
+      xmax[(b * 2 + wg) * 128 + row] = mraw;
+      mbar_arrive(&bars->xbar[b]);
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->xbar[b], static_cast<uint32_t>((j >> 1) & 1), abort_flag))) {
         ok = false;
         break;
       }
+      mraw = fmaxf(mraw, xmax[(b * 2 + (wg ^ 1)) * 128 + row]);
+      const float mx = mraw * scale;
       // Lazy reference max (see attention.cu): moves only past +8 in base 2.
+      // Both halves of a row see the same maxima, so they move it together.
       const bool need = mx > m_ref + 8.f;
       float alpha = 1.f;
       if (need) {
         const float nm = fmaxf(m_ref, mx);
         alpha = exp2f(m_ref - nm);
         m_ref = nm;
-        l_sum *= alpha;
+        l_part *= alpha;
       }
-      if (blk >= 1 && __any_sync(0xffffffffu, need)) {
+      if (j >= 1 && __any_sync(0xffffffffu, need)) {
+        // O must hold every PV up to block j - 1 before it is rescaled
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[(j - 1) & 1],
+                                               static_cast<uint32_t>(((j - 1) >> 1) & 1), abort_flag))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {  // this warpgroup's 64 columns of O
           float o[32];
-          tmem_ld_32cols(lane_addr + kTmemO + c * 32, o);
+          const uint32_t col = kTmemO + wg * 64 + c * 32;
+          tmem_ld_32cols(lane_addr + col, o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] *= alpha;
-          tmem_st_32cols(lane_addr + kTmemO + c * 32, o);
+          tmem_st_32cols(lane_addr + col, o);
         }
       }
-      // P = exp2(s - m_ref) as a two-term bf16 split, K-major 128B-swizzled rows.
+      // P = exp2(s * scale - m_ref) as a two-term bf16 split, written over this
+      // half's S columns: hi in the first 32, lo in the last 32 (keys 2c, 2c+1
+      // in column c), the A operand layout of the PV product.
       float psum = 0.f;
-      uint8_t* prow = base + kOffP;
+      {
+        float ph[32], pl[32];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t ph[4], pl[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float x0 = c < 4 ? s0[c * 8 + 2 * i] : s1[(c - 4) * 8 + 2 * i];
-          const float x1 = c < 4 ? s0[c * 8 + 2 * i + 1] : s1[(c - 4) * 8 + 2 * i + 1];
-          const float e0 = exp2f(x0 - m_ref), e1 = exp2f(x1 - m_ref);
+        for (int c = 0; c < 32; ++c) {
+          const float x0 = c < 16 ? s0[2 * c] : s1[2 * c - 32];
+          const float x1 = c < 16 ? s0[2 * c + 1] : s1[2 * c - 31];
+          const float e0 = fast_exp2(fmaf(x0, scale, -m_ref));
+          const float e1 = fast_exp2(fmaf(x1, scale, -m_ref));
           psum += e0 + e1;
-          split_bf16(e0, e1, ph[i], pl[i]);
+          uint32_t hv, lv;
+          split_bf16(e0, e1, hv, lv);
+          ph[c] = __uint_as_float(hv);
+          pl[c] = __uint_as_float(lv);
         }
-        const uint32_t off = sw_off(row, c);
-        *reinterpret_cast<uint4*>(prow + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-        *reinterpret_cast<uint4*>(prow + kTcPPart + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+        tmem_st_32cols(lane_addr + sp_col, ph);
+        tmem_st_32cols(lane_addr + sp_col + 32, pl);
       }
-      l_sum += psum;
+      l_part += psum;
       // Keys past the document end (tail of the last page, pages not loaded):
       // zero their V rows so stale contents cannot reach O through P = 0.
-      if (valid < kTcBlkKeys) {
-        uint8_t* vst = base + kOffKV + s * kTcStage + 2 * kTcKVHalf;
-        const int t = threadIdx.x - 64;  // 0..127
-        for (int idx = t; idx < (kTcBlkKeys - valid) * 16; idx += 128) {
-          const int r = valid + idx / 16, hc = idx % 16;
-          *reinterpret_cast<uint4*>(vst + (hc / 8) * kTcKVHalf + r * 128 + (hc % 8) * 16) = make_uint4(0, 0, 0, 0);
+      const int vblk = min(kTcBlkKeys, k_hi - (k_lo + j * kTcBlkKeys));
+      if (vblk < kTcBlkKeys) {
+        const int s = j % kTcStages;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->v_full[s], static_cast<uint32_t>((j / kTcStages) & 1),
+                                               abort_flag))) {
+          ok = false;
+          break;
         }
+        uint8_t* vst = base + kOffV + s * kTcStage;
+        for (int idx = sthr; idx < (kTcBlkKeys - vblk) * 16; idx += 256) {
+          const int r = vblk + idx / 16, hc = idx % 16;
+          *reinterpret_cast<uint4*>(vst + (hc / 8) * kTcHalf + r * 128 + (hc % 8) * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
       }
-      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&bars->p_full[b]);
     }
     // Row epilogue once the last PV has landed in TMEM.
-    if (ok && n_blocks > 0 &&
-        __all_sync(0xffffffffu, mbar_wait(p_empty, static_cast<uint32_t>((n_blocks - 1) & 1), abort_flag))) {
+    if (ok && __all_sync(0xffffffffu, mbar_wait(&bars->pv_done[(n_blocks - 1) & 1],
+                                                static_cast<uint32_t>(((n_blocks - 1) >> 1) & 1), abort_flag))) {
       tc_fence_after();
+      xl[wg * 128 + row] = l_part;
+      mbar_arrive(&bars->lbar);
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->lbar, 0u, abort_flag));
+    } else {
+      ok = false;
+    }
+    if (ok) {
+      const float l_sum = l_part + xl[(wg ^ 1) * 128 + row];
       const bool fused = a.n_splits == 1;
       float f1 = 1.f, f2 = 0.f, inv = 1.f;
       const float* to = nullptr;
@@ -371,21 +476,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const size_t pr =
             ((static_cast<size_t>(slot) * a.hkv + g) * a.n_splits + split) * static_cast<size_t>(a.rows_pad) + rr;
         pdst = a.part_o + pr * 128;
-        a.part_ml[pr] = make_float2(m_ref, l_sum);
+        if (wg == 0) a.part_ml[pr] = make_float2(m_ref, l_sum);
       }
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = wg * 2; c < wg * 2 + 2; ++c) {  // this warpgroup's 64 columns of O, 32 at a time
+        float4 t4[8];
+        if (dst != nullptr) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) t4[i] = reinterpret_cast<const float4*>(to + c * 32)[i];
+        }
         float o[32];
         tmem_ld_32cols(lane_addr + kTmemO + c * 32, o);
         if (dst != nullptr) {
+          const float* tv = reinterpret_cast<const float*>(t4);
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {
             uint32_t hv[4], lv[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              const int col = c * 32 + i + 2 * u;
-              split_bf16((f1 * o[i + 2 * u] + f2 * to[col]) * inv, (f1 * o[i + 2 * u + 1] + f2 * to[col + 1]) * inv,
-                         hv[u], lv[u]);
+              const int k = i + 2 * u;
+              split_bf16((f1 * o[k] + f2 * tv[k]) * inv, (f1 * o[k + 1] + f2 * tv[k + 1]) * inv, hv[u], lv[u]);
             }
             *reinterpret_cast<uint4*>(dst + c * 32 + i) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
             *reinterpret_cast<uint4*>(dst + a.hq * 128 + c * 32 + i) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
@@ -410,10 +520,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 }  // namespace
 
-}  // namespace quail
-
-namespace quail {
-
 size_t attn_tc_smem_bytes() { return kTcSmem; }
 
 cudaError_t launch_attn_doc_tc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV, cudaStream_t st) {
@@ -427,8 +533,11 @@ cudaError_t launch_attn_doc_tc(const AttnArgs& a, const CUtensorMap& tmK, const 
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  dim3 grid(a.n_splits, a.hkv * (a.rows_pad / kTcRows), a.n_slots);
-  if (grid.x == 0 || grid.z == 0) return cudaSuccess;
+  if (a.row_tile != kTcRows || a.rows_pad % kTcRows != 0 || a.split_tokens > 16 * kTcMaxPages ||
+      a.split_tokens % 16 != 0)
+    return cudaErrorInvalidValue;
+  dim3 grid(a.rows_pad / kTcRows, a.n_splits * a.hkv, a.n_slots);
+  if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
   attn_doc_tc_kernel<<<grid, kTcThreads, kTcSmem, st>>>(a, make_rope_table(a.theta), tmK, tmV);
   return cudaGetLastError();
 }

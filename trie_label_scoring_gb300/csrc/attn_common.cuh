@@ -48,7 +48,15 @@ __device__ __forceinline__ void rope_cs(int pos, float2 w, float& c, float& s) {
   float r = fmaf(-k, 6.28318548202514648f, a);  // 2*pi rounded to float
   r = fmaf(-k, -1.7484556000744487e-07f, r);    // 2*pi - float(2*pi)
   r += b;
-  sincosf(r, &s, &c);
+  __sincosf(r, &s, &c);  // |r| <= pi + tiny: hardware sin/cos, absolute error ~4e-7
+}
+
+// 2^x with flush-to-zero (one MUFU op); used where x <= 8 and tiny results
+// are negligible (softmax weights).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ int row_doc(const RowMap& m, int slot) { return m.slot_doc ? m.slot_doc[slot] : slot; }
