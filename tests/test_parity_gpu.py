@@ -87,6 +87,44 @@ def _resize_docs(docs, lens, w):
     return S.PagedDocs(np.array(lens, dtype=np.int32), pt, k, v)
 
 
+def _tiny_tree(num_docs, doc_len, num_labels=60):
+    return S.Workload(f"tiny-tree{num_labels}-{num_docs}", S.TINY, num_docs, doc_len, "tree", num_labels, (1, 5))
+
+
+def _rows_per_kv(w, ls):
+    from oracle.trie import build_trie
+    t = build_trie(ls.labels, ls.root_token, w.shape.vocab, ls.continuation)
+    return t["n_eval"] * (w.shape.n_q_heads // w.shape.n_kv_heads)
+
+
+def test_trie_tree_tc_path_tiny_ragged_split():
+    """More than 128 query rows per KV head (the tcgen05 attention, two row
+    tiles, the second partial) on documents split across CTAs (partials and
+    the combine kernel), lengths around page and 128-key block boundaries."""
+    w = _tiny_tree(8, (1, 1000))
+    ls = S.make_labels(w, 5)
+    assert _rows_per_kv(w, ls) > 128
+    lens = np.array([1, 15, 17, 127, 128, 129, 300, 1000], dtype=np.int32)
+    docs = _resize_docs(S.make_docs(w, 5), lens, w)
+    ls, docs, lsc, prob, am = _run_trie_tree(w, seed=5, labels=ls, docs=docs)
+    for i in range(w.num_docs):
+        r = _oracle_full(w, ls, docs, i, seed=5)
+        C.check_scores(lsc[i], prob[i], am[i], r["logscore"], r["prob"], r["argmax"], f"len {lens[i]}")
+
+
+def test_trie_tree_tc_path_tiny_fused_epilogue():
+    """Enough (document, KV head, row tile) items that every document is one
+    split: the tcgen05 attention merges the tree part in its epilogue."""
+    w = _tiny_tree(240, (100, 400))
+    ls = S.make_labels(w, 6)
+    assert _rows_per_kv(w, ls) > 128
+    ls, docs, lsc, prob, am = _run_trie_tree(w, seed=6, labels=ls)
+    assert np.all(np.abs(prob.sum(axis=1) - 1) < 1e-4)
+    for i in [0, 1, 97, 150, 239]:
+        r = _oracle_full(w, ls, docs, i, seed=6)
+        C.check_scores(lsc[i], prob[i], am[i], r["logscore"], r["prob"], r["argmax"], f"doc {i}")
+
+
 def test_trie_tree_prefix_labels_tiny():
     """Labels that are prefixes of other labels (prefix correction on the GPU)."""
     w = S.WORKLOADS["tiny-support10-4x128"]
