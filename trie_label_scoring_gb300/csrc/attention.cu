@@ -24,7 +24,7 @@ namespace {
 constexpr int kPage = 16;
 constexpr int kConsumerWarps = 4;
 constexpr int kAttnThreads = 160;  // warps 0..3 consume, warp 4 loads pages
-constexpr int kAttnStages = 8;     // multiple of kConsumerWarps
+constexpr int kAttnStages = 8;     // a multiple of kConsumerWarps: stage s is always read by warp s % 4
 constexpr uint32_t kHalfBytes = kPage * 64 * 2;   // 16 keys x 64 bf16, 128B-swizzled
 constexpr uint32_t kPageBytes = 4 * kHalfBytes;   // K[0:64) K[64:128) V[0:64) V[64:128)
 
@@ -109,8 +109,14 @@ __global__ void tree_part_kernel(AttnArgs a, RopeTable rt) {
 constexpr uint32_t kQTileBytes = 8 * 2 * 32 * 16;  // ks x {hi, lo} x lane x uint4
 constexpr int kMaxSplitPagesV2 = 256;              // split_tokens <= 4096
 
+// The four consumer warps merge their softmax states through the page ring
+// once every page has been consumed (16 rows x 128 dims + 32 floats each);
+// the ring region is sized to hold that merge too.
+constexpr uint32_t kMergeBytes = kConsumerWarps * (16 * 128 + 32) * 4;
+constexpr uint32_t kRingBytes = kAttnStages * kPageBytes > kMergeBytes ? kAttnStages * kPageBytes : kMergeBytes;
+static_assert(kAttnStages % kConsumerWarps == 0, "each stage must belong to one consumer warp");
 __host__ __device__ constexpr size_t attn_smem_bytes(int q_tiles) {
-  return 1024 + kAttnStages * kPageBytes + q_tiles * kQTileBytes + 2 * kAttnStages * 8 + 16 + kMaxSplitPagesV2 * 4;
+  return 1024 + kRingBytes + q_tiles * kQTileBytes + 2 * kAttnStages * 8 + 16 + kMaxSplitPagesV2 * 4;
 }
 
 __device__ __forceinline__ void mma_pair(float (&d0)[4], float (&d1)[4], const uint4& a, uint32_t b0, uint32_t b1,
@@ -136,7 +142,7 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
   const bool shared_rows = a.row_tile == 16;
   const int q_tiles = shared_rows ? 1 : kConsumerWarps;
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* s_q = base + kAttnStages * kPageBytes;
+  uint8_t* s_q = base + kRingBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(s_q + q_tiles * kQTileBytes);
   uint64_t* empty = full + kAttnStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kAttnStages);
@@ -228,36 +234,53 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
   // into hi/lo bf16 and scattered to their (ks, lane, register, half) slots.
   {
     uint16_t* sq16 = reinterpret_cast<uint16_t*>(s_q);
-    const int items = q_tiles * 16 * 64;
-    for (int it = t; it < items; it += kConsumerWarps * 32) {
-      const int qt = it / (16 * 64);
-      const int r = (it / 64) % 16;
-      const int j = it % 64;
-      const int rr = rg * a.row_tile + qt * 16 + r;  // row within (slot, kv head)
-      float y0 = 0.f, y1 = 0.f;
-      if (rr < rows_per_kv) {
-        const int e = rr / G, hl = rr % G;
-        const int node = row_node(a.map, slot, e);
-        const float* q = a.qkv + static_cast<size_t>(node) * a.ldq + (g * G + hl) * 128;
-        float c, sn;
-        rope_cs(L + a.node_depth[node], rt.w[j], c, sn);
-        const float x1 = q[j], x2 = q[j + 64];
-        y0 = x1 * c - x2 * sn;
-        y1 = x2 * c + x1 * sn;
-      }
-      const int col = j % 16;
-      const int reg = (r >= 8 ? 1 : 0) + (col >= 8 ? 2 : 0);
-      const int ln = (r % 8) * 4 + (col % 8) / 2;
-      const int half = col & 1;
+    constexpr int kPer = 16 * 64 / (kConsumerWarps * 32);  // items per thread and q tile
+    for (int qt = 0; qt < q_tiles; ++qt) {
+      // all loads of this thread's items first (one memory round trip), then
+      // rotate, split and scatter
+      float x1[kPer], x2[kPer];
+      int pos[kPer];
 #pragma unroll
-      for (int w = 0; w < 2; ++w) {  // dims j (ks = j / 16) and j + 64 (ks + 4)
-        const float y = w ? y1 : y0;
-        const int ks = j / 16 + 4 * w;
-        const __nv_bfloat16 hb = __float2bfloat16(y);
-        const __nv_bfloat16 lb = __float2bfloat16(y - __bfloat162float(hb));
-        const int idx = (((qt * 8 + ks) * 2 + 0) * 32 + ln) * 8 + reg * 2 + half;  // in bf16 units
-        sq16[idx] = *reinterpret_cast<const uint16_t*>(&hb);
-        sq16[idx + 32 * 8] = *reinterpret_cast<const uint16_t*>(&lb);
+      for (int k = 0; k < kPer; ++k) {
+        const int it = t + k * kConsumerWarps * 32;
+        const int r = it / 64, j = it % 64;
+        const int rr = rg * a.row_tile + qt * 16 + r;  // row within (slot, kv head)
+        x1[k] = x2[k] = 0.f;
+        pos[k] = -1;
+        if (rr < rows_per_kv) {
+          const int e = rr / G, hl = rr % G;
+          const int node = row_node(a.map, slot, e);
+          const float* q = a.qkv + static_cast<size_t>(node) * a.ldq + (g * G + hl) * 128;
+          x1[k] = q[j];
+          x2[k] = q[j + 64];
+          pos[k] = L + a.node_depth[node];
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int it = t + k * kConsumerWarps * 32;
+        const int r = it / 64, j = it % 64;
+        float y0 = 0.f, y1 = 0.f;
+        if (pos[k] >= 0) {
+          float c, sn;
+          rope_cs(pos[k], rt.w[j], c, sn);
+          y0 = x1[k] * c - x2[k] * sn;
+          y1 = x2[k] * c + x1[k] * sn;
+        }
+        const int col = j % 16;
+        const int reg = (r >= 8 ? 1 : 0) + (col >= 8 ? 2 : 0);
+        const int ln = (r % 8) * 4 + (col % 8) / 2;
+        const int half = col & 1;
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {  // dims j (ks = j / 16) and j + 64 (ks + 4)
+          const float y = w ? y1 : y0;
+          const int ks = j / 16 + 4 * w;
+          const __nv_bfloat16 hb = __float2bfloat16(y);
+          const __nv_bfloat16 lb = __float2bfloat16(y - __bfloat162float(hb));
+          const int idx = (((qt * 8 + ks) * 2 + 0) * 32 + ln) * 8 + reg * 2 + half;  // in bf16 units
+          sq16[idx] = *reinterpret_cast<const uint16_t*>(&hb);
+          sq16[idx + 32 * 8] = *reinterpret_cast<const uint16_t*>(&lb);
+        }
       }
     }
   }
@@ -457,15 +480,18 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
       const int e = r / G, h = g * G + r % G;
       const int node = row_node(a.map, slot, e);
       const float2 tml = a.tree_ml[static_cast<size_t>(node) * a.hq + h];
+      float tv[16];  // this thread's 16 dims of the tree part, loaded before any store
+      const float4* to = reinterpret_cast<const float4*>(a.tree_o + (static_cast<size_t>(node) * a.hq + h) * 128 + d0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) *reinterpret_cast<float4*>(tv + 4 * i) = to[i];
       const float M2 = fmaxf(M, tml.x);
       const float f1 = exp2f(M - M2), f2 = exp2f(tml.x - M2);
       const float inv = 1.f / (f1 * lsum + f2 * tml.y);
-      const float* to = a.tree_o + (static_cast<size_t>(node) * a.hq + h) * 128 + d0;
       const size_t orow = static_cast<size_t>(slot) * a.map.nq + e;
 #pragma unroll
       for (int i = 0; i < 16; i += 2)
-        store_o_split(a.out, a.hq, orow, h * 128 + d0 + i, (f1 * acc[i] + f2 * to[i]) * inv,
-                      (f1 * acc[i + 1] + f2 * to[i + 1]) * inv);
+        store_o_split(a.out, a.hq, orow, h * 128 + d0 + i, (f1 * acc[i] + f2 * tv[i]) * inv,
+                      (f1 * acc[i + 1] + f2 * tv[i + 1]) * inv);
     }
   }
   if (threadIdx.x == 0 && *abort_flag) raise_device_error(a.err, QUAIL_ERR_DEVICE_TIMEOUT, 2000 + slot);
