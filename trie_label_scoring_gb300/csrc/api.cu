@@ -651,7 +651,7 @@ quail_status quail_classify_trie_tree(const quail_model_desc* model, const quail
     CUtensorMap tA, tB;
     s = encode_2d_bf16(&tA, b.z, round_up(rows, 128), d, d, 64, 128);
     if (s != QUAIL_OK) return s;
-    s = encode_2d_bf16(&tB, model->lm_head, model->vocab, d, d, 64, 256);
+    s = encode_2d_bf16(&tB, model->lm_head, model->vocab, d, d, 64, kHeadBBoxRows);
     if (s != QUAIL_OK) return s;
     HeadEpilogueArgs ha{b.lse_part, b.child_logit, img->eval_child_offsets, img->eval_child_tokens, b.z_f32,
                         static_cast<const bf16*>(model->lm_head), d, a, n_child, n_tiles};
@@ -888,7 +888,7 @@ quail_status quail_classify_trie_tree_noalloc(const quail_model_desc* model, con
   CUtensorMap tA, tB;
   s = encode_2d_bf16(&tA, b.z, round_up(rows, 128), d, d, 64, 128);
   if (s != QUAIL_OK) return s;
-  s = encode_2d_bf16(&tB, model->lm_head, model->vocab, d, d, 64, 256);
+  s = encode_2d_bf16(&tB, model->lm_head, model->vocab, d, d, 64, kHeadBBoxRows);
   if (s != QUAIL_OK) return s;
   HeadEpilogueArgs ha{b.lse_part, b.child_logit, img.eval_child_offsets, img.eval_child_tokens, b.z_f32,
                       static_cast<const bf16*>(model->lm_head), d, a, n_child, n_tiles};

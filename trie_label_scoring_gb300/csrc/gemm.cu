@@ -15,6 +15,14 @@ constexpr int kProjStages = 3;  // 64 KB per stage (A_hi, A_lo, B)
 constexpr int kHeadStages = 4;  // 48 KB per stage
 constexpr float kLog2e = 1.4426950408889634f;
 
+// 2^x, one MUFU op with flush-to-zero: the summands of a log-sum-exp are
+// relative to the running maximum, so results below 2^-126 are negligible.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Per 128 x 256 accumulator tile and row: online max / sum of exp over the
 // valid columns (base-2 units: m2 = max * log2 e), from the tensor-core logits.
 // The child tokens of the row's node that fall inside the tile are gathered
@@ -99,9 +107,9 @@ struct EpiHead {
         }
       }
       const float nm = fmaxf(m2, cm);  // finite: column n0 of every tile is a real token
-      float acc = s * exp2f(m2 - nm);
+      float acc = s * fast_exp2(m2 - nm);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) acc += exp2f(v[i] - nm);
+      for (int i = 0; i < 32; ++i) acc += fast_exp2(v[i] - nm);
       m2 = nm;
       s = acc;
     }
@@ -109,11 +117,11 @@ struct EpiHead {
   }
 };
 
-template <int BN, int STAGES, bool SPLIT_A, class Epi>
+template <int BN, int STAGES, bool SPLIT_A, class Epi, int CM = 1>
 cudaError_t launch_umma(const CUtensorMap& tmA, const BSet& bset, int M, int N, int nk, int k_splits, const Epi& epi,
                         int num_sms, int* err, cudaStream_t st) {
   using Cfg = GemmCfg<BN, STAGES, SPLIT_A>;
-  auto kern = umma_gemm_kernel<BN, STAGES, SPLIT_A, Epi>;
+  auto kern = umma_gemm_kernel<BN, STAGES, SPLIT_A, Epi, CM>;
   static int configured_device = -1;  // the attribute is set per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -123,11 +131,28 @@ cudaError_t launch_umma(const CUtensorMap& tmA, const BSet& bset, int M, int N, 
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  const int units = ((M + kGemmBM - 1) / kGemmBM) * ((N + BN - 1) / BN) * k_splits;
-  const int grid = units < num_sms ? units : num_sms;
+  const int m_tiles = (M + kGemmBM - 1) / kGemmBM;
+  const int units = ((m_tiles + CM - 1) / CM * CM) * ((N + BN - 1) / BN) * k_splits;
+  int grid = units < num_sms ? units : num_sms;
+  grid = grid / CM * CM;  // whole clusters; units is a multiple of CM
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, kGemmThreads, Cfg::kSmemBytes, st>>>(tmA, bset, M, N, nk, k_splits, epi, err);
-  return cudaGetLastError();
+  if (CM == 1) {
+    kern<<<grid, kGemmThreads, Cfg::kSmemBytes, st>>>(tmA, bset, M, N, nk, k_splits, epi, err);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CM;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tmA, bset, M, N, nk, k_splits, epi, err);
 }
 
 }  // namespace
@@ -166,7 +191,7 @@ cudaError_t launch_gemm_head(const CUtensorMap& tmA, const CUtensorMap& tmB, int
   b.n_begin[0] = 0;
   b.n_begin[1] = V;
   b.count = 1;
-  return launch_umma<kHeadBN, kHeadStages, false>(tmA, b, M, V, K / kGemmBK, 1, epi, num_sms, err, st);
+  return launch_umma<kHeadBN, kHeadStages, false, EpiHead, 2>(tmA, b, M, V, K / kGemmBK, 1, epi, num_sms, err, st);
 }
 
 }  // namespace quail

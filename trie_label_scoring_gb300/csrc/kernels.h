@@ -42,6 +42,9 @@ struct HeadEpilogueArgs {
   int n_tiles;
 };
 constexpr int kHeadBN = 256;
+// The head runs on CTA pairs that share each 256-row band of W_lm: tmB's box is
+// 64 columns x kHeadBBoxRows rows (half a band, one per CTA, multicast to both).
+constexpr int kHeadBBoxRows = kHeadBN / 2;
 cudaError_t launch_gemm_head(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int V, int K,
                              const HeadEpilogueArgs& args, int num_sms, int* err, cudaStream_t st);
 

@@ -96,13 +96,20 @@ __global__ void qk_head_norm_kernel(const float* __restrict__ part, int k_splits
   if (warp >= rows * heads) return;
   const int r = warp / heads, h = warp % heads;
   const size_t off = static_cast<size_t>(r) * ld + h * 128 + lane * 4;
-  float4 v = *reinterpret_cast<const float4*>(part + off);
-  for (int s = 1; s < k_splits; ++s) {
-    const float4 w = *reinterpret_cast<const float4*>(part + s * slab + off);
-    v.x += w.x;
-    v.y += w.y;
-    v.z += w.z;
-    v.w += w.w;
+  // every slab's load issued before the first add (k_splits <= 8)
+  float4 w[8];
+#pragma unroll
+  for (int s = 0; s < 8; ++s)
+    if (s < k_splits) w[s] = *reinterpret_cast<const float4*>(part + s * slab + off);
+  float4 v = w[0];
+#pragma unroll
+  for (int s = 1; s < 8; ++s) {
+    if (s < k_splits) {
+      v.x += w[s].x;
+      v.y += w[s].y;
+      v.z += w[s].z;
+      v.w += w[s].w;
+    }
   }
   if (h < hq + hkv) {
     const float inv = rsqrtf(warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w) / 128.f + eps);
@@ -117,8 +124,9 @@ __global__ void qk_head_norm_kernel(const float* __restrict__ part, int k_splits
 
 // Block per row: h = x + sum of the k-split slabs, kept in registers; z in bf16
 // (and fp32 when z_f32 is given). float4 / 8-byte vector accesses.
-__global__ void __launch_bounds__(kNormThreads) final_norm_kernel(const float* __restrict__ h_part, int k_splits,
-                                                                  size_t slab, const bf16* __restrict__ embed,
+template <int KS>
+__global__ void __launch_bounds__(kNormThreads) final_norm_kernel(const float* __restrict__ h_part, size_t slab,
+                                                                  const bf16* __restrict__ embed,
                                                                   const int* __restrict__ node_token, RowMap map,
                                                                   int d, const bf16* __restrict__ gain, float eps,
                                                                   bf16* __restrict__ z_bf16,
@@ -132,6 +140,8 @@ __global__ void __launch_bounds__(kNormThreads) final_norm_kernel(const float* _
   const float4* hp = reinterpret_cast<const float4*>(h_part + static_cast<size_t>(r) * d);
   const size_t slab4 = slab >> 2;
   const int nv = d >> 2;
+  // per vector: the residual and the KS k-split slabs are loaded together
+  // (one memory round trip), then summed
   float4 v[kNormMaxVec];
   float ss = 0.f;
 #pragma unroll
@@ -139,13 +149,16 @@ __global__ void __launch_bounds__(kNormThreads) final_norm_kernel(const float* _
     const int c = threadIdx.x + i * kNormThreads;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
     if (c < nv) {
+      float4 p[KS];
+#pragma unroll
+      for (int s = 0; s < KS; ++s) p[s] = hp[s * slab4 + c];
       a = bf16x4_to_float4(__ldg(x + c));
-      for (int s = 0; s < k_splits; ++s) {
-        const float4 p = hp[s * slab4 + c];
-        a.x += p.x;
-        a.y += p.y;
-        a.z += p.z;
-        a.w += p.w;
+#pragma unroll
+      for (int s = 0; s < KS; ++s) {
+        a.x += p[s].x;
+        a.y += p[s].y;
+        a.z += p[s].z;
+        a.w += p[s].w;
       }
     }
     v[i] = a;
@@ -423,6 +436,7 @@ cudaError_t launch_qk_head_norm(const float* part, int k_splits, size_t slab, fl
                                 int hkv, const bf16* gq, const bf16* gk, float eps, cudaStream_t st) {
   const long warps = static_cast<long>(rows) * (hq + 2 * hkv);
   if (warps <= 0) return cudaSuccess;
+  if (k_splits < 1 || k_splits > 8) return cudaErrorInvalidValue;  // the kernel sums at most 8 slabs
   const int blocks = static_cast<int>((warps * 32 + 255) / 256);
   qk_head_norm_kernel<<<blocks, 256, 0, st>>>(part, k_splits, slab, qkv, rows, ld, hq, hkv, gq, gk, eps);
   return cudaGetLastError();
@@ -432,8 +446,24 @@ cudaError_t launch_final_norm(const float* h_part, int k_splits, size_t slab, co
                               const int* node_token, RowMap map, int rows, int d, const bf16* gain, float eps,
                               bf16* z_bf16, float* z_f32, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
-  final_norm_kernel<<<rows, kNormThreads, 0, st>>>(h_part, k_splits, slab, embed, node_token, map, d, gain, eps,
-                                                  z_bf16, z_f32);
+  switch (k_splits) {  // the slab count is a template argument so that every load is issued up front
+#define QUAIL_FINAL_NORM(KS)                                                                                    \
+  case KS:                                                                                                      \
+    final_norm_kernel<KS><<<rows, kNormThreads, 0, st>>>(h_part, slab, embed, node_token, map, d, gain, eps, \
+                                                         z_bf16, z_f32);                                       \
+    break;
+    QUAIL_FINAL_NORM(1)
+    QUAIL_FINAL_NORM(2)
+    QUAIL_FINAL_NORM(3)
+    QUAIL_FINAL_NORM(4)
+    QUAIL_FINAL_NORM(5)
+    QUAIL_FINAL_NORM(6)
+    QUAIL_FINAL_NORM(7)
+    QUAIL_FINAL_NORM(8)
+#undef QUAIL_FINAL_NORM
+    default:
+      return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 

@@ -16,6 +16,13 @@
 //  * Split-K over CTAs: work unit = (tile, k-split); the epilogue receives the
 //    split index and writes its partial tile to its own slab (no atomics); the
 //    next kernel sums the slabs.
+//  * CM = 2: CTA pairs (clusters of two along M) share each B tile. The two
+//    CTAs of a cluster always work on M tiles 2i and 2i+1 of the same N band;
+//    each loads half of the B band with TMA multicast into both CTAs, so every
+//    byte of B crosses from L2 once per pair. A stage is refilled only after
+//    both CTAs' MMAs have released it (a multicast commit to both empty
+//    barriers). An odd M-tile count gets one all-padding tile per band (A
+//    reads past the end fill zeros; the epilogue skips rows >= M).
 //
 // Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM owner + MMA
 // issuer, warps 2..5 = epilogue (warp w reads TMEM lanes 32*(w%4) .. +31).
@@ -31,6 +38,7 @@ namespace quail {
 constexpr int kGemmBM = 128;
 constexpr int kGemmBK = 64;  // 64 bf16 = one 128-byte swizzle row
 constexpr int kGemmThreads = 192;
+constexpr int kPrefetchKb = 8;  // k-blocks of B requested into L2 ahead of their loads (CTA pairs)
 
 // Up to three B operands covering output columns [n_begin[i], n_begin[i+1]).
 struct BSet {
@@ -68,17 +76,42 @@ __device__ __forceinline__ GemmUnit gemm_unit(int u, int m_tiles, int n_tiles, i
   return g;
 }
 
+// L2 prefetch cursor over one CTA's sequence of (unit, k-block) B loads:
+// step() requests the next B tile of that sequence (this CTA's half band).
+struct BPrefetch {
+  int u, kb, kb1, nb;
+  const CUtensorMap* map;
+  __device__ __forceinline__ void step(const BSet& bs, int bn, uint32_t crank, int m_tiles_s, int n_tiles,
+                                       int k_splits, int nk, int num_units) {
+    while (kb >= kb1) {  // advance to this CTA's next unit
+      u += gridDim.x;
+      if (u >= num_units) return;
+      const GemmUnit h = gemm_unit(u, m_tiles_s, n_tiles, k_splits, nk);
+      int bi = 0;
+      while (bi + 1 < bs.count && h.n_blk * bn >= bs.n_begin[bi + 1]) ++bi;
+      map = &bs.map[bi];
+      nb = h.n_blk * bn - bs.n_begin[bi] + static_cast<int>(crank) * (bn / 2);
+      kb = h.kb0;
+      kb1 = h.kb1;
+    }
+    tma_prefetch_l2_2d(map, kb * kGemmBK, nb);
+    ++kb;
+  }
+};
+
 // Epi must provide:
 //   __device__ void operator()(int m_blk, int n_blk, int ks, int lane_row, uint32_t taddr) const;
 // called by each of the 128 epilogue threads for every unit; lane_row in [0,128)
 // is this thread's accumulator row, taddr the TMEM address of (row, column 0).
 // All 32 lanes of a warp must execute the same tcgen05.ld sequence.
 // nk = k-blocks of B's K extent (A has nk k-blocks, or 2*nk with SPLIT_A).
-template <int BN, int STAGES, bool SPLIT_A, class Epi>
+template <int BN, int STAGES, bool SPLIT_A, class Epi, int CM = 1>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ BSet bset, int M, int N,
                      int nk, int k_splits, Epi epi, int* err) {
+  static_assert(CM == 1 || (CM == 2 && !SPLIT_A && BN % 16 == 0), "pairs: plain A, B band split in two halves");
   using Cfg = GemmCfg<BN, STAGES, SPLIT_A>;
+  constexpr uint32_t kBHalf = Cfg::kBBytes / CM;  // bytes of B each CTA of a pair loads
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(base + STAGES * Cfg::kStageBytes);
@@ -92,13 +125,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int m_tiles = (M + kGemmBM - 1) / kGemmBM;
+  const int m_tiles_s = (m_tiles + CM - 1) / CM * CM;  // scheduled M tiles: whole pairs
   const int n_tiles = (N + BN - 1) / BN;
-  const int num_units = m_tiles * n_tiles * k_splits;
+  const int num_units = m_tiles_s * n_tiles * k_splits;
+  const uint32_t crank = CM == 2 ? cluster_ctarank() : 0u;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], CM);  // released by the MMAs of every CTA whose copies land in it
     }
     mbar_init(&tfull[0], 1);
     mbar_init(&tfull[1], 1);
@@ -117,6 +152,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (CM == 2) cluster_sync();  // the peer's barriers exist before any multicast reaches them
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
@@ -128,14 +164,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
+      BPrefetch pf{static_cast<int>(blockIdx.x) - static_cast<int>(gridDim.x), 0, 0, 0, nullptr};
       for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-        const GemmUnit g = gemm_unit(u, m_tiles, n_tiles, k_splits, nk);
+        const GemmUnit g = gemm_unit(u, m_tiles_s, n_tiles, k_splits, nk);
         const int n0 = g.n_blk * BN;
         int bi = 0;
         while (bi + 1 < bset.count && n0 >= bset.n_begin[bi + 1]) ++bi;
         const CUtensorMap* tmB = &bset.map[bi];
         const int nb = n0 - bset.n_begin[bi];
+        const int nb_own = nb + static_cast<int>(crank) * (BN / 2);
         for (int kb = g.kb0; kb < g.kb1; ++kb) {
+          // Pairs stream each B band once from DRAM into L2 and then share it:
+          // this CTA's half-band k-blocks are requested kPrefetchKb loads ahead
+          // (running on into its next unit), so the first pair on a band does
+          // not wait on DRAM at every k-block.
+          if (CM == 2) {
+            const int n = (u == static_cast<int>(blockIdx.x) && kb == g.kb0) ? kPrefetchKb + 1 : 1;
+            for (int p = 0; p < n; ++p) pf.step(bset, BN, crank, m_tiles_s, n_tiles, k_splits, nk, num_units);
+          }
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
             break;
@@ -144,7 +190,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
           tma_load_2d(st, &tmA, &full[stage], kb * kGemmBK, g.m_blk * kGemmBM);
           if (SPLIT_A) tma_load_2d(st + Cfg::kABytes, &tmA, &full[stage], (nk + kb) * kGemmBK, g.m_blk * kGemmBM);
-          tma_load_2d(st + (SPLIT_A ? 2 : 1) * Cfg::kABytes, tmB, &full[stage], kb * kGemmBK, nb);
+          if (CM == 2)
+            tma_load_2d_mcast(st + Cfg::kABytes + crank * kBHalf, tmB, &full[stage], kb * kGemmBK, nb_own,
+                              static_cast<uint16_t>(0x3));
+          else
+            tma_load_2d(st + (SPLIT_A ? 2 : 1) * Cfg::kABytes, tmB, &full[stage], kb * kGemmBK, nb);
           armed_parity[stage] = static_cast<int>(phase);
           if (++stage == STAGES) {
             stage = 0;
@@ -153,14 +203,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
       // Never leave with copies in flight: every armed stage must have landed.
+      // In a pair, also wait until the last fill of every stage has been
+      // released by both CTAs, so that no commit from the peer is still on its
+      // way to this CTA's barriers when the pair synchronises and exits.
       for (int s = 0; s < STAGES; ++s) {
         if (armed_parity[s] < 0) continue;
-        const uint32_t a = smem_u32(&full[s]);
-        const long long t0 = clock64();
-        while (!mbar_try_wait(a, static_cast<uint32_t>(armed_parity[s]))) {
-          if (clock64() - t0 > kWaitLimitCycles) {
-            *abort_flag = 1;
-            break;
+        for (int which = 0; which < CM; ++which) {
+          const uint32_t a = smem_u32(which == 0 ? &full[s] : &empty[s]);
+          const long long t0 = clock64();
+          while (!mbar_try_wait(a, static_cast<uint32_t>(armed_parity[s]))) {
+            if ((which == 1 && *abort_flag) || clock64() - t0 > kWaitLimitCycles) {
+              *abort_flag = 1;
+              break;
+            }
           }
         }
       }
@@ -175,7 +230,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-        const GemmUnit g = gemm_unit(u, m_tiles, n_tiles, k_splits, nk);
+        const GemmUnit g = gemm_unit(u, m_tiles_s, n_tiles, k_splits, nk);
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -196,7 +251,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         (kb > g.kb0 || half > 0 || k > 0) ? 1u : 0u);
             }
           }
-          umma_commit(&empty[stage]);
+          if (CM == 2)
+            umma_commit_mcast(&empty[stage], static_cast<uint16_t>(0x3));
+          else
+            umma_commit(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -227,7 +285,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
       if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) break;
       tc_fence_after();
-      const GemmUnit g = gemm_unit(u, m_tiles, n_tiles, k_splits, nk);
+      const GemmUnit g = gemm_unit(u, m_tiles_s, n_tiles, k_splits, nk);
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
       epi(g.m_blk, g.n_blk, g.ks, lane_row, taddr);
       tc_fence_before();
@@ -244,6 +302,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tmem_dealloc(tmem_base, Cfg::kTmemCols);
   }
   if (threadIdx.x == 0 && *abort_flag) raise_device_error(err, QUAIL_ERR_DEVICE_TIMEOUT, 1000 + blockIdx.x);
+  // Neither CTA of a pair leaves while the other may still multicast into its
+  // shared memory or arrive on its barriers: both producers have drained their
+  // copies and both MMA threads their commits before reaching this point.
+  if (CM == 2) cluster_sync();
 }
 
 // ------------------------------------------------------------ epilogues
