@@ -674,7 +674,7 @@ quail_status quail_classify_trie_tree(const quail_model_desc* model, const quail
                     label_logscore,
                     label_prob,
                     label_argmax};
-  CUDA_TRY(launch_label_score(la, num_docs, st));
+  CUDA_TRY(launch_label_score(la, num_docs, ds->num_sms, st));
   stage_mark(QUAIL_STAGE_SCORING, true, st);
   return QUAIL_OK;
 }
@@ -897,7 +897,7 @@ quail_status quail_classify_trie_tree_noalloc(const quail_model_desc* model, con
                     img.label_term_offsets, img.label_term_eval, img.label_term_slot, img.label_prefix_eval,
                     img.eval_child_offsets, a,                  n_child,        trie->num_labels,
                     label_logscore,      label_prob,          label_argmax};
-  CUDA_TRY(launch_label_score(la, num_docs, st));
+  CUDA_TRY(launch_label_score(la, num_docs, ds->num_sms, st));
   return QUAIL_OK;
 }
 

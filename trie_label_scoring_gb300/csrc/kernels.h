@@ -96,7 +96,10 @@ struct LabelScoreArgs {
   float* prob;      // [N, M]
   int* argmax;      // [N]
 };
-cudaError_t launch_label_score(const LabelScoreArgs& args, int num_docs, cudaStream_t st);
+// One CTA per document when there are at least num_sms documents; else
+// the LSE reduce, per-label scores and per-document softmax as three kernels
+// spread over many CTAs.
+cudaError_t launch_label_score(const LabelScoreArgs& args, int num_docs, int num_sms, cudaStream_t st);
 
 // letters: logits of the M letter rows from z_f32 [N, d], renormalised softmax, argmax.
 cudaError_t launch_letters_head(const float* z, const bf16* lm_head, const int* letter_tokens, int M, int num_docs,

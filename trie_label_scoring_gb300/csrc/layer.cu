@@ -280,6 +280,88 @@ __global__ void label_score_kernel(LabelScoreArgs a) {
   for (int m = threadIdx.x; m < a.M; m += blockDim.x) out_p[m] = expf(out_ls[m] - mx) / total;
 }
 
+// The same scoring split over many CTAs, for calls with few documents (the
+// fused kernel above runs one CTA per document): the LSE rows come from
+// lse_reduce_kernel (warp per row, every document at once); then
+// label_logscore_kernel (CTA per (document, 64 labels), warp per label) and
+// label_softmax_kernel (CTA per document).
+constexpr int kLabelsPerCta = 64;
+__global__ void label_logscore_kernel(LabelScoreArgs a) {
+  const int doc = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const float* cl = a.child_logit + static_cast<size_t>(doc) * a.n_child;
+  const float* lse = a.lse + static_cast<size_t>(doc) * a.a;
+  float* out_ls = a.logscore + static_cast<size_t>(doc) * a.M;
+  const int m_end = min(a.M, static_cast<int>(blockIdx.y + 1) * kLabelsPerCta);
+  for (int m = blockIdx.y * kLabelsPerCta + warp; m < m_end; m += nw) {
+    const int t0 = __ldg(a.term_offsets + m), t1 = __ldg(a.term_offsets + m + 1);
+    float acc = 0.f;
+    for (int t = t0 + lane; t < t1; t += 32) acc += cl[__ldg(a.term_slot + t)] - lse[__ldg(a.term_eval + t)];
+    acc = warp_sum(acc);
+    const int pe = __ldg(a.prefix_eval + m);
+    if (pe >= 0) {  // prefix label: probability of stopping at its end node
+      const int c0 = __ldg(a.eval_child_offsets + pe), c1 = __ldg(a.eval_child_offsets + pe + 1);
+      double cont = 0.0;
+      for (int c = c0 + lane; c < c1; c += 32) cont += exp(static_cast<double>(cl[c]) - static_cast<double>(lse[pe]));
+      cont = warp_sum_d(cont);
+      acc = (cont < 1.0 - 1e-12) ? acc + static_cast<float>(log1p(-cont)) : -INFINITY;
+    }
+    if (lane == 0) out_ls[m] = acc;
+  }
+}
+
+__global__ void label_softmax_kernel(LabelScoreArgs a) {
+  __shared__ float s_max[32];
+  __shared__ int s_arg[32];
+  __shared__ float s_sum[32];
+  const int doc = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const float* ls = a.logscore + static_cast<size_t>(doc) * a.M;
+  float best = -INFINITY;
+  int best_i = 0x7fffffff;
+  for (int m = threadIdx.x; m < a.M; m += blockDim.x) {  // m increases per thread: the first max keeps the lowest index
+    const float v = ls[m];
+    if (v > best) {
+      best = v;
+      best_i = m;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, best_i, o);
+    if (ob > best || (ob == best && oi < best_i)) {
+      best = ob;
+      best_i = oi;
+    }
+  }
+  if (lane == 0) {
+    s_max[warp] = best;
+    s_arg[warp] = best_i;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float b = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int w = 0; w < nw; ++w) {
+      if (s_max[w] > b || (s_max[w] == b && s_arg[w] < bi)) {
+        b = s_max[w];
+        bi = s_arg[w];
+      }
+    }
+    s_max[0] = b;
+    s_arg[0] = (bi == 0x7fffffff) ? 0 : bi;
+  }
+  __syncthreads();
+  const float mx = s_max[0];
+  if (threadIdx.x == 0) a.argmax[doc] = s_arg[0];
+  float part = 0.f;
+  for (int m = threadIdx.x; m < a.M; m += blockDim.x) part += expf(ls[m] - mx);
+  const float total = block_sum(part, s_sum);
+  float* out_p = a.prob + static_cast<size_t>(doc) * a.M;
+  for (int m = threadIdx.x; m < a.M; m += blockDim.x) out_p[m] = expf(ls[m] - mx) / total;
+}
+
 // letters: one block per document, warp per letter row.
 __global__ void letters_head_kernel(const float* __restrict__ z, const bf16* __restrict__ lm_head,
                                     const int* __restrict__ letters, int M, int d, float* __restrict__ logprob,
@@ -473,9 +555,18 @@ cudaError_t launch_lse_reduce(const float2* lse_part, int rows, int n_tiles, flo
   return cudaGetLastError();
 }
 
-cudaError_t launch_label_score(const LabelScoreArgs& args, int num_docs, cudaStream_t st) {
+cudaError_t launch_label_score(const LabelScoreArgs& args, int num_docs, int num_sms, cudaStream_t st) {
   if (num_docs <= 0) return cudaSuccess;
-  label_score_kernel<<<num_docs, 256, 0, st>>>(args);
+  if (num_docs >= num_sms) {  // enough documents to fill the GPU with one CTA each
+    label_score_kernel<<<num_docs, 256, 0, st>>>(args);
+    return cudaGetLastError();
+  }
+  cudaError_t e = launch_lse_reduce(args.lse_part, num_docs * args.a, args.n_tiles, args.lse, st);
+  if (e != cudaSuccess) return e;
+  label_logscore_kernel<<<dim3(num_docs, (args.M + kLabelsPerCta - 1) / kLabelsPerCta), 256, 0, st>>>(args);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  label_softmax_kernel<<<num_docs, 512, 0, st>>>(args);
   return cudaGetLastError();
 }
 
