@@ -265,6 +265,11 @@ quail_status quail_classify_trie_tree_noalloc(const quail_model_desc* model, con
  * (the message names the first failing item), or QUAIL_ERR_CUDA. */
 quail_status quail_device_status(quail_stream_t stream);
 
+/* Number of kernels the last classify call made on this thread launched
+ * (including calls that failed part-way: the launches made before the
+ * failure). Host-side bookkeeping only; no device synchronisation. */
+int32_t quail_launch_count(void);
+
 /* Profiling hook: when events != NULL, each classify call records
  * events[2s] before and events[2s+1] after stage s on its stream, for
  * s < num_stages (stages: 0 node prologue, 1 attention, 2 W_o + RMSNorm,

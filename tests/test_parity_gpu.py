@@ -56,6 +56,15 @@ def test_trie_tree_tiny_all_docs(full_depth):
         assert abs(prob[i].sum() - 1) < 1e-5
 
 
+def test_launch_count_is_reported():
+    """The library counts the kernels one call launches (the bench reports it):
+    node prologue 4, attention 1-2, W_o + norm 2, head 1, scoring 1 or 3."""
+    import trie_label_scoring_gb300 as Q
+    w = S.WORKLOADS["tiny-support10-4x128"]
+    _run_trie_tree(w)
+    assert 9 <= Q.launch_count() <= 12
+
+
 def test_trie_tree_tiny_ragged_lengths():
     """Lengths around page and split boundaries: 1, 15, 16, 17, 255, 256, 257, 700."""
     w = S.with_docs(S.WORKLOADS["tiny-support10-4x128"], 8, (1, 700))

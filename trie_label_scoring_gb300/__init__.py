@@ -15,6 +15,7 @@ Entry points (same names as the C ABI, without the quail_ prefix):
   classify_trie_tree_noalloc(...) -> quail_classify_trie_tree_noalloc
   device_status(...)             -> quail_device_status
   set_stage_events(...)          -> quail_set_stage_events
+  launch_count()                 -> quail_launch_count
 """
 from __future__ import annotations
 
@@ -100,6 +101,7 @@ _SIGNATURES = {
                                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "quail_device_status": (ctypes.c_int, [ctypes.c_void_p]),
     "quail_set_stage_events": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
+    "quail_launch_count": (ctypes.c_int32, []),
 }
 
 _lib = None
@@ -281,3 +283,8 @@ def set_stage_events(events) -> None:
         return
     arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(None if e is None else e.cuda_event) for e in events])
     _check(lib().quail_set_stage_events(arr, len(events) // 2))
+
+
+def launch_count() -> int:
+    """Kernels the last classify call on this thread launched."""
+    return int(lib().quail_launch_count())

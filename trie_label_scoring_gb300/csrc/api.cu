@@ -23,6 +23,7 @@ using namespace quail;
 namespace {
 
 thread_local std::string g_last_error;
+thread_local int32_t g_launches = 0;
 
 quail_status fail(quail_status st, const char* fmt, ...) {
   char buf[512];
@@ -510,9 +511,13 @@ quail_status copy_trie_tree_image(const quail_trie* t, uint8_t* dst, cudaStream_
 }  // namespace
 
 // ================================================================== C ABI
+void quail::count_launch() { ++g_launches; }
+
 extern "C" {
 
 const char* quail_last_error(void) { return g_last_error.c_str(); }
+
+int32_t quail_launch_count(void) { return g_launches; }
 
 quail_status quail_trie_build(const int32_t* tokens, const int64_t* label_offsets, int32_t num_labels,
                               int32_t root_token, int32_t vocab, const uint8_t* word_continuation_bitmap,
@@ -600,6 +605,7 @@ quail_status quail_classify_trie_tree(const quail_model_desc* model, const quail
                                       int32_t num_docs, void* workspace, size_t workspace_bytes,
                                       float* label_logscore, float* label_prob, int32_t* label_argmax,
                                       quail_stream_t stream) {
+  g_launches = 0;
   quail_status s = check_model(model);
   if (s != QUAIL_OK) return s;
   s = check_kv(kv, model);
@@ -684,6 +690,7 @@ quail_status quail_classify_letters(const quail_model_desc* model, const quail_p
                                     int32_t num_docs, void* workspace, size_t workspace_bytes,
                                     float* letter_logprob, float* letter_prob, int32_t* letter_argmax,
                                     quail_stream_t stream) {
+  g_launches = 0;
   quail_status s = check_model(model);
   if (s != QUAIL_OK) return s;
   s = check_kv(kv, model);
@@ -749,6 +756,7 @@ quail_status quail_classify_trie_decode_step(const quail_model_desc* model, cons
                                              quail_trie* trie, int32_t num_docs, int32_t* node_cursor,
                                              int32_t* label_out, int32_t* active_count, uint8_t* touched_nodes,
                                              void* workspace, size_t workspace_bytes, quail_stream_t stream) {
+  g_launches = 0;
   quail_status s = check_model(model);
   if (s != QUAIL_OK) return s;
   s = check_kv(kv, model);
@@ -842,6 +850,7 @@ quail_status quail_set_stage_events(quail_event_t* events, int32_t num_stages) {
 quail_status quail_classify_trie_tree_noalloc(const quail_model_desc* model, const quail_paged_kv* kv,
                                               const quail_trie* trie, int32_t num_docs, float* label_logscore,
                                               float* label_prob, int32_t* label_argmax, quail_stream_t stream) {
+  g_launches = 0;
   quail_status s = check_model(model);
   if (s != QUAIL_OK) return s;
   s = check_kv(kv, model);

@@ -556,6 +556,7 @@ __global__ void attn_combine_kernel(AttnArgs a) {
 cudaError_t launch_tree_part(const AttnArgs& a, cudaStream_t st) {
   const long warps = static_cast<long>(a.n_nodes) * a.hq;
   if (warps <= 0) return cudaSuccess;
+  count_launch();
   tree_part_kernel<<<static_cast<int>((warps * 32 + 255) / 256), 256, 0, st>>>(a, make_rope_table(a.theta));
   return cudaGetLastError();
 }
@@ -576,6 +577,7 @@ cudaError_t launch_attn_doc(const AttnArgs& a, const CUtensorMap& tmK, const CUt
   dim3 grid(a.n_splits, a.hkv * (a.rows_pad / a.row_tile), a.n_slots);
   if (grid.x == 0 || grid.z == 0) return cudaSuccess;
   const size_t smem = attn_smem_bytes(a.row_tile == 16 ? 1 : kConsumerWarps);
+  count_launch();
   attn_doc_kernel<<<grid, kAttnThreads, smem, st>>>(a, make_rope_table(a.theta), tmK, tmV);
   return cudaGetLastError();
 }
@@ -584,6 +586,7 @@ cudaError_t launch_attn_combine(const AttnArgs& a, cudaStream_t st) {
   const int rows = a.n_slots * a.map.nq;
   if (rows <= 0) return cudaSuccess;
   const int threads = (a.hq < 32 ? a.hq : 32) * 32;
+  count_launch();
   attn_combine_kernel<<<rows, threads, 0, st>>>(a);
   return cudaGetLastError();
 }

@@ -538,6 +538,7 @@ cudaError_t launch_attn_doc_tc(const AttnArgs& a, const CUtensorMap& tmK, const 
     return cudaErrorInvalidValue;
   dim3 grid(a.rows_pad / kTcRows, a.n_splits * a.hkv, a.n_slots);
   if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
+  count_launch();
   attn_doc_tc_kernel<<<grid, kTcThreads, kTcSmem, st>>>(a, make_rope_table(a.theta), tmK, tmV);
   return cudaGetLastError();
 }

@@ -137,6 +137,7 @@ cudaError_t launch_umma(const CUtensorMap& tmA, const BSet& bset, int M, int N, 
   grid = grid / CM * CM;  // whole clusters; units is a multiple of CM
   if (grid <= 0) return cudaSuccess;
   if (CM == 1) {
+    count_launch();
     kern<<<grid, kGemmThreads, Cfg::kSmemBytes, st>>>(tmA, bset, M, N, nk, k_splits, epi, err);
     return cudaGetLastError();
   }
@@ -152,6 +153,7 @@ cudaError_t launch_umma(const CUtensorMap& tmA, const BSet& bset, int M, int N, 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  count_launch();
   return cudaLaunchKernelEx(&cfg, kern, tmA, bset, M, N, nk, k_splits, epi, err);
 }
 

@@ -510,6 +510,7 @@ __global__ void decode_select_kernel(DecodeTrie t, const float* __restrict__ z, 
 cudaError_t launch_embed_rmsnorm(const bf16* embed, const int* tokens, int n, int d, const bf16* gain, float eps,
                                  bf16* out, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
+  count_launch();
   embed_rmsnorm_kernel<<<n, kNormThreads, 0, st>>>(embed, tokens, d, gain, eps, out);
   return cudaGetLastError();
 }
@@ -520,6 +521,7 @@ cudaError_t launch_qk_head_norm(const float* part, int k_splits, size_t slab, fl
   if (warps <= 0) return cudaSuccess;
   if (k_splits < 1 || k_splits > 8) return cudaErrorInvalidValue;  // the kernel sums at most 8 slabs
   const int blocks = static_cast<int>((warps * 32 + 255) / 256);
+  count_launch();
   qk_head_norm_kernel<<<blocks, 256, 0, st>>>(part, k_splits, slab, qkv, rows, ld, hq, hkv, gq, gk, eps);
   return cudaGetLastError();
 }
@@ -531,6 +533,7 @@ cudaError_t launch_final_norm(const float* h_part, int k_splits, size_t slab, co
   switch (k_splits) {  // the slab count is a template argument so that every load is issued up front
 #define QUAIL_FINAL_NORM(KS)                                                                                    \
   case KS:                                                                                                      \
+    count_launch();                                                                                          \
     final_norm_kernel<KS><<<rows, kNormThreads, 0, st>>>(h_part, slab, embed, node_token, map, d, gain, eps, \
                                                          z_bf16, z_f32);                                       \
     break;
@@ -551,6 +554,7 @@ cudaError_t launch_final_norm(const float* h_part, int k_splits, size_t slab, co
 
 cudaError_t launch_lse_reduce(const float2* lse_part, int rows, int n_tiles, float* lse, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
+  count_launch();
   lse_reduce_kernel<<<(rows * 32 + 255) / 256, 256, 0, st>>>(lse_part, rows, n_tiles, lse);
   return cudaGetLastError();
 }
@@ -558,14 +562,17 @@ cudaError_t launch_lse_reduce(const float2* lse_part, int rows, int n_tiles, flo
 cudaError_t launch_label_score(const LabelScoreArgs& args, int num_docs, int num_sms, cudaStream_t st) {
   if (num_docs <= 0) return cudaSuccess;
   if (num_docs >= num_sms) {  // enough documents to fill the GPU with one CTA each
+    count_launch();
     label_score_kernel<<<num_docs, 256, 0, st>>>(args);
     return cudaGetLastError();
   }
   cudaError_t e = launch_lse_reduce(args.lse_part, num_docs * args.a, args.n_tiles, args.lse, st);
   if (e != cudaSuccess) return e;
+  count_launch();
   label_logscore_kernel<<<dim3(num_docs, (args.M + kLabelsPerCta - 1) / kLabelsPerCta), 256, 0, st>>>(args);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  count_launch();
   label_softmax_kernel<<<num_docs, 512, 0, st>>>(args);
   return cudaGetLastError();
 }
@@ -573,6 +580,7 @@ cudaError_t launch_label_score(const LabelScoreArgs& args, int num_docs, int num
 cudaError_t launch_letters_head(const float* z, const bf16* lm_head, const int* letter_tokens, int M, int num_docs,
                                 int d, float* logprob, float* prob, int* argmax, cudaStream_t st) {
   if (num_docs <= 0) return cudaSuccess;
+  count_launch();
   letters_head_kernel<<<num_docs, 256, M * sizeof(float), st>>>(z, lm_head, letter_tokens, M, d, logprob, prob,
                                                                 argmax);
   return cudaGetLastError();
@@ -580,6 +588,7 @@ cudaError_t launch_letters_head(const float* z, const bf16* lm_head, const int* 
 
 cudaError_t launch_decode_prepare(DecodeTrie t, int num_docs, int* node_cursor, int* label_out, int* slot_doc,
                                   int* slot_node, int* n_slots, int* active_count, cudaStream_t st) {
+  count_launch();
   decode_prepare_kernel<<<1, 1024, 0, st>>>(t, num_docs, node_cursor, label_out, slot_doc, slot_node, n_slots,
                                             active_count);
   return cudaGetLastError();
@@ -589,6 +598,7 @@ cudaError_t launch_decode_select(DecodeTrie t, const float* z, const bf16* lm_he
                                  const int* slot_doc, const int* n_slots, int* node_cursor, int* label_out,
                                  int* active_count, uint8_t* touched, cudaStream_t st) {
   if (num_docs <= 0) return cudaSuccess;
+  count_launch();
   decode_select_kernel<<<num_docs, 256, 0, st>>>(t, z, lm_head, d, slot_doc, n_slots, node_cursor, label_out,
                                                  active_count, touched);
   return cudaGetLastError();

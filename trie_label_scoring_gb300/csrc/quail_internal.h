@@ -6,6 +6,10 @@
 
 namespace quail {
 
+// Kernels launched by the current classify call on this thread (reset at the
+// call's start; read back through quail_launch_count).
+void count_launch();
+
 // Device error word indices.
 constexpr int kErrCode = 0;
 constexpr int kErrDetail = 1;
