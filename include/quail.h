@@ -260,6 +260,61 @@ quail_status quail_classify_trie_tree_noalloc(const quail_model_desc* model, con
                                               const quail_trie* trie, int32_t num_docs, float* label_logscore,
                                               float* label_prob, int32_t* label_argmax, quail_stream_t stream);
 
+/* ------------------------------------------------------------ cost model
+ * Speed-of-light estimates of the three ways to classify and the choice
+ * among them ("To Classify, Try a Trie Tree", sec. 4): for each method the
+ * total tokens n_tok = L1 + N (q_pre + q_tail + a) and forward passes
+ * K = ceil(n_tok / C) (sec. 4.1), the cached-KV tokens read R (prompt once;
+ * trie_decode (b - 1) times), the attention bytes B_kv (W + R) with W = n_tok,
+ * the output head F = 2 d V_out N a, B = 2 d V_out K, T_head = max(F/Pi, B/beta),
+ * projections and MLP in the same roofline form over their weights, attention
+ * as B_attn / beta, and T_classify = T_proj + T_attn + T_mlp + T_head.
+ * Per method: trie_tree a = |P| and V_out = vocab; letters q_tail + 2M + 3
+ * instruction tokens, a = 1, V_out = M (sec. 4.2); trie_decode b requests
+ * (mean branching nodes per label path, sec. 4.3) over E[1 + depth of the
+ * deciding node] tokens, V_out = vocab, not runnable when probabilities are
+ * requested or a label prefixes another. The pick is the runnable method with
+ * the lowest T_classify (sec. 4.4; ties in the order decode, tree, letters).
+ * Host only; no device work. */
+typedef enum {
+  QUAIL_METHOD_TRIE_DECODE = 0,
+  QUAIL_METHOD_TRIE_TREE = 1,
+  QUAIL_METHOD_LETTERS = 2,
+  QUAIL_NUM_METHODS = 3
+} quail_method;
+
+typedef struct {
+  int32_t d_model, vocab;
+  double proj_params;        /* q, k, v and output-projection weights summed over layers (elements) */
+  double mlp_params;         /* MLP weights summed over layers (elements) */
+  double kv_bytes_per_token; /* B_kv: one token's K and V over all layers (bytes) */
+  double peak_flops;         /* Pi: bf16 FLOP/s, > 0 */
+  double hbm_bytes_per_s;    /* beta: bytes/s, > 0 */
+} quail_cost_model;
+
+typedef struct {
+  int32_t num_docs;           /* N >= 0 */
+  double doc_tokens;          /* L1 = sum of the documents' token counts, >= 0 */
+  int32_t q_pre;              /* preamble tokens per request, >= 0 */
+  int32_t q_tail;             /* instruction tokens of the trie methods, >= 0 */
+  int32_t max_pass_tokens;    /* C: tokens per forward pass, >= 1 */
+  int32_t need_probabilities; /* 1: the query asks for label probabilities */
+} quail_cost_workload;
+
+typedef struct {
+  int32_t runnable;                          /* 0: the other fields are zero */
+  double q_tail, a, v_out, requests;         /* the method's shape */
+  double n_tok, passes, kv_read_tokens, attn_bytes;
+  double head_flops, head_bytes;
+  double t_head, t_proj, t_attn, t_mlp, t_classify; /* seconds */
+} quail_method_cost;
+
+/* Fills costs[QUAIL_NUM_METHODS] (indexed by quail_method) for the labels of
+ * `trie` and writes the chosen method to *best. QUAIL_ERR_INVALID_ARG on a
+ * null pointer or a value outside the ranges above. */
+quail_status quail_estimate_methods(const quail_cost_model* model, const quail_cost_workload* work,
+                                    const quail_trie* trie, quail_method_cost* costs, int32_t* best);
+
 /* Synchronises `stream`, then reads and clears the current device's error
  * word. Returns QUAIL_OK, QUAIL_ERR_DEVICE_BOUNDS or QUAIL_ERR_DEVICE_TIMEOUT
  * (the message names the first failing item), or QUAIL_ERR_CUDA. */

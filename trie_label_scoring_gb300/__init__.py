@@ -16,6 +16,7 @@ Entry points (same names as the C ABI, without the quail_ prefix):
   device_status(...)             -> quail_device_status
   set_stage_events(...)          -> quail_set_stage_events
   launch_count()                 -> quail_launch_count
+  estimate_methods(...)          -> quail_estimate_methods
 """
 from __future__ import annotations
 
@@ -46,6 +47,27 @@ class QuailError(RuntimeError):
 
 
 _i32p = ctypes.POINTER(ctypes.c_int32)
+
+
+METHODS = ("trie_decode", "trie_tree", "letters")  # quail_method order
+
+
+class CostModel(ctypes.Structure):
+    _fields_ = [("d_model", ctypes.c_int32), ("vocab", ctypes.c_int32), ("proj_params", ctypes.c_double),
+                ("mlp_params", ctypes.c_double), ("kv_bytes_per_token", ctypes.c_double),
+                ("peak_flops", ctypes.c_double), ("hbm_bytes_per_s", ctypes.c_double)]
+
+
+class CostWorkload(ctypes.Structure):
+    _fields_ = [("num_docs", ctypes.c_int32), ("doc_tokens", ctypes.c_double), ("q_pre", ctypes.c_int32),
+                ("q_tail", ctypes.c_int32), ("max_pass_tokens", ctypes.c_int32),
+                ("need_probabilities", ctypes.c_int32)]
+
+
+class MethodCost(ctypes.Structure):
+    _fields_ = [("runnable", ctypes.c_int32)] + [(n, ctypes.c_double) for n in (
+        "q_tail", "a", "v_out", "requests", "n_tok", "passes", "kv_read_tokens", "attn_bytes", "head_flops",
+        "head_bytes", "t_head", "t_proj", "t_attn", "t_mlp", "t_classify")]
 
 
 class ModelDesc(ctypes.Structure):
@@ -102,6 +124,9 @@ _SIGNATURES = {
     "quail_device_status": (ctypes.c_int, [ctypes.c_void_p]),
     "quail_set_stage_events": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
     "quail_launch_count": (ctypes.c_int32, []),
+    "quail_estimate_methods": (ctypes.c_int, [ctypes.POINTER(CostModel), ctypes.POINTER(CostWorkload),
+                                              ctypes.c_void_p, ctypes.POINTER(MethodCost),
+                                              ctypes.POINTER(ctypes.c_int32)]),
 }
 
 _lib = None
@@ -288,3 +313,23 @@ def set_stage_events(events) -> None:
 def launch_count() -> int:
     """Kernels the last classify call on this thread launched."""
     return int(lib().quail_launch_count())
+
+
+def estimate_methods(model: dict, workload: dict, trie: "Trie") -> tuple:
+    """Speed-of-light estimates of trie_decode / trie_tree / letters for the
+    labels of `trie` and the method the cost model picks.
+    model: d_model, vocab, proj_params, mlp_params, kv_bytes_per_token,
+    peak_flops, hbm_bytes_per_s; workload: num_docs, doc_tokens, q_pre, q_tail,
+    max_pass_tokens, need_probabilities. Returns (best method name, {name: dict
+    of the estimate, or None when the method cannot run})."""
+    m = CostModel(**{k: model[k] for k, _ in CostModel._fields_})
+    w = CostWorkload(**{k: int(workload[k]) if t is not ctypes.c_double else float(workload[k])
+                        for k, t in CostWorkload._fields_})
+    out = (MethodCost * 3)()
+    best = ctypes.c_int32(-1)
+    _check(lib().quail_estimate_methods(ctypes.byref(m), ctypes.byref(w), trie.handle, out, ctypes.byref(best)))
+    res = {}
+    for i, name in enumerate(METHODS):
+        c = out[i]
+        res[name] = ({k: getattr(c, k) for k, _ in MethodCost._fields_ if k != "runnable"} if c.runnable else None)
+    return METHODS[best.value], res

@@ -513,11 +513,24 @@ quail_status copy_trie_tree_image(const quail_trie* t, uint8_t* dst, cudaStream_
 // ================================================================== C ABI
 void quail::count_launch() { ++g_launches; }
 
+namespace quail {
+quail_status estimate_methods_host(const quail_cost_model* md, const quail_cost_workload* w, const quail_trie* t,
+                                   quail_method_cost* costs, int32_t* best, std::string* msg);
+}
+
 extern "C" {
 
 const char* quail_last_error(void) { return g_last_error.c_str(); }
 
 int32_t quail_launch_count(void) { return g_launches; }
+
+quail_status quail_estimate_methods(const quail_cost_model* model, const quail_cost_workload* work,
+                                    const quail_trie* trie, quail_method_cost* costs, int32_t* best) {
+  std::string msg;
+  const quail_status s = estimate_methods_host(model, work, trie, costs, best, &msg);
+  if (s != QUAIL_OK) return fail(s, "%s", msg.c_str());
+  return QUAIL_OK;
+}
 
 quail_status quail_trie_build(const int32_t* tokens, const int64_t* label_offsets, int32_t num_labels,
                               int32_t root_token, int32_t vocab, const uint8_t* word_continuation_bitmap,
