@@ -397,6 +397,106 @@ def run_ours(args, world, rank, local):
         print(json.dumps(out), flush=True)
 
 
+def run_join(args, world, rank, local):
+    """AI.IF over joined pairs: every anchor document against every partner
+    (quail_join_if). One step = one call over all anchors; metric = pairs/s."""
+    import torch
+
+    import synthetic as S
+    import trie_label_scoring_gb300 as Q
+    from tests import gpu_cases as C
+    from trie_label_scoring_gb300.torch_inputs import kv_from_docs
+
+    Q.build()
+    w = S.WORKLOADS[args.workload]
+    if args.docs:
+        w = S.with_docs(w, args.docs)
+    model = C.device_model(w.shape, 0)
+    partners = S.make_labels(w, 0)
+    yes, no = S.make_answers(0, w.shape.vocab)
+    docs = S.make_docs(w, rank)
+    kv = kv_from_docs(docs)
+    trie = Q.Trie(partners.labels, partners.root_token, w.shape.vocab, all_nodes=True)
+    trie.upload()
+    N, M = w.num_docs, len(partners.labels)
+    ws = torch.empty(Q.workspace_size(model, trie, len(yes) + len(no), N, docs.max_doc_len, Q.MODE_JOIN_IF),
+                     dtype=torch.uint8, device="cuda")
+    p_true = torch.empty((N, M), device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        Q.join_if(model, kv, trie, N, yes, no, ws, p_true, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    Q.device_status()
+    launches_per_step = Q.launch_count()
+    steps = args.steps if args.steps is not None else 50
+    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(10)] for _ in range(steps)]
+    for evs in stage_ev:
+        for e in evs:
+            e.record(stream)
+    clocks = ClockSampler(str(torch.cuda.get_device_properties(local).pci_bus_id))
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for k in range(steps):
+        Q.set_stage_events(stage_ev[k])
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    Q.set_stage_events(None)
+    Q.device_status()
+    elapsed_ms = max_over_ranks(world, start.elapsed_time(end))
+    stages_ms = {name: statistics.mean(ev[2 * i].elapsed_time(ev[2 * i + 1]) for ev in stage_ev)
+                 for i, name in enumerate(Q.STAGES[:4])}
+    ms_per_step = elapsed_ms / steps
+    pairs = N * M
+    # dominant kernel: the doc-part attention (tcgen05, G * M query rows per KV head);
+    # its algorithmic work is 4 * 128 FLOP per (query row, anchor key)
+    G = w.shape.n_q_heads // w.shape.n_kv_heads
+    keys = float(docs.doc_len.sum())
+    attn_flops = 4.0 * 128 * keys * w.shape.n_kv_heads * G * M
+    peaks = measured_peaks()
+    achieved = attn_flops / (stages_ms["attention"] / 1e3) / 1e12
+    kv_bytes = keys * w.shape.n_kv_heads * 128 * 2 * 2
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "traffic": None, "kernel": "attn_doc_tc_kernel",
+                "attention_ms": stages_ms["attention"], "peak_kind": f"bf16 burst ({peaks['source']})",
+                "note": "FLOPs counted once per query row (the hi/lo splits double the issued work)"}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import join as J
+        L = C.oracle_layer(w.shape, 0)
+        t0 = time.time()
+        done = 0
+        dk, dv = C.oracle_doc_kv(docs, 0)
+        while done < M and time.time() - t0 < 15.0:
+            J.join_if(L, dk, dv, partners.root_token, [partners.labels[done]], yes, no)
+            done += 1
+        sec = time.time() - t0
+        cpu = {"value": done / sec, "unit": "pairs/s", "cores": cores(), "kind": "oracle",
+               "sample": f"anchor 0 with its first {done} partners ({sec:.1f} s)"}
+    if rank == 0:
+        out = {
+            "metric": "joined pairs scored/sec at 1 GB300 (AI.IF, TRUE/FALSE head)",
+            "value": pairs * world * steps / (elapsed_ms / 1e3), "unit": "pairs/s", "n_gpus": world,
+            "steps": steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, random-init weights)",
+            "config": {"workload": w.name, "anchors_per_gpu": N, "partners": M, "partner_trie_nodes": trie.n_nodes,
+                       "answer_spellings": len(yes) + len(no), "anchor_tokens_per_gpu": int(keys),
+                       "l2": "anchor KV %.2f GB per step" % (kv_bytes / 1e9),
+                       "parallelism": f"replicas x{world} (anchors sharded, no collective)"},
+            "roofline": roofline, "stages_ms": stages_ms, "cpu_baseline": cpu, "e2e": None,
+            "gpu_launches": launches_per_step * steps, "clocks": clk,
+        }
+        print(json.dumps(out), flush=True)
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -405,7 +505,10 @@ def main():
         run_reference(args, world, rank)
         return
     world, rank, local = dist_setup()
-    run_ours(args, world, rank, local)
+    if "-join" in args.workload:  # AI.IF join workloads (synthetic labels kind "join")
+        run_join(args, world, rank, local)
+    else:
+        run_ours(args, world, rank, local)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

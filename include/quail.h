@@ -81,7 +81,7 @@ const char* quail_last_error(void);
  */
 typedef struct quail_trie quail_trie;
 
-enum { QUAIL_TRIE_FULL_DEPTH = 1 };
+enum { QUAIL_TRIE_FULL_DEPTH = 1, QUAIL_TRIE_ALL_NODES = 2 };
 
 /*
  * tokens:        host, concatenated label token ids (label m = tokens[label_offsets[m] .. label_offsets[m+1]))
@@ -91,7 +91,8 @@ enum { QUAIL_TRIE_FULL_DEPTH = 1 };
  * vocab:         vocabulary size V
  * word_continuation_bitmap: host, nullable; ceil(V/8) bytes, bit t (byte t>>3, bit t&7) set
  *                when token t continues the previous word instead of starting one
- * flags:         0 or QUAIL_TRIE_FULL_DEPTH
+ * flags:         0, QUAIL_TRIE_FULL_DEPTH, and/or QUAIL_TRIE_ALL_NODES (every node
+ *                is an evaluated position: the partner tries of quail_join_if)
  * out:           receives a library-owned trie; free with quail_trie_free
  * Errors: INVALID_ARG, EMPTY_LABEL, DUPLICATE_LABEL, TOKEN_RANGE. Host only; no GPU needed.
  */
@@ -185,7 +186,7 @@ typedef struct {
   int32_t max_doc_len;
 } quail_paged_kv;
 
-typedef enum { QUAIL_MODE_TRIE_TREE = 0, QUAIL_MODE_LETTERS = 1, QUAIL_MODE_TRIE_DECODE = 2 } quail_mode;
+typedef enum { QUAIL_MODE_TRIE_TREE = 0, QUAIL_MODE_LETTERS = 1, QUAIL_MODE_TRIE_DECODE = 2, QUAIL_MODE_JOIN_IF = 3 } quail_mode;
 
 /* Bytes of device workspace one classify call of `mode` needs (256-byte aligned
  * base required). trie may be NULL for QUAIL_MODE_LETTERS; num_letters is used
@@ -259,6 +260,32 @@ quail_status quail_classify_trie_decode_step(const quail_model_desc* model, cons
 quail_status quail_classify_trie_tree_noalloc(const quail_model_desc* model, const quail_paged_kv* kv,
                                               const quail_trie* trie, int32_t num_docs, float* label_logscore,
                                               float* label_prob, int32_t* label_argmax, quail_stream_t stream);
+
+/* AI.IF over joined pairs ("Building an Ultra-High Throughput AI-SQL Engine",
+ * sec. 3.2.4 "specialize attention for joins"; Quail docs "Execution",
+ * Joins): every anchor document, whose KV is cached, is paired with every
+ * partner. A partner is a token sequence that follows the anchor's prompt
+ * (its text, the join question, the answer token) and attends to the anchor
+ * and to its own earlier tokens only; partners share no tokens with one
+ * another. The partners are the labels of a trie built with
+ * QUAIL_TRIE_ALL_NODES, whose root token is the first token every partner
+ * starts with; shared leading tokens (the join instructions) are one path.
+ * The anchor KV is read once per KV head for all partners (as in
+ * trie_tree); the partner-internal attention is computed once per call; the
+ * two parts merge by log-sum-exp. At each partner's last token the output
+ * head is restricted to the R answer spellings (sec. 3.2.4: "8 rows instead
+ * of 151,936"): p_true = softmax over those R logits, summed over the first
+ * n_true (the TRUE spellings).
+ *   kv:          anchors' paged KV (doc = anchor)
+ *   partners:    trie built with QUAIL_TRIE_ALL_NODES (else QUAIL_ERR_INVALID_ARG)
+ *   answer_tokens: host, R = n_true + n_false distinct ids, TRUE spellings first,
+ *                1 <= R <= 64
+ *   p_true:      device [num_anchors, num_partners] fp32, row-major
+ * Errors as quail_classify_trie_tree; QUAIL_ERR_DUPLICATE_LABEL for repeated
+ * answer tokens. Workspace: quail_workspace_size(..., num_letters = R, ..., QUAIL_MODE_JOIN_IF). */
+quail_status quail_join_if(const quail_model_desc* model, const quail_paged_kv* kv, quail_trie* partners,
+                           int32_t num_anchors, const int32_t* answer_tokens, int32_t n_true, int32_t n_false,
+                           void* workspace, size_t workspace_bytes, float* p_true, quail_stream_t stream);
 
 /* ------------------------------------------------------------ cost model
  * Speed-of-light estimates of the three ways to classify and the choice

@@ -34,7 +34,8 @@ def _is_continuation(bitmap, t: int) -> bool:
     return bool((int(bitmap[t >> 3]) >> (t & 7)) & 1)
 
 
-def build_trie(labels, root_token: int, vocab: int, continuation=None, full_depth: bool = False) -> dict:
+def build_trie(labels, root_token: int, vocab: int, continuation=None, full_depth: bool = False,
+               all_nodes: bool = False) -> dict:
     """Builds the trie of `labels` (lists of token ids) and its derived sets.
 
     Returns a dict of numpy arrays named like the fields of the library's
@@ -149,6 +150,8 @@ def build_trie(labels, root_token: int, vocab: int, continuation=None, full_dept
         if children[end]:
             has_prefix = 1
             evalset.add(end)
+    if all_nodes:  # every node evaluated (partner tries of a join)
+        evalset = set(range(n))
     eval_nodes = np.array(sorted(evalset), dtype=np.int32)
     eval_index_of_node = np.full(n, -1, dtype=np.int32)
     eval_index_of_node[eval_nodes] = np.arange(len(eval_nodes), dtype=np.int32)

@@ -117,6 +117,7 @@ WORKLOADS = {
         Workload("qwen3-4b-letters255-64x2048", QWEN3_4B, 64, (2048, 2048), "letters", 255, (1, 1)),
         Workload("qwen3-4b-tree20-32x8192", QWEN3_4B, 32, (8192, 8192), "tree", 20, (1, 5)),
         Workload("qwen3-4b-tree5000-16x1024", QWEN3_4B, 16, (1024, 1024), "tree", 5000, (2, 10)),
+        Workload("qwen3-4b-join128-64x2048", QWEN3_4B, 64, (2048, 2048), "join", 128, (3, 9)),
     ]
 }
 
@@ -300,4 +301,31 @@ def make_labels(w: Workload, seed: int = 0) -> LabelSet:
     if w.labels == "letters":
         ids = _distinct(rng, w.num_labels + 1, V)
         return LabelSet([[t] for t in ids[1:]], ids[0], None)
+    if w.labels == "join":
+        return join_partners(w.num_labels, w.label_len[0], w.label_len[1], V, rng)
     raise ValueError(w.labels)
+
+
+def join_partners(n: int, lo: int, hi: int, V: int, rng) -> LabelSet:
+    """Partners of a model join ("Building an Ultra-High Throughput AI-SQL
+    Engine", sec. 3.2.4): after the root token, a shared instruction of 24
+    tokens, the partner's own text of lo..hi tokens, and a closing answer
+    token shared by all; distinct partners."""
+    ids = _distinct(rng, 26, V)
+    root, shared, answer = ids[0], list(ids[1:25]), ids[25]
+    seen = set()
+    labels = []
+    while len(labels) < n:
+        text = tuple(int(t) for t in rng.integers(0, V, size=int(rng.integers(lo, hi + 1))))
+        if text in seen:
+            continue
+        seen.add(text)
+        labels.append(shared + list(text) + [answer])
+    return LabelSet(labels, root, None)
+
+
+def make_answers(seed: int, V: int) -> tuple:
+    """Token ids of the TRUE and FALSE spellings (4 each, distinct)."""
+    rng = np.random.Generator(np.random.PCG64(_streams(seed)[_STREAM["letters"]]))
+    ids = [int(t) for t in _distinct(rng, 8, V)]
+    return ids[:4], ids[4:]

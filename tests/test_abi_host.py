@@ -60,6 +60,20 @@ def test_trie_bit_exact_on_workloads(name, full):
     assert_same_trie(t.view(), o)
 
 
+@pytest.mark.parametrize("seed", range(8))
+def test_trie_all_nodes_flag_bit_exact(seed):
+    """QUAIL_TRIE_ALL_NODES: every node is an evaluated position (join partner tries)."""
+    rng = np.random.default_rng(100 + seed)
+    labels = set()
+    while len(labels) < 12:
+        labels.add(tuple(int(x) for x in rng.integers(0, 9, size=int(rng.integers(1, 6)))))
+    labels = [list(l) for l in labels]
+    t = Q.Trie(labels, 20, 64, all_nodes=True)
+    o = build_trie(labels, 20, 64, all_nodes=True)
+    assert o["n_eval"] == o["n_nodes"]
+    assert_same_trie(t.view(), o)
+
+
 @pytest.mark.parametrize("seed", range(40))
 def test_trie_bit_exact_random_with_prefix_labels(seed):
     rng = np.random.default_rng(seed)

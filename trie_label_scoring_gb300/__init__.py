@@ -13,6 +13,7 @@ Entry points (same names as the C ABI, without the quail_ prefix):
   classify_letters(...)          -> quail_classify_letters
   classify_trie_decode_step(...) -> quail_classify_trie_decode_step
   classify_trie_tree_noalloc(...) -> quail_classify_trie_tree_noalloc
+  join_if(...)                   -> quail_join_if
   device_status(...)             -> quail_device_status
   set_stage_events(...)          -> quail_set_stage_events
   launch_count()                 -> quail_launch_count
@@ -27,8 +28,9 @@ import numpy as np
 
 from ._build import LIB, build  # noqa: F401  (build() compiles the library in-tree)
 
-MODE_TRIE_TREE, MODE_LETTERS, MODE_TRIE_DECODE = 0, 1, 2
+MODE_TRIE_TREE, MODE_LETTERS, MODE_TRIE_DECODE, MODE_JOIN_IF = 0, 1, 2, 3
 TRIE_FULL_DEPTH = 1
+TRIE_ALL_NODES = 2
 STAGES = ("prologue", "attention", "wo_norm", "head", "scoring")
 
 STATUS = {
@@ -121,6 +123,9 @@ _SIGNATURES = {
     "quail_classify_trie_tree_noalloc": (ctypes.c_int, [ctypes.POINTER(ModelDesc), ctypes.POINTER(PagedKV),
                                                         ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
                                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "quail_join_if": (ctypes.c_int, [ctypes.POINTER(ModelDesc), ctypes.POINTER(PagedKV), ctypes.c_void_p,
+                                     ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                     ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
     "quail_device_status": (ctypes.c_int, [ctypes.c_void_p]),
     "quail_set_stage_events": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
     "quail_launch_count": (ctypes.c_int32, []),
@@ -172,7 +177,8 @@ def _stream(stream) -> int | None:
 class Trie:
     """Library-owned label trie (quail_trie_build). labels: list of token-id lists."""
 
-    def __init__(self, labels, root_token: int, vocab: int, continuation=None, full_depth: bool = False):
+    def __init__(self, labels, root_token: int, vocab: int, continuation=None, full_depth: bool = False,
+                 all_nodes: bool = False):
         offs = np.zeros(len(labels) + 1, dtype=np.int64)
         offs[1:] = np.cumsum([len(l) for l in labels])
         toks = np.ascontiguousarray(np.array([t for l in labels for t in l], dtype=np.int32))
@@ -182,7 +188,8 @@ class Trie:
         h = ctypes.c_void_p()
         st = lib().quail_trie_build(toks.ctypes.data, offs.ctypes.data, len(labels), int(root_token), int(vocab),
                                     None if cont is None else cont.ctypes.data,
-                                    TRIE_FULL_DEPTH if full_depth else 0, ctypes.byref(h))
+                                    (TRIE_FULL_DEPTH if full_depth else 0) | (TRIE_ALL_NODES if all_nodes else 0),
+                                    ctypes.byref(h))
         _check(st)
         self._h = h
         self.num_labels = len(labels)
@@ -279,6 +286,17 @@ def classify_letters(model: Model, kv: KV, letter_tokens, root_token: int, num_d
         ctypes.byref(model.desc), ctypes.byref(kv.desc), lt.ctypes.data, len(lt), int(root_token), int(num_docs),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(letter_logprob), _ptr(letter_prob),
         _ptr(letter_argmax), _stream(stream)))
+
+
+def join_if(model: Model, kv: KV, partners: Trie, num_anchors: int, true_tokens, false_tokens, workspace, p_true,
+            stream=None) -> None:
+    """p_true [num_anchors, num_partners]: P(TRUE) at the end of every (anchor, partner) pair."""
+    tok = np.ascontiguousarray(np.concatenate([np.asarray(true_tokens, dtype=np.int32),
+                                               np.asarray(false_tokens, dtype=np.int32)]))
+    _check(lib().quail_join_if(
+        ctypes.byref(model.desc), ctypes.byref(kv.desc), partners.handle, int(num_anchors), tok.ctypes.data,
+        len(true_tokens), len(false_tokens), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(p_true), _stream(stream)))
 
 
 def classify_trie_decode_step(model: Model, kv: KV, trie: Trie, num_docs: int, node_cursor, label_out,

@@ -610,6 +610,10 @@ size_t quail_workspace_size(const quail_model_desc* model, const quail_trie* tri
       if (trie == nullptr) return 0;
       return plan(nullptr, model, trie->n_int(), num_docs, 1, max_doc_len, false, 0, true, 2 * num_docs + 4,
                   nullptr);
+    case QUAIL_MODE_JOIN_IF:
+      if (trie == nullptr || num_letters < 1) return 0;
+      return plan(nullptr, model, trie->n_eval(), num_docs, trie->num_labels, max_doc_len, false, 0, true,
+                  trie->num_labels + num_letters, nullptr);
   }
   return 0;
 }
@@ -761,6 +765,78 @@ quail_status quail_classify_letters(const quail_model_desc* model, const quail_p
   stage_mark(QUAIL_STAGE_HEAD, false, st);
   CUDA_TRY(launch_letters_head(b.z_f32, static_cast<const bf16*>(model->lm_head), b.small + 4, num_letters,
                                num_docs, model->hidden, letter_logprob, letter_prob, letter_argmax, st));
+  stage_mark(QUAIL_STAGE_HEAD, true, st);
+  return QUAIL_OK;
+}
+
+quail_status quail_join_if(const quail_model_desc* model, const quail_paged_kv* kv, quail_trie* partners,
+                           int32_t num_anchors, const int32_t* answer_tokens, int32_t n_true, int32_t n_false,
+                           void* workspace, size_t workspace_bytes, float* p_true, quail_stream_t stream) {
+  g_launches = 0;
+  quail_status s = check_model(model);
+  if (s != QUAIL_OK) return s;
+  s = check_kv(kv, model);
+  if (s != QUAIL_OK) return s;
+  if (partners == nullptr) return fail(QUAIL_ERR_INVALID_ARG, "partner trie is null");
+  if (partners->vocab != model->vocab)
+    return fail(QUAIL_ERR_INVALID_ARG, "trie vocab %d != model vocab %d", partners->vocab, model->vocab);
+  if (partners->n_eval() != partners->n_nodes())
+    return fail(QUAIL_ERR_INVALID_ARG, "the partner trie must be built with QUAIL_TRIE_ALL_NODES");
+  const int R = n_true + n_false;
+  if (answer_tokens == nullptr || n_true < 0 || n_false < 0 || R < 1 || R > kJoinMaxRows)
+    return fail(QUAIL_ERR_INVALID_ARG, "need 1..%d answer tokens (n_true, n_false >= 0)", kJoinMaxRows);
+  for (int i = 0; i < R; ++i) {
+    if (answer_tokens[i] < 0 || answer_tokens[i] >= model->vocab)
+      return fail(QUAIL_ERR_TOKEN_RANGE, "answer token %d is %d, outside [0, vocab)", i, answer_tokens[i]);
+  }
+  {
+    std::vector<int32_t> sorted(answer_tokens, answer_tokens + R);
+    std::sort(sorted.begin(), sorted.end());
+    if (std::adjacent_find(sorted.begin(), sorted.end()) != sorted.end())
+      return fail(QUAIL_ERR_DUPLICATE_LABEL, "answer tokens must be distinct");
+  }
+  if (num_anchors < 0) return fail(QUAIL_ERR_INVALID_ARG, "num_anchors < 0");
+  if (num_anchors == 0) return QUAIL_OK;
+  if (num_anchors > 65535) return fail(QUAIL_ERR_UNSUPPORTED_SHAPE, "at most 65535 anchors per call");
+  if (p_true == nullptr) return fail(QUAIL_ERR_INVALID_ARG, "p_true is null");
+  const int nodes = partners->n_eval();
+  const int M = partners->num_labels;
+  const size_t need = plan(nullptr, model, nodes, num_anchors, M, kv->max_doc_len, false, 0, true, M + R, nullptr);
+  s = check_workspace(workspace, workspace_bytes, need);
+  if (s != QUAIL_OK) return s;
+  DeviceState* ds = nullptr;
+  s = device_state(&ds);
+  if (s != QUAIL_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const quail_trie::DeviceImage* img = nullptr;
+  s = upload_trie(partners, st, &img);
+  if (s != QUAIL_OK) return s;
+  Buffers b;
+  plan(static_cast<uint8_t*>(workspace), model, nodes, num_anchors, M, kv->max_doc_len, false, 0, true, M + R, &b);
+  // small ints: [0, M) the node row of each partner's last token, [M, M + R) the answer tokens
+  std::vector<int32_t> host(M + R);
+  for (int m = 0; m < M; ++m) host[m] = partners->eval_index_of_node[partners->label_end_node[m]];
+  std::memcpy(host.data() + M, answer_tokens, R * sizeof(int32_t));
+  CUDA_TRY(cudaMemcpyAsync(b.small, host.data(), host.size() * sizeof(int32_t), cudaMemcpyHostToDevice, st));
+  const NodeTables nt{img->eval_token, img->eval_depth, img->eval_parent, nodes};
+  const RowMap map{M, nullptr, nullptr, nullptr, b.small};
+  const int rows = num_anchors * M;
+
+  stage_mark(QUAIL_STAGE_PROLOGUE, false, st);
+  s = run_prologue(model, nt, b, ds, st);
+  if (s != QUAIL_OK) return s;
+  stage_mark(QUAIL_STAGE_PROLOGUE, true, st);
+  stage_mark(QUAIL_STAGE_ATTENTION, false, st);
+  s = run_attention(model, kv, nt, map, num_anchors, b, ds, st);
+  if (s != QUAIL_OK) return s;
+  stage_mark(QUAIL_STAGE_ATTENTION, true, st);
+  stage_mark(QUAIL_STAGE_WO_NORM, false, st);
+  s = run_wo_norm(model, nt, map, rows, b, ds, st);
+  if (s != QUAIL_OK) return s;
+  stage_mark(QUAIL_STAGE_WO_NORM, true, st);
+  stage_mark(QUAIL_STAGE_HEAD, false, st);
+  CUDA_TRY(launch_join_head(b.z_f32, static_cast<const bf16*>(model->lm_head), b.small + M, n_true, R, rows, M,
+                            model->hidden, p_true, st));
   stage_mark(QUAIL_STAGE_HEAD, true, st);
   return QUAIL_OK;
 }

@@ -66,6 +66,7 @@ struct RowMap {
   const int* slot_node;   // nullable
   const int* slot_doc;    // nullable: slot -> document (identity when null)
   const int* n_slots_dev; // nullable: rows of slots >= *n_slots_dev are skipped
+  const int* row_nodes;   // nullable: query row e of every slot -> node row (identity when null)
 };
 
 // z = RMSNorm(sum_s h_part[s][r] + E[node_token[node(r)]]) * g_f over the
@@ -100,6 +101,13 @@ struct LabelScoreArgs {
 // the LSE reduce, per-label scores and per-document softmax as three kernels
 // spread over many CTAs.
 cudaError_t launch_label_score(const LabelScoreArgs& args, int num_docs, int num_sms, cudaStream_t st);
+
+// AI.IF on joined pairs: for every row of z_f32 [rows, d] (anchor * M +
+// partner), the softmax over the R answer-spelling rows of W_lm (tokens[0,
+// n_true) spell TRUE) and p_true[row] = the TRUE rows' share.
+constexpr int kJoinMaxRows = 64;
+cudaError_t launch_join_head(const float* z, const bf16* lm_head, const int* tokens, int n_true, int R, int rows,
+                             int M, int d, float* p_true, cudaStream_t st);
 
 // letters: logits of the M letter rows from z_f32 [N, d], renormalised softmax, argmax.
 cudaError_t launch_letters_head(const float* z, const bf16* lm_head, const int* letter_tokens, int M, int num_docs,

@@ -135,7 +135,8 @@ __global__ void __launch_bounds__(kNormThreads) final_norm_kernel(const float* _
   const int r = blockIdx.x;
   const int slot = r / map.nq;
   if (map.n_slots_dev != nullptr && slot >= *map.n_slots_dev) return;
-  const int node = map.slot_node ? map.slot_node[slot] : (r - slot * map.nq);
+  const int e = r - slot * map.nq;
+  const int node = map.slot_node ? map.slot_node[slot] : (map.row_nodes ? map.row_nodes[e] : e);
   const uint2* x = reinterpret_cast<const uint2*>(embed + static_cast<size_t>(__ldg(node_token + node)) * d);
   const float4* hp = reinterpret_cast<const float4*>(h_part + static_cast<size_t>(r) * d);
   const size_t slab4 = slab >> 2;
@@ -362,6 +363,41 @@ __global__ void label_softmax_kernel(LabelScoreArgs a) {
   for (int m = threadIdx.x; m < a.M; m += blockDim.x) out_p[m] = expf(ls[m] - mx) / total;
 }
 
+// AI.IF on joined pairs: CTA per (anchor, partner), warp per restricted row.
+// logit_r = z_f32[row] . W_lm[token_r] in fp32 for the R answer spellings
+// (the first n_true are TRUE's); p_true = sum of the TRUE rows' softmax over
+// the R rows.
+__global__ void join_head_kernel(const float* __restrict__ z, const bf16* __restrict__ lm_head,
+                                 const int* __restrict__ tokens, int n_true, int R, int M, int d,
+                                 float* __restrict__ p_true) {
+  __shared__ float s_logit[kJoinMaxRows];
+  const int row = blockIdx.x;  // anchor * M + partner
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const float* zr = z + static_cast<size_t>(row) * d;
+  for (int r = warp; r < R; r += nw) {
+    const bf16* w = lm_head + static_cast<size_t>(__ldg(tokens + r)) * d;
+    float acc = 0.f;
+    for (int i = lane * 2; i < d; i += 64) {
+      const float2 wv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(w + i));
+      acc += zr[i] * wv.x + zr[i + 1] * wv.y;
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) s_logit[r] = acc;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float mx = -INFINITY;
+    for (int r = 0; r < R; ++r) mx = fmaxf(mx, s_logit[r]);
+    float all = 0.f, yes = 0.f;
+    for (int r = 0; r < R; ++r) {
+      const float e = expf(s_logit[r] - mx);
+      all += e;
+      if (r < n_true) yes += e;
+    }
+    p_true[row] = yes / all;
+  }
+}
+
 // letters: one block per document, warp per letter row.
 __global__ void letters_head_kernel(const float* __restrict__ z, const bf16* __restrict__ lm_head,
                                     const int* __restrict__ letters, int M, int d, float* __restrict__ logprob,
@@ -574,6 +610,15 @@ cudaError_t launch_label_score(const LabelScoreArgs& args, int num_docs, int num
   if (e != cudaSuccess) return e;
   count_launch();
   label_softmax_kernel<<<num_docs, 512, 0, st>>>(args);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_join_head(const float* z, const bf16* lm_head, const int* tokens, int n_true, int R, int rows,
+                             int M, int d, float* p_true, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  if (R < 1 || R > kJoinMaxRows || n_true < 0 || n_true > R) return cudaErrorInvalidValue;
+  count_launch();
+  join_head_kernel<<<rows, 256, 0, st>>>(z, lm_head, tokens, n_true, R, M, d, p_true);
   return cudaGetLastError();
 }
 

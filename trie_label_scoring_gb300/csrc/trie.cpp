@@ -32,7 +32,7 @@ quail_status quail_build_trie_host(const int32_t* tokens, const int64_t* label_o
     *msg = "need at least 2 labels";
     return QUAIL_ERR_INVALID_ARG;
   }
-  if (vocab <= 0 || (flags & ~QUAIL_TRIE_FULL_DEPTH) != 0) {
+  if (vocab <= 0 || (flags & ~(QUAIL_TRIE_FULL_DEPTH | QUAIL_TRIE_ALL_NODES)) != 0) {
     *msg = "bad vocab or flags";
     return QUAIL_ERR_INVALID_ARG;
   }
@@ -188,6 +188,7 @@ quail_status quail_build_trie_host(const int32_t* tokens, const int64_t* label_o
       in_eval[end] = 1;
     }
   }
+  if (flags & QUAIL_TRIE_ALL_NODES) std::fill(in_eval.begin(), in_eval.end(), 1);  // every node evaluated
   t->eval_nodes.clear();
   t->eval_index_of_node.assign(n, -1);
   for (int32_t u = 0; u < n; ++u) {
