@@ -261,6 +261,53 @@ quail_status quail_classify_trie_tree_noalloc(const quail_model_desc* model, con
                                               const quail_trie* trie, int32_t num_docs, float* label_logscore,
                                               float* label_prob, int32_t* label_argmax, quail_stream_t stream);
 
+/* ------------------------------------------------------------ multi-layer
+ * trie_tree through a whole decoder stack ("To Classify, Try a Trie Tree",
+ * sec. 3.2 and 4.2: every answer position "goes through the whole LLM").
+ * Per layer (Qwen3-style): x = RMSNorm(h) g_in; q, k, v projections; per-head
+ * q/k RMSNorm; RoPE at l_i + depth; attention over the document's cached KV
+ * of that layer and the node's own path (ancestors and itself) at that layer;
+ * h += O W_o^T; h += W_down (SiLU(W_gate y) * W_up y), y = RMSNorm(h) g_post.
+ * Then z = RMSNorm(h) g_f and the output head, LSE and label scoring as in
+ * quail_classify_trie_tree. From layer 1 on a node's state depends on the
+ * document, so the rows are (document, evaluated node) pairs; the path part
+ * is computed per document. */
+typedef struct {
+  const void *w_q, *w_k, *w_v;      /* [H_q*128, d], [H_kv*128, d], [H_kv*128, d] */
+  const void *q_norm, *k_norm;      /* [128] */
+  const void *w_o;                  /* [d, H_q*128] */
+  const void *in_norm, *post_norm;  /* [d] */
+  const void *w_gate, *w_up;        /* [I, d] */
+  const void *w_down;               /* [d, I] */
+} quail_layer_weights;              /* device bf16, caller-owned */
+
+typedef struct {
+  int32_t hidden, n_q_heads, n_kv_heads, head_dim, vocab, intermediate, n_layers;
+  float rms_eps, rope_theta;
+  const void *embed, *final_norm, *lm_head;  /* device bf16 */
+  const quail_layer_weights* layers;         /* host array [n_layers] */
+} quail_model_ml_desc;
+
+typedef struct {
+  const void* const* k_pools;  /* host array [n_layers] of device pools [num_pages, n_kv_heads, 16, 128] */
+  const void* const* v_pools;
+  int32_t num_pages, page_size; /* page_size 16 */
+  const int32_t* page_table;    /* device [N, max_pages], shared by the layers */
+  int32_t max_pages;
+  const int32_t* doc_len;       /* device [N] */
+  int32_t max_doc_len;
+} quail_paged_kv_ml;
+
+/* Workspace bytes of quail_classify_trie_tree_ml; 0 on invalid arguments.
+ * intermediate must be a multiple of 256 (SwiGLU width). */
+size_t quail_workspace_size_ml(const quail_model_ml_desc* model, const quail_trie* trie, int32_t num_docs,
+                               int32_t max_doc_len);
+/* As quail_classify_trie_tree, through model->n_layers layers. */
+quail_status quail_classify_trie_tree_ml(const quail_model_ml_desc* model, const quail_paged_kv_ml* kv,
+                                         quail_trie* trie, int32_t num_docs, void* workspace, size_t workspace_bytes,
+                                         float* label_logscore, float* label_prob, int32_t* label_argmax,
+                                         quail_stream_t stream);
+
 /* AI.IF over joined pairs ("Building an Ultra-High Throughput AI-SQL Engine",
  * sec. 3.2.4 "specialize attention for joins"; Quail docs "Execution",
  * Joins): every anchor document, whose KV is cached, is paired with every

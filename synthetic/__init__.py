@@ -122,6 +122,7 @@ WORKLOADS = {
 }
 
 
+
 def with_docs(w: Workload, num_docs: int, doc_len: tuple | None = None) -> Workload:
     """The same workload with fewer/more documents (or other lengths): parity cases."""
     return dataclasses.replace(w, num_docs=num_docs, doc_len=doc_len or w.doc_len,
@@ -203,6 +204,74 @@ def make_docs(w: Workload, seed: int = 0) -> PagedDocs:
             k_pool[last, :, r:, :] = BF16_NAN
             v_pool[last, :, r:, :] = BF16_NAN
     return PagedDocs(lens, table, k_pool, v_pool)
+
+
+# --------------------------------------------------------------- multi-layer
+@dataclasses.dataclass(frozen=True)
+class MLWorkload:
+    """A Workload run through n_layers decoder layers (attention + SwiGLU MLP
+    of width `intermediate`) instead of the single attention block."""
+    name: str
+    base: Workload
+    n_layers: int
+    intermediate: int
+
+
+def _layer_streams(seed: int, layer: int, kind: int) -> list:
+    return np.random.SeedSequence([seed, kind, layer]).spawn(8)
+
+
+def make_model_ml(shape: LayerShape, n_layers: int, intermediate: int, seed: int = 0) -> dict:
+    """Random-init weights of an n_layers model: embed, lm_head, final_norm as
+    make_model, then per layer w_q, w_k, w_v, w_o, w_gate, w_up, w_down
+    (~N(0, std^2), nn.Linear layout) and unit norm gains (q, k, input,
+    post-attention). Layer l draws from SeedSequence([seed, 1, l])."""
+    base = make_model(shape, seed)
+    d, hq, hkv, hd = shape.hidden, shape.n_q_heads, shape.n_kv_heads, shape.head_dim
+    I, st = intermediate, shape.weight_std
+    layers = []
+    for l in range(n_layers):
+        ss = _layer_streams(seed, l, 1)
+        layers.append({
+            "w_q": _normal_bf16(ss[0], hq * hd * d, st).reshape(hq * hd, d),
+            "w_k": _normal_bf16(ss[1], hkv * hd * d, st).reshape(hkv * hd, d),
+            "w_v": _normal_bf16(ss[2], hkv * hd * d, st).reshape(hkv * hd, d),
+            "w_o": _normal_bf16(ss[3], d * hq * hd, st).reshape(d, hq * hd),
+            "w_gate": _normal_bf16(ss[4], I * d, st).reshape(I, d),
+            "w_up": _normal_bf16(ss[5], I * d, st).reshape(I, d),
+            "w_down": _normal_bf16(ss[6], d * I, st).reshape(d, I),
+            "q_norm": np.full(hd, BF16_ONE, dtype=np.uint16),
+            "k_norm": np.full(hd, BF16_ONE, dtype=np.uint16),
+            "in_norm": np.full(d, BF16_ONE, dtype=np.uint16),
+            "post_norm": np.full(d, BF16_ONE, dtype=np.uint16),
+        })
+    return {"embed": base["embed"], "lm_head": base["lm_head"], "final_norm": base["final_norm"], "layers": layers}
+
+
+def make_docs_ml(w: Workload, n_layers: int, seed: int = 0) -> tuple:
+    """Paged document KV of every layer: lengths, page table and layer 0's
+    pools as make_docs; layer l >= 1 pools from SeedSequence([seed, 2, l]),
+    NaN past each document's end likewise. Returns (PagedDocs of layer 0,
+    [k_pool per layer], [v_pool per layer])."""
+    d0 = make_docs(w, seed)
+    ks, vs = [d0.k_pool], [d0.v_pool]
+    sh = w.shape
+    shape = d0.k_pool.shape
+    n = int(np.prod(shape))
+    npages = (d0.doc_len + PAGE_SIZE - 1) // PAGE_SIZE
+    for l in range(1, n_layers):
+        ss = _layer_streams(seed, l, 2)
+        k = _normal_bf16(ss[0], n, sh.kv_std).reshape(shape)
+        v = _normal_bf16(ss[1], n, sh.kv_std).reshape(shape)
+        for i in range(w.num_docs):
+            r = int(d0.doc_len[i]) % PAGE_SIZE
+            if r:
+                last = d0.page_table[i, npages[i] - 1]
+                k[last, :, r:, :] = BF16_NAN
+                v[last, :, r:, :] = BF16_NAN
+        ks.append(k)
+        vs.append(v)
+    return d0, ks, vs
 
 
 # --------------------------------------------------------------- labels
@@ -329,3 +398,13 @@ def make_answers(seed: int, V: int) -> tuple:
     rng = np.random.Generator(np.random.PCG64(_streams(seed)[_STREAM["letters"]]))
     ids = [int(t) for t in _distinct(rng, 8, V)]
     return ids[:4], ids[4:]
+
+
+ML_WORKLOADS = {
+    w.name: w
+    for w in (
+        MLWorkload("tiny-L3-support10-4x128", WORKLOADS["tiny-support10-4x128"], 3, 1024),
+        MLWorkload("qwen3-4b-L36-support10-64docs",
+                   Workload("qwen3-4b-support10-64docs", QWEN3_4B, 64, (128, 1024), "support"), 36, 9728),
+    )
+}

@@ -14,6 +14,8 @@ Entry points (same names as the C ABI, without the quail_ prefix):
   classify_trie_decode_step(...) -> quail_classify_trie_decode_step
   classify_trie_tree_noalloc(...) -> quail_classify_trie_tree_noalloc
   join_if(...)                   -> quail_join_if
+  ModelML, KVML, workspace_size_ml(...), classify_trie_tree_ml(...)
+                                 -> quail_workspace_size_ml / quail_classify_trie_tree_ml
   device_status(...)             -> quail_device_status
   set_stage_events(...)          -> quail_set_stage_events
   launch_count()                 -> quail_launch_count
@@ -72,6 +74,25 @@ class MethodCost(ctypes.Structure):
         "head_bytes", "t_head", "t_proj", "t_attn", "t_mlp", "t_classify")]
 
 
+class LayerWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("w_q", "w_k", "w_v", "q_norm", "k_norm", "w_o", "in_norm",
+                                               "post_norm", "w_gate", "w_up", "w_down")]
+
+
+class ModelMLDesc(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("vocab", ctypes.c_int32), ("intermediate", ctypes.c_int32),
+                ("n_layers", ctypes.c_int32), ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float),
+                ("embed", ctypes.c_void_p), ("final_norm", ctypes.c_void_p), ("lm_head", ctypes.c_void_p),
+                ("layers", ctypes.POINTER(LayerWeights))]
+
+
+class PagedKVML(ctypes.Structure):
+    _fields_ = [("k_pools", ctypes.POINTER(ctypes.c_void_p)), ("v_pools", ctypes.POINTER(ctypes.c_void_p)),
+                ("num_pages", ctypes.c_int32), ("page_size", ctypes.c_int32), ("page_table", ctypes.c_void_p),
+                ("max_pages", ctypes.c_int32), ("doc_len", ctypes.c_void_p), ("max_doc_len", ctypes.c_int32)]
+
+
 class ModelDesc(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("vocab", ctypes.c_int32), ("rms_eps", ctypes.c_float),
@@ -126,6 +147,12 @@ _SIGNATURES = {
     "quail_join_if": (ctypes.c_int, [ctypes.POINTER(ModelDesc), ctypes.POINTER(PagedKV), ctypes.c_void_p,
                                      ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                      ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
+    "quail_workspace_size_ml": (ctypes.c_size_t, [ctypes.POINTER(ModelMLDesc), ctypes.c_void_p, ctypes.c_int32,
+                                                  ctypes.c_int32]),
+    "quail_classify_trie_tree_ml": (ctypes.c_int, [ctypes.POINTER(ModelMLDesc), ctypes.POINTER(PagedKVML),
+                                                   ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t,
+                                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                   ctypes.c_void_p]),
     "quail_device_status": (ctypes.c_int, [ctypes.c_void_p]),
     "quail_set_stage_events": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
     "quail_launch_count": (ctypes.c_int32, []),
@@ -261,6 +288,32 @@ class KV:
                             int(page_table.shape[1]), _ptr(doc_len), int(max_doc_len))
 
 
+class ModelML:
+    """quail_model_ml_desc over device bf16 tensors: shared (embed, final_norm,
+    lm_head) and per-layer dicts of w_q, w_k, w_v, q_norm, k_norm, w_o, in_norm,
+    post_norm, w_gate, w_up, w_down (kept alive by this object)."""
+
+    def __init__(self, shared: dict, layers: list, hidden: int, n_q_heads: int, n_kv_heads: int, vocab: int,
+                 intermediate: int, rms_eps: float = 1e-6, rope_theta: float = 1e6, head_dim: int = 128):
+        self.shared, self.layers = shared, layers
+        self._lw = (LayerWeights * len(layers))(*[LayerWeights(*[_ptr(l[n]) for n, _ in LayerWeights._fields_])
+                                                  for l in layers])
+        self.desc = ModelMLDesc(hidden, n_q_heads, n_kv_heads, head_dim, vocab, intermediate, len(layers), rms_eps,
+                                rope_theta, _ptr(shared["embed"]), _ptr(shared["final_norm"]),
+                                _ptr(shared["lm_head"]), self._lw)
+
+
+class KVML:
+    """quail_paged_kv_ml: one K and one V pool per layer, a shared page table."""
+
+    def __init__(self, k_pools: list, v_pools: list, page_table, doc_len, max_doc_len: int):
+        self.tensors = (k_pools, v_pools, page_table, doc_len)
+        self._k = (ctypes.c_void_p * len(k_pools))(*[_ptr(t) for t in k_pools])
+        self._v = (ctypes.c_void_p * len(v_pools))(*[_ptr(t) for t in v_pools])
+        self.desc = PagedKVML(self._k, self._v, int(k_pools[0].shape[0]), 16, _ptr(page_table),
+                              int(page_table.shape[1]), _ptr(doc_len), int(max_doc_len))
+
+
 # ------------------------------------------------------------------ calls
 def workspace_size(model: Model, trie: Trie | None, num_letters: int, num_docs: int, max_doc_len: int,
                    mode: int) -> int:
@@ -351,3 +404,18 @@ def estimate_methods(model: dict, workload: dict, trie: "Trie") -> tuple:
         c = out[i]
         res[name] = ({k: getattr(c, k) for k, _ in MethodCost._fields_ if k != "runnable"} if c.runnable else None)
     return METHODS[best.value], res
+
+
+def workspace_size_ml(model: ModelML, trie: Trie, num_docs: int, max_doc_len: int) -> int:
+    n = lib().quail_workspace_size_ml(ctypes.byref(model.desc), trie.handle, int(num_docs), int(max_doc_len))
+    if n == 0:
+        raise QuailError(-1, "workspace_size_ml: invalid arguments")
+    return int(n)
+
+
+def classify_trie_tree_ml(model: ModelML, kv: KVML, trie: Trie, num_docs: int, workspace, label_logscore,
+                          label_prob, label_argmax, stream=None) -> None:
+    _check(lib().quail_classify_trie_tree_ml(
+        ctypes.byref(model.desc), ctypes.byref(kv.desc), trie.handle, int(num_docs), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(label_logscore), _ptr(label_prob), _ptr(label_argmax),
+        _stream(stream)))

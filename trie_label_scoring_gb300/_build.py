@@ -14,7 +14,7 @@ OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libquail.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-CUDA_SOURCES = ["api.cu", "gemm.cu", "attention.cu", "attention_tc.cu", "layer.cu"]
+CUDA_SOURCES = ["api.cu", "gemm.cu", "attention.cu", "attention_tc.cu", "layer.cu", "mlp.cu"]
 CXX_SOURCES = ["trie.cpp", "cost.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -297,12 +297,21 @@ struct NodeTables {
 // Node prologue: x^ = RMSNorm(E[tok]) g_in (two-term bf16 split);
 // q|k|v = x^ W^T in one launch when the three weight blocks align to 256 rows;
 // per-head q/k RMSNorm while summing the k-split slabs.
+quail_status run_qkv(const quail_model_desc* m, const NodeTables& nt, const Buffers& b, DeviceState* ds,
+                     cudaStream_t st);
+
 quail_status run_prologue(const quail_model_desc* m, const NodeTables& nt, const Buffers& b, DeviceState* ds,
                           cudaStream_t st) {
+  CUDA_TRY(launch_embed_rmsnorm(static_cast<const bf16*>(m->embed), nt.token, nt.nodes, m->hidden,
+                                static_cast<const bf16*>(m->in_norm), m->rms_eps, b.xhat, st));
+  return run_qkv(m, nt, b, ds, st);
+}
+
+// q|k|v = x^ W^T from the split rows already in b.xhat; per-head q/k RMSNorm.
+quail_status run_qkv(const quail_model_desc* m, const NodeTables& nt, const Buffers& b, DeviceState* ds,
+                     cudaStream_t st) {
   const int d = m->hidden, hq = m->n_q_heads, hkv = m->n_kv_heads;
   const int ldq = (hq + 2 * hkv) * 128;
-  CUDA_TRY(launch_embed_rmsnorm(static_cast<const bf16*>(m->embed), nt.token, nt.nodes, d,
-                                static_cast<const bf16*>(m->in_norm), m->rms_eps, b.xhat, st));
   CUtensorMap tA;
   quail_status s = encode_2d_bf16(&tA, b.xhat, round_up(nt.nodes, 128), 2 * d, 2 * d, 64, 128);
   if (s != QUAIL_OK) return s;
@@ -384,8 +393,20 @@ quail_status run_attention(const quail_model_desc* m, const quail_paged_kv* kv, 
 }
 
 // h = x + O W_o^T (O as a two-term bf16 split); z = RMSNorm(h) g_f.
+quail_status run_wo_gemm(const quail_model_desc* m, int rows, const Buffers& b, DeviceState* ds, cudaStream_t st);
+
 quail_status run_wo_norm(const quail_model_desc* m, const NodeTables& nt, RowMap map, int rows, const Buffers& b,
                          DeviceState* ds, cudaStream_t st) {
+  quail_status s = run_wo_gemm(m, rows, b, ds, st);
+  if (s != QUAIL_OK) return s;
+  const size_t slab = static_cast<size_t>(rows) * m->hidden;
+  CUDA_TRY(launch_final_norm(b.h_part, b.gp.ks_wo, slab, static_cast<const bf16*>(m->embed), nt.token, map, rows,
+                             m->hidden, static_cast<const bf16*>(m->final_norm), m->rms_eps, b.z, b.z_f32, st));
+  return QUAIL_OK;
+}
+
+// W_o projection of the split O rows into b.h_part (ks_wo fp32 slabs).
+quail_status run_wo_gemm(const quail_model_desc* m, int rows, const Buffers& b, DeviceState* ds, cudaStream_t st) {
   const int d = m->hidden, hq = m->n_q_heads;
   CUtensorMap tA;
   quail_status s = encode_2d_bf16(&tA, b.attn_out, round_up(rows, 128), 2 * hq * 128, 2 * hq * 128, 64, 128);
@@ -398,8 +419,6 @@ quail_status run_wo_norm(const quail_model_desc* m, const NodeTables& nt, RowMap
   bs.count = 1;
   const size_t slab = static_cast<size_t>(rows) * d;
   CUDA_TRY(launch_gemm_proj(tA, bs, rows, d, hq * 128, b.gp.ks_wo, b.h_part, slab, d, ds->num_sms, ds->err, st));
-  CUDA_TRY(launch_final_norm(b.h_part, b.gp.ks_wo, slab, static_cast<const bf16*>(m->embed), nt.token, map, rows, d,
-                             static_cast<const bf16*>(m->final_norm), m->rms_eps, b.z, b.z_f32, st));
   return QUAIL_OK;
 }
 
@@ -505,6 +524,116 @@ quail_status copy_trie_tree_image(const quail_trie* t, uint8_t* dst, cudaStream_
     *fields[i] = reinterpret_cast<const int32_t*>(dst + off);
     off += round_up(std::max<size_t>(arrays[i]->size(), 1) * 4, 256);
   }
+  return QUAIL_OK;
+}
+
+
+// ------------------------------------------------------------------ multi-layer path
+// One layer of the stack as a single-layer descriptor (the shared steps take it).
+quail_model_desc layer_desc(const quail_model_ml_desc* m, int l) {
+  quail_model_desc d{};
+  d.hidden = m->hidden;
+  d.n_q_heads = m->n_q_heads;
+  d.n_kv_heads = m->n_kv_heads;
+  d.head_dim = m->head_dim;
+  d.vocab = m->vocab;
+  d.rms_eps = m->rms_eps;
+  d.rope_theta = m->rope_theta;
+  d.embed = m->embed;
+  d.final_norm = m->final_norm;
+  d.lm_head = m->lm_head;
+  const quail_layer_weights& w = m->layers[l];
+  d.w_q = w.w_q;
+  d.w_k = w.w_k;
+  d.w_v = w.w_v;
+  d.q_norm = w.q_norm;
+  d.k_norm = w.k_norm;
+  d.w_o = w.w_o;
+  d.in_norm = w.in_norm;
+  return d;
+}
+
+quail_status check_model_ml(const quail_model_ml_desc* m) {
+  if (m == nullptr) return fail(QUAIL_ERR_INVALID_ARG, "model is null");
+  if (m->n_layers < 1 || m->layers == nullptr) return fail(QUAIL_ERR_INVALID_ARG, "need n_layers >= 1 and layers");
+  if (m->intermediate < 256 || m->intermediate % 256 != 0 || m->intermediate > 65536)
+    return fail(QUAIL_ERR_UNSUPPORTED_SHAPE, "intermediate must be a multiple of 256 in [256, 65536] (got %d)",
+                m->intermediate);
+  for (int l = 0; l < m->n_layers; ++l) {
+    const quail_model_desc d = layer_desc(m, l);
+    const quail_status s = check_model(&d);
+    if (s != QUAIL_OK) return s;
+    const quail_layer_weights& w = m->layers[l];
+    for (const void* p : {w.post_norm, w.w_gate, w.w_up, w.w_down}) {
+      if (p == nullptr || !aligned16(p)) return fail(QUAIL_ERR_INVALID_ARG, "layer %d: MLP weight null or misaligned", l);
+    }
+  }
+  return QUAIL_OK;
+}
+
+quail_paged_kv layer_kv(const quail_paged_kv_ml* kv, int l) {
+  quail_paged_kv k{};
+  k.k_pool = kv->k_pools[l];
+  k.v_pool = kv->v_pools[l];
+  k.num_pages = kv->num_pages;
+  k.page_size = kv->page_size;
+  k.page_table = kv->page_table;
+  k.max_pages = kv->max_pages;
+  k.doc_len = kv->doc_len;
+  k.max_doc_len = kv->max_doc_len;
+  return k;
+}
+
+struct MLBuffers {
+  Buffers b;        // rows of the shared steps = (document, evaluated node)
+  float* h;         // [rows, d] residual stream
+  bf16* act;        // [rows_p, 2I] SiLU(gate) * up, split
+  float* gu_part;   // [ks_gu, rows, 2I]
+  float* dn_part;   // [ks_dn, rows, d]
+  int ks_gu, ks_dn;
+};
+
+size_t plan_ml(uint8_t* base, const quail_model_ml_desc* m, const quail_trie* t, int N, int max_doc_len,
+               MLBuffers* out) {
+  const quail_model_desc d0 = layer_desc(m, 0);
+  const int a = t->n_eval();
+  const int rows = N * a;
+  MLBuffers x{};
+  const size_t base_bytes = round_up(plan(base, &d0, rows, N, a, max_doc_len, true, t->eval_child_offsets.back(),
+                                           false, 3 * rows, base ? &x.b : nullptr),
+                                      256);  // the extras start 256-byte aligned like every carved buffer
+  const int sms = planning_sms();
+  const int I = m->intermediate, d = m->hidden;
+  const int m_tiles = static_cast<int>(round_up(rows, 128) / 128);
+  x.ks_gu = choose_k_splits(m_tiles * (2 * I / 256), d / 64, sms);
+  x.ks_dn = choose_k_splits(m_tiles * static_cast<int>(round_up(d, 256) / 256), I / 64, sms);
+  Carver c{base ? base + base_bytes : nullptr};
+  x.h = c.take<float>(static_cast<size_t>(rows) * d);
+  x.act = c.take<bf16>(round_up(rows, 128) * 2 * I);
+  x.gu_part = c.take<float>(static_cast<size_t>(x.ks_gu) * rows * 2 * I);
+  x.dn_part = c.take<float>(static_cast<size_t>(x.ks_dn) * rows * d);
+  if (out) *out = x;
+  return base_bytes + c.off + 256;
+}
+
+// C[ks] = A W^T over the split A rows (A [rows_p, 2K] bf16, W [n, K] bf16 blocks).
+quail_status run_split_gemm(const bf16* A, int rows, int K, const void* const* w, const int* nrows, int count,
+                            int ks, float* C, int ldc, DeviceState* ds, cudaStream_t st) {
+  CUtensorMap tA;
+  quail_status s = encode_2d_bf16(&tA, A, round_up(rows, 128), 2 * K, 2 * K, 64, 128);
+  if (s != QUAIL_OK) return s;
+  BSet bs{};
+  int col = 0;
+  for (int i = 0; i < count; ++i) {
+    s = encode_2d_bf16(&bs.map[i], w[i], nrows[i], K, K, 64, 256);
+    if (s != QUAIL_OK) return s;
+    bs.n_begin[i] = col;
+    col += nrows[i];
+    bs.n_begin[i + 1] = col;
+  }
+  bs.count = count;
+  const size_t slab = static_cast<size_t>(rows) * ldc;
+  CUDA_TRY(launch_gemm_proj(tA, bs, rows, col, K, ks, C, slab, ldc, ds->num_sms, ds->err, st));
   return QUAIL_OK;
 }
 
@@ -766,6 +895,126 @@ quail_status quail_classify_letters(const quail_model_desc* model, const quail_p
   CUDA_TRY(launch_letters_head(b.z_f32, static_cast<const bf16*>(model->lm_head), b.small + 4, num_letters,
                                num_docs, model->hidden, letter_logprob, letter_prob, letter_argmax, st));
   stage_mark(QUAIL_STAGE_HEAD, true, st);
+  return QUAIL_OK;
+}
+
+size_t quail_workspace_size_ml(const quail_model_ml_desc* model, const quail_trie* trie, int32_t num_docs,
+                               int32_t max_doc_len) {
+  if (model == nullptr || trie == nullptr || num_docs < 0 || max_doc_len <= 0 || model->n_layers < 1 ||
+      model->layers == nullptr || model->intermediate < 256 || model->intermediate % 256 != 0)
+    return 0;
+  if (model->n_kv_heads <= 0 || model->n_q_heads <= 0 || model->hidden <= 0 || model->vocab <= 0) return 0;
+  return plan_ml(nullptr, model, trie, num_docs, max_doc_len, nullptr);
+}
+
+quail_status quail_classify_trie_tree_ml(const quail_model_ml_desc* model, const quail_paged_kv_ml* kv,
+                                         quail_trie* trie, int32_t num_docs, void* workspace, size_t workspace_bytes,
+                                         float* label_logscore, float* label_prob, int32_t* label_argmax,
+                                         quail_stream_t stream) {
+  g_launches = 0;
+  quail_status s = check_model_ml(model);
+  if (s != QUAIL_OK) return s;
+  if (kv == nullptr || kv->k_pools == nullptr || kv->v_pools == nullptr) return fail(QUAIL_ERR_INVALID_ARG, "kv is null");
+  const quail_model_desc d0 = layer_desc(model, 0);
+  for (int l = 0; l < model->n_layers; ++l) {
+    const quail_paged_kv kl = layer_kv(kv, l);
+    s = check_kv(&kl, &d0);
+    if (s != QUAIL_OK) return s;
+  }
+  if (trie == nullptr) return fail(QUAIL_ERR_INVALID_ARG, "trie is null");
+  if (trie->vocab != model->vocab)
+    return fail(QUAIL_ERR_INVALID_ARG, "trie vocab %d != model vocab %d", trie->vocab, model->vocab);
+  if (num_docs < 0) return fail(QUAIL_ERR_INVALID_ARG, "num_docs < 0");
+  if (num_docs == 0) return QUAIL_OK;
+  if (num_docs > 65535) return fail(QUAIL_ERR_UNSUPPORTED_SHAPE, "at most 65535 documents per call");
+  if (label_logscore == nullptr || label_prob == nullptr || label_argmax == nullptr)
+    return fail(QUAIL_ERR_INVALID_ARG, "an output pointer is null");
+  const int a = trie->n_eval();
+  const int rows = num_docs * a;
+  const int n_child = trie->eval_child_offsets.back();
+  const size_t need = plan_ml(nullptr, model, trie, num_docs, kv->max_doc_len, nullptr);
+  s = check_workspace(workspace, workspace_bytes, need);
+  if (s != QUAIL_OK) return s;
+  DeviceState* ds = nullptr;
+  s = device_state(&ds);
+  if (s != QUAIL_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const quail_trie::DeviceImage* img = nullptr;
+  s = upload_trie(trie, st, &img);
+  if (s != QUAIL_OK) return s;
+  MLBuffers x;
+  plan_ml(static_cast<uint8_t*>(workspace), model, trie, num_docs, kv->max_doc_len, &x);
+  const Buffers& b = x.b;
+  // node tables of the (document, evaluated node) rows: N disjoint copies of P
+  std::vector<int32_t> host(3 * static_cast<size_t>(rows));
+  for (int i = 0; i < num_docs; ++i) {
+    for (int e = 0; e < a; ++e) {
+      const size_t r = static_cast<size_t>(i) * a + e;
+      host[r] = trie->eval_token[e];
+      host[rows + r] = trie->eval_depth[e];
+      host[2 * static_cast<size_t>(rows) + r] = trie->eval_parent[e] < 0 ? -1 : i * a + trie->eval_parent[e];
+    }
+  }
+  CUDA_TRY(cudaMemcpyAsync(b.small, host.data(), host.size() * sizeof(int32_t), cudaMemcpyHostToDevice, st));
+  const NodeTables nt{b.small, b.small + rows, b.small + 2 * static_cast<size_t>(rows), rows};
+  const RowMap map{a, nullptr, nullptr, nullptr, nullptr, a};
+  const int d = model->hidden, I = model->intermediate;
+
+  stage_mark(QUAIL_STAGE_PROLOGUE, false, st);
+  CUDA_TRY(launch_gather_embed(static_cast<const bf16*>(model->embed), nt.token, rows, d, x.h, st));
+  for (int l = 0; l < model->n_layers; ++l) {
+    const quail_model_desc ml = layer_desc(model, l);
+    const quail_paged_kv kl = layer_kv(kv, l);
+    const quail_layer_weights& w = model->layers[l];
+    // h += previous layer's MLP output (none before layer 0); x^ = split(RMSNorm(h) g_in)
+    CUDA_TRY(launch_residual_norm(x.h, x.dn_part, l == 0 ? 0 : x.ks_dn, static_cast<size_t>(rows) * d, rows, d,
+                                  static_cast<const bf16*>(w.in_norm), model->rms_eps, b.xhat, st));
+    s = run_qkv(&ml, nt, b, ds, st);
+    if (s != QUAIL_OK) return s;
+    s = run_attention(&ml, &kl, nt, map, num_docs, b, ds, st);
+    if (s != QUAIL_OK) return s;
+    s = run_wo_gemm(&ml, rows, b, ds, st);
+    if (s != QUAIL_OK) return s;
+    // h += O W_o^T; y = split(RMSNorm(h) g_post)
+    CUDA_TRY(launch_residual_norm(x.h, b.h_part, b.gp.ks_wo, static_cast<size_t>(rows) * d, rows, d,
+                                  static_cast<const bf16*>(w.post_norm), model->rms_eps, b.xhat, st));
+    const void* gu[2] = {w.w_gate, w.w_up};
+    const int gu_rows[2] = {I, I};
+    s = run_split_gemm(b.xhat, rows, d, gu, gu_rows, 2, x.ks_gu, x.gu_part, 2 * I, ds, st);
+    if (s != QUAIL_OK) return s;
+    CUDA_TRY(launch_silu_mul_split(x.gu_part, x.ks_gu, static_cast<size_t>(rows) * 2 * I, rows, I, x.act, st));
+    const void* dn[1] = {w.w_down};
+    const int dn_rows[1] = {d};
+    s = run_split_gemm(x.act, rows, I, dn, dn_rows, 1, x.ks_dn, x.dn_part, d, ds, st);
+    if (s != QUAIL_OK) return s;
+  }
+  CUDA_TRY(launch_residual_norm(x.h, x.dn_part, x.ks_dn, static_cast<size_t>(rows) * d, rows, d, nullptr,
+                                model->rms_eps, nullptr, st));
+  CUDA_TRY(launch_norm_out(x.h, rows, d, static_cast<const bf16*>(model->final_norm), model->rms_eps, b.z, b.z_f32,
+                           st));
+  stage_mark(QUAIL_STAGE_PROLOGUE, true, st);
+
+  stage_mark(QUAIL_STAGE_HEAD, false, st);
+  {
+    const int n_tiles = (model->vocab + kHeadBN - 1) / kHeadBN;
+    CUtensorMap tA, tB;
+    s = encode_2d_bf16(&tA, b.z, round_up(rows, 128), d, d, 64, 128);
+    if (s != QUAIL_OK) return s;
+    s = encode_2d_bf16(&tB, model->lm_head, model->vocab, d, d, 64, kHeadBBoxRows);
+    if (s != QUAIL_OK) return s;
+    HeadEpilogueArgs ha{b.lse_part, b.child_logit, img->eval_child_offsets, img->eval_child_tokens, b.z_f32,
+                        static_cast<const bf16*>(model->lm_head), d, a, n_child, n_tiles};
+    CUDA_TRY(launch_gemm_head(tA, tB, rows, model->vocab, d, ha, ds->num_sms, ds->err, st));
+  }
+  stage_mark(QUAIL_STAGE_HEAD, true, st);
+  stage_mark(QUAIL_STAGE_SCORING, false, st);
+  LabelScoreArgs la{b.child_logit,          b.lse_part,           (model->vocab + kHeadBN - 1) / kHeadBN,
+                    b.lse,                  img->label_term_offsets, img->label_term_eval,
+                    img->label_term_slot,   img->label_prefix_eval,  img->eval_child_offsets,
+                    a,                      n_child,              trie->num_labels,
+                    label_logscore,         label_prob,           label_argmax};
+  CUDA_TRY(launch_label_score(la, num_docs, ds->num_sms, st));
+  stage_mark(QUAIL_STAGE_SCORING, true, st);
   return QUAIL_OK;
 }
 

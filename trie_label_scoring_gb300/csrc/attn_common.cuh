@@ -61,7 +61,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 __device__ __forceinline__ int row_doc(const RowMap& m, int slot) { return m.slot_doc ? m.slot_doc[slot] : slot; }
 __device__ __forceinline__ int row_node(const RowMap& m, int slot, int e) {
-  return m.slot_node ? m.slot_node[slot] : (m.row_nodes ? m.row_nodes[e] : e);
+  return m.slot_node ? m.slot_node[slot] : slot * m.slot_stride + (m.row_nodes ? m.row_nodes[e] : e);
 }
 
 }  // namespace quail

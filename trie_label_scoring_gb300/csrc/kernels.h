@@ -67,6 +67,7 @@ struct RowMap {
   const int* slot_doc;    // nullable: slot -> document (identity when null)
   const int* n_slots_dev; // nullable: rows of slots >= *n_slots_dev are skipped
   const int* row_nodes;   // nullable: query row e of every slot -> node row (identity when null)
+  int slot_stride;        // node rows of slot s start at s * slot_stride (0: shared by all slots)
 };
 
 // z = RMSNorm(sum_s h_part[s][r] + E[node_token[node(r)]]) * g_f over the
@@ -101,6 +102,19 @@ struct LabelScoreArgs {
 // the LSE reduce, per-label scores and per-document softmax as three kernels
 // spread over many CTAs.
 cudaError_t launch_label_score(const LabelScoreArgs& args, int num_docs, int num_sms, cudaStream_t st);
+
+// Multi-layer path (mlp.cu): the fp32 residual stream h [rows, d].
+// h[r] = E[tokens[r]].
+cudaError_t launch_gather_embed(const bf16* embed, const int* tokens, int rows, int d, float* h, cudaStream_t st);
+// h += sum of ks slabs of part (ks may be 0); out (nullable) = split(RMSNorm(h) * gain) [rows, 2d].
+cudaError_t launch_residual_norm(float* h, const float* part, int ks, size_t slab, int rows, int d, const bf16* gain,
+                                 float eps, bf16* out, cudaStream_t st);
+// act [rows, 2I] = split(SiLU(gate) * up) from ks slabs of [rows, 2I] (gate | up).
+cudaError_t launch_silu_mul_split(const float* part, int ks, size_t slab, int rows, int I, bf16* act,
+                                  cudaStream_t st);
+// z = RMSNorm(h) * gain as bf16 [rows, d] and fp32 (nullable).
+cudaError_t launch_norm_out(const float* h, int rows, int d, const bf16* gain, float eps, bf16* z, float* z_f32,
+                            cudaStream_t st);
 
 // AI.IF on joined pairs: for every row of z_f32 [rows, d] (anchor * M +
 // partner), the softmax over the R answer-spelling rows of W_lm (tokens[0,

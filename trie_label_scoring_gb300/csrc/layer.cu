@@ -136,7 +136,8 @@ __global__ void __launch_bounds__(kNormThreads) final_norm_kernel(const float* _
   const int slot = r / map.nq;
   if (map.n_slots_dev != nullptr && slot >= *map.n_slots_dev) return;
   const int e = r - slot * map.nq;
-  const int node = map.slot_node ? map.slot_node[slot] : (map.row_nodes ? map.row_nodes[e] : e);
+  const int node =
+      map.slot_node ? map.slot_node[slot] : slot * map.slot_stride + (map.row_nodes ? map.row_nodes[e] : e);
   const uint2* x = reinterpret_cast<const uint2*>(embed + static_cast<size_t>(__ldg(node_token + node)) * d);
   const float4* hp = reinterpret_cast<const float4*>(h_part + static_cast<size_t>(r) * d);
   const size_t slab4 = slab >> 2;
