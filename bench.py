@@ -200,6 +200,9 @@ def run_reference(args, world, rank):
     from oracle import scoring as OS
     from oracle.trie import build_trie
     from tests import gpu_cases as C
+    if args.workload in S.ML_WORKLOADS:
+        run_reference_ml(args, world)
+        return
     w = S.WORKLOADS[args.workload]
     if args.docs:
         w = S.with_docs(w, args.docs)
@@ -227,6 +230,31 @@ def run_reference(args, world, rank):
         "warmup": args.warmup, "ms_per_step": 1e3 * el / steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
         "config": {"workload": w.name, "docs_per_step": 1},
+        "cpu_baseline": {"value": value, "unit": "docs/s", "cores": cores(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "docs/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def run_reference_ml(args, world):
+    """The multi-layer oracle on one document per step (see time_oracle_ml)."""
+    import synthetic as S
+    mw = S.ML_WORKLOADS[args.workload]
+    base = S.with_docs(mw.base, args.docs) if args.docs else mw.base
+    bits = S.make_model_ml(base.shape, 2, mw.intermediate, 0)
+    docs_ml = S.make_docs_ml(base, 2, 0)
+    labels = S.make_labels(base, 0)
+    steps = args.steps if args.steps is not None else 1
+    rates = [time_oracle_ml(mw, base, bits, docs_ml, labels, budget_s=60.0) for _ in range(steps)]
+    value = statistics.mean(r["docs_per_s"] for r in rates)
+    sample = (f"document 0 of {base.name} through the first 1 and 2 layers per step; time per document "
+              f"extrapolated to {mw.n_layers} layers")
+    out = {
+        "impl": "reference", "metric": f"documents classified/sec at 1 GB300 (trie_tree through {mw.n_layers} "
+                                       f"decoder layers)",
+        "value": value, "unit": "docs/s", "n_gpus": world, "steps": steps, "warmup": 0,
+        "ms_per_step": 1e3 / value, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded)", "config": {"workload": mw.name, "docs_per_step": 1},
         "cpu_baseline": {"value": value, "unit": "docs/s", "cores": cores(), "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "docs/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -497,6 +525,217 @@ def run_join(args, world, rank, local):
         print(json.dumps(out), flush=True)
 
 
+def time_oracle_ml(mw, base, bits, docs_ml, labels, budget_s: float) -> dict:
+    """The multi-layer oracle, as it stands, on document 0 through the first
+    one and the first two layers of the stack; the full stack's time per
+    document is extrapolated as t1 + (n_layers - 1) * (t2 - t1)."""
+    import numpy as np
+
+    from oracle import multilayer as ML
+    from oracle.trie import build_trie
+    d0, ks, vs = docs_ml
+    n = int(d0.doc_len[0])
+    pages = d0.page_table[0, : (n + 15) // 16]
+
+    def kv(l):
+        import oracle.model as OM
+        k = ks[l][pages].transpose(0, 2, 1, 3).reshape(-1, ks[l].shape[1], ks[l].shape[3])[:n]
+        v = vs[l][pages].transpose(0, 2, 1, 3).reshape(-1, vs[l].shape[1], vs[l].shape[3])[:n]
+        return OM.bf16_to_f64(k), OM.bf16_to_f64(v)
+
+    t = build_trie(labels.labels, labels.root_token, base.shape.vocab, labels.continuation)
+    head = np.float64 if base.shape.vocab <= 16384 else np.float32
+    times = {}
+    t_all = time.perf_counter()
+    for L in (1, 2):
+        md = ML.ModelML(dict(bits, layers=bits["layers"][:L]), base.shape, head_dtype=head)
+        md.lm_head()  # widen the head once (model load, not timed)
+        doc_kv = [kv(l) for l in range(L)]
+        t0 = time.perf_counter()
+        ML.trie_tree(md, doc_kv, t)
+        times[L] = time.perf_counter() - t0
+        if time.perf_counter() - t_all > budget_s:
+            break
+    t1 = times[1]
+    t2 = times.get(2, 2 * t1)
+    per_layer = max(t2 - t1, t1 / 2)
+    t_doc = t1 + (mw.n_layers - 1) * per_layer
+    return {"docs_per_s": 1.0 / t_doc, "t1": t1, "t2": t2, "t_doc": t_doc}
+
+
+def run_ml(args, world, rank, local):
+    """trie_tree through the whole decoder stack (quail_classify_trie_tree_ml).
+    One step = one call over all documents; metric = documents/s."""
+    import torch
+
+    import synthetic as S
+    import trie_label_scoring_gb300 as Q
+    from trie_label_scoring_gb300.torch_inputs import kv_ml_from_docs, model_ml_from_bits
+
+    Q.build()
+    mw = S.ML_WORKLOADS[args.workload]
+    base = S.with_docs(mw.base, args.docs) if args.docs else mw.base
+    L, I = mw.n_layers, mw.intermediate
+    sh = base.shape
+    bits = S.make_model_ml(sh, L, I, 0)
+    model = model_ml_from_bits(bits, sh, I)
+    labels = S.make_labels(base, 0)
+    docs_ml = S.make_docs_ml(base, L, rank)
+    d0 = docs_ml[0]
+    kv = kv_ml_from_docs(*docs_ml)
+    trie = Q.Trie(labels.labels, labels.root_token, sh.vocab, labels.continuation)
+    trie.upload()
+    N, M, a = base.num_docs, len(labels.labels), trie.n_eval
+    rows = N * a
+    ws = torch.empty(Q.workspace_size_ml(model, trie, N, d0.max_doc_len), dtype=torch.uint8, device="cuda")
+    lsc = torch.empty((N, M), device="cuda")
+    prob = torch.empty((N, M), device="cuda")
+    am = torch.empty((N,), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        Q.classify_trie_tree_ml(model, kv, trie, N, ws, lsc, prob, am, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    Q.device_status()
+    launches_per_step = Q.launch_count()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    step()
+    t1.record(stream)
+    t1.synchronize()
+    est_ms = t0.elapsed_time(t1)
+    steps = args.steps if args.steps is not None else int(min(400, max(20, 2000.0 / max(est_ms, 1e-3))))
+    n_ev = 2 * (len(Q.STAGES) + len(Q.LAYER_SPANS) * L)
+    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(steps)]
+    for evs in stage_ev:
+        for e in evs:
+            e.record(stream)
+    clocks = ClockSampler(str(torch.cuda.get_device_properties(local).pci_bus_id))
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for k in range(steps):
+        Q.set_stage_events(stage_ev[k])
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    Q.set_stage_events(None)
+    Q.device_status()
+    elapsed_ms = max_over_ranks(world, start.elapsed_time(end))
+    ms_per_step = elapsed_ms / steps
+    value = N * world * steps / (elapsed_ms / 1e3)
+    stages_ms = {name: statistics.mean(ev[2 * i].elapsed_time(ev[2 * i + 1]) for ev in stage_ev)
+                 for i, name in enumerate(Q.STAGES) if name != "attention" and name != "wo_norm"}
+    s0 = len(Q.STAGES)
+    span_ms = {}
+    for j, name in enumerate(Q.LAYER_SPANS):
+        span_ms[name] = statistics.mean(ev[2 * (s0 + l * len(Q.LAYER_SPANS) + j)].elapsed_time(
+            ev[2 * (s0 + l * len(Q.LAYER_SPANS) + j) + 1]) for ev in stage_ev for l in range(L))
+
+    # ---- e2e: every layer's document KV from pinned host memory, results back
+    e2e = None
+    if not args.no_e2e:
+        from trie_label_scoring_gb300.torch_inputs import bf16_tensor
+        _, ks, vs = docs_ml
+        dks, dvs, dpt, ddl = kv.tensors
+        hks = [bf16_tensor(k, "cpu").pin_memory() for k in ks]
+        hvs = [bf16_tensor(v, "cpu").pin_memory() for v in vs]
+        hpt = torch.from_numpy(d0.page_table).pin_memory()
+        hdl = torch.from_numpy(d0.doc_len).pin_memory()
+        o_ls = torch.empty((N, M)).pin_memory()
+        o_pr = torch.empty((N, M)).pin_memory()
+        o_am = torch.empty((N,), dtype=torch.int32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in hks + hvs + [hpt, hdl])
+        d2h = sum(t.numel() * t.element_size() for t in (o_ls, o_pr, o_am))
+
+        def e2e_step():
+            for dst, src in zip(dks + dvs, hks + hvs):
+                dst.copy_(src, non_blocking=True)
+            dpt.copy_(hpt, non_blocking=True)
+            ddl.copy_(hdl, non_blocking=True)
+            step()
+            o_ls.copy_(lsc, non_blocking=True)
+            o_pr.copy_(prob, non_blocking=True)
+            o_am.copy_(am, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        k_e2e = max(3, min(steps, 10))
+        barrier(world)
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(k_e2e):
+            e2e_step()
+        e2.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(world, s2.elapsed_time(e2))
+        e2e = {"value": N * world * k_e2e / (e2e_ms / 1e3), "unit": "docs/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": k_e2e}
+
+    # ---- roofline of the dominant kernel: the gate|up GEMM of a layer
+    peaks = measured_peaks()
+    d, V = sh.hidden, sh.vocab
+    gu_bytes = 2.0 * d * 2 * I + 2.0 * rows * d + 4.0 * rows * 2 * I
+    gu_flops = 2.0 * rows * d * 2 * I
+    t_gu = span_ms["gate_up"] / 1e3
+    if gu_bytes / (peaks["hbm_gbs"] * 1e9) >= gu_flops / (peaks["bf16_tflops"] * 1e12):
+        achieved = gu_bytes / t_gu / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": achieved / peaks["hbm_gbs"], "peak_kind": f"HBM copy ({peaks['source']})"}
+    else:
+        achieved = gu_flops / t_gu / 1e12
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": achieved / peaks["bf16_tflops"], "peak_kind": f"bf16 burst ({peaks['source']})"}
+    roofline.update({"traffic": None, "kernel": "umma_gemm_kernel<EpiStoreF32> (gate|up, split A)",
+                     "gate_up_ms": span_ms["gate_up"], "algorithmic_bytes": gu_bytes,
+                     "algorithmic_flops": gu_flops,
+                     "issued_tflops": 2 * gu_flops / t_gu / 1e12,
+                     "note": "A is a two-term bf16 split, so the issued MMA work is twice the algorithmic FLOPs"})
+    # ---- path roofline: all weight and document-KV bytes vs all GEMM FLOPs
+    hq, hkv, hd = sh.n_q_heads, sh.n_kv_heads, sh.head_dim
+    layer_params = d * (hq + 2 * hkv) * hd + hq * hd * d + 3 * d * I
+    keys = float(d0.doc_len.sum())
+    kv_bytes = keys * hkv * hd * 2 * 2 * L
+    path_bytes = 2.0 * layer_params * L + kv_bytes + 2.0 * d * V
+    path_flops = 2.0 * rows * (layer_params * L + d * V) + 4.0 * hd * keys * hq * a * L
+    t_b = path_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_f = path_flops / (peaks["bf16_tflops"] * 1e12)
+    path = {"t_bytes_us": t_b * 1e6, "t_flops_us": t_f * 1e6, "t_star_us": max(t_b, t_f) * 1e6,
+            "ms_per_step": ms_per_step, "frac": max(t_b, t_f) * 1e3 / ms_per_step,
+            "bytes_per_step": path_bytes, "flops_per_step": path_flops}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r = time_oracle_ml(mw, base, bits, docs_ml, labels, budget_s=60.0)
+        cpu = {"value": r["docs_per_s"], "unit": "docs/s", "cores": cores(), "kind": "oracle",
+               "sample": f"document 0 of {base.name} through the first 1 and 2 layers ({r['t1']:.1f} s, "
+                         f"{r['t2']:.1f} s); per-document time extrapolated to {L} layers = {r['t_doc']:.1f} s"}
+    if rank == 0:
+        out = {
+            "metric": f"documents classified/sec at 1 GB300 (trie_tree through {L} decoder layers)",
+            "value": value, "unit": "docs/s", "n_gpus": world, "steps": steps, "warmup": max(args.warmup, 3),
+            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded, random-init weights)",
+            "config": {"workload": mw.name, "docs_per_gpu": N, "labels": M, "eval_positions_per_doc": a,
+                       "rows": rows, "layers": L, "intermediate": I, "hidden": d, "vocab": V,
+                       "doc_tokens_per_gpu": int(keys),
+                       "l2": "inputs larger than L2 (weights %.2f GB + document KV %.2f GB per step)" % (
+                           2.0 * layer_params * L / 1e9, kv_bytes / 1e9),
+                       "parallelism": f"replicas x{world} (documents sharded, no collective)"},
+            "roofline": roofline, "path_roofline": path, "stages_ms": stages_ms, "layer_spans_ms": span_ms,
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * steps, "clocks": clk,
+        }
+        print(json.dumps(out), flush=True)
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -505,7 +744,10 @@ def main():
         run_reference(args, world, rank)
         return
     world, rank, local = dist_setup()
-    if "-join" in args.workload:  # AI.IF join workloads (synthetic labels kind "join")
+    import synthetic as S
+    if args.workload in S.ML_WORKLOADS:  # the whole decoder stack
+        run_ml(args, world, rank, local)
+    elif "-join" in args.workload:  # AI.IF join workloads (synthetic labels kind "join")
         run_join(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)

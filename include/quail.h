@@ -302,7 +302,17 @@ typedef struct {
  * intermediate must be a multiple of 256 (SwiGLU width). */
 size_t quail_workspace_size_ml(const quail_model_ml_desc* model, const quail_trie* trie, int32_t num_docs,
                                int32_t max_doc_len);
-/* As quail_classify_trie_tree, through model->n_layers layers. */
+/* trie_tree through the whole decoder stack ("To Classify, Try a Trie
+ * Tree", sec. 3.2 and 4.2: every evaluated answer position goes through every
+ * layer and attends, at each layer, to the document and to its own path).
+ * Each layer is Qwen3-style: h += W_o attn(q, k, v of RMSNorm(h) g_in, per-head
+ * q/k RMSNorm, RoPE at doc_len + depth); h += W_down (SiLU(W_gate y) * W_up y),
+ * y = RMSNorm(h) g_post. Then z = RMSNorm(h) final_norm and the output head
+ * and label scoring as in quail_classify_trie_tree. kv holds every layer's
+ * document K and V (one shared page table). Rows are (document, evaluated
+ * node), so the workspace grows with num_docs x evaluated nodes. Outputs,
+ * ownership and errors as quail_classify_trie_tree; n_layers must be in
+ * [1, QUAIL_MAX_LAYERS]. */
 quail_status quail_classify_trie_tree_ml(const quail_model_ml_desc* model, const quail_paged_kv_ml* kv,
                                          quail_trie* trie, int32_t num_docs, void* workspace, size_t workspace_bytes,
                                          float* label_logscore, float* label_prob, int32_t* label_argmax,
@@ -403,9 +413,18 @@ int32_t quail_launch_count(void);
  * events[2s] before and events[2s+1] after stage s on its stream, for
  * s < num_stages (stages: 0 node prologue, 1 attention, 2 W_o + RMSNorm,
  * 3 output-head GEMM alone, 4 log-sum-exp reduction + label scoring). NULL
- * entries are skipped; events == NULL switches the hook off. Process-wide. */
+ * entries are skipped; events == NULL switches the hook off. Process-wide.
+ *
+ * quail_classify_trie_tree_ml marks stage 0 around the whole layer stack and
+ * in addition, for layer l, span j at stage QUAIL_NUM_STAGES +
+ * l * QUAIL_LAYER_SPANS + j (spans: 0 residual + RMSNorm + q|k|v GEMM + q/k
+ * norms, 1 attention, 2 W_o GEMM + residual + post-norm, 3 gate|up GEMM
+ * alone, 4 SiLU(gate) * up, 5 down GEMM alone); num_stages may then reach
+ * QUAIL_NUM_STAGES + QUAIL_LAYER_SPANS * QUAIL_MAX_LAYERS. */
 enum { QUAIL_STAGE_PROLOGUE = 0, QUAIL_STAGE_ATTENTION = 1, QUAIL_STAGE_WO_NORM = 2, QUAIL_STAGE_HEAD = 3,
        QUAIL_STAGE_SCORING = 4, QUAIL_NUM_STAGES = 5 };
+enum { QUAIL_SPAN_QKV = 0, QUAIL_SPAN_ATTENTION = 1, QUAIL_SPAN_WO_NORM = 2, QUAIL_SPAN_GATE_UP = 3,
+       QUAIL_SPAN_SILU_MUL = 4, QUAIL_SPAN_DOWN = 5, QUAIL_LAYER_SPANS = 6, QUAIL_MAX_LAYERS = 1024 };
 quail_status quail_set_stage_events(quail_event_t* events, int32_t num_stages);
 
 #ifdef __cplusplus

@@ -34,6 +34,8 @@ MODE_TRIE_TREE, MODE_LETTERS, MODE_TRIE_DECODE, MODE_JOIN_IF = 0, 1, 2, 3
 TRIE_FULL_DEPTH = 1
 TRIE_ALL_NODES = 2
 STAGES = ("prologue", "attention", "wo_norm", "head", "scoring")
+# per-layer spans of classify_trie_tree_ml; layer l's span j is stage len(STAGES) + l * len(LAYER_SPANS) + j
+LAYER_SPANS = ("qkv", "attention", "wo_norm", "gate_up", "silu_mul", "down")
 
 STATUS = {
     0: "QUAIL_OK", -1: "QUAIL_ERR_INVALID_ARG", -2: "QUAIL_ERR_EMPTY_LABEL", -3: "QUAIL_ERR_DUPLICATE_LABEL",

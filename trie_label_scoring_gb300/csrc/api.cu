@@ -555,7 +555,8 @@ quail_model_desc layer_desc(const quail_model_ml_desc* m, int l) {
 
 quail_status check_model_ml(const quail_model_ml_desc* m) {
   if (m == nullptr) return fail(QUAIL_ERR_INVALID_ARG, "model is null");
-  if (m->n_layers < 1 || m->layers == nullptr) return fail(QUAIL_ERR_INVALID_ARG, "need n_layers >= 1 and layers");
+  if (m->n_layers < 1 || m->n_layers > QUAIL_MAX_LAYERS || m->layers == nullptr)
+    return fail(QUAIL_ERR_INVALID_ARG, "need n_layers in [1, %d] and layers", QUAIL_MAX_LAYERS);
   if (m->intermediate < 256 || m->intermediate % 256 != 0 || m->intermediate > 65536)
     return fail(QUAIL_ERR_UNSUPPORTED_SHAPE, "intermediate must be a multiple of 256 in [256, 65536] (got %d)",
                 m->intermediate);
@@ -966,27 +967,40 @@ quail_status quail_classify_trie_tree_ml(const quail_model_ml_desc* model, const
     const quail_model_desc ml = layer_desc(model, l);
     const quail_paged_kv kl = layer_kv(kv, l);
     const quail_layer_weights& w = model->layers[l];
+    auto span = [&](int j, bool end) { stage_mark(QUAIL_NUM_STAGES + l * QUAIL_LAYER_SPANS + j, end, st); };
     // h += previous layer's MLP output (none before layer 0); x^ = split(RMSNorm(h) g_in)
+    span(QUAIL_SPAN_QKV, false);
     CUDA_TRY(launch_residual_norm(x.h, x.dn_part, l == 0 ? 0 : x.ks_dn, static_cast<size_t>(rows) * d, rows, d,
                                   static_cast<const bf16*>(w.in_norm), model->rms_eps, b.xhat, st));
     s = run_qkv(&ml, nt, b, ds, st);
     if (s != QUAIL_OK) return s;
+    span(QUAIL_SPAN_QKV, true);
+    span(QUAIL_SPAN_ATTENTION, false);
     s = run_attention(&ml, &kl, nt, map, num_docs, b, ds, st);
     if (s != QUAIL_OK) return s;
+    span(QUAIL_SPAN_ATTENTION, true);
+    span(QUAIL_SPAN_WO_NORM, false);
     s = run_wo_gemm(&ml, rows, b, ds, st);
     if (s != QUAIL_OK) return s;
     // h += O W_o^T; y = split(RMSNorm(h) g_post)
     CUDA_TRY(launch_residual_norm(x.h, b.h_part, b.gp.ks_wo, static_cast<size_t>(rows) * d, rows, d,
                                   static_cast<const bf16*>(w.post_norm), model->rms_eps, b.xhat, st));
+    span(QUAIL_SPAN_WO_NORM, true);
     const void* gu[2] = {w.w_gate, w.w_up};
     const int gu_rows[2] = {I, I};
+    span(QUAIL_SPAN_GATE_UP, false);
     s = run_split_gemm(b.xhat, rows, d, gu, gu_rows, 2, x.ks_gu, x.gu_part, 2 * I, ds, st);
     if (s != QUAIL_OK) return s;
+    span(QUAIL_SPAN_GATE_UP, true);
+    span(QUAIL_SPAN_SILU_MUL, false);
     CUDA_TRY(launch_silu_mul_split(x.gu_part, x.ks_gu, static_cast<size_t>(rows) * 2 * I, rows, I, x.act, st));
+    span(QUAIL_SPAN_SILU_MUL, true);
     const void* dn[1] = {w.w_down};
     const int dn_rows[1] = {d};
+    span(QUAIL_SPAN_DOWN, false);
     s = run_split_gemm(x.act, rows, I, dn, dn_rows, 1, x.ks_dn, x.dn_part, d, ds, st);
     if (s != QUAIL_OK) return s;
+    span(QUAIL_SPAN_DOWN, true);
   }
   CUDA_TRY(launch_residual_norm(x.h, x.dn_part, x.ks_dn, static_cast<size_t>(rows) * d, rows, d, nullptr,
                                 model->rms_eps, nullptr, st));
@@ -1174,7 +1188,8 @@ quail_status quail_set_stage_events(quail_event_t* events, int32_t num_stages) {
   std::lock_guard<std::mutex> lk(g_ev_mu);
   g_events.clear();
   if (events == nullptr || num_stages <= 0) return QUAIL_OK;
-  if (num_stages > QUAIL_NUM_STAGES) return fail(QUAIL_ERR_INVALID_ARG, "at most %d stages", QUAIL_NUM_STAGES);
+  if (num_stages > QUAIL_NUM_STAGES + QUAIL_LAYER_SPANS * QUAIL_MAX_LAYERS)
+    return fail(QUAIL_ERR_INVALID_ARG, "at most %d stages", QUAIL_NUM_STAGES + QUAIL_LAYER_SPANS * QUAIL_MAX_LAYERS);
   for (int i = 0; i < 2 * num_stages; ++i) g_events.push_back(reinterpret_cast<cudaEvent_t>(events[i]));
   return QUAIL_OK;
 }
