@@ -39,6 +39,8 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--docs", type=int, default=None, help="override documents per GPU (small profiling cases)")
+    p.add_argument("--layers", type=int, default=None, help="override the decoder layers of a multi-layer workload "
+                                                            "(small profiling cases)")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -574,6 +576,8 @@ def run_ml(args, world, rank, local):
 
     Q.build()
     mw = S.ML_WORKLOADS[args.workload]
+    if args.layers:
+        mw = S.MLWorkload(f"{mw.name}[{args.layers} layers]", mw.base, args.layers, mw.intermediate)
     base = S.with_docs(mw.base, args.docs) if args.docs else mw.base
     L, I = mw.n_layers, mw.intermediate
     sh = base.shape
