@@ -408,3 +408,38 @@ ML_WORKLOADS = {
                    Workload("qwen3-4b-support10-64docs", QWEN3_4B, 64, (128, 1024), "support"), 36, 9728),
     )
 }
+
+
+# --------------------------------------------------------------- huge label sets
+@dataclasses.dataclass(frozen=True)
+class ShortlistWorkload:
+    """A large tree label set scored through a shortlist: the labels split
+    into `groups` groups (0: ceil(sqrt K)) named by one distinct token each,
+    the `beam` most likely group names kept per document, exact scores for
+    the labels in them."""
+    name: str
+    base: Workload
+    groups: int
+    beam: int
+
+
+def make_group_names(seed: int, G: int, name_len: int, V: int) -> list:
+    """G distinct group names of name_len token ids each."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 3, G, name_len])))
+    seen, out = set(), []
+    while len(out) < G:
+        nm = tuple(int(t) for t in rng.integers(0, V, size=name_len))
+        if nm not in seen:
+            seen.add(nm)
+            out.append(list(nm))
+    return out
+
+
+SHORTLIST_WORKLOADS = {
+    w.name: w
+    for w in (
+        ShortlistWorkload("qwen3-4b-grouped60k-16x1024",
+                          Workload("qwen3-4b-tree60000-16x1024", QWEN3_4B, 16, (1024, 1024), "tree", 60000, (2, 10)),
+                          0, 4),
+    )
+}
