@@ -344,6 +344,76 @@ quail_status quail_join_if(const quail_model_desc* model, const quail_paged_kv* 
                            int32_t num_anchors, const int32_t* answer_tokens, int32_t n_true, int32_t n_false,
                            void* workspace, size_t workspace_bytes, float* p_true, quail_stream_t stream);
 
+/* ------------------------------------------------------------ huge label sets
+ * Two ways to keep a very large label set cheap ("Trie Automata for
+ * Constrained Decoding over Large Finite Sets", the extensions for
+ * K > 50,000 labels):
+ *  - hierarchical schema rewriting: the K labels split into G ~ sqrt(K)
+ *    groups, each label spelled as its group's name followed by the label
+ *    (no step then chooses among more than max(G, ceil(K / G)) tokens,
+ *    smallest at G = ceil(sqrt K): Proposition 2);
+ *  - a shortlist: a cheap score keeps the best candidates and exact trie
+ *    scoring runs on those only.
+ * Here the cheap score of the labels that share their first D tokens p is
+ * the exact log-probability that the answer starts with p, sum over k <= D of
+ * log P(p_k | context, p_1 .. p_{k-1}) (one trie_tree pass over the trie of
+ * the distinct D-prefixes, to full depth). Each document keeps its B best
+ * prefixes (ties: the lower prefix index, prefixes numbered in lexicographic
+ * token order); its labels under them get their exact trie_tree log scores
+ * ("To Classify, Try a Trie Tree", sec. 3.2), every other label -inf and
+ * probability 0, and the probabilities are renormalised over the kept labels.
+ * With B >= the number of prefixes the result is quail_classify_trie_tree's.
+ * Hierarchical grouping is the case D = the group-name length. */
+
+/* Trie of the grouped labels: the labels sorted by token sequence and cut
+ * into num_groups contiguous runs whose sizes differ by at most one
+ * (num_groups <= 0: ceil(sqrt(num_labels))); label m becomes
+ * group_names[g * name_len .. + name_len) followed by label m (g its run).
+ * Label indices are kept. group_names: host, num_groups * name_len ids, the
+ * names distinct; group_of_label: host [num_labels] or NULL. Other arguments
+ * and errors as quail_trie_build; QUAIL_ERR_DUPLICATE_LABEL for repeated
+ * names. */
+quail_status quail_trie_build_grouped(const int32_t* tokens, const int64_t* label_offsets, int32_t num_labels,
+                                      int32_t root_token, int32_t vocab, const uint8_t* word_continuation_bitmap,
+                                      int32_t flags, int32_t num_groups, const int32_t* group_names,
+                                      int32_t name_len, quail_trie** out, int32_t* group_of_label);
+
+/* Shortlist plan of `trie` at cut depth D >= 1 (host only): its groups (the
+ * distinct D-prefixes, every label at least D tokens long, at least two
+ * groups; else QUAIL_ERR_INVALID_ARG), the prefix trie and the per-group
+ * tables of the second pass. Valid for that trie only; free it with
+ * quail_shortlist_free before the trie. */
+typedef struct quail_shortlist quail_shortlist;
+quail_status quail_shortlist_create(const quail_trie* trie, int32_t cut_depth, quail_shortlist** out);
+void quail_shortlist_free(quail_shortlist* sl);
+/* Number of groups; group_of_label[m] for m < num_labels when the pointer is
+ * not NULL (host). */
+int32_t quail_shortlist_groups(const quail_shortlist* sl, int32_t* group_of_label);
+
+/* Workspace bytes of quail_classify_trie_tree_shortlist; 0 on invalid
+ * arguments. */
+size_t quail_workspace_size_shortlist(const quail_model_desc* model, const quail_trie* trie,
+                                      const quail_shortlist* sl, int32_t beam, int32_t num_docs,
+                                      int32_t max_doc_len);
+/* The shortlisted trie_tree: the prefix pass, each document's best
+ * min(beam, groups) prefixes, then one pass over the rows of the kept groups
+ * (document by document, padded to the largest group) and the kept labels'
+ * scores.
+ *   label_logscore, label_prob: device [num_docs, num_labels] fp32
+ *   label_argmax:   device [num_docs] int32 (lowest index of the maximum)
+ *   group_selected: device [num_docs, min(beam, groups)] int32, best first,
+ *                   or NULL
+ * Errors as quail_classify_trie_tree; QUAIL_ERR_INVALID_ARG when sl was made
+ * from another trie or beam < 1. Stage events: 0 prefix pass + selection +
+ * row layout, 1 second pass prologue + attention, 2 W_o + RMSNorm, 3 the
+ * second pass's output-head GEMM alone, 4 log-sum-exp + child log-probs +
+ * label scores. */
+quail_status quail_classify_trie_tree_shortlist(const quail_model_desc* model, const quail_paged_kv* kv,
+                                                quail_trie* trie, quail_shortlist* sl, int32_t beam,
+                                                int32_t num_docs, void* workspace, size_t workspace_bytes,
+                                                float* label_logscore, float* label_prob, int32_t* label_argmax,
+                                                int32_t* group_selected, quail_stream_t stream);
+
 /* ------------------------------------------------------------ cost model
  * Speed-of-light estimates of the three ways to classify and the choice
  * among them ("To Classify, Try a Trie Tree", sec. 4): for each method the

@@ -131,6 +131,27 @@ def select_top(scores: np.ndarray, B: int) -> list:
     return sorted(range(len(scores)), key=lambda i: (-scores[i], i))[: max(0, min(B, len(scores)))]
 
 
+def _restricted(rows: _Rows, trie: dict, gol: np.ndarray, groups) -> tuple:
+    """Exact log scores of the labels in `groups`, -inf elsewhere; P^ over them."""
+    keep = np.isin(gol, np.array(list(groups), dtype=np.int32))
+    ls = np.full(trie["num_labels"], -np.inf)
+    for m in np.nonzero(keep)[0]:
+        ls[m] = OS.label_logscore(trie, int(m), rows.logp)
+    prob, am = OS.normalise(ls)
+    return ls, np.where(keep, prob, 0.0), am
+
+
+def scores_for_groups(L, doc_k, doc_v, trie: dict, D: int, groups) -> dict:
+    """The prefix scores S of every group, and the label scores of the
+    shortlist made of `groups` (any set of prefix indices)."""
+    prefixes, gol = prefix_groups(trie, D)
+    rows = _Rows(L, doc_k, doc_v, trie)
+    S = prefix_logscores(rows, trie, D, prefixes)
+    ls, prob, am = _restricted(rows, trie, gol, groups)
+    return {"logscore": ls, "prob": prob, "argmax": am, "prefix_logscore": S, "group_of_label": gol,
+            "prefixes": prefixes}
+
+
 def shortlist(L, doc_k, doc_v, trie: dict, D: int, B: int) -> dict:
     """Shortlisted trie_tree for one document: the B prefixes of highest S,
     exact log scores for the labels under them, -inf for the rest."""
@@ -138,11 +159,6 @@ def shortlist(L, doc_k, doc_v, trie: dict, D: int, B: int) -> dict:
     rows = _Rows(L, doc_k, doc_v, trie)
     S = prefix_logscores(rows, trie, D, prefixes)
     sel = select_top(S, B)
-    keep = np.isin(gol, np.array(sel, dtype=np.int32))
-    ls = np.full(trie["num_labels"], -np.inf)
-    for m in np.nonzero(keep)[0]:
-        ls[m] = OS.label_logscore(trie, int(m), rows.logp)
-    prob, am = OS.normalise(ls)
-    prob = np.where(keep, prob, 0.0)
+    ls, prob, am = _restricted(rows, trie, gol, sel)
     return {"logscore": ls, "prob": prob, "argmax": am, "selected": sel, "prefix_logscore": S,
             "group_of_label": gol, "prefixes": prefixes}

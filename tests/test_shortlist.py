@@ -117,3 +117,184 @@ def test_shortlist_is_the_renormalised_restriction(D, B):
     pk = full["prob"][keep]
     np.testing.assert_allclose(r["prob"][keep], pk / pk.sum(), rtol=1e-12, atol=0)
     assert keep[r["argmax"]]
+
+
+# ------------------------------------------------------- library host tables
+def _view_equal(view, ref):
+    for k in ("parent", "depth", "token", "subtree_size", "child_offsets", "child_tokens", "label_end_node",
+              "label_decide_depth", "eval_nodes", "eval_child_offsets"):
+        np.testing.assert_array_equal(view[k], ref[k], err_msg=k)
+
+
+@pytest.mark.parametrize("G", [0, 5, 40])
+def test_grouped_trie_is_the_oracle_rewrite(G):
+    import trie_label_scoring_gb300 as Q
+    from oracle import shortlist as SL
+    from oracle.trie import build_trie
+    w, ls = _tiny_tree(4, M=40)
+    K = len(ls.labels)
+    Gr = G or SL.default_groups(K)
+    names = S.make_group_names(0, Gr, 2, w.shape.vocab)
+    t, gol = Q.Trie.grouped(ls.labels, ls.root_token, w.shape.vocab, names, num_groups=G)
+    ref_g = SL.group_labels(ls.labels, Gr)
+    np.testing.assert_array_equal(gol, ref_g)
+    rw = SL.rewrite_grouped(ls.labels, names, ref_g)
+    _view_equal(t.view(), build_trie(rw, ls.root_token, w.shape.vocab))
+
+
+def test_shortlist_plan_groups_are_the_oracle_prefixes():
+    import trie_label_scoring_gb300 as Q
+    from oracle import shortlist as SL
+    from oracle.trie import build_trie
+    w, ls = _tiny_tree(5, M=60, lens=(2, 6))
+    t = Q.Trie(ls.labels, ls.root_token, w.shape.vocab)
+    ref = build_trie(ls.labels, ls.root_token, w.shape.vocab)
+    for D in (1, 2):
+        sl = Q.Shortlist(t, D)
+        pref, gol = SL.prefix_groups(ref, D)
+        assert sl.num_groups == len(pref)
+        np.testing.assert_array_equal(sl.group_of_label(), gol)
+        sl.close()
+
+
+def test_shortlist_and_grouping_reject_bad_arguments():
+    import trie_label_scoring_gb300 as Q
+    labels = [[5, 6], [5, 7], [9], [3, 3, 3]]
+    t = Q.Trie(labels, 0, 100)
+    with pytest.raises(Q.QuailError):
+        Q.Shortlist(t, 2)  # [9] is shorter than the cut
+    with pytest.raises(Q.QuailError):
+        Q.Shortlist(Q.Trie([[5, 6], [5, 7]], 0, 100), 1)  # a single group
+    with pytest.raises(Q.QuailError):
+        Q.Trie.grouped(labels, 0, 100, [[1], [1]], num_groups=2)  # equal names
+    with pytest.raises(Q.QuailError):
+        Q.Trie.grouped(labels, 0, 100, [[1], [2], [3], [4], [5]], num_groups=5)  # more groups than labels
+
+
+def test_scores_for_the_selected_groups_are_the_shortlist():
+    from oracle import shortlist as SL
+    from oracle.trie import build_trie
+    w, ls = _tiny_tree(6)
+    t = build_trie(ls.labels, ls.root_token, w.shape.vocab)
+    L = C.oracle_layer(w.shape, 0)
+    dk, dv = C.oracle_doc_kv(S.make_docs(w, 0), 0)
+    r = SL.shortlist(L, dk, dv, t, 2, 3)
+    q = SL.scores_for_groups(L, dk, dv, t, 2, r["selected"])
+    np.testing.assert_array_equal(q["logscore"], r["logscore"])
+    np.testing.assert_array_equal(q["prob"], r["prob"])
+
+
+# ------------------------------------------------------------------ GPU parity
+def _run_shortlist(w, docs, trie, sl, beam, seed=0):
+    import torch
+    import trie_label_scoring_gb300 as Q
+    from trie_label_scoring_gb300.torch_inputs import kv_from_docs
+    model = C.device_model(w.shape, seed)
+    kv = kv_from_docs(docs)
+    N, M = len(docs.doc_len), trie.num_labels
+    B = min(beam, sl.num_groups)
+    ws = torch.empty(Q.workspace_size_shortlist(model, trie, sl, beam, N, docs.max_doc_len), dtype=torch.uint8,
+                     device="cuda")
+    lsc = torch.full((N, M), float("nan"), device="cuda")
+    prob = torch.full((N, M), float("nan"), device="cuda")
+    am = torch.full((N,), -1, dtype=torch.int32, device="cuda")
+    sel = torch.full((N, B), -1, dtype=torch.int32, device="cuda")
+    Q.classify_trie_tree_shortlist(model, kv, trie, sl, beam, N, ws, lsc, prob, am, sel)
+    Q.device_status()
+    return lsc.cpu().numpy(), prob.cpu().numpy(), am.cpu().numpy(), sel.cpu().numpy()
+
+
+def _check_shortlist(w, docs, ref_trie, D, beam, docs_idx, out, seed=0):
+    """Per document: the GPU's kept groups are a valid top-B set of the
+    oracle's prefix scores (equal to the oracle's set where its B-th and
+    next scores differ by more than twice the log-score tolerance), and the
+    scores equal the oracle's for that kept set."""
+    from oracle import shortlist as SL
+    lsc, prob, am, sel = out
+    L = C.oracle_layer(w.shape, seed)
+    for i in docs_idx:
+        dk, dv = C.oracle_doc_kv(docs, i)
+        g_sel = [int(g) for g in sel[i]]
+        r = SL.scores_for_groups(L, dk, dv, ref_trie, D, g_sel)
+        S_ = r["prefix_logscore"]
+        top = SL.select_top(S_, beam)
+        B = len(top)
+        assert len(g_sel) == B and len(set(g_sel)) == B, f"doc {i}: selection {g_sel}"
+        kth = S_[top[-1]]
+        assert all(S_[g] >= kth - C.TOL_LOGSCORE for g in g_sel), f"doc {i}: {g_sel} vs {top}"
+        rest = [S_[g] for g in range(len(S_)) if g not in top]
+        if not rest or kth - max(rest) > 2 * C.TOL_LOGSCORE:
+            assert set(g_sel) == set(top), f"doc {i}: {g_sel} vs {top}"
+        C.check_scores(lsc[i], prob[i], am[i], r["logscore"], r["prob"], r["argmax"], f"doc {i}")
+
+
+@pytest.mark.gpu
+def test_shortlist_full_beam_is_trie_tree_gpu():
+    import trie_label_scoring_gb300 as Q
+    from oracle import scoring as OS
+    from oracle.trie import build_trie
+    w, ls = _tiny_tree(7, M=40)
+    w = S.with_docs(w, 5, (1, 600))
+    docs = S.make_docs(w, 7)
+    t = Q.Trie(ls.labels, ls.root_token, w.shape.vocab)
+    sl = Q.Shortlist(t, 1)
+    lsc, prob, am, sel = _run_shortlist(w, docs, t, sl, 10 ** 4)
+    ref_t = build_trie(ls.labels, ls.root_token, w.shape.vocab)
+    L = C.oracle_layer(w.shape, 0)
+    for i in range(5):
+        dk, dv = C.oracle_doc_kv(docs, i)
+        r = OS.trie_tree(L, dk, dv, ref_t)
+        C.check_scores(lsc[i], prob[i], am[i], r["logscore"], r["prob"], r["argmax"], f"doc {i}")
+        assert sorted(sel[i]) == list(range(sl.num_groups))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("D,beam", [(1, 1), (1, 2), (2, 3)])
+def test_shortlist_tiny_gpu(D, beam):
+    import trie_label_scoring_gb300 as Q
+    from oracle.trie import build_trie
+    w, ls = _tiny_tree(8, M=60, lens=(2, 6))
+    w = S.with_docs(w, 6, (1, 500))
+    docs = S.make_docs(w, 8)
+    t = Q.Trie(ls.labels, ls.root_token, w.shape.vocab)
+    sl = Q.Shortlist(t, D)
+    out = _run_shortlist(w, docs, t, sl, beam)
+    _check_shortlist(w, docs, build_trie(ls.labels, ls.root_token, w.shape.vocab), D, beam, range(6), out)
+
+
+@pytest.mark.gpu
+def test_grouped_labels_tiny_gpu():
+    """Hierarchical grouping: ceil(sqrt K) one-token group names, the two most
+    likely groups kept; more than 128 query rows per KV head per document."""
+    import trie_label_scoring_gb300 as Q
+    from oracle import shortlist as SL
+    from oracle.trie import build_trie
+    w, ls = _tiny_tree(9, M=400, lens=(2, 6))
+    w = S.with_docs(w, 4, (100, 700))
+    docs = S.make_docs(w, 9)
+    G = SL.default_groups(len(ls.labels))
+    names = S.make_group_names(9, G, 1, w.shape.vocab)
+    t, gol = Q.Trie.grouped(ls.labels, ls.root_token, w.shape.vocab, names)
+    sl = Q.Shortlist(t, 1)
+    assert sl.num_groups == G
+    out = _run_shortlist(w, docs, t, sl, 2)
+    rw = SL.rewrite_grouped(ls.labels, names, SL.group_labels(ls.labels, G))
+    _check_shortlist(w, docs, build_trie(rw, ls.root_token, w.shape.vocab), 1, 2, range(4), out)
+
+
+@pytest.mark.gpu
+def test_grouped_labels_qwen_shape_sampled():
+    import trie_label_scoring_gb300 as Q
+    from oracle import shortlist as SL
+    from oracle.trie import build_trie
+    base = S.SHORTLIST_WORKLOADS["qwen3-4b-grouped60k-16x1024"].base
+    w = S.dataclasses.replace(S.with_docs(base, 4, (256, 1024)), num_labels=2000)
+    ls = S.make_labels(w, 0)
+    docs = S.make_docs(w, 0)
+    G = SL.default_groups(len(ls.labels))
+    names = S.make_group_names(0, G, 1, w.shape.vocab)
+    t, _ = Q.Trie.grouped(ls.labels, ls.root_token, w.shape.vocab, names)
+    sl = Q.Shortlist(t, 1)
+    out = _run_shortlist(w, docs, t, sl, 2)
+    rw = SL.rewrite_grouped(ls.labels, names, SL.group_labels(ls.labels, G))
+    _check_shortlist(w, docs, build_trie(rw, ls.root_token, w.shape.vocab), 1, 2, [0, 3], out)

@@ -20,6 +20,10 @@ Entry points (same names as the C ABI, without the quail_ prefix):
   set_stage_events(...)          -> quail_set_stage_events
   launch_count()                 -> quail_launch_count
   estimate_methods(...)          -> quail_estimate_methods
+  Trie.grouped(...)              -> quail_trie_build_grouped
+  Shortlist(...)                 -> quail_shortlist_create / quail_shortlist_groups / quail_shortlist_free
+  workspace_size_shortlist(...), classify_trie_tree_shortlist(...)
+                                 -> quail_workspace_size_shortlist / quail_classify_trie_tree_shortlist
 """
 from __future__ import annotations
 
@@ -155,6 +159,19 @@ _SIGNATURES = {
                                                    ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t,
                                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                    ctypes.c_void_p]),
+    "quail_trie_build_grouped": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                                ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                                ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]),
+    "quail_shortlist_create": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]),
+    "quail_shortlist_free": (None, [ctypes.c_void_p]),
+    "quail_shortlist_groups": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_void_p]),
+    "quail_workspace_size_shortlist": (ctypes.c_size_t, [ctypes.POINTER(ModelDesc), ctypes.c_void_p, ctypes.c_void_p,
+                                                         ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
+    "quail_classify_trie_tree_shortlist": (ctypes.c_int, [ctypes.POINTER(ModelDesc), ctypes.POINTER(PagedKV),
+                                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                                          ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t,
+                                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                          ctypes.c_void_p, ctypes.c_void_p]),
     "quail_device_status": (ctypes.c_int, [ctypes.c_void_p]),
     "quail_set_stage_events": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
     "quail_launch_count": (ctypes.c_int32, []),
@@ -203,23 +220,31 @@ def _stream(stream) -> int | None:
 
 
 # ------------------------------------------------------------------ trie
+def _flat_labels(labels) -> tuple:
+    offs = np.zeros(len(labels) + 1, dtype=np.int64)
+    offs[1:] = np.cumsum([len(l) for l in labels])
+    toks = np.ascontiguousarray(np.array([t for l in labels for t in l], dtype=np.int32))
+    if toks.size == 0:
+        toks = np.zeros(1, dtype=np.int32)
+    return toks, offs
+
+
 class Trie:
     """Library-owned label trie (quail_trie_build). labels: list of token-id lists."""
 
     def __init__(self, labels, root_token: int, vocab: int, continuation=None, full_depth: bool = False,
-                 all_nodes: bool = False):
-        offs = np.zeros(len(labels) + 1, dtype=np.int64)
-        offs[1:] = np.cumsum([len(l) for l in labels])
-        toks = np.ascontiguousarray(np.array([t for l in labels for t in l], dtype=np.int32))
-        if toks.size == 0:
-            toks = np.zeros(1, dtype=np.int32)
-        cont = None if continuation is None else np.ascontiguousarray(continuation, dtype=np.uint8)
-        h = ctypes.c_void_p()
-        st = lib().quail_trie_build(toks.ctypes.data, offs.ctypes.data, len(labels), int(root_token), int(vocab),
-                                    None if cont is None else cont.ctypes.data,
-                                    (TRIE_FULL_DEPTH if full_depth else 0) | (TRIE_ALL_NODES if all_nodes else 0),
-                                    ctypes.byref(h))
-        _check(st)
+                 all_nodes: bool = False, _handle=None):
+        if _handle is None:
+            toks, offs = _flat_labels(labels)
+            cont = None if continuation is None else np.ascontiguousarray(continuation, dtype=np.uint8)
+            h = ctypes.c_void_p()
+            st = lib().quail_trie_build(toks.ctypes.data, offs.ctypes.data, len(labels), int(root_token), int(vocab),
+                                        None if cont is None else cont.ctypes.data,
+                                        (TRIE_FULL_DEPTH if full_depth else 0) | (TRIE_ALL_NODES if all_nodes else 0),
+                                        ctypes.byref(h))
+            _check(st)
+        else:
+            h = _handle
         self._h = h
         self.num_labels = len(labels)
         self.vocab = int(vocab)
@@ -256,9 +281,60 @@ class Trie:
     def upload(self, stream=None) -> None:
         _check(lib().quail_trie_upload(self._h, _stream(stream)))
 
+    @classmethod
+    def grouped(cls, labels, root_token: int, vocab: int, group_names, num_groups: int = 0, continuation=None,
+                full_depth: bool = False) -> tuple:
+        """(trie, group_of_label) of the grouped labels (quail_trie_build_grouped):
+        label m spelled as its group's name followed by the label; group_names
+        lists num_groups (0: ceil(sqrt K)) token sequences of one length."""
+        toks, offs = _flat_labels(labels)
+        names = np.ascontiguousarray(np.array(group_names, dtype=np.int32).reshape(len(group_names), -1))
+        cont = None if continuation is None else np.ascontiguousarray(continuation, dtype=np.uint8)
+        gol = np.zeros(len(labels), dtype=np.int32)
+        h = ctypes.c_void_p()
+        _check(lib().quail_trie_build_grouped(toks.ctypes.data, offs.ctypes.data, len(labels), int(root_token),
+                                              int(vocab), None if cont is None else cont.ctypes.data,
+                                              TRIE_FULL_DEPTH if full_depth else 0, int(num_groups or 0),
+                                              names.ctypes.data, int(names.shape[1]), ctypes.byref(h),
+                                              gol.ctypes.data))
+        return cls(labels, root_token, vocab, _handle=h), gol
+
     def close(self) -> None:
         if getattr(self, "_h", None) is not None and self._h.value:
             lib().quail_trie_free(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Shortlist:
+    """Shortlist plan of a trie at cut depth D (quail_shortlist_create): the
+    groups of labels sharing their first D tokens. Keep the trie alive."""
+
+    def __init__(self, trie: Trie, cut_depth: int):
+        h = ctypes.c_void_p()
+        _check(lib().quail_shortlist_create(trie.handle, int(cut_depth), ctypes.byref(h)))
+        self._h = h
+        self.trie = trie
+        self.cut_depth = int(cut_depth)
+        self.num_groups = int(lib().quail_shortlist_groups(h, None))
+
+    @property
+    def handle(self):
+        return self._h
+
+    def group_of_label(self) -> np.ndarray:
+        out = np.zeros(self.trie.num_labels, dtype=np.int32)
+        lib().quail_shortlist_groups(self._h, out.ctypes.data)
+        return out
+
+    def close(self) -> None:
+        if getattr(self, "_h", None) is not None and self._h.value:
+            lib().quail_shortlist_free(self._h)
             self._h = ctypes.c_void_p()
 
     def __del__(self):
@@ -413,6 +489,24 @@ def workspace_size_ml(model: ModelML, trie: Trie, num_docs: int, max_doc_len: in
     if n == 0:
         raise QuailError(-1, "workspace_size_ml: invalid arguments")
     return int(n)
+
+
+def workspace_size_shortlist(model: Model, trie: Trie, sl: Shortlist, beam: int, num_docs: int,
+                             max_doc_len: int) -> int:
+    n = lib().quail_workspace_size_shortlist(ctypes.byref(model.desc), trie.handle, sl.handle, int(beam),
+                                             int(num_docs), int(max_doc_len))
+    if n == 0:
+        raise QuailError(-1, "workspace_size_shortlist: invalid arguments")
+    return int(n)
+
+
+def classify_trie_tree_shortlist(model: Model, kv: KV, trie: Trie, sl: Shortlist, beam: int, num_docs: int,
+                                 workspace, label_logscore, label_prob, label_argmax, group_selected=None,
+                                 stream=None) -> None:
+    _check(lib().quail_classify_trie_tree_shortlist(
+        ctypes.byref(model.desc), ctypes.byref(kv.desc), trie.handle, sl.handle, int(beam), int(num_docs),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(label_logscore), _ptr(label_prob),
+        _ptr(label_argmax), None if group_selected is None else _ptr(group_selected), _stream(stream)))
 
 
 def classify_trie_tree_ml(model: ModelML, kv: KVML, trie: Trie, num_docs: int, workspace, label_logscore,

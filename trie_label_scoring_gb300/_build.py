@@ -14,8 +14,8 @@ OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libquail.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-CUDA_SOURCES = ["api.cu", "gemm.cu", "attention.cu", "attention_tc.cu", "layer.cu", "mlp.cu"]
-CXX_SOURCES = ["trie.cpp", "cost.cpp"]
+CUDA_SOURCES = ["api.cu", "gemm.cu", "attention.cu", "attention_tc.cu", "layer.cu", "mlp.cu", "shortlist.cu"]
+CXX_SOURCES = ["trie.cpp", "cost.cpp", "shortlist.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

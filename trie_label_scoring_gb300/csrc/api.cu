@@ -16,6 +16,7 @@
 #include "umma_gemm.cuh"
 #include "quail_internal.h"
 #include "trie.h"
+#include "shortlist.h"
 
 using namespace quail;
 
@@ -638,6 +639,157 @@ quail_status run_split_gemm(const bf16* A, int rows, int K, const void* const* w
   return QUAIL_OK;
 }
 
+// The trie_tree pass over num_docs documents with the trie's device image
+// and the buffers of plan(..., a, N, a, ..., head = true, n_child, ...);
+// stage events when `marks`.
+quail_status trie_tree_pass(const quail_model_desc* model, const quail_paged_kv* kv, const quail_trie* trie,
+                            const quail_trie::DeviceImage* img, int num_docs, const Buffers& b, DeviceState* ds,
+                            cudaStream_t st, float* label_logscore, float* label_prob, int32_t* label_argmax,
+                            bool marks) {
+  const int a = trie->n_eval();
+  const int n_child = trie->eval_child_offsets.back();
+  const NodeTables nt{img->eval_token, img->eval_depth, img->eval_parent, a};
+  const RowMap map{a, nullptr, nullptr, nullptr};
+  const int rows = num_docs * a;
+  auto mark = [&](int stage, bool end) {
+    if (marks) stage_mark(stage, end, st);
+  };
+
+  mark(QUAIL_STAGE_PROLOGUE, false);
+  quail_status s = run_prologue(model, nt, b, ds, st);
+  if (s != QUAIL_OK) return s;
+  mark(QUAIL_STAGE_PROLOGUE, true);
+
+  mark(QUAIL_STAGE_ATTENTION, false);
+  s = run_attention(model, kv, nt, map, num_docs, b, ds, st);
+  if (s != QUAIL_OK) return s;
+  mark(QUAIL_STAGE_ATTENTION, true);
+
+  mark(QUAIL_STAGE_WO_NORM, false);
+  s = run_wo_norm(model, nt, map, rows, b, ds, st);
+  if (s != QUAIL_OK) return s;
+  mark(QUAIL_STAGE_WO_NORM, true);
+
+  mark(QUAIL_STAGE_HEAD, false);
+  {
+    const int d = model->hidden;
+    const int n_tiles = (model->vocab + kHeadBN - 1) / kHeadBN;
+    CUtensorMap tA, tB;
+    s = encode_2d_bf16(&tA, b.z, round_up(rows, 128), d, d, 64, 128);
+    if (s != QUAIL_OK) return s;
+    s = encode_2d_bf16(&tB, model->lm_head, model->vocab, d, d, 64, kHeadBBoxRows);
+    if (s != QUAIL_OK) return s;
+    HeadEpilogueArgs ha{b.lse_part, b.child_logit, img->eval_child_offsets, img->eval_child_tokens, b.z_f32,
+                        static_cast<const bf16*>(model->lm_head), d, a, n_child, n_tiles};
+    CUDA_TRY(launch_gemm_head(tA, tB, rows, model->vocab, d, ha, ds->num_sms, ds->err, st));
+    mark(QUAIL_STAGE_HEAD, true);
+  }
+  mark(QUAIL_STAGE_SCORING, false);
+  LabelScoreArgs la{b.child_logit,
+                    b.lse_part,
+                    (model->vocab + kHeadBN - 1) / kHeadBN,
+                    b.lse,
+                    img->label_term_offsets,
+                    img->label_term_eval,
+                    img->label_term_slot,
+                    img->label_prefix_eval,
+                    img->eval_child_offsets,
+                    a,
+                    n_child,
+                    trie->num_labels,
+                    label_logscore,
+                    label_prob,
+                    label_argmax};
+  CUDA_TRY(launch_label_score(la, num_docs, ds->num_sms, st));
+  mark(QUAIL_STAGE_SCORING, true);
+  return QUAIL_OK;
+}
+
+// ------------------------------------------------------------------ shortlist
+quail_status upload_shortlist(quail_shortlist* sl, cudaStream_t st, const quail_shortlist::DeviceImage** out) {
+  int dev = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lk(sl->mu);
+  auto it = sl->images.find(dev);
+  if (it != sl->images.end()) {
+    *out = &it->second;
+    return QUAIL_OK;
+  }
+  const std::vector<int32_t>* arrays[] = {&sl->row_off, &sl->row_eval, &sl->row_parent, &sl->child_off,
+                                          &sl->child_row, &sl->child_tok, &sl->lab_off, &sl->lab_id,
+                                          &sl->term_off, &sl->term_t, &sl->pref_t0, &sl->pref_t1};
+  const int na = sizeof(arrays) / sizeof(arrays[0]);
+  std::vector<size_t> offs(na);
+  size_t total = 0;
+  for (int i = 0; i < na; ++i) {
+    offs[i] = total;
+    total += round_up(std::max<size_t>(arrays[i]->size(), 1) * 4, 256);
+  }
+  std::vector<uint8_t> host(total, 0);
+  for (int i = 0; i < na; ++i)
+    if (!arrays[i]->empty()) std::memcpy(host.data() + offs[i], arrays[i]->data(), arrays[i]->size() * 4);
+  void* dptr = nullptr;
+  CUDA_TRY(cudaMalloc(&dptr, total));
+  cudaError_t e = cudaMemcpyAsync(dptr, host.data(), total, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) {
+    cudaFree(dptr);
+    return fail(QUAIL_ERR_CUDA, "shortlist upload: %s", cudaGetErrorString(e));
+  }
+  quail_shortlist::DeviceImage img;
+  img.base = dptr;
+  const int32_t** fields[] = {&img.row_off,   &img.row_eval, &img.row_parent, &img.child_off,
+                              &img.child_row, &img.child_tok, &img.lab_off,   &img.lab_id,
+                              &img.term_off,  &img.term_t,   &img.pref_t0,    &img.pref_t1};
+  for (int i = 0; i < na; ++i)
+    *fields[i] = reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(dptr) + offs[i]);
+  auto res = sl->images.emplace(dev, img);
+  *out = &res.first->second;
+  return QUAIL_OK;
+}
+
+// A plan made from this trie (the counts it was built from agree).
+bool shortlist_matches(const quail_shortlist* sl, const quail_trie* t) {
+  return sl->num_labels == t->num_labels && sl->trie_nodes == t->n_nodes() && sl->trie_eval == t->n_eval() &&
+         sl->prefix_trie != nullptr && sl->prefix_trie->vocab == t->vocab;
+}
+
+// Workspace of the shortlisted call: the prefix pass and the second pass
+// share one region (the second starts after the first has finished on the
+// stream); the selection, child log-probs and prefix scores follow it.
+struct ShortlistBuffers {
+  Buffers b1, b2;
+  int* sel;       // [N, B]
+  float* clp;     // [N * B, max_children]
+  float* ls1;     // [N, G] prefix log scores
+  float* prob1;   // [N, G]
+  int* am1;       // [N]
+  int B, Bq;      // kept groups per document; rows per document (B * max_rows)
+  int R;          // second-pass rows (N * Bq)
+};
+
+size_t plan_shortlist(uint8_t* base, const quail_model_desc* m, const quail_shortlist* sl, int beam, int N,
+                      int max_doc_len, ShortlistBuffers* out) {
+  const quail_trie* pt = sl->prefix_trie;
+  ShortlistBuffers x{};
+  x.B = std::min(beam, sl->num_groups);
+  x.Bq = x.B * sl->max_rows;
+  x.R = N * x.Bq;
+  const int a1 = pt->n_eval();
+  const size_t p1 = plan(base, m, a1, N, a1, max_doc_len, true, pt->eval_child_offsets.back(), false, 0,
+                         base ? &x.b1 : nullptr);
+  const size_t p2 = plan(base, m, x.R, N, x.Bq, max_doc_len, true, 0, true, 4 * x.R + 2, base ? &x.b2 : nullptr);
+  const size_t shared = round_up(std::max(p1, p2), 256);
+  Carver c{base ? base + shared : nullptr};
+  x.sel = c.take<int>(static_cast<size_t>(N) * x.B);
+  x.clp = c.take<float>(static_cast<size_t>(N) * x.B * std::max(sl->max_children, 1));
+  x.ls1 = c.take<float>(static_cast<size_t>(N) * sl->num_groups);
+  x.prob1 = c.take<float>(static_cast<size_t>(N) * sl->num_groups);
+  x.am1 = c.take<int>(N);
+  if (out) *out = x;
+  return shared + c.off + 256;
+}
+
 }  // namespace
 
 // ================================================================== C ABI
@@ -778,58 +930,7 @@ quail_status quail_classify_trie_tree(const quail_model_desc* model, const quail
   if (s != QUAIL_OK) return s;
   Buffers b;
   plan(static_cast<uint8_t*>(workspace), model, a, num_docs, a, kv->max_doc_len, true, n_child, false, 0, &b);
-  const NodeTables nt{img->eval_token, img->eval_depth, img->eval_parent, a};
-  const RowMap map{a, nullptr, nullptr, nullptr};
-  const int rows = num_docs * a;
-
-  stage_mark(QUAIL_STAGE_PROLOGUE, false, st);
-  s = run_prologue(model, nt, b, ds, st);
-  if (s != QUAIL_OK) return s;
-  stage_mark(QUAIL_STAGE_PROLOGUE, true, st);
-
-  stage_mark(QUAIL_STAGE_ATTENTION, false, st);
-  s = run_attention(model, kv, nt, map, num_docs, b, ds, st);
-  if (s != QUAIL_OK) return s;
-  stage_mark(QUAIL_STAGE_ATTENTION, true, st);
-
-  stage_mark(QUAIL_STAGE_WO_NORM, false, st);
-  s = run_wo_norm(model, nt, map, rows, b, ds, st);
-  if (s != QUAIL_OK) return s;
-  stage_mark(QUAIL_STAGE_WO_NORM, true, st);
-
-  stage_mark(QUAIL_STAGE_HEAD, false, st);
-  {
-    const int d = model->hidden;
-    const int n_tiles = (model->vocab + kHeadBN - 1) / kHeadBN;
-    CUtensorMap tA, tB;
-    s = encode_2d_bf16(&tA, b.z, round_up(rows, 128), d, d, 64, 128);
-    if (s != QUAIL_OK) return s;
-    s = encode_2d_bf16(&tB, model->lm_head, model->vocab, d, d, 64, kHeadBBoxRows);
-    if (s != QUAIL_OK) return s;
-    HeadEpilogueArgs ha{b.lse_part, b.child_logit, img->eval_child_offsets, img->eval_child_tokens, b.z_f32,
-                        static_cast<const bf16*>(model->lm_head), d, a, n_child, n_tiles};
-    CUDA_TRY(launch_gemm_head(tA, tB, rows, model->vocab, d, ha, ds->num_sms, ds->err, st));
-    stage_mark(QUAIL_STAGE_HEAD, true, st);
-  }
-  stage_mark(QUAIL_STAGE_SCORING, false, st);
-  LabelScoreArgs la{b.child_logit,
-                    b.lse_part,
-                    (model->vocab + kHeadBN - 1) / kHeadBN,
-                    b.lse,
-                    img->label_term_offsets,
-                    img->label_term_eval,
-                    img->label_term_slot,
-                    img->label_prefix_eval,
-                    img->eval_child_offsets,
-                    a,
-                    n_child,
-                    trie->num_labels,
-                    label_logscore,
-                    label_prob,
-                    label_argmax};
-  CUDA_TRY(launch_label_score(la, num_docs, ds->num_sms, st));
-  stage_mark(QUAIL_STAGE_SCORING, true, st);
-  return QUAIL_OK;
+  return trie_tree_pass(model, kv, trie, img, num_docs, b, ds, st, label_logscore, label_prob, label_argmax, true);
 }
 
 quail_status quail_classify_letters(const quail_model_desc* model, const quail_paged_kv* kv,
@@ -1260,6 +1361,209 @@ quail_status quail_classify_trie_tree_noalloc(const quail_model_desc* model, con
                     img.eval_child_offsets, a,                  n_child,        trie->num_labels,
                     label_logscore,      label_prob,          label_argmax};
   CUDA_TRY(launch_label_score(la, num_docs, ds->num_sms, st));
+  return QUAIL_OK;
+}
+
+
+// ------------------------------------------------------------------ huge label sets
+quail_status quail_trie_build_grouped(const int32_t* tokens, const int64_t* label_offsets, int32_t num_labels,
+                                      int32_t root_token, int32_t vocab, const uint8_t* word_continuation_bitmap,
+                                      int32_t flags, int32_t num_groups, const int32_t* group_names,
+                                      int32_t name_len, quail_trie** out, int32_t* group_of_label) {
+  if (out == nullptr) return fail(QUAIL_ERR_INVALID_ARG, "out is null");
+  *out = nullptr;
+  if (tokens == nullptr || label_offsets == nullptr || group_names == nullptr)
+    return fail(QUAIL_ERR_INVALID_ARG, "null argument");
+  if (num_labels < 2) return fail(QUAIL_ERR_INVALID_ARG, "need at least 2 labels");
+  if (name_len < 1) return fail(QUAIL_ERR_INVALID_ARG, "name_len must be >= 1");
+  if (label_offsets[0] != 0) return fail(QUAIL_ERR_INVALID_ARG, "label_offsets[0] must be 0");
+  for (int32_t m = 0; m < num_labels; ++m)
+    if (label_offsets[m + 1] < label_offsets[m]) return fail(QUAIL_ERR_INVALID_ARG, "label_offsets decrease at %d", m);
+  int32_t G = num_groups;
+  if (G <= 0) {  // ceil(sqrt(K))
+    G = static_cast<int32_t>(std::sqrt(static_cast<double>(num_labels)));
+    while (static_cast<int64_t>(G) * G < num_labels) ++G;
+    while (G > 1 && static_cast<int64_t>(G - 1) * (G - 1) >= num_labels) --G;
+  }
+  if (G > num_labels) return fail(QUAIL_ERR_INVALID_ARG, "num_groups %d > num_labels %d", G, num_labels);
+  for (int64_t i = 0; i < static_cast<int64_t>(G) * name_len; ++i)
+    if (group_names[i] < 0 || group_names[i] >= vocab)
+      return fail(QUAIL_ERR_TOKEN_RANGE, "group name token %d outside [0, vocab)", group_names[i]);
+  {
+    std::vector<int32_t> order(G);
+    for (int32_t g = 0; g < G; ++g) order[g] = g;
+    auto name = [&](int32_t g) { return group_names + static_cast<int64_t>(g) * name_len; };
+    std::sort(order.begin(), order.end(), [&](int32_t a, int32_t b) {
+      return std::lexicographical_compare(name(a), name(a) + name_len, name(b), name(b) + name_len);
+    });
+    for (int32_t i = 1; i < G; ++i)
+      if (std::equal(name(order[i]), name(order[i]) + name_len, name(order[i - 1])))
+        return fail(QUAIL_ERR_DUPLICATE_LABEL, "group names %d and %d are equal", order[i - 1], order[i]);
+  }
+  std::vector<int32_t> gol(num_labels);
+  quail_group_labels_host(tokens, label_offsets, num_labels, G, gol.data());
+  std::vector<int32_t> toks;
+  std::vector<int64_t> offs(num_labels + 1, 0);
+  toks.reserve(static_cast<size_t>(label_offsets[num_labels]) + static_cast<size_t>(num_labels) * name_len);
+  for (int32_t m = 0; m < num_labels; ++m) {
+    const int32_t* nm = group_names + static_cast<int64_t>(gol[m]) * name_len;
+    toks.insert(toks.end(), nm, nm + name_len);
+    toks.insert(toks.end(), tokens + label_offsets[m], tokens + label_offsets[m + 1]);
+    offs[m + 1] = static_cast<int64_t>(toks.size());
+  }
+  quail_trie* t = new quail_trie();
+  std::string msg;
+  const quail_status s = quail_build_trie_host(toks.data(), offs.data(), num_labels, root_token, vocab,
+                                               word_continuation_bitmap, flags, t, &msg);
+  if (s != QUAIL_OK) {
+    delete t;
+    return fail(s, "%s", msg.c_str());
+  }
+  if (group_of_label != nullptr) std::copy(gol.begin(), gol.end(), group_of_label);
+  *out = t;
+  return QUAIL_OK;
+}
+
+quail_status quail_shortlist_create(const quail_trie* trie, int32_t cut_depth, quail_shortlist** out) {
+  if (out == nullptr || trie == nullptr) return fail(QUAIL_ERR_INVALID_ARG, "null argument");
+  *out = nullptr;
+  quail_shortlist* sl = new quail_shortlist();
+  std::string msg;
+  const quail_status s = quail_build_shortlist_host(trie, cut_depth, sl, &msg);
+  if (s != QUAIL_OK) {
+    quail_trie_free(sl->prefix_trie);
+    delete sl;
+    return fail(s, "%s", msg.c_str());
+  }
+  *out = sl;
+  return QUAIL_OK;
+}
+
+void quail_shortlist_free(quail_shortlist* sl) {
+  if (sl == nullptr) return;
+  int cur = -1;
+  cudaGetDevice(&cur);
+  for (auto& kv : sl->images) {
+    if (kv.second.base == nullptr) continue;
+    if (cudaSetDevice(kv.first) == cudaSuccess) cudaFree(kv.second.base);
+  }
+  if (cur >= 0 && !sl->images.empty()) cudaSetDevice(cur);
+  quail_trie_free(sl->prefix_trie);
+  delete sl;
+}
+
+int32_t quail_shortlist_groups(const quail_shortlist* sl, int32_t* group_of_label) {
+  if (sl == nullptr) return 0;
+  if (group_of_label != nullptr) std::copy(sl->group_of_label.begin(), sl->group_of_label.end(), group_of_label);
+  return sl->num_groups;
+}
+
+size_t quail_workspace_size_shortlist(const quail_model_desc* model, const quail_trie* trie,
+                                      const quail_shortlist* sl, int32_t beam, int32_t num_docs,
+                                      int32_t max_doc_len) {
+  if (model == nullptr || trie == nullptr || sl == nullptr || beam < 1 || num_docs < 0 || max_doc_len <= 0) return 0;
+  if (!shortlist_matches(sl, trie)) return 0;
+  if (model->n_kv_heads <= 0 || model->n_q_heads <= 0 || model->hidden <= 0 || model->vocab <= 0) return 0;
+  return plan_shortlist(nullptr, model, sl, beam, num_docs, max_doc_len, nullptr);
+}
+
+quail_status quail_classify_trie_tree_shortlist(const quail_model_desc* model, const quail_paged_kv* kv,
+                                                quail_trie* trie, quail_shortlist* sl, int32_t beam,
+                                                int32_t num_docs, void* workspace, size_t workspace_bytes,
+                                                float* label_logscore, float* label_prob, int32_t* label_argmax,
+                                                int32_t* group_selected, quail_stream_t stream) {
+  g_launches = 0;
+  quail_status s = check_model(model);
+  if (s != QUAIL_OK) return s;
+  s = check_kv(kv, model);
+  if (s != QUAIL_OK) return s;
+  if (trie == nullptr || sl == nullptr) return fail(QUAIL_ERR_INVALID_ARG, "trie or shortlist is null");
+  if (trie->vocab != model->vocab)
+    return fail(QUAIL_ERR_INVALID_ARG, "trie vocab %d != model vocab %d", trie->vocab, model->vocab);
+  if (!shortlist_matches(sl, trie)) return fail(QUAIL_ERR_INVALID_ARG, "the shortlist was made from another trie");
+  if (beam < 1) return fail(QUAIL_ERR_INVALID_ARG, "beam must be >= 1");
+  if (num_docs < 0) return fail(QUAIL_ERR_INVALID_ARG, "num_docs < 0");
+  if (num_docs == 0) return QUAIL_OK;
+  if (num_docs > 65535) return fail(QUAIL_ERR_UNSUPPORTED_SHAPE, "at most 65535 documents per call");
+  if (label_logscore == nullptr || label_prob == nullptr || label_argmax == nullptr)
+    return fail(QUAIL_ERR_INVALID_ARG, "an output pointer is null");
+  const size_t need = plan_shortlist(nullptr, model, sl, beam, num_docs, kv->max_doc_len, nullptr);
+  s = check_workspace(workspace, workspace_bytes, need);
+  if (s != QUAIL_OK) return s;
+  DeviceState* ds = nullptr;
+  s = device_state(&ds);
+  if (s != QUAIL_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const quail_trie::DeviceImage* img = nullptr;
+  s = upload_trie(trie, st, &img);
+  if (s != QUAIL_OK) return s;
+  const quail_trie::DeviceImage* img1 = nullptr;
+  s = upload_trie(sl->prefix_trie, st, &img1);
+  if (s != QUAIL_OK) return s;
+  const quail_shortlist::DeviceImage* simg = nullptr;
+  s = upload_shortlist(sl, st, &simg);
+  if (s != QUAIL_OK) return s;
+  ShortlistBuffers x;
+  plan_shortlist(static_cast<uint8_t*>(workspace), model, sl, beam, num_docs, kv->max_doc_len, &x);
+  const ShortlistTables T{simg->row_off, simg->row_eval, simg->row_parent, simg->child_off, simg->child_row,
+                          simg->child_tok, simg->lab_off, simg->lab_id, simg->term_off, simg->term_t,
+                          simg->pref_t0, simg->pref_t1, sl->num_groups, sl->max_rows, sl->max_children};
+  const int G = sl->num_groups, B = x.B, R = x.R;
+  const int d = model->hidden;
+
+  // prefix pass (every group's prefix, every document), selection, row layout
+  stage_mark(QUAIL_STAGE_PROLOGUE, false, st);
+  s = trie_tree_pass(model, kv, sl->prefix_trie, img1, num_docs, x.b1, ds, st, x.ls1, x.prob1, x.am1, false);
+  if (s != QUAIL_OK) return s;
+  CUDA_TRY(launch_shortlist_select(x.ls1, num_docs, G, B, x.sel, st));
+  const Buffers& b = x.b2;
+  int* row_token = b.small;
+  int* row_depth = b.small + R;
+  int* row_parent = b.small + 2 * static_cast<size_t>(R);
+  int* row_eval = b.small + 3 * static_cast<size_t>(R);
+  int* zeros = b.small + 4 * static_cast<size_t>(R);
+  CUDA_TRY(cudaMemsetAsync(zeros, 0, 2 * sizeof(int), st));
+  CUDA_TRY(launch_shortlist_expand(T, x.sel, num_docs, B, img->eval_token, img->eval_depth, row_token, row_depth,
+                                   row_parent, row_eval, st));
+  stage_mark(QUAIL_STAGE_PROLOGUE, true, st);
+
+  // second pass over the kept groups' rows: slot = document, Bq rows each
+  const NodeTables nt{row_token, row_depth, row_parent, R};
+  const RowMap map{x.Bq, nullptr, nullptr, nullptr, nullptr, x.Bq};
+  stage_mark(QUAIL_STAGE_ATTENTION, false, st);
+  s = run_prologue(model, nt, b, ds, st);
+  if (s != QUAIL_OK) return s;
+  s = run_attention(model, kv, nt, map, num_docs, b, ds, st);
+  if (s != QUAIL_OK) return s;
+  stage_mark(QUAIL_STAGE_ATTENTION, true, st);
+  stage_mark(QUAIL_STAGE_WO_NORM, false, st);
+  s = run_wo_norm(model, nt, map, R, b, ds, st);
+  if (s != QUAIL_OK) return s;
+  stage_mark(QUAIL_STAGE_WO_NORM, true, st);
+  const int n_tiles = (model->vocab + kHeadBN - 1) / kHeadBN;
+  stage_mark(QUAIL_STAGE_HEAD, false, st);
+  {
+    CUtensorMap tA, tB;
+    s = encode_2d_bf16(&tA, b.z, round_up(R, 128), d, d, 64, 128);
+    if (s != QUAIL_OK) return s;
+    s = encode_2d_bf16(&tB, model->lm_head, model->vocab, d, d, 64, kHeadBBoxRows);
+    if (s != QUAIL_OK) return s;
+    // log-sum-exp partials only: one row per slot and an empty child list
+    HeadEpilogueArgs ha{b.lse_part, reinterpret_cast<float*>(zeros), zeros, zeros, b.z_f32,
+                        static_cast<const bf16*>(model->lm_head), d, 1, 0, n_tiles};
+    CUDA_TRY(launch_gemm_head(tA, tB, R, model->vocab, d, ha, ds->num_sms, ds->err, st));
+  }
+  stage_mark(QUAIL_STAGE_HEAD, true, st);
+  stage_mark(QUAIL_STAGE_SCORING, false, st);
+  CUDA_TRY(launch_lse_reduce(b.lse_part, R, n_tiles, b.lse, st));
+  CUDA_TRY(launch_shortlist_child_logprob(T, x.sel, num_docs, B, b.z_f32, static_cast<const bf16*>(model->lm_head),
+                                          d, b.lse, x.clp, st));
+  CUDA_TRY(launch_shortlist_label_score(T, x.sel, num_docs, B, trie->num_labels, x.clp, label_logscore, label_prob,
+                                        label_argmax, st));
+  stage_mark(QUAIL_STAGE_SCORING, true, st);
+  if (group_selected != nullptr)
+    CUDA_TRY(cudaMemcpyAsync(group_selected, x.sel, static_cast<size_t>(num_docs) * B * sizeof(int),
+                             cudaMemcpyDeviceToDevice, st));
   return QUAIL_OK;
 }
 

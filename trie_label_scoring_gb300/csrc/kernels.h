@@ -147,6 +147,34 @@ cudaError_t launch_decode_select(DecodeTrie t, const float* z, const bf16* lm_he
                                  int* active_count, uint8_t* touched, cudaStream_t st);
 
 // ------------------------------------------------------------ attention (attention.cu)
+// ------------------------------------------------------------ shortlist (shortlist.cu)
+// Device view of a shortlist plan (see shortlist.h for the table layout).
+struct ShortlistTables {
+  const int *row_off, *row_eval, *row_parent, *child_off, *child_row, *child_tok;
+  const int *lab_off, *lab_id, *term_off, *term_t, *pref_t0, *pref_t1;
+  int num_groups;
+  int max_rows;      // rows per (document, kept group) block
+  int max_children;  // child log-prob slots per block
+};
+// sel[doc * B + b]: the B groups of highest prefix log score (ties: lower group).
+cudaError_t launch_shortlist_select(const float* prefix_logscore, int num_docs, int G, int B, int* sel,
+                                    cudaStream_t st);
+// Row tables of the second pass: block (doc, b) holds group sel[doc * B + b]'s
+// rows, padded to max_rows with copies of the root row (row_eval -1).
+cudaError_t launch_shortlist_expand(const ShortlistTables& T, const int* sel, int num_docs, int B,
+                                    const int* eval_token, const int* eval_depth, int* row_token, int* row_depth,
+                                    int* row_parent, int* row_eval, cudaStream_t st);
+// clp[blk * max_children + t] = z32[row] . W_lm[tok] - lse[row] (fp32) for
+// every child t of the block's group.
+cudaError_t launch_shortlist_child_logprob(const ShortlistTables& T, const int* sel, int num_docs, int B,
+                                           const float* z32, const bf16* lm_head, int d, const float* lse,
+                                           float* clp, cudaStream_t st);
+// Label scores of the kept groups' labels (-inf / 0 elsewhere), softmax over
+// the kept labels, argmax (lowest label index of the maximum).
+cudaError_t launch_shortlist_label_score(const ShortlistTables& T, const int* sel, int num_docs, int B, int M,
+                                         const float* clp, float* logscore, float* prob, int* argmax,
+                                         cudaStream_t st);
+
 struct AttnArgs {
   // paged document KV
   int num_pages, max_pages, max_doc_len;

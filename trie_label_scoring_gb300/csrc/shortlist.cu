@@ -1,0 +1,275 @@
+// Kernels of the shortlisted trie_tree for huge label sets ("Trie Automata
+// for Constrained Decoding over Large Finite Sets": a top-k shortlist ahead
+// of exact trie scoring; hierarchical groups are the special case whose
+// prefixes are the group names). The first pass scores every group's prefix
+// with the ordinary trie_tree kernels; these kernels pick each document's best
+// groups, lay out the second pass's rows, and score the kept labels from the
+// second pass's hidden states (label scores as in "To Classify, Try a Trie
+// Tree", sec. 3.2).
+#include <algorithm>
+#include <cfloat>
+
+#include "kernels.h"
+#include "quail_internal.h"
+
+namespace quail {
+
+namespace {
+
+constexpr int kSelectThreads = 256;
+constexpr int kScoreThreads = 512;
+
+// (value, index) order of the shortlist: higher value first, lower index on ties.
+__device__ __forceinline__ bool ranks_before(float v, int i, float bv, int bi) {
+  return v > bv || (v == bv && i < bi);
+}
+
+// Block-wide best (value, index) under ranks_before; blockDim.x <= 1024.
+__device__ void block_best(float& v, int& i, float* s_v, int* s_i) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+    if (ranks_before(ov, oi, v, i)) {
+      v = ov;
+      i = oi;
+    }
+  }
+  __syncthreads();
+  if (lane == 0) {
+    s_v[warp] = v;
+    s_i[warp] = i;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < nw; ++w)
+      if (ranks_before(s_v[w], s_i[w], s_v[0], s_i[0])) {
+        s_v[0] = s_v[w];
+        s_i[0] = s_i[w];
+      }
+  }
+  __syncthreads();
+  v = s_v[0];
+  i = s_i[0];
+}
+
+__device__ float block_sum_f(float v, float* s) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if (lane == 0) s[warp] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < nw; ++w) t += s[w];
+    s[0] = t;
+  }
+  __syncthreads();
+  return s[0];
+}
+
+// CTA per document: B rounds, each taking the best group ranked after the
+// previous pick (so no group is taken twice and no mark table is needed).
+__global__ void __launch_bounds__(kSelectThreads) shortlist_select_kernel(const float* __restrict__ ls, int G, int B,
+                                                                          int* __restrict__ sel) {
+  __shared__ float s_v[32];
+  __shared__ int s_i[32];
+  const int doc = blockIdx.x;
+  const float* row = ls + static_cast<size_t>(doc) * G;
+  float pv = INFINITY;
+  int pi = -1;
+  for (int b = 0; b < B; ++b) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int g = threadIdx.x; g < G; g += blockDim.x) {
+      float v = row[g];
+      if (v != v) v = -INFINITY;  // a NaN score ranks last
+      const bool after = v < pv || (v == pv && g > pi);
+      if (after && ranks_before(v, g, bv, bi)) {
+        bv = v;
+        bi = g;
+      }
+    }
+    block_best(bv, bi, s_v, s_i);
+    if (threadIdx.x == 0) sel[doc * B + b] = bi;
+    pv = bv;
+    pi = bi;
+  }
+}
+
+// Block per (document, kept group): that group's rows, then root-row padding.
+__global__ void shortlist_expand_kernel(ShortlistTables T, const int* __restrict__ sel,
+                                        const int* __restrict__ eval_token, const int* __restrict__ eval_depth,
+                                        int* __restrict__ row_token, int* __restrict__ row_depth,
+                                        int* __restrict__ row_parent, int* __restrict__ row_eval) {
+  const int blk = blockIdx.x;
+  const int g = sel[blk];
+  const int r0 = blk * T.max_rows;
+  const int off = T.row_off[g];
+  const int n = T.row_off[g + 1] - off;
+  for (int j = threadIdx.x; j < T.max_rows; j += blockDim.x) {
+    const int r = r0 + j;
+    if (j < n) {
+      const int e = T.row_eval[off + j];
+      const int p = T.row_parent[off + j];
+      row_token[r] = eval_token[e];
+      row_depth[r] = eval_depth[e];
+      row_parent[r] = p >= 0 ? r0 + p : -1;
+      row_eval[r] = e;
+    } else {
+      row_token[r] = eval_token[0];
+      row_depth[r] = eval_depth[0];
+      row_parent[r] = -1;
+      row_eval[r] = -1;
+    }
+  }
+}
+
+// Warp per (block, child slot): the child token's logit from the unrounded
+// hidden state in fp32 (z32 . W_lm[tok]), minus the row's log-sum-exp.
+__global__ void shortlist_child_logprob_kernel(ShortlistTables T, const int* __restrict__ sel, int n_blocks,
+                                               const float* __restrict__ z32, const bf16* __restrict__ lm_head, int d,
+                                               const float* __restrict__ lse, float* __restrict__ clp) {
+  const int lane = threadIdx.x & 31;
+  const long long total = static_cast<long long>(n_blocks) * T.max_children;
+  for (long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < total;
+       w += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
+    const int blk = static_cast<int>(w / T.max_children);
+    const int t = static_cast<int>(w - static_cast<long long>(blk) * T.max_children);
+    const int g = sel[blk];
+    const int c0 = T.child_off[g];
+    if (t >= T.child_off[g + 1] - c0) continue;
+    const int r = blk * T.max_rows + T.child_row[c0 + t];
+    const int tok = T.child_tok[c0 + t];
+    const float4* zr = reinterpret_cast<const float4*>(z32 + static_cast<size_t>(r) * d);
+    const uint2* wr = reinterpret_cast<const uint2*>(lm_head + static_cast<size_t>(tok) * d);
+    float acc = 0.f;
+    for (int i = lane; i < (d >> 2); i += 32) {
+      const float4 z4 = zr[i];
+      const uint2 w4 = __ldg(wr + i);
+      const float2 w01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4.x));
+      const float2 w23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4.y));
+      acc = fmaf(z4.x, w01.x, acc);
+      acc = fmaf(z4.y, w01.y, acc);
+      acc = fmaf(z4.z, w23.x, acc);
+      acc = fmaf(z4.w, w23.y, acc);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) clp[w] = acc - lse[r];
+  }
+}
+
+// CTA per document: clear the row, score the kept groups' labels (warp per
+// label), then softmax and argmax over the kept labels.
+__global__ void __launch_bounds__(kScoreThreads) shortlist_label_score_kernel(
+    ShortlistTables T, const int* __restrict__ sel, int B, int M, const float* __restrict__ clp,
+    float* __restrict__ logscore, float* __restrict__ prob, int* __restrict__ argmax) {
+  __shared__ float s_v[32];
+  __shared__ int s_i[32];
+  const int doc = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  float* ls = logscore + static_cast<size_t>(doc) * M;
+  float* pr = prob + static_cast<size_t>(doc) * M;
+  for (int m = threadIdx.x; m < M; m += blockDim.x) {
+    ls[m] = -INFINITY;
+    pr[m] = 0.f;
+  }
+  __syncthreads();
+  for (int b = 0; b < B; ++b) {
+    const int blk = doc * B + b;
+    const int g = sel[blk];
+    const float* cl = clp + static_cast<size_t>(blk) * T.max_children;
+    for (int li = T.lab_off[g] + warp; li < T.lab_off[g + 1]; li += nw) {
+      float acc = 0.f;
+      for (int k = T.term_off[li] + lane; k < T.term_off[li + 1]; k += 32) acc += cl[T.term_t[k]];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      const int p0 = T.pref_t0[li], p1 = T.pref_t1[li];
+      if (p1 > p0) {  // prefix label: probability of stopping at its end node
+        double cont = 0.0;
+        for (int c = p0 + lane; c < p1; c += 32) cont += exp(static_cast<double>(cl[c]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) cont += __shfl_xor_sync(0xffffffffu, cont, o);
+        acc = (cont < 1.0 - 1e-12) ? acc + static_cast<float>(log1p(-cont)) : -INFINITY;
+      }
+      if (lane == 0) ls[T.lab_id[li]] = acc;
+    }
+  }
+  __syncthreads();
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int b = 0; b < B; ++b) {
+    const int g = sel[doc * B + b];
+    for (int li = T.lab_off[g] + threadIdx.x; li < T.lab_off[g + 1]; li += blockDim.x) {
+      const int m = T.lab_id[li];
+      if (ranks_before(ls[m], m, bv, bi)) {
+        bv = ls[m];
+        bi = m;
+      }
+    }
+  }
+  block_best(bv, bi, s_v, s_i);
+  float part = 0.f;
+  for (int b = 0; b < B; ++b) {
+    const int g = sel[doc * B + b];
+    for (int li = T.lab_off[g] + threadIdx.x; li < T.lab_off[g + 1]; li += blockDim.x)
+      part += expf(ls[T.lab_id[li]] - bv);
+  }
+  const float sum = block_sum_f(part, s_v);
+  const float inv = (bv == -INFINITY) ? __int_as_float(0x7fc00000) : 1.f / sum;
+  for (int b = 0; b < B; ++b) {
+    const int g = sel[doc * B + b];
+    for (int li = T.lab_off[g] + threadIdx.x; li < T.lab_off[g + 1]; li += blockDim.x) {
+      const int m = T.lab_id[li];
+      pr[m] = (bv == -INFINITY) ? inv : expf(ls[m] - bv) * inv;
+    }
+  }
+  if (threadIdx.x == 0) argmax[doc] = bi == 0x7fffffff ? 0 : bi;
+}
+
+}  // namespace
+
+cudaError_t launch_shortlist_select(const float* prefix_logscore, int num_docs, int G, int B, int* sel,
+                                    cudaStream_t st) {
+  if (num_docs <= 0) return cudaSuccess;
+  if (B < 1 || B > G) return cudaErrorInvalidValue;
+  count_launch();
+  shortlist_select_kernel<<<num_docs, kSelectThreads, 0, st>>>(prefix_logscore, G, B, sel);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_shortlist_expand(const ShortlistTables& T, const int* sel, int num_docs, int B,
+                                    const int* eval_token, const int* eval_depth, int* row_token, int* row_depth,
+                                    int* row_parent, int* row_eval, cudaStream_t st) {
+  if (num_docs <= 0) return cudaSuccess;
+  count_launch();
+  shortlist_expand_kernel<<<num_docs * B, 128, 0, st>>>(T, sel, eval_token, eval_depth, row_token, row_depth,
+                                                        row_parent, row_eval);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_shortlist_child_logprob(const ShortlistTables& T, const int* sel, int num_docs, int B,
+                                           const float* z32, const bf16* lm_head, int d, const float* lse,
+                                           float* clp, cudaStream_t st) {
+  if (num_docs <= 0 || T.max_children <= 0) return cudaSuccess;
+  if (d % 4 != 0) return cudaErrorInvalidValue;
+  const long long warps = static_cast<long long>(num_docs) * B * T.max_children;
+  const int blocks = static_cast<int>(std::min<long long>((warps + 7) / 8, 1 << 16));
+  count_launch();
+  shortlist_child_logprob_kernel<<<blocks, 256, 0, st>>>(T, sel, num_docs * B, z32, lm_head, d, lse, clp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_shortlist_label_score(const ShortlistTables& T, const int* sel, int num_docs, int B, int M,
+                                         const float* clp, float* logscore, float* prob, int* argmax,
+                                         cudaStream_t st) {
+  if (num_docs <= 0) return cudaSuccess;
+  count_launch();
+  shortlist_label_score_kernel<<<num_docs, kScoreThreads, 0, st>>>(T, sel, B, M, clp, logscore, prob, argmax);
+  return cudaGetLastError();
+}
+
+}  // namespace quail
