@@ -18,6 +18,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -205,6 +206,9 @@ def run_reference(args, world, rank):
     if args.workload in S.ML_WORKLOADS:
         run_reference_ml(args, world)
         return
+    if args.workload in S.SHORTLIST_WORKLOADS:
+        run_reference_shortlist(args, world)
+        return
     w = S.WORKLOADS[args.workload]
     if args.docs:
         w = S.with_docs(w, args.docs)
@@ -258,6 +262,49 @@ def run_reference_ml(args, world):
         "ms_per_step": 1e3 / value, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded)", "config": {"workload": mw.name, "docs_per_step": 1},
         "cpu_baseline": {"value": value, "unit": "docs/s", "cores": cores(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "docs/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def run_reference_shortlist(args, world):
+    """The shortlist oracle on one document per step."""
+    import synthetic as S
+    from oracle import shortlist as OSL
+    from oracle.trie import build_trie
+    from tests import gpu_cases as C
+    sw = S.SHORTLIST_WORKLOADS[args.workload]
+    w = S.with_docs(sw.base, args.docs) if args.docs else sw.base
+    labels = S.make_labels(w, 0)
+    K = len(labels.labels)
+    G = sw.groups or OSL.default_groups(K)
+    names = S.make_group_names(0, G, 1, w.shape.vocab)
+    rw = OSL.rewrite_grouped(labels.labels, names, OSL.group_labels(labels.labels, G))
+    t = build_trie(rw, labels.root_token, w.shape.vocab)
+    docs = S.make_docs(w, 0)
+    L = C.oracle_layer(w.shape)
+    L.lm_head()
+    steps = args.steps if args.steps is not None else 3
+
+    def step(i):
+        dk, dv = C.oracle_doc_kv(docs, i % w.num_docs)
+        OSL.shortlist(L, dk, dv, t, 1, sw.beam)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        step(args.warmup + i)
+    el = time.perf_counter() - t0
+    value = steps / el
+    out = {
+        "impl": "reference", "metric": "documents classified/sec at 1 GB300 (shortlisted trie_tree over grouped "
+                                       "labels)",
+        "value": value, "unit": "docs/s", "n_gpus": world, "steps": steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * el / steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded)", "config": {"workload": sw.name, "docs_per_step": 1},
+        "cpu_baseline": {"value": value, "unit": "docs/s", "cores": cores(), "kind": "oracle",
+                         "sample": f"1 document of {w.name} per step (oracle shortlist, {G} groups, beam {sw.beam})"},
         "e2e": {"value": value, "unit": "docs/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(out), flush=True)
@@ -740,6 +787,220 @@ def run_ml(args, world, rank, local):
         print(json.dumps(out), flush=True)
 
 
+def _group_rows(view, D: int) -> dict:
+    """Rows of each group of a shortlist plan at cut depth D: the evaluated
+    ancestors of the group's depth-D node plus the evaluated nodes of its
+    subtree (node order = group order)."""
+    import numpy as np
+    depth, parent, sub, ev = view["depth"], view["parent"], view["subtree_size"], view["eval_index_of_node"] >= 0
+    nodes = np.nonzero(depth == D)[0]
+    cum = np.concatenate([[0], np.cumsum(ev)])
+    rows = []
+    for c in nodes:
+        up, u = 0, int(parent[c])
+        while u >= 0:
+            up += int(ev[u])
+            u = int(parent[u])
+        rows.append(up + int(cum[c + sub[c]] - cum[c]))
+    return np.array(rows)
+
+
+def run_shortlist(args, world, rank, local):
+    """Huge label sets: grouped labels scored through the shortlist
+    (quail_classify_trie_tree_shortlist). One step = one call over all
+    documents; metric = documents/s."""
+    import numpy as np
+    import torch
+
+    import synthetic as S
+    import trie_label_scoring_gb300 as Q
+    from tests import gpu_cases as C
+    from trie_label_scoring_gb300.torch_inputs import bf16_tensor, kv_from_docs
+
+    Q.build()
+    sw = S.SHORTLIST_WORKLOADS[args.workload]
+    w = S.with_docs(sw.base, args.docs) if args.docs else sw.base
+    model = C.device_model(w.shape, 0)
+    labels = S.make_labels(w, 0)
+    K = len(labels.labels)
+    G = sw.groups or (math.isqrt(K - 1) + 1)  # ceil(sqrt K)
+    names = S.make_group_names(0, G, 1, w.shape.vocab)
+    trie, _ = Q.Trie.grouped(labels.labels, labels.root_token, w.shape.vocab, names, num_groups=G)
+    trie.upload()
+    sl = Q.Shortlist(trie, 1)
+    beam = sw.beam
+    docs = S.make_docs(w, rank)
+    kv = kv_from_docs(docs)
+    N = w.num_docs
+    ws = torch.empty(Q.workspace_size_shortlist(model, trie, sl, beam, N, docs.max_doc_len), dtype=torch.uint8,
+                     device="cuda")
+    lsc = torch.empty((N, K), device="cuda")
+    prob = torch.empty((N, K), device="cuda")
+    am = torch.empty((N,), dtype=torch.int32, device="cuda")
+    sel = torch.empty((N, beam), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        Q.classify_trie_tree_shortlist(model, kv, trie, sl, beam, N, ws, lsc, prob, am, sel, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    Q.device_status()
+    launches_per_step = Q.launch_count()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    step()
+    t1.record(stream)
+    t1.synchronize()
+    est_ms = t0.elapsed_time(t1)
+    steps = args.steps if args.steps is not None else int(min(2000, max(20, 2000.0 / max(est_ms, 1e-3))))
+    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(10)] for _ in range(steps)]
+    for evs in stage_ev:
+        for e in evs:
+            e.record(stream)
+    clocks = ClockSampler(str(torch.cuda.get_device_properties(local).pci_bus_id))
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for k in range(steps):
+        Q.set_stage_events(stage_ev[k])
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    Q.set_stage_events(None)
+    Q.device_status()
+    elapsed_ms = max_over_ranks(world, start.elapsed_time(end))
+    ms_per_step = elapsed_ms / steps
+    value = N * world * steps / (elapsed_ms / 1e3)
+    names5 = ("prefix_pass_select_layout", "prologue_attention", "wo_norm", "head", "scoring")
+    stages_ms = {nm: statistics.mean(ev[2 * i].elapsed_time(ev[2 * i + 1]) for ev in stage_ev)
+                 for i, nm in enumerate(names5)}
+
+    # rows of the second pass: real (the kept groups' rows) and padded
+    view = trie.view()
+    grows = _group_rows(view, 1)
+    selected = sel.cpu().numpy()
+    real_rows = int(grows[selected].sum())
+    pad_rows = N * beam * int(grows.max())
+
+    # the flat trie_tree over the same grouped trie, for context (one timed call)
+    flat_ms = None
+    try:
+        a = trie.n_eval
+        wsf = torch.empty(Q.workspace_size(model, trie, 0, N, docs.max_doc_len, Q.MODE_TRIE_TREE),
+                          dtype=torch.uint8, device="cuda")
+        Q.classify_trie_tree(model, kv, trie, N, wsf, lsc, prob, am, stream)
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        Q.classify_trie_tree(model, kv, trie, N, wsf, lsc, prob, am, stream)
+        f1.record(stream)
+        f1.synchronize()
+        flat_ms = f0.elapsed_time(f1)
+        del wsf
+        step()  # leave the shortlisted outputs in place
+        torch.cuda.synchronize()
+    except Q.QuailError:
+        a = None
+
+    # e2e: document KV from pinned host memory, every label's scores back
+    e2e = None
+    if not args.no_e2e:
+        hk = bf16_tensor(docs.k_pool, "cpu").pin_memory()
+        hv = bf16_tensor(docs.v_pool, "cpu").pin_memory()
+        hpt = torch.from_numpy(docs.page_table).pin_memory()
+        hdl = torch.from_numpy(docs.doc_len).pin_memory()
+        dk, dv, dpt, ddl = kv.tensors
+        o_ls = torch.empty((N, K)).pin_memory()
+        o_pr = torch.empty((N, K)).pin_memory()
+        o_am = torch.empty((N,), dtype=torch.int32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (hk, hv, hpt, hdl))
+        d2h = sum(t.numel() * t.element_size() for t in (o_ls, o_pr, o_am))
+
+        def e2e_step():
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            dpt.copy_(hpt, non_blocking=True)
+            ddl.copy_(hdl, non_blocking=True)
+            step()
+            o_ls.copy_(lsc, non_blocking=True)
+            o_pr.copy_(prob, non_blocking=True)
+            o_am.copy_(am, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        k_e2e = max(3, min(steps, int(3000.0 / max(est_ms + 3.0, 1e-3))))
+        barrier(world)
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(k_e2e):
+            e2e_step()
+        e2.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(world, s2.elapsed_time(e2))
+        e2e = {"value": N * world * k_e2e / (e2e_ms / 1e3), "unit": "docs/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": k_e2e}
+
+    # roofline: the second pass's output-head GEMM, FLOPs of the real rows
+    peaks = measured_peaks()
+    d, V = w.shape.hidden, w.shape.vocab
+    flops = 2.0 * d * V * real_rows
+    achieved = flops / (stages_ms["head"] / 1e3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                "kernel": "umma_gemm_kernel<EpiHead> (second pass)", "head_ms": stages_ms["head"],
+                "real_rows": real_rows, "padded_rows": pad_rows,
+                "peak_kind": f"bf16 burst ({peaks['source']})",
+                "note": "FLOPs of the kept groups' rows; padding rows (copies of the root) are extra work"}
+    kv_bytes = float(docs.doc_len.sum()) * w.shape.n_kv_heads * w.shape.head_dim * 2 * 2
+    path_bytes = 2 * kv_bytes + 2 * 2.0 * d * V
+    path_flops = 2.0 * d * V * (N + real_rows)
+    t_b = path_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_f = path_flops / (peaks["bf16_tflops"] * 1e12)
+    path = {"t_bytes_us": t_b * 1e6, "t_flops_us": t_f * 1e6, "t_star_us": max(t_b, t_f) * 1e6,
+            "ms_per_step": ms_per_step, "frac": max(t_b, t_f) * 1e3 / ms_per_step}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import shortlist as OSL
+        from oracle.trie import build_trie
+        rw = OSL.rewrite_grouped(labels.labels, names, OSL.group_labels(labels.labels, G))
+        ref_t = build_trie(rw, labels.root_token, V)
+        L = C.oracle_layer(w.shape, 0)
+        L.lm_head()
+        c0 = time.perf_counter()
+        done = 0
+        while done < N and (done == 0 or time.perf_counter() - c0 < 15.0):
+            dk_, dv_ = C.oracle_doc_kv(docs, done)
+            OSL.shortlist(L, dk_, dv_, ref_t, 1, beam)
+            done += 1
+        sec = time.perf_counter() - c0
+        cpu = {"value": done / sec, "unit": "docs/s", "cores": cores(), "kind": "oracle",
+               "sample": f"first {done} documents of {w.name} ({sec:.1f} s, oracle shortlist with the same "
+                         f"groups and beam)"}
+    if rank == 0:
+        out = {
+            "metric": "documents classified/sec at 1 GB300 (shortlisted trie_tree over grouped labels)",
+            "value": value, "unit": "docs/s", "n_gpus": world, "steps": steps, "warmup": max(args.warmup, 3),
+            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded, random-init weights)",
+            "config": {"workload": sw.name, "docs_per_gpu": N, "labels": K, "groups": G, "beam": beam,
+                       "trie_nodes": trie.n_nodes, "eval_positions_flat": a, "second_pass_rows": real_rows,
+                       "second_pass_rows_padded": pad_rows, "hidden": d, "vocab": V,
+                       "l2": "inputs larger than L2 (output head 0.78 GB read twice per step)",
+                       "parallelism": f"replicas x{world} (documents sharded, no collective)"},
+            "roofline": roofline, "path_roofline": path, "stages_ms": stages_ms,
+            "flat_trie_tree_ms": flat_ms, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches_per_step * steps, "clocks": clk,
+        }
+        print(json.dumps(out), flush=True)
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -751,6 +1012,8 @@ def main():
     import synthetic as S
     if args.workload in S.ML_WORKLOADS:  # the whole decoder stack
         run_ml(args, world, rank, local)
+    elif args.workload in S.SHORTLIST_WORKLOADS:  # grouped labels through the shortlist
+        run_shortlist(args, world, rank, local)
     elif "-join" in args.workload:  # AI.IF join workloads (synthetic labels kind "join")
         run_join(args, world, rank, local)
     else:

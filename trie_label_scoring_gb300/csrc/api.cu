@@ -299,18 +299,19 @@ struct NodeTables {
 // q|k|v = x^ W^T in one launch when the three weight blocks align to 256 rows;
 // per-head q/k RMSNorm while summing the k-split slabs.
 quail_status run_qkv(const quail_model_desc* m, const NodeTables& nt, const Buffers& b, DeviceState* ds,
-                     cudaStream_t st);
+                     cudaStream_t st, const int* m_live = nullptr);
 
 quail_status run_prologue(const quail_model_desc* m, const NodeTables& nt, const Buffers& b, DeviceState* ds,
-                          cudaStream_t st) {
+                          cudaStream_t st, const int* m_live = nullptr) {
   CUDA_TRY(launch_embed_rmsnorm(static_cast<const bf16*>(m->embed), nt.token, nt.nodes, m->hidden,
                                 static_cast<const bf16*>(m->in_norm), m->rms_eps, b.xhat, st));
-  return run_qkv(m, nt, b, ds, st);
+  return run_qkv(m, nt, b, ds, st, m_live);
 }
 
 // q|k|v = x^ W^T from the split rows already in b.xhat; per-head q/k RMSNorm.
+// m_live (optional): device count of the node rows present; the GEMM skips the rest.
 quail_status run_qkv(const quail_model_desc* m, const NodeTables& nt, const Buffers& b, DeviceState* ds,
-                     cudaStream_t st) {
+                     cudaStream_t st, const int* m_live) {
   const int d = m->hidden, hq = m->n_q_heads, hkv = m->n_kv_heads;
   const int ldq = (hq + 2 * hkv) * 128;
   CUtensorMap tA;
@@ -331,14 +332,14 @@ quail_status run_qkv(const quail_model_desc* m, const NodeTables& nt, const Buff
     if (!aligned) {
       bs.count = 1;
       CUDA_TRY(launch_gemm_proj(tA, bs, nt.nodes, nrows[i], d, b.gp.ks_qkv, b.qkv_part + col, slab, ldq, ds->num_sms,
-                                ds->err, st));
+                                ds->err, st, m_live));
     }
     col += nrows[i];
   }
   if (aligned) {
     bs.count = 3;
     CUDA_TRY(launch_gemm_proj(tA, bs, nt.nodes, ldq, d, b.gp.ks_qkv, b.qkv_part, slab, ldq, ds->num_sms, ds->err,
-                              st));
+                              st, m_live));
   }
   CUDA_TRY(launch_qk_head_norm(b.qkv_part, b.gp.ks_qkv, slab, b.qkv, nt.nodes, ldq, hq, hkv,
                                static_cast<const bf16*>(m->q_norm), static_cast<const bf16*>(m->k_norm), m->rms_eps,
@@ -761,6 +762,7 @@ struct ShortlistBuffers {
   Buffers b1, b2;
   int* sel;       // [N, B]
   float* clp;     // [N * B, max_children]
+  bf16* attn_c;   // [round_up(R, 128), 2 hq 128] attention output of the real rows, compacted
   float* ls1;     // [N, G] prefix log scores
   float* prob1;   // [N, G]
   int* am1;       // [N]
@@ -778,11 +780,15 @@ size_t plan_shortlist(uint8_t* base, const quail_model_desc* m, const quail_shor
   const int a1 = pt->n_eval();
   const size_t p1 = plan(base, m, a1, N, a1, max_doc_len, true, pt->eval_child_offsets.back(), false, 0,
                          base ? &x.b1 : nullptr);
-  const size_t p2 = plan(base, m, x.R, N, x.Bq, max_doc_len, true, 0, true, 4 * x.R + 2, base ? &x.b2 : nullptr);
+  // small ints: token, depth, parent, padded row of every row; 2 zeros; count; block bases; document bases
+  // and row counts
+  const size_t p2 = plan(base, m, x.R, N, x.Bq, max_doc_len, true, 0, true, 4 * x.R + 3 + N * x.B + 2 * N,
+                         base ? &x.b2 : nullptr);
   const size_t shared = round_up(std::max(p1, p2), 256);
   Carver c{base ? base + shared : nullptr};
   x.sel = c.take<int>(static_cast<size_t>(N) * x.B);
   x.clp = c.take<float>(static_cast<size_t>(N) * x.B * std::max(sl->max_children, 1));
+  x.attn_c = c.take<bf16>(round_up(x.R, 128) * 2 * m->n_q_heads * 128);
   x.ls1 = c.take<float>(static_cast<size_t>(N) * sl->num_groups);
   x.prob1 = c.take<float>(static_cast<size_t>(N) * sl->num_groups);
   x.am1 = c.take<int>(N);
@@ -1520,25 +1526,55 @@ quail_status quail_classify_trie_tree_shortlist(const quail_model_desc* model, c
   int* row_token = b.small;
   int* row_depth = b.small + R;
   int* row_parent = b.small + 2 * static_cast<size_t>(R);
-  int* row_eval = b.small + 3 * static_cast<size_t>(R);
-  int* zeros = b.small + 4 * static_cast<size_t>(R);
+  int* padded_of = b.small + 3 * static_cast<size_t>(R);
+  int* zeros = b.small + 4 * static_cast<size_t>(R);  // [2]
+  int* count = zeros + 2;
+  int* block_base = count + 1;
+  int* doc_base = block_base + static_cast<size_t>(num_docs) * B;
+  int* doc_rows = doc_base + num_docs;
   CUDA_TRY(cudaMemsetAsync(zeros, 0, 2 * sizeof(int), st));
-  CUDA_TRY(launch_shortlist_expand(T, x.sel, num_docs, B, img->eval_token, img->eval_depth, row_token, row_depth,
-                                   row_parent, row_eval, st));
+  CUDA_TRY(launch_shortlist_scan(T, x.sel, num_docs, B, block_base, doc_base, doc_rows, count, st));
+  CUDA_TRY(launch_shortlist_expand(T, x.sel, num_docs, B, x.Bq, R, block_base, doc_base, count, img->eval_token,
+                                   img->eval_depth, row_token, row_depth, row_parent, padded_of, st));
   stage_mark(QUAIL_STAGE_PROLOGUE, true, st);
 
-  // second pass over the kept groups' rows: slot = document, Bq rows each
+  // second pass over the kept groups' rows, numbered compactly document by
+  // document (count real rows, then root copies up to the bound R): the
+  // GEMMs skip the M tiles past count; the attention sees Bq padded rows per
+  // document (row e of document i is node doc_base[i] + e, padding reads its
+  // last row) and skips row tiles of padding only; its padded output rows are
+  // gathered back into the compact order before W_o.
   const NodeTables nt{row_token, row_depth, row_parent, R};
-  const RowMap map{x.Bq, nullptr, nullptr, nullptr, nullptr, x.Bq};
+  RowMap map{x.Bq, nullptr, nullptr, nullptr, nullptr, 0};
+  map.slot_base = doc_base;
+  map.slot_rows = doc_rows;
+  const int hq = model->n_q_heads;
   stage_mark(QUAIL_STAGE_ATTENTION, false, st);
-  s = run_prologue(model, nt, b, ds, st);
+  s = run_prologue(model, nt, b, ds, st, count);
   if (s != QUAIL_OK) return s;
   s = run_attention(model, kv, nt, map, num_docs, b, ds, st);
   if (s != QUAIL_OK) return s;
   stage_mark(QUAIL_STAGE_ATTENTION, true, st);
   stage_mark(QUAIL_STAGE_WO_NORM, false, st);
-  s = run_wo_norm(model, nt, map, R, b, ds, st);
-  if (s != QUAIL_OK) return s;
+  CUDA_TRY(launch_gather_rows(b.attn_out, padded_of, count, R, static_cast<size_t>(2) * hq * 128 * sizeof(bf16),
+                              x.attn_c, st));
+  {
+    CUtensorMap tA;
+    s = encode_2d_bf16(&tA, x.attn_c, round_up(R, 128), 2 * hq * 128, 2 * hq * 128, 64, 128);
+    if (s != QUAIL_OK) return s;
+    BSet bs{};
+    s = encode_2d_bf16(&bs.map[0], model->w_o, d, hq * 128, hq * 128, 64, 256);
+    if (s != QUAIL_OK) return s;
+    bs.n_begin[0] = 0;
+    bs.n_begin[1] = d;
+    bs.count = 1;
+    const size_t slab = static_cast<size_t>(R) * d;
+    CUDA_TRY(launch_gemm_proj(tA, bs, R, d, hq * 128, b.gp.ks_wo, b.h_part, slab, d, ds->num_sms, ds->err, st,
+                              count));
+    const RowMap cmap{1, nullptr, nullptr, count, nullptr, 1};  // row r is node r; rows past count skipped
+    CUDA_TRY(launch_final_norm(b.h_part, b.gp.ks_wo, slab, static_cast<const bf16*>(model->embed), nt.token, cmap, R,
+                               d, static_cast<const bf16*>(model->final_norm), model->rms_eps, b.z, b.z_f32, st));
+  }
   stage_mark(QUAIL_STAGE_WO_NORM, true, st);
   const int n_tiles = (model->vocab + kHeadBN - 1) / kHeadBN;
   stage_mark(QUAIL_STAGE_HEAD, false, st);
@@ -1551,13 +1587,13 @@ quail_status quail_classify_trie_tree_shortlist(const quail_model_desc* model, c
     // log-sum-exp partials only: one row per slot and an empty child list
     HeadEpilogueArgs ha{b.lse_part, reinterpret_cast<float*>(zeros), zeros, zeros, b.z_f32,
                         static_cast<const bf16*>(model->lm_head), d, 1, 0, n_tiles};
-    CUDA_TRY(launch_gemm_head(tA, tB, R, model->vocab, d, ha, ds->num_sms, ds->err, st));
+    CUDA_TRY(launch_gemm_head(tA, tB, R, model->vocab, d, ha, ds->num_sms, ds->err, st, count));
   }
   stage_mark(QUAIL_STAGE_HEAD, true, st);
   stage_mark(QUAIL_STAGE_SCORING, false, st);
   CUDA_TRY(launch_lse_reduce(b.lse_part, R, n_tiles, b.lse, st));
-  CUDA_TRY(launch_shortlist_child_logprob(T, x.sel, num_docs, B, b.z_f32, static_cast<const bf16*>(model->lm_head),
-                                          d, b.lse, x.clp, st));
+  CUDA_TRY(launch_shortlist_child_logprob(T, x.sel, num_docs, B, block_base, b.z_f32,
+                                          static_cast<const bf16*>(model->lm_head), d, b.lse, x.clp, st));
   CUDA_TRY(launch_shortlist_label_score(T, x.sel, num_docs, B, trie->num_labels, x.clp, label_logscore, label_prob,
                                         label_argmax, st));
   stage_mark(QUAIL_STAGE_SCORING, true, st);

@@ -154,6 +154,7 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
   const int n_row_groups = a.rows_pad / a.row_tile;
   const int g = blockIdx.y / n_row_groups;
   const int rg = blockIdx.y % n_row_groups;
+  if (rows_past_end(a.map, slot, rg * a.row_tile / (a.hq / a.hkv))) return;  // a row group of padding only
   const int doc = row_doc(a.map, slot);
   const int L = a.doc_len[doc];
   if (L < 1 || L > a.max_doc_len) {
@@ -505,6 +506,7 @@ __global__ void attn_combine_kernel(AttnArgs a) {
   const int nq = a.map.nq;
   const int slot = row / nq, e = row % nq;
   if (a.map.n_slots_dev != nullptr && slot >= *a.map.n_slots_dev) return;
+  if (rows_past_end(a.map, slot, e)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.hq / a.hkv;
   const int doc = row_doc(a.map, slot);

@@ -136,6 +136,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // together and re-read it from L2), y = split + n_splits * kv head, z = slot
   const int slot = blockIdx.z;
   if (a.map.n_slots_dev != nullptr && slot >= *a.map.n_slots_dev) return;
+  if (rows_past_end(a.map, slot, static_cast<int>(blockIdx.x) * kTcRows / (a.hq / a.hkv))) return;  // padding tile
   const int rt_idx = blockIdx.x;
   const int split = blockIdx.y % a.n_splits;
   const int g = blockIdx.y / a.n_splits;

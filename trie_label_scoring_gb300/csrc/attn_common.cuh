@@ -61,7 +61,15 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 __device__ __forceinline__ int row_doc(const RowMap& m, int slot) { return m.slot_doc ? m.slot_doc[slot] : slot; }
 __device__ __forceinline__ int row_node(const RowMap& m, int slot, int e) {
+  if (m.slot_base) {
+    const int n = m.slot_rows[slot];
+    return m.slot_base[slot] + (e < n ? e : n - 1);
+  }
   return m.slot_node ? m.slot_node[slot] : slot * m.slot_stride + (m.row_nodes ? m.row_nodes[e] : e);
+}
+// True when every query row from e on is padding of its slot.
+__device__ __forceinline__ bool rows_past_end(const RowMap& m, int slot, int e) {
+  return m.slot_rows != nullptr && e >= m.slot_rows[slot];
 }
 
 }  // namespace quail

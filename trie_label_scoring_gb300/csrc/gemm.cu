@@ -119,7 +119,7 @@ struct EpiHead {
 
 template <int BN, int STAGES, bool SPLIT_A, class Epi, int CM = 1>
 cudaError_t launch_umma(const CUtensorMap& tmA, const BSet& bset, int M, int N, int nk, int k_splits, const Epi& epi,
-                        int num_sms, int* err, cudaStream_t st) {
+                        int num_sms, int* err, cudaStream_t st, const int* m_live = nullptr) {
   using Cfg = GemmCfg<BN, STAGES, SPLIT_A>;
   auto kern = umma_gemm_kernel<BN, STAGES, SPLIT_A, Epi, CM>;
   static int configured_device = -1;  // the attribute is set per device
@@ -138,7 +138,7 @@ cudaError_t launch_umma(const CUtensorMap& tmA, const BSet& bset, int M, int N, 
   if (grid <= 0) return cudaSuccess;
   if (CM == 1) {
     count_launch();
-    kern<<<grid, kGemmThreads, Cfg::kSmemBytes, st>>>(tmA, bset, M, N, nk, k_splits, epi, err);
+    kern<<<grid, kGemmThreads, Cfg::kSmemBytes, st>>>(tmA, bset, M, N, nk, k_splits, epi, err, m_live);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -154,7 +154,7 @@ cudaError_t launch_umma(const CUtensorMap& tmA, const BSet& bset, int M, int N, 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   count_launch();
-  return cudaLaunchKernelEx(&cfg, kern, tmA, bset, M, N, nk, k_splits, epi, err);
+  return cudaLaunchKernelEx(&cfg, kern, tmA, bset, M, N, nk, k_splits, epi, err, m_live);
 }
 
 }  // namespace
@@ -180,20 +180,23 @@ int choose_k_splits(int tiles, int nk, int num_sms) {
 }
 
 cudaError_t launch_gemm_proj(const CUtensorMap& tmA, const BSet& bset, int M, int N, int K, int k_splits, float* C,
-                             size_t slab, int ldc, int num_sms, int* err, cudaStream_t st) {
+                             size_t slab, int ldc, int num_sms, int* err, cudaStream_t st, const int* m_live) {
   EpiStoreF32<kProjBN> epi{C, slab, ldc, M, N};
-  return launch_umma<kProjBN, kProjStages, true>(tmA, bset, M, N, K / kGemmBK, k_splits, epi, num_sms, err, st);
+  return launch_umma<kProjBN, kProjStages, true>(tmA, bset, M, N, K / kGemmBK, k_splits, epi, num_sms, err, st,
+                                                 m_live);
 }
 
 cudaError_t launch_gemm_head(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int V, int K,
-                             const HeadEpilogueArgs& args, int num_sms, int* err, cudaStream_t st) {
+                             const HeadEpilogueArgs& args, int num_sms, int* err, cudaStream_t st,
+                             const int* m_live) {
   EpiHead epi{args, M, V};
   BSet b{};
   b.map[0] = tmB;
   b.n_begin[0] = 0;
   b.n_begin[1] = V;
   b.count = 1;
-  return launch_umma<kHeadBN, kHeadStages, false, EpiHead, 2>(tmA, b, M, V, K / kGemmBK, 1, epi, num_sms, err, st);
+  return launch_umma<kHeadBN, kHeadStages, false, EpiHead, 2>(tmA, b, M, V, K / kGemmBK, 1, epi, num_sms, err, st,
+                                                              m_live);
 }
 
 }  // namespace quail

@@ -19,8 +19,10 @@ using bf16 = __nv_bfloat16;
 // multiples of 256): partial tiles of k-split s go to C + s * slab
 // ([M, ldc] fp32 each); the consumer sums the k_splits slabs.
 struct BSet;
+// m_live (optional): device count of the rows present (<= M); M tiles past it are skipped.
 cudaError_t launch_gemm_proj(const CUtensorMap& tmA, const BSet& bset, int M, int N, int K, int k_splits, float* C,
-                             size_t slab, int ldc, int num_sms, int* err, cudaStream_t st);
+                             size_t slab, int ldc, int num_sms, int* err, cudaStream_t st,
+                             const int* m_live = nullptr);
 // k-splits that balance `tiles` work tiles of nk k-blocks over num_sms SMs.
 int choose_k_splits(int tiles, int nk, int num_sms);
 
@@ -46,7 +48,8 @@ constexpr int kHeadBN = 256;
 // 64 columns x kHeadBBoxRows rows (half a band, one per CTA, multicast to both).
 constexpr int kHeadBBoxRows = kHeadBN / 2;
 cudaError_t launch_gemm_head(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int V, int K,
-                             const HeadEpilogueArgs& args, int num_sms, int* err, cudaStream_t st);
+                             const HeadEpilogueArgs& args, int num_sms, int* err, cudaStream_t st,
+                             const int* m_live = nullptr);
 
 // ------------------------------------------------------------ layer kernels (layer.cu)
 // y = RMSNorm(E[tokens[r]]) * gain as a two-term bf16 split:
@@ -68,6 +71,9 @@ struct RowMap {
   const int* n_slots_dev; // nullable: rows of slots >= *n_slots_dev are skipped
   const int* row_nodes;   // nullable: query row e of every slot -> node row (identity when null)
   int slot_stride;        // node rows of slot s start at s * slot_stride (0: shared by all slots)
+  const int* slot_base;   // nullable: slot s's rows are nodes slot_base[s] + e for e < slot_rows[s]
+  const int* slot_rows;   //   (rows past slot_rows[s] are padding: they read its last row and are skipped
+                          //   where whole row tiles are padding)
 };
 
 // z = RMSNorm(sum_s h_part[s][r] + E[node_token[node(r)]]) * g_f over the
@@ -159,16 +165,26 @@ struct ShortlistTables {
 // sel[doc * B + b]: the B groups of highest prefix log score (ties: lower group).
 cudaError_t launch_shortlist_select(const float* prefix_logscore, int num_docs, int G, int B, int* sel,
                                     cudaStream_t st);
-// Row tables of the second pass: block (doc, b) holds group sel[doc * B + b]'s
-// rows, padded to max_rows with copies of the root row (row_eval -1).
-cudaError_t launch_shortlist_expand(const ShortlistTables& T, const int* sel, int num_docs, int B,
+// Node tables of the second pass in that compact numbering (rows count..R-1
+// are root copies with no parent), and padded_of[c] = doc * Bq + the row's
+// index within its document (the attention's padded output row).
+cudaError_t launch_shortlist_expand(const ShortlistTables& T, const int* sel, int num_docs, int B, int Bq, int R,
+                                    const int* block_base, const int* doc_base, const int* count,
                                     const int* eval_token, const int* eval_depth, int* row_token, int* row_depth,
-                                    int* row_parent, int* row_eval, cudaStream_t st);
+                                    int* row_parent, int* padded_of, cudaStream_t st);
+// The kept groups' rows numbered compactly, document by document and group by
+// group: block_base[doc * B + b] (first row of that group's block), count,
+// doc_base / doc_rows (each document's first row and row count).
+cudaError_t launch_shortlist_scan(const ShortlistTables& T, const int* sel, int num_docs, int B, int* block_base,
+                                  int* doc_base, int* doc_rows, int* count, cudaStream_t st);
+// dst[c] = src[padded_of[c]] for c < *count (rows of row_bytes, a multiple of 16).
+cudaError_t launch_gather_rows(const void* src, const int* padded_of, const int* count, int max_rows,
+                               size_t row_bytes, void* dst, cudaStream_t st);
 // clp[blk * max_children + t] = z32[row] . W_lm[tok] - lse[row] (fp32) for
-// every child t of the block's group.
+// every child t of the block's group; row = block_base[blk] + the child's row.
 cudaError_t launch_shortlist_child_logprob(const ShortlistTables& T, const int* sel, int num_docs, int B,
-                                           const float* z32, const bf16* lm_head, int d, const float* lse,
-                                           float* clp, cudaStream_t st);
+                                           const int* block_base, const float* z32, const bf16* lm_head, int d,
+                                           const float* lse, float* clp, cudaStream_t st);
 // Label scores of the kept groups' labels (-inf / 0 elsewhere), softmax over
 // the kept labels, argmax (lowest label index of the maximum).
 cudaError_t launch_shortlist_label_score(const ShortlistTables& T, const int* sel, int num_docs, int B, int M,

@@ -99,39 +99,12 @@ __global__ void __launch_bounds__(kSelectThreads) shortlist_select_kernel(const 
   }
 }
 
-// Block per (document, kept group): that group's rows, then root-row padding.
-__global__ void shortlist_expand_kernel(ShortlistTables T, const int* __restrict__ sel,
-                                        const int* __restrict__ eval_token, const int* __restrict__ eval_depth,
-                                        int* __restrict__ row_token, int* __restrict__ row_depth,
-                                        int* __restrict__ row_parent, int* __restrict__ row_eval) {
-  const int blk = blockIdx.x;
-  const int g = sel[blk];
-  const int r0 = blk * T.max_rows;
-  const int off = T.row_off[g];
-  const int n = T.row_off[g + 1] - off;
-  for (int j = threadIdx.x; j < T.max_rows; j += blockDim.x) {
-    const int r = r0 + j;
-    if (j < n) {
-      const int e = T.row_eval[off + j];
-      const int p = T.row_parent[off + j];
-      row_token[r] = eval_token[e];
-      row_depth[r] = eval_depth[e];
-      row_parent[r] = p >= 0 ? r0 + p : -1;
-      row_eval[r] = e;
-    } else {
-      row_token[r] = eval_token[0];
-      row_depth[r] = eval_depth[0];
-      row_parent[r] = -1;
-      row_eval[r] = -1;
-    }
-  }
-}
-
 // Warp per (block, child slot): the child token's logit from the unrounded
 // hidden state in fp32 (z32 . W_lm[tok]), minus the row's log-sum-exp.
 __global__ void shortlist_child_logprob_kernel(ShortlistTables T, const int* __restrict__ sel, int n_blocks,
-                                               const float* __restrict__ z32, const bf16* __restrict__ lm_head, int d,
-                                               const float* __restrict__ lse, float* __restrict__ clp) {
+                                               const int* __restrict__ block_base, const float* __restrict__ z32,
+                                               const bf16* __restrict__ lm_head, int d, const float* __restrict__ lse,
+                                               float* __restrict__ clp) {
   const int lane = threadIdx.x & 31;
   const long long total = static_cast<long long>(n_blocks) * T.max_children;
   for (long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < total;
@@ -141,7 +114,7 @@ __global__ void shortlist_child_logprob_kernel(ShortlistTables T, const int* __r
     const int g = sel[blk];
     const int c0 = T.child_off[g];
     if (t >= T.child_off[g + 1] - c0) continue;
-    const int r = blk * T.max_rows + T.child_row[c0 + t];
+    const int r = block_base[blk] + T.child_row[c0 + t];
     const int tok = T.child_tok[c0 + t];
     const float4* zr = reinterpret_cast<const float4*>(z32 + static_cast<size_t>(r) * d);
     const uint2* wr = reinterpret_cast<const uint2*>(lm_head + static_cast<size_t>(tok) * d);
@@ -160,6 +133,90 @@ __global__ void shortlist_child_logprob_kernel(ShortlistTables T, const int* __r
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) clp[w] = acc - lse[r];
   }
+}
+
+// One CTA: exclusive scan of the kept groups' row counts in (document, group)
+// order, each document's first row and row count, and the total.
+__global__ void __launch_bounds__(1024) shortlist_scan_kernel(ShortlistTables T, const int* __restrict__ sel,
+                                                              int num_docs, int B, int* __restrict__ block_base,
+                                                              int* __restrict__ doc_base, int* __restrict__ doc_rows,
+                                                              int* __restrict__ count) {
+  __shared__ int s_part[1024];
+  __shared__ int s_total;
+  const int n_blocks = num_docs * B;
+  const int per = (n_blocks + blockDim.x - 1) / blockDim.x;
+  const int b0 = min(n_blocks, static_cast<int>(threadIdx.x) * per), b1 = min(n_blocks, b0 + per);
+  int sum = 0;
+  for (int b = b0; b < b1; ++b) sum += T.row_off[sel[b] + 1] - T.row_off[sel[b]];
+  s_part[threadIdx.x] = sum;
+  __syncthreads();
+  if (threadIdx.x == 0) {  // exclusive scan of the per-thread sums
+    int run = 0;
+    for (int i = 0; i < static_cast<int>(blockDim.x); ++i) {
+      const int v = s_part[i];
+      s_part[i] = run;
+      run += v;
+    }
+    s_total = run;
+    *count = run;
+  }
+  __syncthreads();
+  int base = s_part[threadIdx.x];
+  for (int b = b0; b < b1; ++b) {
+    block_base[b] = base;
+    base += T.row_off[sel[b] + 1] - T.row_off[sel[b]];
+  }
+  __syncthreads();
+  for (int d = threadIdx.x; d < num_docs; d += blockDim.x) {
+    const int first = block_base[d * B];
+    const int end = d + 1 < num_docs ? block_base[(d + 1) * B] : s_total;
+    doc_base[d] = first;
+    doc_rows[d] = end - first;
+  }
+}
+
+// Block per (document, kept group): that group's rows at their compact
+// numbers; one more block fills rows count..R-1 with root copies.
+__global__ void shortlist_expand_kernel(ShortlistTables T, const int* __restrict__ sel, int B, int Bq, int R,
+                                        const int* __restrict__ block_base, const int* __restrict__ doc_base,
+                                        const int* __restrict__ count, const int* __restrict__ eval_token,
+                                        const int* __restrict__ eval_depth, int* __restrict__ row_token,
+                                        int* __restrict__ row_depth, int* __restrict__ row_parent,
+                                        int* __restrict__ padded_of) {
+  const int blk = blockIdx.x;
+  if (blk == static_cast<int>(gridDim.x) - 1) {
+    for (int c = *count + threadIdx.x; c < R; c += blockDim.x) {
+      row_token[c] = eval_token[0];
+      row_depth[c] = eval_depth[0];
+      row_parent[c] = -1;
+    }
+    return;
+  }
+  const int doc = blk / B;
+  const int g = sel[blk];
+  const int base = block_base[blk];
+  const int local0 = base - doc_base[doc];  // first row of this group within its document
+  const int off = T.row_off[g];
+  const int n = T.row_off[g + 1] - off;
+  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    const int e = T.row_eval[off + j];
+    const int p = T.row_parent[off + j];
+    const int c = base + j;
+    row_token[c] = eval_token[e];
+    row_depth[c] = eval_depth[e];
+    row_parent[c] = p >= 0 ? base + p : -1;
+    padded_of[c] = doc * Bq + local0 + j;
+  }
+}
+
+// Block per compact row c < *count: 16-byte copies of row padded_of[c].
+__global__ void gather_rows_kernel(const uint4* __restrict__ src, const int* __restrict__ padded_of,
+                                   const int* __restrict__ count, int vec_per_row, uint4* __restrict__ dst) {
+  const int c = blockIdx.x;
+  if (c >= *count) return;
+  const uint4* s = src + static_cast<size_t>(padded_of[c]) * vec_per_row;
+  uint4* d = dst + static_cast<size_t>(c) * vec_per_row;
+  for (int i = threadIdx.x; i < vec_per_row; i += blockDim.x) d[i] = s[i];
 }
 
 // CTA per document: clear the row, score the kept groups' labels (warp per
@@ -241,25 +298,46 @@ cudaError_t launch_shortlist_select(const float* prefix_logscore, int num_docs, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_shortlist_expand(const ShortlistTables& T, const int* sel, int num_docs, int B,
-                                    const int* eval_token, const int* eval_depth, int* row_token, int* row_depth,
-                                    int* row_parent, int* row_eval, cudaStream_t st) {
+cudaError_t launch_shortlist_scan(const ShortlistTables& T, const int* sel, int num_docs, int B, int* block_base,
+                                  int* doc_base, int* doc_rows, int* count, cudaStream_t st) {
   if (num_docs <= 0) return cudaSuccess;
   count_launch();
-  shortlist_expand_kernel<<<num_docs * B, 128, 0, st>>>(T, sel, eval_token, eval_depth, row_token, row_depth,
-                                                        row_parent, row_eval);
+  shortlist_scan_kernel<<<1, 1024, 0, st>>>(T, sel, num_docs, B, block_base, doc_base, doc_rows, count);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_shortlist_expand(const ShortlistTables& T, const int* sel, int num_docs, int B, int Bq, int R,
+                                    const int* block_base, const int* doc_base, const int* count,
+                                    const int* eval_token, const int* eval_depth, int* row_token, int* row_depth,
+                                    int* row_parent, int* padded_of, cudaStream_t st) {
+  if (num_docs <= 0) return cudaSuccess;
+  count_launch();
+  shortlist_expand_kernel<<<num_docs * B + 1, 128, 0, st>>>(T, sel, B, Bq, R, block_base, doc_base, count,
+                                                            eval_token, eval_depth, row_token, row_depth, row_parent,
+                                                            padded_of);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const void* src, const int* padded_of, const int* count, int max_rows,
+                               size_t row_bytes, void* dst, cudaStream_t st) {
+  if (max_rows <= 0) return cudaSuccess;
+  if (row_bytes % 16 != 0) return cudaErrorInvalidValue;
+  count_launch();
+  gather_rows_kernel<<<max_rows, 256, 0, st>>>(static_cast<const uint4*>(src), padded_of, count,
+                                               static_cast<int>(row_bytes / 16), static_cast<uint4*>(dst));
   return cudaGetLastError();
 }
 
 cudaError_t launch_shortlist_child_logprob(const ShortlistTables& T, const int* sel, int num_docs, int B,
-                                           const float* z32, const bf16* lm_head, int d, const float* lse,
-                                           float* clp, cudaStream_t st) {
+                                           const int* block_base, const float* z32, const bf16* lm_head, int d,
+                                           const float* lse, float* clp, cudaStream_t st) {
   if (num_docs <= 0 || T.max_children <= 0) return cudaSuccess;
   if (d % 4 != 0) return cudaErrorInvalidValue;
   const long long warps = static_cast<long long>(num_docs) * B * T.max_children;
   const int blocks = static_cast<int>(std::min<long long>((warps + 7) / 8, 1 << 16));
   count_launch();
-  shortlist_child_logprob_kernel<<<blocks, 256, 0, st>>>(T, sel, num_docs * B, z32, lm_head, d, lse, clp);
+  shortlist_child_logprob_kernel<<<blocks, 256, 0, st>>>(T, sel, num_docs * B, block_base, z32, lm_head, d, lse,
+                                                         clp);
   return cudaGetLastError();
 }
 

@@ -105,10 +105,13 @@ struct BPrefetch {
 // is this thread's accumulator row, taddr the TMEM address of (row, column 0).
 // All 32 lanes of a warp must execute the same tcgen05.ld sequence.
 // nk = k-blocks of B's K extent (A has nk k-blocks, or 2*nk with SPLIT_A).
+// m_live (may be null): the rows actually present, written by an earlier
+// kernel; M is then the bound the grid and A's tensor map were sized for, and
+// M tiles past m_live are not computed.
 template <int BN, int STAGES, bool SPLIT_A, class Epi, int CM = 1>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ BSet bset, int M, int N,
-                     int nk, int k_splits, Epi epi, int* err) {
+                     int nk, int k_splits, Epi epi, int* err, const int* m_live) {
   static_assert(CM == 1 || (CM == 2 && !SPLIT_A && BN % 16 == 0), "pairs: plain A, B band split in two halves");
   using Cfg = GemmCfg<BN, STAGES, SPLIT_A>;
   constexpr uint32_t kBHalf = Cfg::kBBytes / CM;  // bytes of B each CTA of a pair loads
@@ -124,7 +127,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int m_tiles = (M + kGemmBM - 1) / kGemmBM;
+  const int M_eff = m_live != nullptr ? min(M, max(*m_live, 0)) : M;
+  const int m_tiles = (M_eff + kGemmBM - 1) / kGemmBM;
   const int m_tiles_s = (m_tiles + CM - 1) / CM * CM;  // scheduled M tiles: whole pairs
   const int n_tiles = (N + BN - 1) / BN;
   const int num_units = m_tiles_s * n_tiles * k_splits;
