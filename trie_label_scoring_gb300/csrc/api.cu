@@ -304,7 +304,7 @@ quail_status run_qkv(const quail_model_desc* m, const NodeTables& nt, const Buff
 quail_status run_prologue(const quail_model_desc* m, const NodeTables& nt, const Buffers& b, DeviceState* ds,
                           cudaStream_t st, const int* m_live = nullptr) {
   CUDA_TRY(launch_embed_rmsnorm(static_cast<const bf16*>(m->embed), nt.token, nt.nodes, m->hidden,
-                                static_cast<const bf16*>(m->in_norm), m->rms_eps, b.xhat, st));
+                                static_cast<const bf16*>(m->in_norm), m->rms_eps, b.xhat, st, m_live));
   return run_qkv(m, nt, b, ds, st, m_live);
 }
 
@@ -343,13 +343,14 @@ quail_status run_qkv(const quail_model_desc* m, const NodeTables& nt, const Buff
   }
   CUDA_TRY(launch_qk_head_norm(b.qkv_part, b.gp.ks_qkv, slab, b.qkv, nt.nodes, ldq, hq, hkv,
                                static_cast<const bf16*>(m->q_norm), static_cast<const bf16*>(m->k_norm), m->rms_eps,
-                               st));
+                               st, m_live));
   return QUAIL_OK;
 }
 
 // Attention (tree part, paged doc part, combine) for rows = slots x nq.
 quail_status run_attention(const quail_model_desc* m, const quail_paged_kv* kv, const NodeTables& nt, RowMap map,
-                           int slots, const Buffers& b, DeviceState* ds, cudaStream_t st) {
+                           int slots, const Buffers& b, DeviceState* ds, cudaStream_t st,
+                           const int* nodes_live = nullptr) {
   const int hq = m->n_q_heads, hkv = m->n_kv_heads;
   const AttnShape as = attn_shape(m, map.nq, slots, kv->max_doc_len, ds->num_sms);
   AttnArgs a{};
@@ -366,6 +367,7 @@ quail_status run_attention(const quail_model_desc* m, const quail_paged_kv* kv, 
   a.node_depth = nt.depth;
   a.node_parent = nt.parent;
   a.n_nodes = nt.nodes;
+  a.nodes_live = nodes_live;
   a.map = map;
   a.n_slots = slots;
   a.split_tokens = as.split_tokens;
@@ -1552,7 +1554,7 @@ quail_status quail_classify_trie_tree_shortlist(const quail_model_desc* model, c
   stage_mark(QUAIL_STAGE_ATTENTION, false, st);
   s = run_prologue(model, nt, b, ds, st, count);
   if (s != QUAIL_OK) return s;
-  s = run_attention(model, kv, nt, map, num_docs, b, ds, st);
+  s = run_attention(model, kv, nt, map, num_docs, b, ds, st, count);
   if (s != QUAIL_OK) return s;
   stage_mark(QUAIL_STAGE_ATTENTION, true, st);
   stage_mark(QUAIL_STAGE_WO_NORM, false, st);

@@ -57,6 +57,7 @@ __global__ void tree_part_kernel(AttnArgs a, RopeTable rt) {
   const int lane = threadIdx.x & 31;
   if (warp >= a.n_nodes * a.hq) return;
   const int node = warp / a.hq, h = warp % a.hq;
+  if (a.nodes_live != nullptr && node >= *a.nodes_live) return;
   const int G = a.hq / a.hkv, g = h / G;
   const float* qr = a.qkv + static_cast<size_t>(node) * a.ldq + h * 128;
   const float q0 = qr[lane], q1 = qr[lane + 32], q2 = qr[lane + 64], q3 = qr[lane + 96];

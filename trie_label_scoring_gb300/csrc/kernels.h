@@ -54,13 +54,15 @@ cudaError_t launch_gemm_head(const CUtensorMap& tmA, const CUtensorMap& tmB, int
 // ------------------------------------------------------------ layer kernels (layer.cu)
 // y = RMSNorm(E[tokens[r]]) * gain as a two-term bf16 split:
 // out[r, 0:d] = bf16(y), out[r, d:2d] = bf16(y - bf16(y)); rows = n
+// live (optional): device count of the rows present; rows past it are skipped.
 cudaError_t launch_embed_rmsnorm(const bf16* embed, const int* tokens, int n, int d, const bf16* gain, float eps,
-                                 bf16* out, cudaStream_t st);
+                                 bf16* out, cudaStream_t st, const int* live = nullptr);
 // qkv[r] = sum over the k_splits slabs of part (slab stride `slab`), then
 // per-head RMSNorm of the q heads [0, hq) with gq and k heads [hq, hq + hkv)
 // with gk; v heads copied. qkv and each slab are [rows, ld].
 cudaError_t launch_qk_head_norm(const float* part, int k_splits, size_t slab, float* qkv, int rows, int ld, int hq,
-                                int hkv, const bf16* gq, const bf16* gk, float eps, cudaStream_t st);
+                                int hkv, const bf16* gq, const bf16* gk, float eps, cudaStream_t st,
+                                const int* live = nullptr);
 
 // Maps an attention/output row to its trie node: slot = row / nq, e = row % nq,
 // node = slot_node ? slot_node[slot] : e.
@@ -205,6 +207,7 @@ struct AttnArgs {
   const int* node_depth;
   const int* node_parent;  // tree part
   int n_nodes;             // rows of qkv
+  const int* nodes_live;   // nullable: device count of the nodes present (tree part skips the rest)
   RowMap map;
   int n_slots;             // host bound on slots (documents)
   // split-KV decomposition

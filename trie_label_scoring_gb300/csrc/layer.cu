@@ -55,7 +55,9 @@ __device__ __forceinline__ uint32_t f2_to_bf16x2(float a, float b) {
 __global__ void __launch_bounds__(kNormThreads) embed_rmsnorm_kernel(const bf16* __restrict__ embed,
                                                                      const int* __restrict__ tokens, int d,
                                                                      const bf16* __restrict__ gain, float eps,
-                                                                     bf16* __restrict__ out) {
+                                                                     bf16* __restrict__ out,
+                                                                     const int* __restrict__ live) {
+  if (live != nullptr && static_cast<int>(blockIdx.x) >= *live) return;
   __shared__ float scratch[32];
   const int r = blockIdx.x;
   const uint2* x = reinterpret_cast<const uint2*>(embed + static_cast<size_t>(__ldg(tokens + r)) * d);
@@ -89,8 +91,9 @@ __global__ void __launch_bounds__(kNormThreads) embed_rmsnorm_kernel(const bf16*
 // per-head RMSNorm for q and k heads (v heads are only summed).
 __global__ void qk_head_norm_kernel(const float* __restrict__ part, int k_splits, size_t slab, float* qkv, int rows,
                                     int ld, int hq, int hkv, const bf16* __restrict__ gq,
-                                    const bf16* __restrict__ gk, float eps) {
+                                    const bf16* __restrict__ gk, float eps, const int* __restrict__ live) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (live != nullptr) rows = min(rows, *live);
   const int lane = threadIdx.x & 31;
   const int heads = hq + 2 * hkv;
   if (warp >= rows * heads) return;
@@ -545,21 +548,21 @@ __global__ void decode_select_kernel(DecodeTrie t, const float* __restrict__ z, 
 }  // namespace
 
 cudaError_t launch_embed_rmsnorm(const bf16* embed, const int* tokens, int n, int d, const bf16* gain, float eps,
-                                 bf16* out, cudaStream_t st) {
+                                 bf16* out, cudaStream_t st, const int* live) {
   if (n <= 0) return cudaSuccess;
   count_launch();
-  embed_rmsnorm_kernel<<<n, kNormThreads, 0, st>>>(embed, tokens, d, gain, eps, out);
+  embed_rmsnorm_kernel<<<n, kNormThreads, 0, st>>>(embed, tokens, d, gain, eps, out, live);
   return cudaGetLastError();
 }
 
 cudaError_t launch_qk_head_norm(const float* part, int k_splits, size_t slab, float* qkv, int rows, int ld, int hq,
-                                int hkv, const bf16* gq, const bf16* gk, float eps, cudaStream_t st) {
+                                int hkv, const bf16* gq, const bf16* gk, float eps, cudaStream_t st, const int* live) {
   const long warps = static_cast<long>(rows) * (hq + 2 * hkv);
   if (warps <= 0) return cudaSuccess;
   if (k_splits < 1 || k_splits > 8) return cudaErrorInvalidValue;  // the kernel sums at most 8 slabs
   const int blocks = static_cast<int>((warps * 32 + 255) / 256);
   count_launch();
-  qk_head_norm_kernel<<<blocks, 256, 0, st>>>(part, k_splits, slab, qkv, rows, ld, hq, hkv, gq, gk, eps);
+  qk_head_norm_kernel<<<blocks, 256, 0, st>>>(part, k_splits, slab, qkv, rows, ld, hq, hkv, gq, gk, eps, live);
   return cudaGetLastError();
 }
 

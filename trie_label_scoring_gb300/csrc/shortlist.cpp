@@ -111,8 +111,27 @@ quail_status quail_build_shortlist_host(const quail_trie* t, int32_t D, quail_sh
     for (int32_t u = c; u < c + t->subtree_size[c]; ++u)
       if (t->eval_index_of_node[u] >= 0) nodes.push_back(u);
     const int32_t rows = static_cast<int32_t>(nodes.size());
-    std::vector<int32_t> row_child_base(rows + 1, 0);
     for (int32_t j = 0; j < rows; ++j) local[nodes[j]] = j;
+    // every child of every row, numbered row by row ...
+    std::vector<int32_t> full_base(rows + 1, 0);
+    for (int32_t j = 0; j < rows; ++j) {
+      const int32_t e = t->eval_index_of_node[nodes[j]];
+      full_base[j + 1] = full_base[j] + (t->eval_child_offsets[e + 1] - t->eval_child_offsets[e]);
+    }
+    // ... of which the group keeps those its labels read: the scored child of
+    // each term, and all children of a prefix label's end row
+    std::vector<int32_t> keep(full_base[rows], -1);
+    for (const int32_t m : labels_of[g]) {
+      for (int32_t k = t->label_term_offsets[m]; k < t->label_term_offsets[m + 1]; ++k) {
+        const int32_t e = t->label_term_eval[k];
+        keep[full_base[local[t->eval_nodes[e]]] + (t->label_term_slot[k] - t->eval_child_offsets[e])] = 0;
+      }
+      const int32_t pe = t->label_prefix_eval[m];
+      if (pe >= 0) {
+        const int32_t j = local[t->eval_nodes[pe]];
+        for (int32_t i = full_base[j]; i < full_base[j + 1]; ++i) keep[i] = 0;
+      }
+    }
     for (int32_t j = 0; j < rows; ++j) {
       const int32_t u = nodes[j];
       const int32_t e = t->eval_index_of_node[u];
@@ -123,26 +142,25 @@ quail_status quail_build_shortlist_host(const quail_trie* t, int32_t D, quail_sh
       }
       sl->row_eval.push_back(e);
       sl->row_parent.push_back(p >= 0 ? local[p] : -1);
-      row_child_base[j] = static_cast<int32_t>(sl->child_tok.size()) - sl->child_off.back();
-      for (int32_t k = t->eval_child_offsets[e]; k < t->eval_child_offsets[e + 1]; ++k) {
+      for (int32_t i = full_base[j]; i < full_base[j + 1]; ++i) {
+        if (keep[i] < 0) continue;
+        keep[i] = static_cast<int32_t>(sl->child_tok.size()) - sl->child_off.back();  // index in the group's list
         sl->child_row.push_back(j);
-        sl->child_tok.push_back(t->eval_child_tokens[k]);
+        sl->child_tok.push_back(t->eval_child_tokens[t->eval_child_offsets[e] + (i - full_base[j])]);
       }
     }
-    row_child_base[rows] = static_cast<int32_t>(sl->child_tok.size()) - sl->child_off.back();
     for (const int32_t m : labels_of[g]) {
       sl->lab_id.push_back(m);
       for (int32_t k = t->label_term_offsets[m]; k < t->label_term_offsets[m + 1]; ++k) {
         const int32_t e = t->label_term_eval[k];
-        const int32_t j = local[t->eval_nodes[e]];
-        sl->term_t.push_back(row_child_base[j] + (t->label_term_slot[k] - t->eval_child_offsets[e]));
+        sl->term_t.push_back(keep[full_base[local[t->eval_nodes[e]]] + (t->label_term_slot[k] - t->eval_child_offsets[e])]);
       }
       sl->term_off.push_back(static_cast<int32_t>(sl->term_t.size()));
       const int32_t pe = t->label_prefix_eval[m];
-      if (pe >= 0) {
+      if (pe >= 0) {  // all of the end row's children are kept, in order
         const int32_t j = local[t->eval_nodes[pe]];
-        sl->pref_t0.push_back(row_child_base[j]);
-        sl->pref_t1.push_back(row_child_base[j + 1]);
+        sl->pref_t0.push_back(keep[full_base[j]]);
+        sl->pref_t1.push_back(keep[full_base[j + 1] - 1] + 1);
       } else {
         sl->pref_t0.push_back(0);
         sl->pref_t1.push_back(0);

@@ -219,8 +219,17 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ src, const int* __r
   for (int i = threadIdx.x; i < vec_per_row; i += blockDim.x) d[i] = s[i];
 }
 
-// CTA per document: clear the row, score the kept groups' labels (warp per
-// label), then softmax and argmax over the kept labels.
+// Every label's score -inf and probability 0 (the kept ones are overwritten next).
+__global__ void shortlist_clear_kernel(float* __restrict__ logscore, float* __restrict__ prob, size_t n) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    logscore[i] = -INFINITY;
+    prob[i] = 0.f;
+  }
+}
+
+// CTA per document: score the kept groups' labels (warp per label), then
+// softmax and argmax over the kept labels.
 __global__ void __launch_bounds__(kScoreThreads) shortlist_label_score_kernel(
     ShortlistTables T, const int* __restrict__ sel, int B, int M, const float* __restrict__ clp,
     float* __restrict__ logscore, float* __restrict__ prob, int* __restrict__ argmax) {
@@ -230,11 +239,6 @@ __global__ void __launch_bounds__(kScoreThreads) shortlist_label_score_kernel(
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   float* ls = logscore + static_cast<size_t>(doc) * M;
   float* pr = prob + static_cast<size_t>(doc) * M;
-  for (int m = threadIdx.x; m < M; m += blockDim.x) {
-    ls[m] = -INFINITY;
-    pr[m] = 0.f;
-  }
-  __syncthreads();
   for (int b = 0; b < B; ++b) {
     const int blk = doc * B + b;
     const int g = sel[blk];
@@ -345,6 +349,11 @@ cudaError_t launch_shortlist_label_score(const ShortlistTables& T, const int* se
                                          const float* clp, float* logscore, float* prob, int* argmax,
                                          cudaStream_t st) {
   if (num_docs <= 0) return cudaSuccess;
+  const size_t n = static_cast<size_t>(num_docs) * M;
+  count_launch();
+  shortlist_clear_kernel<<<static_cast<int>(std::min<size_t>((n + 255) / 256, 4096)), 256, 0, st>>>(logscore, prob, n);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   count_launch();
   shortlist_label_score_kernel<<<num_docs, kScoreThreads, 0, st>>>(T, sel, B, M, clp, logscore, prob, argmax);
   return cudaGetLastError();

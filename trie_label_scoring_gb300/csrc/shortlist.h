@@ -29,7 +29,8 @@ struct quail_shortlist {
   // then the evaluated nodes of its subtree (node order). Row entries hold the
   // trie's evaluated-node index and the row index of the parent (-1: root).
   std::vector<int32_t> row_off, row_eval, row_parent;
-  // Group g's child tokens, row by row: [child_off[g], child_off[g+1]).
+  // Group g's child tokens that its labels read (each term's scored child, and
+  // every child of a prefix label's end row), row by row: [child_off[g], child_off[g+1]).
   std::vector<int32_t> child_off, child_row, child_tok;
   // Group g's labels (ascending label index); each label's terms as indices
   // into its group's child list (CSR term_off over all groups' labels in
