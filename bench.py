@@ -119,11 +119,11 @@ def head_kernel_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str, rows: int):
-    """Per-launch DRAM bytes of the head GEMM from the committed ncu summary,
-    scaled to `rows` if the capture used fewer rows; None once the kernel
-    source has changed since the capture."""
-    p = os.path.join(ROOT, "profiles", "lm_head_gemm_traffic.json")
+def recorded_traffic(workload: str, rows: int, record: str = "lm_head_gemm_traffic.json"):
+    """Per-launch DRAM bytes of a GEMM from a committed ncu summary under
+    profiles/, scaled to `rows` if the capture used fewer rows; None once the
+    GEMM sources have changed since the capture or for another workload."""
+    p = os.path.join(ROOT, "profiles", record)
     if not os.path.exists(p):
         return None
     with open(p) as f:
@@ -745,7 +745,8 @@ def run_ml(args, world, rank, local):
         achieved = gu_flops / t_gu / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                     "frac": achieved / peaks["bf16_tflops"], "peak_kind": f"bf16 burst ({peaks['source']})"}
-    roofline.update({"traffic": None, "kernel": "umma_gemm_kernel<EpiStoreF32> (gate|up, split A)",
+    roofline.update({"traffic": recorded_traffic(mw.name, rows, "gate_up_gemm_traffic.json"),
+                     "kernel": "umma_gemm_kernel<EpiStoreF32> (gate|up, split A)",
                      "gate_up_ms": span_ms["gate_up"], "algorithmic_bytes": gu_bytes,
                      "algorithmic_flops": gu_flops,
                      "issued_tflops": 2 * gu_flops / t_gu / 1e12,
@@ -952,7 +953,8 @@ def run_shortlist(args, world, rank, local):
     flops = 2.0 * d * V * real_rows
     achieved = flops / (stages_ms["head"] / 1e3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                "frac": achieved / peaks["bf16_tflops"],
+                "traffic": recorded_traffic(sw.name, real_rows, "lm_head_gemm_shortlist_traffic.json"),
                 "kernel": "umma_gemm_kernel<EpiHead> (second pass)", "head_ms": stages_ms["head"],
                 "real_rows": real_rows, "padded_rows": pad_rows,
                 "peak_kind": f"bf16 burst ({peaks['source']})",
