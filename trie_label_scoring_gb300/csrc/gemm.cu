@@ -33,11 +33,12 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // binary search per tile finds the first candidate and a cursor walks the
 // 32-column chunks in order.
 struct EpiHead {
+  static constexpr uint32_t kScratchBytes = 0;
   HeadEpilogueArgs a;
   int M;
   int V;
-  __device__ __forceinline__ void operator()(int m_blk, int n_blk, int /*ks*/, int lane_row,
-                                             uint32_t taddr) const {
+  __device__ __forceinline__ void operator()(int m_blk, int n_blk, int /*ks*/, int lane_row, uint32_t taddr,
+                                             float* /*warp_scratch*/) const {
     const int row = m_blk * kGemmBM + lane_row;
     const int lane = threadIdx.x & 31;
     const bool valid = row < M;
@@ -121,13 +122,15 @@ template <int BN, int STAGES, bool SPLIT_A, class Epi, int CM = 1>
 cudaError_t launch_umma(const CUtensorMap& tmA, const BSet& bset, int M, int N, int nk, int k_splits, const Epi& epi,
                         int num_sms, int* err, cudaStream_t st, const int* m_live = nullptr) {
   using Cfg = GemmCfg<BN, STAGES, SPLIT_A>;
+  constexpr size_t smem = Cfg::kSmemBytes + Epi::kScratchBytes;
+  static_assert(smem <= 232448, "shared memory per CTA");
   auto kern = umma_gemm_kernel<BN, STAGES, SPLIT_A, Epi, CM>;
   static int configured_device = -1;  // the attribute is set per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(Cfg::kSmemBytes));
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
@@ -138,13 +141,13 @@ cudaError_t launch_umma(const CUtensorMap& tmA, const BSet& bset, int M, int N, 
   if (grid <= 0) return cudaSuccess;
   if (CM == 1) {
     count_launch();
-    kern<<<grid, kGemmThreads, Cfg::kSmemBytes, st>>>(tmA, bset, M, N, nk, k_splits, epi, err, m_live);
+    kern<<<grid, kGemmThreads, smem, st>>>(tmA, bset, M, N, nk, k_splits, epi, err, m_live);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
-  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;

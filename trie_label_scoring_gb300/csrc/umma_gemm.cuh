@@ -100,10 +100,12 @@ struct BPrefetch {
 };
 
 // Epi must provide:
-//   __device__ void operator()(int m_blk, int n_blk, int ks, int lane_row, uint32_t taddr) const;
+//   static constexpr uint32_t kScratchBytes;   // shared memory it needs (a multiple of 64; 0 for none)
+//   __device__ void operator()(int m_blk, int n_blk, int ks, int lane_row, uint32_t taddr, float* warp_scratch) const;
 // called by each of the 128 epilogue threads for every unit; lane_row in [0,128)
-// is this thread's accumulator row, taddr the TMEM address of (row, column 0).
-// All 32 lanes of a warp must execute the same tcgen05.ld sequence.
+// is this thread's accumulator row, taddr the TMEM address of (row, column 0),
+// warp_scratch this warp's quarter of the scratch. All 32 lanes of a warp
+// must execute the same tcgen05.ld sequence.
 // nk = k-blocks of B's K extent (A has nk k-blocks, or 2*nk with SPLIT_A).
 // m_live (may be null): the rows actually present, written by an earlier
 // kernel; M is then the bound the grid and A's tensor map were sized for, and
@@ -117,7 +119,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   constexpr uint32_t kBHalf = Cfg::kBBytes / CM;  // bytes of B each CTA of a pair loads
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(base + STAGES * Cfg::kStageBytes);
+  // the epilogue's scratch (Epi::kScratchBytes) follows the ring, then the barriers
+  uint8_t* epi_scratch = base + STAGES * Cfg::kStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(epi_scratch + Epi::kScratchBytes);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;  // [2]
   uint64_t* tempty = tfull + 2;      // [2]
@@ -291,7 +295,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const GemmUnit g = gemm_unit(u, m_tiles_s, n_tiles, k_splits, nk);
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      epi(g.m_blk, g.n_blk, g.ks, lane_row, taddr);
+      epi(g.m_blk, g.n_blk, g.ks, lane_row, taddr,
+          reinterpret_cast<float*>(epi_scratch) + quarter * (Epi::kScratchBytes / 16));
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
       acc ^= 1;
@@ -316,33 +321,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 // fp32 store of the partial tile of k-split ks:
 //   C[ks * slab + row * ldc + col] = acc   (row < M, col < N)
+// Each warp passes its 32 rows x 32 columns through a padded shared-memory
+// block (stride 33: conflict-free both ways), so that every global store
+// instruction writes one row's 32 consecutive floats (128 bytes).
 template <int BN>
 struct EpiStoreF32 {
+  static constexpr uint32_t kScratchBytes = 4 * 32 * 33 * 4;
   float* C;
   size_t slab;
   int ldc;
   int M;
   int N;
-  __device__ __forceinline__ void operator()(int m_blk, int n_blk, int ks, int lane_row, uint32_t taddr) const {
-    const int row = m_blk * kGemmBM + lane_row;
+  __device__ __forceinline__ void operator()(int m_blk, int n_blk, int ks, int lane_row, uint32_t taddr,
+                                             float* ws) const {
+    const int lane = threadIdx.x & 31;
+    const int row0 = m_blk * kGemmBM + lane_row - lane;  // this warp's first row
     const int n0 = n_blk * BN;
-    float* out = C + ks * slab + static_cast<size_t>(row) * ldc;
+    float* out = C + ks * slab;
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       float v[32];
       tmem_ld_32cols(taddr + c * 32, v);
-      if (row < M) {
-        const int col0 = n0 + c * 32;
-        if (col0 + 32 <= N && (ldc & 3) == 0) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(out + col0 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (col0 + i < N) out[col0 + i] = v[i];
-        }
+      for (int i = 0; i < 32; ++i) ws[lane * 33 + i] = v[i];
+      __syncwarp();
+      const int col = n0 + c * 32 + lane;
+      const int rows = min(32, M - row0);
+      if (col < N) {
+#pragma unroll 4
+        for (int j = 0; j < rows; ++j) out[static_cast<size_t>(row0 + j) * ldc + col] = ws[j * 33 + lane];
       }
+      __syncwarp();
     }
   }
 };
