@@ -1521,8 +1521,25 @@ quail_status quail_classify_trie_tree_shortlist(const quail_model_desc* model, c
 
   // prefix pass (every group's prefix, every document), selection, row layout
   stage_mark(QUAIL_STAGE_PROLOGUE, false, st);
-  s = trie_tree_pass(model, kv, sl->prefix_trie, img1, num_docs, x.b1, ds, st, x.ls1, x.prob1, x.am1, false);
-  if (s != QUAIL_OK) return s;
+  const int a1 = sl->prefix_trie->n_eval();
+  if (sl->cut_depth == 1 && a1 == 1) {
+    // One-token prefixes: S(p) = logit(p) - LSE with one LSE per document, so
+    // the ranking is that of the G logits; the prefix pass is the root row and
+    // the G prefix tokens' logits (the root's children, in group order).
+    const NodeTables nt1{img1->eval_token, img1->eval_depth, img1->eval_parent, a1};
+    const RowMap map1{a1, nullptr, nullptr, nullptr};
+    s = run_prologue(model, nt1, x.b1, ds, st);
+    if (s != QUAIL_OK) return s;
+    s = run_attention(model, kv, nt1, map1, num_docs, x.b1, ds, st);
+    if (s != QUAIL_OK) return s;
+    s = run_wo_norm(model, nt1, map1, num_docs, x.b1, ds, st);
+    if (s != QUAIL_OK) return s;
+    CUDA_TRY(launch_restricted_logits(x.b1.z_f32, static_cast<const bf16*>(model->lm_head), img1->eval_child_tokens,
+                                      G, num_docs, d, x.ls1, st));
+  } else {
+    s = trie_tree_pass(model, kv, sl->prefix_trie, img1, num_docs, x.b1, ds, st, x.ls1, x.prob1, x.am1, false);
+    if (s != QUAIL_OK) return s;
+  }
   CUDA_TRY(launch_shortlist_select(x.ls1, num_docs, G, B, x.sel, st));
   const Buffers& b = x.b2;
   int* row_token = b.small;

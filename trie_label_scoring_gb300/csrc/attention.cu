@@ -50,21 +50,45 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
 }
 
 // ------------------------------------------------------------------ tree part
-// Warp per (node, q head): online softmax over the node's ancestors and itself
-// with relative RoPE; fp32 q, k, v straight from the projection.
+// Warp per (node, KV head, group of up to kTreeHeads query heads): online
+// softmax over the node's ancestors and itself with relative RoPE; fp32 q, k,
+// v straight from the projection. Each ancestor's k and v row and its
+// rotation are loaded and computed once for the query heads that share them.
+constexpr int kTreeHeads = 4;
+
 __global__ void tree_part_kernel(AttnArgs a, RopeTable rt) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (warp >= a.n_nodes * a.hq) return;
-  const int node = warp / a.hq, h = warp % a.hq;
+  const int G = a.hq / a.hkv;
+  const int chunks = (G + kTreeHeads - 1) / kTreeHeads;
+  const int per_node = a.hkv * chunks;
+  if (warp >= a.n_nodes * per_node) return;
+  const int node = warp / per_node, rem = warp - node * per_node;
+  const int g = rem / chunks, ch = rem - g * chunks;
   if (a.nodes_live != nullptr && node >= *a.nodes_live) return;
-  const int G = a.hq / a.hkv, g = h / G;
-  const float* qr = a.qkv + static_cast<size_t>(node) * a.ldq + h * 128;
-  const float q0 = qr[lane], q1 = qr[lane + 32], q2 = qr[lane + 64], q3 = qr[lane + 96];
+  const int h0 = g * G + ch * kTreeHeads;
+  const int nh = min(kTreeHeads, G - ch * kTreeHeads);
+  float q[kTreeHeads][4];
+#pragma unroll
+  for (int i = 0; i < kTreeHeads; ++i) {
+    if (i < nh) {
+      const float* qr = a.qkv + static_cast<size_t>(node) * a.ldq + (h0 + i) * 128;
+      q[i][0] = qr[lane];
+      q[i][1] = qr[lane + 32];
+      q[i][2] = qr[lane + 64];
+      q[i][3] = qr[lane + 96];
+    }
+  }
   const float2 w0 = rt.w[lane], w1 = rt.w[lane + 32];
   const float scale = kAttnLog2e * 0.08838834764831845f;  // log2(e) / sqrt(128)
   const int dnode = a.node_depth[node];
-  float m = -INFINITY, l = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+  float m[kTreeHeads], l[kTreeHeads], o[kTreeHeads][4];
+#pragma unroll
+  for (int i = 0; i < kTreeHeads; ++i) {
+    m[i] = -INFINITY;
+    l[i] = 0.f;
+    o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  }
   int anc = node;
   for (int guard = 0; anc >= 0 && guard < 4096; ++guard) {
     const float* kr = a.qkv + static_cast<size_t>(anc) * a.ldq + (a.hq + g) * 128;
@@ -74,27 +98,39 @@ __global__ void tree_part_kernel(AttnArgs a, RopeTable rt) {
     sincosf(delta * w0.x, &s0, &c0);
     sincosf(delta * w1.x, &s1, &c1);
     const float k0 = kr[lane], k1 = kr[lane + 32], k2 = kr[lane + 64], k3 = kr[lane + 96];
-    float dot = q0 * (k0 * c0 - k2 * s0) + q2 * (k2 * c0 + k0 * s0) + q1 * (k1 * c1 - k3 * s1) +
-                q3 * (k3 * c1 + k1 * s1);
+    const float v0 = vr[lane], v1 = vr[lane + 32], v2 = vr[lane + 64], v3 = vr[lane + 96];
+    const float r0 = k0 * c0 - k2 * s0, r2 = k2 * c0 + k0 * s0, r1 = k1 * c1 - k3 * s1, r3 = k3 * c1 + k1 * s1;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-    const float sc = dot * scale;
-    const float nm = fmaxf(m, sc);
-    const float alpha = exp2f(m - nm), p = exp2f(sc - nm);
-    l = l * alpha + p;
-    o0 = o0 * alpha + p * vr[lane];
-    o1 = o1 * alpha + p * vr[lane + 32];
-    o2 = o2 * alpha + p * vr[lane + 64];
-    o3 = o3 * alpha + p * vr[lane + 96];
-    m = nm;
+    for (int i = 0; i < kTreeHeads; ++i) {
+      if (i < nh) {
+        float dot = q[i][0] * r0 + q[i][2] * r2 + q[i][1] * r1 + q[i][3] * r3;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+        const float sc = dot * scale;
+        const float nm = fmaxf(m[i], sc);
+        const float alpha = exp2f(m[i] - nm), p = exp2f(sc - nm);
+        l[i] = l[i] * alpha + p;
+        o[i][0] = o[i][0] * alpha + p * v0;
+        o[i][1] = o[i][1] * alpha + p * v1;
+        o[i][2] = o[i][2] * alpha + p * v2;
+        o[i][3] = o[i][3] * alpha + p * v3;
+        m[i] = nm;
+      }
+    }
     anc = a.node_parent[anc];
   }
-  float* to = a.tree_o + (static_cast<size_t>(node) * a.hq + h) * 128;
-  to[lane] = o0;
-  to[lane + 32] = o1;
-  to[lane + 64] = o2;
-  to[lane + 96] = o3;
-  if (lane == 0) a.tree_ml[static_cast<size_t>(node) * a.hq + h] = make_float2(m, l);
+#pragma unroll
+  for (int i = 0; i < kTreeHeads; ++i) {
+    if (i < nh) {
+      const int h = h0 + i;
+      float* to = a.tree_o + (static_cast<size_t>(node) * a.hq + h) * 128;
+      to[lane] = o[i][0];
+      to[lane + 32] = o[i][1];
+      to[lane + 64] = o[i][2];
+      to[lane + 96] = o[i][3];
+      if (lane == 0) a.tree_ml[static_cast<size_t>(node) * a.hq + h] = make_float2(m[i], l[i]);
+    }
+  }
 }
 
 // ------------------------------------------------------------------ doc part
@@ -557,7 +593,8 @@ __global__ void attn_combine_kernel(AttnArgs a) {
 }  // namespace
 
 cudaError_t launch_tree_part(const AttnArgs& a, cudaStream_t st) {
-  const long warps = static_cast<long>(a.n_nodes) * a.hq;
+  const int G = a.hq / a.hkv;
+  const long warps = static_cast<long>(a.n_nodes) * a.hkv * ((G + kTreeHeads - 1) / kTreeHeads);
   if (warps <= 0) return cudaSuccess;
   count_launch();
   tree_part_kernel<<<static_cast<int>((warps * 32 + 255) / 256), 256, 0, st>>>(a, make_rope_table(a.theta));

@@ -131,6 +131,9 @@ constexpr int kJoinMaxRows = 64;
 cudaError_t launch_join_head(const float* z, const bf16* lm_head, const int* tokens, int n_true, int R, int rows,
                              int M, int d, float* p_true, cudaStream_t st);
 
+// logits[doc * M + m] = z_f32[doc] . W_lm[tokens[m]] in fp32 (d a multiple of 8).
+cudaError_t launch_restricted_logits(const float* z, const bf16* lm_head, const int* tokens, int M, int num_docs,
+                                     int d, float* logits, cudaStream_t st);
 // letters: logits of the M letter rows from z_f32 [N, d], renormalised softmax, argmax.
 cudaError_t launch_letters_head(const float* z, const bf16* lm_head, const int* letter_tokens, int M, int num_docs,
                                 int d, float* logprob, float* prob, int* argmax, cudaStream_t st);

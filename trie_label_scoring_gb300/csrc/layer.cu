@@ -403,24 +403,38 @@ __global__ void join_head_kernel(const float* __restrict__ z, const bf16* __rest
 }
 
 // letters: one block per document, warp per letter row.
-__global__ void letters_head_kernel(const float* __restrict__ z, const bf16* __restrict__ lm_head,
-                                    const int* __restrict__ letters, int M, int d, float* __restrict__ logprob,
-                                    float* __restrict__ prob, int* __restrict__ argmax) {
+// Warp per (document, listed token): logit = z32[doc] . W_lm[token] in fp32,
+// 16-byte weight loads; 8 tokens per CTA, documents along y.
+__global__ void restricted_logits_kernel(const float* __restrict__ z, const bf16* __restrict__ lm_head,
+                                         const int* __restrict__ tokens, int M, int d, float* __restrict__ logits) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int m = blockIdx.x * (blockDim.x >> 5) + warp;
+  const int doc = blockIdx.y;
+  if (m >= M) return;
+  const float4* zr = reinterpret_cast<const float4*>(z + static_cast<size_t>(doc) * d);
+  const uint4* w = reinterpret_cast<const uint4*>(lm_head + static_cast<size_t>(__ldg(tokens + m)) * d);
+  float acc = 0.f;
+#pragma unroll 4
+  for (int i = lane; i < (d >> 3); i += 32) {
+    const uint4 wv = __ldg(w + i);
+    const float4 w0 = bf16x4_to_float4(make_uint2(wv.x, wv.y)), w1 = bf16x4_to_float4(make_uint2(wv.z, wv.w));
+    const float4 z0 = zr[2 * i], z1 = zr[2 * i + 1];
+    acc = fmaf(z0.x, w0.x, fmaf(z0.y, w0.y, fmaf(z0.z, w0.z, fmaf(z0.w, w0.w, acc))));
+    acc = fmaf(z1.x, w1.x, fmaf(z1.y, w1.y, fmaf(z1.z, w1.z, fmaf(z1.w, w1.w, acc))));
+  }
+  acc = warp_sum(acc);
+  if (lane == 0) logits[static_cast<size_t>(doc) * M + m] = acc;
+}
+
+// CTA per document: the row of M logits (in logprob) renormalised in place:
+// log-softmax and softmax over the M entries, argmax (lowest index of the max).
+__global__ void letters_softmax_kernel(int M, float* __restrict__ logprob, float* __restrict__ prob,
+                                       int* __restrict__ argmax) {
   extern __shared__ float s_logit[];
   __shared__ float s_red[32];
   const int doc = blockIdx.x;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const float* zr = z + static_cast<size_t>(doc) * d;
-  for (int m = warp; m < M; m += nw) {
-    const bf16* w = lm_head + static_cast<size_t>(__ldg(letters + m)) * d;
-    float acc = 0.f;
-    for (int i = lane * 2; i < d; i += 64) {
-      const float2 wv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(w + i));
-      acc += zr[i] * wv.x + zr[i + 1] * wv.y;
-    }
-    acc = warp_sum(acc);
-    if (lane == 0) s_logit[m] = acc;
-  }
+  float* row = logprob + static_cast<size_t>(doc) * M;
+  for (int m = threadIdx.x; m < M; m += blockDim.x) s_logit[m] = row[m];
   __syncthreads();
   if (threadIdx.x == 0) {
     float b = -INFINITY;
@@ -442,7 +456,7 @@ __global__ void letters_head_kernel(const float* __restrict__ z, const bf16* __r
   const float lt = logf(total);
   for (int m = threadIdx.x; m < M; m += blockDim.x) {
     const float lp = s_logit[m] - mx - lt;
-    logprob[static_cast<size_t>(doc) * M + m] = lp;
+    row[m] = lp;
     prob[static_cast<size_t>(doc) * M + m] = expf(lp);
   }
 }
@@ -626,12 +640,22 @@ cudaError_t launch_join_head(const float* z, const bf16* lm_head, const int* tok
   return cudaGetLastError();
 }
 
+cudaError_t launch_restricted_logits(const float* z, const bf16* lm_head, const int* tokens, int M, int num_docs,
+                                     int d, float* logits, cudaStream_t st) {
+  if (num_docs <= 0 || M <= 0) return cudaSuccess;
+  if (d % 8 != 0 || num_docs > 65535) return cudaErrorInvalidValue;
+  count_launch();
+  restricted_logits_kernel<<<dim3((M + 7) / 8, num_docs), 256, 0, st>>>(z, lm_head, tokens, M, d, logits);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_letters_head(const float* z, const bf16* lm_head, const int* letter_tokens, int M, int num_docs,
                                 int d, float* logprob, float* prob, int* argmax, cudaStream_t st) {
   if (num_docs <= 0) return cudaSuccess;
+  cudaError_t e = launch_restricted_logits(z, lm_head, letter_tokens, M, num_docs, d, logprob, st);
+  if (e != cudaSuccess) return e;
   count_launch();
-  letters_head_kernel<<<num_docs, 256, M * sizeof(float), st>>>(z, lm_head, letter_tokens, M, d, logprob, prob,
-                                                                argmax);
+  letters_softmax_kernel<<<num_docs, 256, M * sizeof(float), st>>>(M, logprob, prob, argmax);
   return cudaGetLastError();
 }
 
