@@ -1610,7 +1610,7 @@ quail_status quail_classify_trie_tree_shortlist(const quail_model_desc* model, c
   }
   stage_mark(QUAIL_STAGE_HEAD, true, st);
   stage_mark(QUAIL_STAGE_SCORING, false, st);
-  CUDA_TRY(launch_lse_reduce(b.lse_part, R, n_tiles, b.lse, st));
+  CUDA_TRY(launch_lse_reduce(b.lse_part, R, n_tiles, b.lse, st, count));
   CUDA_TRY(launch_shortlist_child_logprob(T, x.sel, num_docs, B, block_base, b.z_f32,
                                           static_cast<const bf16*>(model->lm_head), d, b.lse, x.clp, st));
   CUDA_TRY(launch_shortlist_label_score(T, x.sel, num_docs, B, trie->num_labels, x.clp, label_logscore, label_prob,

@@ -84,7 +84,8 @@ cudaError_t launch_final_norm(const float* h_part, int k_splits, size_t slab, co
                               const int* node_token, RowMap map, int rows, int d, const bf16* gain, float eps,
                               bf16* z_bf16, float* z_f32, cudaStream_t st);
 // lse[r] = log-sum-exp over the n_tiles partials of row r.
-cudaError_t launch_lse_reduce(const float2* lse_part, int rows, int n_tiles, float* lse, cudaStream_t st);
+cudaError_t launch_lse_reduce(const float2* lse_part, int rows, int n_tiles, float* lse, cudaStream_t st,
+                              const int* live = nullptr);
 
 // Label path sums, prefix correction, softmax over labels and argmax, one block
 // per document; the block first reduces its a rows' log-sum-exp from the

@@ -185,10 +185,11 @@ __global__ void __launch_bounds__(kNormThreads) final_norm_kernel(const float* _
 }
 
 // One warp per row: max over the tile partials, then the rescaled sum.
-__global__ void lse_reduce_kernel(const float2* __restrict__ part, int rows, int n_tiles, float* __restrict__ lse) {
+__global__ void lse_reduce_kernel(const float2* __restrict__ part, int rows, int n_tiles, float* __restrict__ lse,
+                                  const int* __restrict__ live) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (warp >= rows) return;
+  if (warp >= rows || (live != nullptr && warp >= *live)) return;
   const float2* p = part + static_cast<size_t>(warp) * n_tiles;
   float m = -INFINITY;
 #pragma unroll 4
@@ -606,10 +607,11 @@ cudaError_t launch_final_norm(const float* h_part, int k_splits, size_t slab, co
   return cudaGetLastError();
 }
 
-cudaError_t launch_lse_reduce(const float2* lse_part, int rows, int n_tiles, float* lse, cudaStream_t st) {
+cudaError_t launch_lse_reduce(const float2* lse_part, int rows, int n_tiles, float* lse, cudaStream_t st,
+                              const int* live) {
   if (rows <= 0) return cudaSuccess;
   count_launch();
-  lse_reduce_kernel<<<(rows * 32 + 255) / 256, 256, 0, st>>>(lse_part, rows, n_tiles, lse);
+  lse_reduce_kernel<<<(rows * 32 + 255) / 256, 256, 0, st>>>(lse_part, rows, n_tiles, lse, live);
   return cudaGetLastError();
 }
 

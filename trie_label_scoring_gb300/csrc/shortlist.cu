@@ -228,38 +228,45 @@ __global__ void shortlist_clear_kernel(float* __restrict__ logscore, float* __re
   }
 }
 
-// CTA per document: score the kept groups' labels (warp per label), then
-// softmax and argmax over the kept labels.
+// CTA per (document, kept group): warp per label of that group, its terms
+// summed from the child log-probs plus the prefix-label correction.
 __global__ void __launch_bounds__(kScoreThreads) shortlist_label_score_kernel(
     ShortlistTables T, const int* __restrict__ sel, int B, int M, const float* __restrict__ clp,
-    float* __restrict__ logscore, float* __restrict__ prob, int* __restrict__ argmax) {
+    float* __restrict__ logscore) {
+  const int doc = blockIdx.x, b = blockIdx.y;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int blk = doc * B + b;
+  const int g = sel[blk];
+  const float* cl = clp + static_cast<size_t>(blk) * T.max_children;
+  float* ls = logscore + static_cast<size_t>(doc) * M;
+  for (int li = T.lab_off[g] + warp; li < T.lab_off[g + 1]; li += nw) {
+    float acc = 0.f;
+    for (int k = T.term_off[li] + lane; k < T.term_off[li + 1]; k += 32) acc += cl[T.term_t[k]];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    const int p0 = T.pref_t0[li], p1 = T.pref_t1[li];
+    if (p1 > p0) {  // prefix label: probability of stopping at its end node
+      double cont = 0.0;
+      for (int c = p0 + lane; c < p1; c += 32) cont += exp(static_cast<double>(cl[c]));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) cont += __shfl_xor_sync(0xffffffffu, cont, o);
+      acc = (cont < 1.0 - 1e-12) ? acc + static_cast<float>(log1p(-cont)) : -INFINITY;
+    }
+    if (lane == 0) ls[T.lab_id[li]] = acc;
+  }
+}
+
+// CTA per document: softmax and argmax over the kept labels' scores.
+__global__ void __launch_bounds__(kScoreThreads) shortlist_softmax_kernel(ShortlistTables T,
+                                                                          const int* __restrict__ sel, int B, int M,
+                                                                          const float* __restrict__ logscore,
+                                                                          float* __restrict__ prob,
+                                                                          int* __restrict__ argmax) {
   __shared__ float s_v[32];
   __shared__ int s_i[32];
   const int doc = blockIdx.x;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  float* ls = logscore + static_cast<size_t>(doc) * M;
+  const float* ls = logscore + static_cast<size_t>(doc) * M;
   float* pr = prob + static_cast<size_t>(doc) * M;
-  for (int b = 0; b < B; ++b) {
-    const int blk = doc * B + b;
-    const int g = sel[blk];
-    const float* cl = clp + static_cast<size_t>(blk) * T.max_children;
-    for (int li = T.lab_off[g] + warp; li < T.lab_off[g + 1]; li += nw) {
-      float acc = 0.f;
-      for (int k = T.term_off[li] + lane; k < T.term_off[li + 1]; k += 32) acc += cl[T.term_t[k]];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      const int p0 = T.pref_t0[li], p1 = T.pref_t1[li];
-      if (p1 > p0) {  // prefix label: probability of stopping at its end node
-        double cont = 0.0;
-        for (int c = p0 + lane; c < p1; c += 32) cont += exp(static_cast<double>(cl[c]));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) cont += __shfl_xor_sync(0xffffffffu, cont, o);
-        acc = (cont < 1.0 - 1e-12) ? acc + static_cast<float>(log1p(-cont)) : -INFINITY;
-      }
-      if (lane == 0) ls[T.lab_id[li]] = acc;
-    }
-  }
-  __syncthreads();
   float bv = -INFINITY;
   int bi = 0x7fffffff;
   for (int b = 0; b < B; ++b) {
@@ -349,13 +356,18 @@ cudaError_t launch_shortlist_label_score(const ShortlistTables& T, const int* se
                                          const float* clp, float* logscore, float* prob, int* argmax,
                                          cudaStream_t st) {
   if (num_docs <= 0) return cudaSuccess;
+  if (B > 65535) return cudaErrorInvalidValue;
   const size_t n = static_cast<size_t>(num_docs) * M;
   count_launch();
   shortlist_clear_kernel<<<static_cast<int>(std::min<size_t>((n + 255) / 256, 4096)), 256, 0, st>>>(logscore, prob, n);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   count_launch();
-  shortlist_label_score_kernel<<<num_docs, kScoreThreads, 0, st>>>(T, sel, B, M, clp, logscore, prob, argmax);
+  shortlist_label_score_kernel<<<dim3(num_docs, B), kScoreThreads, 0, st>>>(T, sel, B, M, clp, logscore);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  count_launch();
+  shortlist_softmax_kernel<<<num_docs, kScoreThreads, 0, st>>>(T, sel, B, M, logscore, prob, argmax);
   return cudaGetLastError();
 }
 
