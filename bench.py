@@ -731,10 +731,12 @@ def run_ml(args, world, rank, local):
         e2e = {"value": N * world * k_e2e / (e2e_ms / 1e3), "unit": "docs/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": k_e2e}
 
-    # ---- roofline of the dominant kernel: the gate|up GEMM of a layer
+    # ---- roofline of the dominant kernel: the gate|up GEMM of a layer, with
+    # SiLU(gate) * up fused into its epilogue (output: the two-term bf16 split
+    # of the activation, 4 bytes per element)
     peaks = measured_peaks()
     d, V = sh.hidden, sh.vocab
-    gu_bytes = 2.0 * d * 2 * I + 2.0 * rows * d + 4.0 * rows * 2 * I
+    gu_bytes = 2.0 * d * 2 * I + 2.0 * rows * d + 4.0 * rows * I
     gu_flops = 2.0 * rows * d * 2 * I
     t_gu = span_ms["gate_up"] / 1e3
     if gu_bytes / (peaks["hbm_gbs"] * 1e9) >= gu_flops / (peaks["bf16_tflops"] * 1e12):
@@ -746,7 +748,7 @@ def run_ml(args, world, rank, local):
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                     "frac": achieved / peaks["bf16_tflops"], "peak_kind": f"bf16 burst ({peaks['source']})"}
     roofline.update({"traffic": recorded_traffic(mw.name, rows, "gate_up_gemm_traffic.json"),
-                     "kernel": "umma_gemm_kernel<EpiStoreF32> (gate|up, split A)",
+                     "kernel": "umma_gemm_kernel<EpiSwiGLU> (gate|up, split A, SwiGLU epilogue)",
                      "gate_up_ms": span_ms["gate_up"], "algorithmic_bytes": gu_bytes,
                      "algorithmic_flops": gu_flops,
                      "issued_tflops": 2 * gu_flops / t_gu / 1e12,

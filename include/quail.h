@@ -488,8 +488,10 @@ int32_t quail_launch_count(void);
  * quail_classify_trie_tree_ml marks stage 0 around the whole layer stack and
  * in addition, for layer l, span j at stage QUAIL_NUM_STAGES +
  * l * QUAIL_LAYER_SPANS + j (spans: 0 residual + RMSNorm + q|k|v GEMM + q/k
- * norms, 1 attention, 2 W_o GEMM + residual + post-norm, 3 gate|up GEMM
- * alone, 4 SiLU(gate) * up, 5 down GEMM alone); num_stages may then reach
+ * norms, 1 attention, 2 W_o GEMM + residual + post-norm, 3 gate|up GEMM,
+ * with SiLU(gate) * up fused into its epilogue when the projection
+ * runs without a k-split, 4 SiLU(gate) * up when it runs as its own kernel,
+ * 5 down GEMM alone); num_stages may then reach
  * QUAIL_NUM_STAGES + QUAIL_LAYER_SPANS * QUAIL_MAX_LAYERS. */
 enum { QUAIL_STAGE_PROLOGUE = 0, QUAIL_STAGE_ATTENTION = 1, QUAIL_STAGE_WO_NORM = 2, QUAIL_STAGE_HEAD = 3,
        QUAIL_STAGE_SCORING = 4, QUAIL_NUM_STAGES = 5 };

@@ -1095,15 +1095,34 @@ quail_status quail_classify_trie_tree_ml(const quail_model_ml_desc* model, const
     CUDA_TRY(launch_residual_norm(x.h, b.h_part, b.gp.ks_wo, static_cast<size_t>(rows) * d, rows, d,
                                   static_cast<const bf16*>(w.post_norm), model->rms_eps, b.xhat, st));
     span(QUAIL_SPAN_WO_NORM, true);
-    const void* gu[2] = {w.w_gate, w.w_up};
-    const int gu_rows[2] = {I, I};
     span(QUAIL_SPAN_GATE_UP, false);
-    s = run_split_gemm(b.xhat, rows, d, gu, gu_rows, 2, x.ks_gu, x.gu_part, 2 * I, ds, st);
-    if (s != QUAIL_OK) return s;
-    span(QUAIL_SPAN_GATE_UP, true);
-    span(QUAIL_SPAN_SILU_MUL, false);
-    CUDA_TRY(launch_silu_mul_split(x.gu_part, x.ks_gu, static_cast<size_t>(rows) * 2 * I, rows, I, x.act, st));
-    span(QUAIL_SPAN_SILU_MUL, true);
+    if (x.ks_gu == 1) {
+      // one k-split: SiLU(gate) * up fused into the projection's epilogue
+      CUtensorMap tA;
+      s = encode_2d_bf16(&tA, b.xhat, round_up(rows, 128), 2 * d, 2 * d, 64, 128);
+      if (s != QUAIL_OK) return s;
+      BSet bs{};
+      s = encode_2d_bf16(&bs.map[0], w.w_gate, I, d, d, 64, 128);
+      if (s != QUAIL_OK) return s;
+      s = encode_2d_bf16(&bs.map[1], w.w_up, I, d, d, 64, 128);
+      if (s != QUAIL_OK) return s;
+      bs.count = 2;
+      bs.glu = 1;
+      bs.n_begin[1] = bs.n_begin[2] = 2 * I;
+      CUDA_TRY(launch_gemm_swiglu(tA, bs, rows, I, d, x.act, ds->num_sms, ds->err, st));
+      span(QUAIL_SPAN_GATE_UP, true);
+      span(QUAIL_SPAN_SILU_MUL, false);
+      span(QUAIL_SPAN_SILU_MUL, true);
+    } else {
+      const void* gu[2] = {w.w_gate, w.w_up};
+      const int gu_rows[2] = {I, I};
+      s = run_split_gemm(b.xhat, rows, d, gu, gu_rows, 2, x.ks_gu, x.gu_part, 2 * I, ds, st);
+      if (s != QUAIL_OK) return s;
+      span(QUAIL_SPAN_GATE_UP, true);
+      span(QUAIL_SPAN_SILU_MUL, false);
+      CUDA_TRY(launch_silu_mul_split(x.gu_part, x.ks_gu, static_cast<size_t>(rows) * 2 * I, rows, I, x.act, st));
+      span(QUAIL_SPAN_SILU_MUL, true);
+    }
     const void* dn[1] = {w.w_down};
     const int dn_rows[1] = {d};
     span(QUAIL_SPAN_DOWN, false);

@@ -189,6 +189,54 @@ cudaError_t launch_gemm_proj(const CUtensorMap& tmA, const BSet& bset, int M, in
                                                  m_live);
 }
 
+// SwiGLU epilogue of a gate|up GEMM in glu mode (one k-split): columns
+// [0, BN/2) of the tile are gate, [BN/2, BN) up, for outputs j0 = n_blk BN/2 ..
+// act[row][j] = split(SiLU(gate) * up) as [hi (I) | lo (I)] bf16, through a
+// padded shared-memory block per warp so each store covers one row's 32
+// consecutive outputs.
+template <int BN>
+struct EpiSwiGLU {
+  static constexpr uint32_t kScratchBytes = 4 * 32 * 33 * 4;
+  bf16* act;
+  int I;
+  int M;
+  __device__ __forceinline__ void operator()(int m_blk, int n_blk, int /*ks*/, int lane_row, uint32_t taddr,
+                                             float* ws) const {
+    const int lane = threadIdx.x & 31;
+    const int row0 = m_blk * kGemmBM + lane_row - lane;
+    const int j0 = n_blk * (BN / 2);
+    const int rows = min(32, M - row0);
+#pragma unroll 1
+    for (int c = 0; c < BN / 64; ++c) {
+      float gv[32], uv[32];
+      tmem_ld_32cols(taddr + c * 32, gv);
+      tmem_ld_32cols(taddr + BN / 2 + c * 32, uv);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) ws[lane * 33 + i] = gv[i] / (1.f + expf(-gv[i])) * uv[i];
+      __syncwarp();
+      const int j = j0 + c * 32 + lane;
+      if (j < I) {
+#pragma unroll 4
+        for (int r = 0; r < rows; ++r) {
+          const float a = ws[r * 33 + lane];
+          const bf16 hi = __float2bfloat16(a);
+          bf16* o = act + static_cast<size_t>(row0 + r) * 2 * I;
+          o[j] = hi;
+          o[I + j] = __float2bfloat16(a - __bfloat162float(hi));
+        }
+      }
+      __syncwarp();
+    }
+  }
+};
+
+cudaError_t launch_gemm_swiglu(const CUtensorMap& tmA, const BSet& bset, int M, int I, int K, bf16* act,
+                               int num_sms, int* err, cudaStream_t st) {
+  if (!bset.glu || bset.count != 2 || I % (kProjBN / 2) != 0) return cudaErrorInvalidValue;
+  EpiSwiGLU<kProjBN> epi{act, I, M};
+  return launch_umma<kProjBN, kProjStages, true>(tmA, bset, M, 2 * I, K / kGemmBK, 1, epi, num_sms, err, st);
+}
+
 cudaError_t launch_gemm_head(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int V, int K,
                              const HeadEpilogueArgs& args, int num_sms, int* err, cudaStream_t st,
                              const int* m_live) {

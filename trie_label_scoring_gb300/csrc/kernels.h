@@ -23,6 +23,12 @@ struct BSet;
 cudaError_t launch_gemm_proj(const CUtensorMap& tmA, const BSet& bset, int M, int N, int K, int k_splits, float* C,
                              size_t slab, int ldc, int num_sms, int* err, cudaStream_t st,
                              const int* m_live = nullptr);
+// Fused SwiGLU input projection: A = split y [M, 2K]; bset in glu mode (map[0]
+// = W_gate, map[1] = W_up, boxes of kProjBN/2 rows); writes
+// act = split(SiLU(y W_gate^T) * (y W_up^T)) [round_up(M,128), 2I] bf16 directly
+// (no k-split). I must be a multiple of 128.
+cudaError_t launch_gemm_swiglu(const CUtensorMap& tmA, const BSet& bset, int M, int I, int K, bf16* act,
+                               int num_sms, int* err, cudaStream_t st);
 // k-splits that balance `tiles` work tiles of nk k-blocks over num_sms SMs.
 int choose_k_splits(int tiles, int nk, int num_sms);
 

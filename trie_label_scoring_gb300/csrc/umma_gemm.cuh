@@ -41,10 +41,15 @@ constexpr int kGemmThreads = 192;
 constexpr int kPrefetchKb = 8;  // k-blocks of B requested into L2 ahead of their loads (CTA pairs)
 
 // Up to three B operands covering output columns [n_begin[i], n_begin[i+1]).
+// glu != 0: two operands of equal shape whose rows pair up (gate and up
+// projections). Unit n's B band is rows [n BN/2, (n+1) BN/2) of map[0]
+// followed by the same rows of map[1] (boxes of BN/2 rows), so accumulator
+// column c < BN/2 and column BN/2 + c hold the two halves of one output.
 struct BSet {
   CUtensorMap map[3];
   int n_begin[4];
   int count;
+  int glu;
 };
 
 template <int BN, int STAGES, bool SPLIT_A>
@@ -198,11 +203,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
           tma_load_2d(st, &tmA, &full[stage], kb * kGemmBK, g.m_blk * kGemmBM);
           if (SPLIT_A) tma_load_2d(st + Cfg::kABytes, &tmA, &full[stage], (nk + kb) * kGemmBK, g.m_blk * kGemmBM);
-          if (CM == 2)
+          if (CM == 2) {
             tma_load_2d_mcast(st + Cfg::kABytes + crank * kBHalf, tmB, &full[stage], kb * kGemmBK, nb_own,
                               static_cast<uint16_t>(0x3));
-          else
+          } else if (bset.glu) {
+            uint8_t* b_st = st + (SPLIT_A ? 2 : 1) * Cfg::kABytes;
+            tma_load_2d(b_st, &bset.map[0], &full[stage], kb * kGemmBK, g.n_blk * (BN / 2));
+            tma_load_2d(b_st + Cfg::kBBytes / 2, &bset.map[1], &full[stage], kb * kGemmBK, g.n_blk * (BN / 2));
+          } else {
             tma_load_2d(st + (SPLIT_A ? 2 : 1) * Cfg::kABytes, tmB, &full[stage], kb * kGemmBK, nb);
+          }
           armed_parity[stage] = static_cast<int>(phase);
           if (++stage == STAGES) {
             stage = 0;
