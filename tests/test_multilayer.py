@@ -152,3 +152,14 @@ def test_ml_qwen_shape_two_layers_sampled():
     labels = S.make_labels(base, 0)
     bits, lsc, prob, am = _run_ml(mw, docs_ml, labels)
     _check_ml(mw, bits, docs_ml, labels, [0, 31, 63], lsc, prob, am)
+
+
+@pytest.mark.gpu
+def test_ml_full_depth_36_layers_sampled():
+    """The bench workload itself: 36 Qwen3-4B-shaped layers, 64 documents;
+    two documents checked against the oracle through the whole stack."""
+    mw = S.ML_WORKLOADS["qwen3-4b-L36-support10-64docs"]
+    docs_ml = S.make_docs_ml(mw.base, mw.n_layers, 0)
+    labels = S.make_labels(mw.base, 0)
+    bits, lsc, prob, am = _run_ml(mw, docs_ml, labels)
+    _check_ml(mw, bits, docs_ml, labels, [0, 63], lsc, prob, am)

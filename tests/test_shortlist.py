@@ -298,3 +298,23 @@ def test_grouped_labels_qwen_shape_sampled():
     out = _run_shortlist(w, docs, t, sl, 2)
     rw = SL.rewrite_grouped(ls.labels, names, SL.group_labels(ls.labels, G))
     _check_shortlist(w, docs, build_trie(rw, ls.root_token, w.shape.vocab), 1, 2, [0, 3], out)
+
+
+@pytest.mark.gpu
+def test_grouped_labels_full_size_sampled():
+    """The bench workload itself: 60,000 labels in ceil(sqrt K) one-token
+    groups, 16 documents of 1,024 tokens, beam 4; two documents checked."""
+    import trie_label_scoring_gb300 as Q
+    from oracle import shortlist as SL
+    from oracle.trie import build_trie
+    sw = S.SHORTLIST_WORKLOADS["qwen3-4b-grouped60k-16x1024"]
+    w = sw.base
+    ls = S.make_labels(w, 0)
+    docs = S.make_docs(w, 0)
+    G = SL.default_groups(len(ls.labels))
+    names = S.make_group_names(0, G, 1, w.shape.vocab)
+    t, _ = Q.Trie.grouped(ls.labels, ls.root_token, w.shape.vocab, names, num_groups=G)
+    sl = Q.Shortlist(t, 1)
+    out = _run_shortlist(w, docs, t, sl, sw.beam)
+    rw = SL.rewrite_grouped(ls.labels, names, SL.group_labels(ls.labels, G))
+    _check_shortlist(w, docs, build_trie(rw, ls.root_token, w.shape.vocab), 1, sw.beam, [0, 15], out)
