@@ -45,6 +45,9 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--decode", action="store_true", help="greedy trie_decode instead of trie_tree on a tree workload")
+    p.add_argument("--oracle-rate", action="store_true", help=argparse.SUPPRESS)
+    p.add_argument("--budget", type=float, default=10.0, help=argparse.SUPPRESS)
     return p.parse_args()
 
 
@@ -188,6 +191,33 @@ def time_oracle(w, docs, labels, budget_s: float, max_docs: int | None = None) -
     return {"docs": n, "seconds": el, "docs_per_s": n / el}
 
 
+def oracle_rate_one_core(workload: str, docs: int | None, budget_s: float):
+    """The oracle's docs/s with BLAS held to one thread: this script re-run in
+    --oracle-rate mode in a fresh process (thread counts are read at import)."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[k] = "1"
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--oracle-rate", "--workload", workload,
+           "--budget", str(budget_s)] + (["--docs", str(docs)] if docs else [])
+    try:
+        out = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
+        line = [l for l in out.stdout.splitlines() if l.startswith("{")][-1]
+        return json.loads(line)
+    except (subprocess.SubprocessError, IndexError, ValueError, OSError):
+        return None
+
+
+def run_oracle_rate(args):
+    """--oracle-rate: the oracle alone on a bounded sample; one JSON line."""
+    import synthetic as S
+    w = S.WORKLOADS[args.workload]
+    if args.docs:
+        w = S.with_docs(w, args.docs)
+    r = time_oracle(w, S.make_docs(w, 0), S.make_labels(w, 0), budget_s=args.budget)
+    print(json.dumps({"value": r["docs_per_s"], "unit": "docs/s", "cores": 1, "docs": r["docs"],
+                      "seconds": r["seconds"], "threads_env": os.environ.get("OPENBLAS_NUM_THREADS")}), flush=True)
+
+
 def cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -328,9 +358,17 @@ def run_ours(args, world, rank, local):
     labels = S.make_labels(w, 0)
     docs = S.make_docs(w, rank)  # each rank scores its own documents
     kv = kv_from_docs(docs)
+    tb0 = time.perf_counter()
     trie = Q.Trie(labels.labels, labels.root_token, w.shape.vocab, labels.continuation)
+    trie_build_ms = 1e3 * (time.perf_counter() - tb0)  # host build, outside the timed region
     trie.upload()
     N, M, a = w.num_docs, len(labels.labels), trie.n_eval
+    view = trie.view()
+    n_children = np.diff(view["child_offsets"])
+    trie_stats = {"nodes": int(view["n_nodes"]), "evaluated": int(a), "build_ms": trie_build_ms,
+                  "depth_histogram": np.bincount(view["depth"]).tolist(),
+                  "mean_branching": float(n_children[n_children > 0].mean()),
+                  "branching_nodes": int(view["is_branching"].sum())}
     ws = torch.empty(Q.workspace_size(model, trie, 0, N, docs.max_doc_len, Q.MODE_TRIE_TREE), dtype=torch.uint8,
                      device="cuda")
     lsc = torch.empty((N, M), device="cuda")
@@ -449,13 +487,17 @@ def run_ours(args, world, rank, local):
     path = {"t_kv_us": t_kv * 1e6, "t_head_us": t_head * 1e6, "t_star_us": t_star * 1e6,
             "ms_per_step": ms_per_step, "frac": t_star * 1e3 / ms_per_step}
 
-    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only)
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only),
+    # on all host cores and, in a subprocess with single-threaded BLAS, on one
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         r = time_oracle(w, docs, labels, budget_s=15.0)
         cpu = {"value": r["docs_per_s"], "unit": "docs/s", "cores": cores(), "kind": "oracle",
                "sample": f"first {r['docs']} documents of {w.name} ({r['seconds']:.1f} s); numpy BLAS threads "
                          f"default to all {cores()} cores"}
+        one = oracle_rate_one_core(w.name, args.docs, budget_s=10.0)
+        if one is not None:
+            cpu["one_core"] = one
 
     if rank == 0:
         out = {
@@ -463,7 +505,8 @@ def run_ours(args, world, rank, local):
             "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, random-init weights)",
             "config": {"workload": w.name, "docs_per_gpu": N, "labels": M, "eval_positions_per_doc": a,
-                       "trie_nodes": trie.n_nodes, "hidden": d, "vocab": V, "q_heads": w.shape.n_q_heads,
+                       "trie_nodes": trie.n_nodes, "trie": trie_stats, "hidden": d, "vocab": V,
+                       "q_heads": w.shape.n_q_heads,
                        "kv_heads": w.shape.n_kv_heads, "doc_tokens_per_gpu": int(docs.doc_len.sum()),
                        "l2": "inputs larger than L2 (doc KV %.2f GB + output head %.2f GB per step)" % (
                            kv_bytes / 1e9, 2.0 * d * V / 1e9),
@@ -1005,10 +1048,180 @@ def run_shortlist(args, world, rank, local):
         print(json.dumps(out), flush=True)
 
 
+def _timed_loop(stream, steps, world, call, n_stage_events=0):
+    """K calls between CUDA events on `stream`, barrier + synchronize on both
+    sides; per-call stage events when n_stage_events > 0. Returns
+    (elapsed ms, stage events per call, clocks)."""
+    import torch
+
+    import trie_label_scoring_gb300 as Q
+    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_stage_events)] for _ in range(steps)]
+    for evs in stage_ev:
+        for e in evs:
+            e.record(stream)
+    clocks = ClockSampler(str(torch.cuda.get_device_properties(torch.cuda.current_device()).pci_bus_id))
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for k in range(steps):
+        if n_stage_events:
+            Q.set_stage_events(stage_ev[k])
+        call()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    Q.set_stage_events(None)
+    Q.device_status()
+    return max_over_ranks(world, start.elapsed_time(end)), stage_ev, clk
+
+
+def run_letters(args, world, rank, local):
+    """The letters variant ("To Classify, Try a Trie Tree", sec. 3.3): one
+    answer position per document scored against the letter tokens
+    (quail_classify_letters). One step = one call over all documents."""
+    import torch
+
+    import synthetic as S
+    import trie_label_scoring_gb300 as Q
+    from tests import gpu_cases as C
+    from trie_label_scoring_gb300.torch_inputs import kv_from_docs
+
+    Q.build()
+    w = S.WORKLOADS[args.workload]
+    if args.docs:
+        w = S.with_docs(w, args.docs)
+    model = C.device_model(w.shape, 0)
+    letters = S.make_labels(w, 0)
+    tokens = [l[0] for l in letters.labels]
+    docs = S.make_docs(w, rank)
+    kv = kv_from_docs(docs)
+    N, M = w.num_docs, len(tokens)
+    ws = torch.empty(Q.workspace_size(model, None, M, N, docs.max_doc_len, Q.MODE_LETTERS), dtype=torch.uint8,
+                     device="cuda")
+    lp = torch.empty((N, M), device="cuda")
+    pr = torch.empty((N, M), device="cuda")
+    am = torch.empty((N,), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        Q.classify_letters(model, kv, tokens, letters.root_token, N, ws, lp, pr, am, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    Q.device_status()
+    launches = Q.launch_count()
+    steps = args.steps if args.steps is not None else 200
+    elapsed_ms, stage_ev, clk = _timed_loop(stream, steps, world, step, 10)
+    stages_ms = {name: statistics.mean(ev[2 * i].elapsed_time(ev[2 * i + 1]) for ev in stage_ev)
+                 for i, name in enumerate(Q.STAGES[:4])}
+    ms = elapsed_ms / steps
+    peaks = measured_peaks()
+    kv_bytes = float(docs.doc_len.sum()) * w.shape.n_kv_heads * w.shape.head_dim * 2 * 2
+    att = kv_bytes / (stages_ms["attention"] / 1e3) / 1e9
+    t_kv = kv_bytes / (peaks["hbm_gbs"] * 1e9)
+    if rank == 0:
+        out = {
+            "metric": "documents classified/sec at 1 GB300 (letters)", "value": N * world * steps / (elapsed_ms / 1e3),
+            "unit": "docs/s", "n_gpus": world, "steps": steps, "warmup": max(args.warmup, 3), "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded, random-init weights)",
+            "config": {"workload": w.name, "docs_per_gpu": N, "letters": M, "doc_tokens_per_gpu": int(docs.doc_len.sum()),
+                       "l2": "doc KV %.2f GB per step" % (kv_bytes / 1e9),
+                       "parallelism": f"replicas x{world} (documents sharded, no collective)"},
+            "roofline": {"bound": "hbm", "achieved": att, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": att / peaks["hbm_gbs"], "traffic": None, "kernel": "doc attention (one row per document)",
+                         "attention_ms": stages_ms["attention"], "peak_kind": f"HBM copy ({peaks['source']})"},
+            "path_roofline": {"t_kv_us": t_kv * 1e6, "ms_per_step": ms, "frac": t_kv * 1e3 / ms},
+            "stages_ms": stages_ms, "cpu_baseline": None, "e2e": None, "gpu_launches": launches * steps,
+            "clocks": clk,
+        }
+        print(json.dumps(out), flush=True)
+
+
+def run_decode(args, world, rank, local):
+    """Greedy trie_decode ("To Classify, Try a Trie Tree", sec. 3.1) over a
+    tree workload: one step of the bench = the decode steps it takes for every
+    document to reach a label (quail_classify_trie_decode_step, called that
+    many times; the count is fixed in the warm-up, so no host read happens
+    inside the timed region)."""
+    import torch
+
+    import synthetic as S
+    import trie_label_scoring_gb300 as Q
+    from tests import gpu_cases as C
+    from trie_label_scoring_gb300.torch_inputs import kv_from_docs
+
+    Q.build()
+    w = S.WORKLOADS[args.workload]
+    if args.docs:
+        w = S.with_docs(w, args.docs)
+    model = C.device_model(w.shape, 0)
+    labels = S.make_labels(w, 0)
+    docs = S.make_docs(w, rank)
+    kv = kv_from_docs(docs)
+    trie = Q.Trie(labels.labels, labels.root_token, w.shape.vocab, labels.continuation)
+    trie.upload()
+    N = w.num_docs
+    ws = torch.empty(Q.workspace_size(model, trie, 0, N, docs.max_doc_len, Q.MODE_TRIE_DECODE), dtype=torch.uint8,
+                     device="cuda")
+    cur = torch.zeros(N, dtype=torch.int32, device="cuda")
+    lab = torch.full((N,), -1, dtype=torch.int32, device="cuda")
+    act = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    n_steps = 0
+    while True:  # warm-up: how many decode steps this batch takes
+        Q.classify_trie_decode_step(model, kv, trie, N, cur, lab, act, ws, None, stream)
+        n_steps += 1
+        if int(act.item()) == 0 or n_steps >= 64:
+            break
+    launches_per_step_call = Q.launch_count()
+
+    def decode():
+        cur.zero_()
+        lab.fill_(-1)
+        for _ in range(n_steps):
+            Q.classify_trie_decode_step(model, kv, trie, N, cur, lab, act, ws, None, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        decode()
+    Q.device_status()
+    steps = args.steps if args.steps is not None else 100
+    elapsed_ms, _, clk = _timed_loop(stream, steps, world, decode)
+    ms = elapsed_ms / steps
+    peaks = measured_peaks()
+    kv_bytes = float(docs.doc_len.sum()) * w.shape.n_kv_heads * w.shape.head_dim * 2 * 2
+    if rank == 0:
+        out = {
+            "metric": "documents classified/sec at 1 GB300 (greedy trie_decode)",
+            "value": N * world * steps / (elapsed_ms / 1e3), "unit": "docs/s", "n_gpus": world, "steps": steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, random-init weights)",
+            "config": {"workload": w.name, "docs_per_gpu": N, "labels": len(labels.labels),
+                       "decode_steps": n_steps, "doc_tokens_per_gpu": int(docs.doc_len.sum()),
+                       "parallelism": f"replicas x{world} (documents sharded, no collective)"},
+            "roofline": {"bound": "hbm", "achieved": n_steps * kv_bytes / (ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": n_steps * kv_bytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                         "traffic": None, "kernel": "whole decode (document KV re-read at every step)",
+                         "peak_kind": f"HBM copy ({peaks['source']})",
+                         "note": "the bytes are those of all documents at every step; decided documents skip "
+                                 "their attention, so this overstates the work of the later steps"},
+            "cpu_baseline": None, "e2e": None,
+            "gpu_launches": launches_per_step_call * n_steps * steps, "clocks": clk,
+        }
+        print(json.dumps(out), flush=True)
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if args.oracle_rate:
+        run_oracle_rate(args)
+        return
     if args.impl == "reference":
         run_reference(args, world, rank)
         return
@@ -1020,6 +1233,10 @@ def main():
         run_shortlist(args, world, rank, local)
     elif "-join" in args.workload:  # AI.IF join workloads (synthetic labels kind "join")
         run_join(args, world, rank, local)
+    elif "-letters" in args.workload:  # the letters variant
+        run_letters(args, world, rank, local)
+    elif args.decode:  # greedy trie_decode on a tree workload
+        run_decode(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:
