@@ -411,9 +411,14 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
+    # Inside the timed loop only the head GEMM's pair of events is recorded (the
+    # roofline kernel); an event between two kernels keeps the second from
+    # launching while the first drains, so the other stage boundaries are timed
+    # in a separate loop after this one.
+    hs = Q.STAGES.index("head")
     start.record(stream)
     for k in range(steps):
-        Q.set_stage_events(stage_ev[k])
+        Q.set_stage_events([None] * (2 * hs) + stage_ev[k][2 * hs: 2 * hs + 2])
         step()
     end.record(stream)
     torch.cuda.synchronize()
@@ -423,11 +428,20 @@ def run_ours(args, world, rank, local):
     Q.device_status()
     elapsed_ms = start.elapsed_time(end)
     elapsed_ms = max_over_ranks(world, elapsed_ms)
-    stages_ms = {name: statistics.mean(ev[2 * i].elapsed_time(ev[2 * i + 1]) for ev in stage_ev)
-                 for i, name in enumerate(Q.STAGES)}
-    head_ms = stages_ms["head"]
+    head_ms = statistics.mean(ev[2 * hs].elapsed_time(ev[2 * hs + 1]) for ev in stage_ev)
     ms_per_step = elapsed_ms / steps
     value = N * world * steps / (elapsed_ms / 1e3)
+    # stage breakdown (every boundary marked), after the timed region
+    n_bd = min(steps, 50)
+    bd_ev = stage_ev[:n_bd]
+    torch.cuda.synchronize()
+    for k in range(n_bd):
+        Q.set_stage_events(bd_ev[k])
+        step()
+    torch.cuda.synchronize()
+    Q.set_stage_events(None)
+    stages_ms = {name: statistics.mean(ev[2 * i].elapsed_time(ev[2 * i + 1]) for ev in bd_ev)
+                 for i, name in enumerate(Q.STAGES)}
 
     # ---- e2e: host buffers through the C ABI, copies inside the timed region
     e2e = None
@@ -706,6 +720,17 @@ def run_ml(args, world, rank, local):
     for evs in stage_ev:
         for e in evs:
             e.record(stream)
+    # inside the timed loop only the gate|up spans (the roofline kernel) are
+    # marked, since an event between two kernels keeps the second from
+    # launching while the first drains; the full breakdown is a separate loop
+    s0, nsp, gu = len(Q.STAGES), len(Q.LAYER_SPANS), Q.LAYER_SPANS.index("gate_up")
+    gu_idx = [2 * (s0 + l * nsp + gu) + j for l in range(L) for j in (0, 1)]
+
+    def timed_events(evs):
+        sel = [None] * len(evs)
+        for i in gu_idx:
+            sel[i] = evs[i]
+        return sel
     clocks = ClockSampler(str(torch.cuda.get_device_properties(local).pci_bus_id))
     clocks.start()
     time.sleep(0.3)
@@ -714,7 +739,7 @@ def run_ml(args, world, rank, local):
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
     for k in range(steps):
-        Q.set_stage_events(stage_ev[k])
+        Q.set_stage_events(timed_events(stage_ev[k]))
         step()
     end.record(stream)
     torch.cuda.synchronize()
@@ -725,13 +750,21 @@ def run_ml(args, world, rank, local):
     elapsed_ms = max_over_ranks(world, start.elapsed_time(end))
     ms_per_step = elapsed_ms / steps
     value = N * world * steps / (elapsed_ms / 1e3)
-    stages_ms = {name: statistics.mean(ev[2 * i].elapsed_time(ev[2 * i + 1]) for ev in stage_ev)
+    gate_up_ms = statistics.mean(ev[i].elapsed_time(ev[i + 1]) for ev in stage_ev for i in gu_idx[::2])
+    # breakdown with every stage and span marked, after the timed region
+    bd_ev = stage_ev[:min(steps, 10)]
+    torch.cuda.synchronize()
+    for evs in bd_ev:
+        Q.set_stage_events(evs)
+        step()
+    torch.cuda.synchronize()
+    Q.set_stage_events(None)
+    stages_ms = {name: statistics.mean(ev[2 * i].elapsed_time(ev[2 * i + 1]) for ev in bd_ev)
                  for i, name in enumerate(Q.STAGES) if name != "attention" and name != "wo_norm"}
-    s0 = len(Q.STAGES)
     span_ms = {}
     for j, name in enumerate(Q.LAYER_SPANS):
-        span_ms[name] = statistics.mean(ev[2 * (s0 + l * len(Q.LAYER_SPANS) + j)].elapsed_time(
-            ev[2 * (s0 + l * len(Q.LAYER_SPANS) + j) + 1]) for ev in stage_ev for l in range(L))
+        span_ms[name] = statistics.mean(ev[2 * (s0 + l * nsp + j)].elapsed_time(ev[2 * (s0 + l * nsp + j) + 1])
+                                        for ev in bd_ev for l in range(L))
 
     # ---- e2e: every layer's document KV from pinned host memory, results back
     e2e = None
@@ -781,7 +814,7 @@ def run_ml(args, world, rank, local):
     d, V = sh.hidden, sh.vocab
     gu_bytes = 2.0 * d * 2 * I + 2.0 * rows * d + 4.0 * rows * I
     gu_flops = 2.0 * rows * d * 2 * I
-    t_gu = span_ms["gate_up"] / 1e3
+    t_gu = gate_up_ms / 1e3
     if gu_bytes / (peaks["hbm_gbs"] * 1e9) >= gu_flops / (peaks["bf16_tflops"] * 1e12):
         achieved = gu_bytes / t_gu / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -792,7 +825,7 @@ def run_ml(args, world, rank, local):
                     "frac": achieved / peaks["bf16_tflops"], "peak_kind": f"bf16 burst ({peaks['source']})"}
     roofline.update({"traffic": recorded_traffic(mw.name, rows, "gate_up_gemm_traffic.json"),
                      "kernel": "umma_gemm_kernel<EpiSwiGLU> (gate|up, split A, SwiGLU epilogue)",
-                     "gate_up_ms": span_ms["gate_up"], "algorithmic_bytes": gu_bytes,
+                     "gate_up_ms": gate_up_ms, "algorithmic_bytes": gu_bytes,
                      "algorithmic_flops": gu_flops,
                      "issued_tflops": 2 * gu_flops / t_gu / 1e12,
                      "note": "A is a two-term bf16 split, so the issued MMA work is twice the algorithmic FLOPs"})
@@ -910,9 +943,10 @@ def run_shortlist(args, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    hs = Q.STAGES.index("head")  # only the roofline kernel's events inside the timed loop
     start.record(stream)
     for k in range(steps):
-        Q.set_stage_events(stage_ev[k])
+        Q.set_stage_events([None] * (2 * hs) + stage_ev[k][2 * hs: 2 * hs + 2])
         step()
     end.record(stream)
     torch.cuda.synchronize()
@@ -923,8 +957,16 @@ def run_shortlist(args, world, rank, local):
     elapsed_ms = max_over_ranks(world, start.elapsed_time(end))
     ms_per_step = elapsed_ms / steps
     value = N * world * steps / (elapsed_ms / 1e3)
+    head_ms = statistics.mean(ev[2 * hs].elapsed_time(ev[2 * hs + 1]) for ev in stage_ev)
+    bd_ev = stage_ev[:min(steps, 50)]  # stage breakdown, after the timed region
+    torch.cuda.synchronize()
+    for evs in bd_ev:
+        Q.set_stage_events(evs)
+        step()
+    torch.cuda.synchronize()
+    Q.set_stage_events(None)
     names5 = ("prefix_pass_select_layout", "prologue_attention", "wo_norm", "head", "scoring")
-    stages_ms = {nm: statistics.mean(ev[2 * i].elapsed_time(ev[2 * i + 1]) for ev in stage_ev)
+    stages_ms = {nm: statistics.mean(ev[2 * i].elapsed_time(ev[2 * i + 1]) for ev in bd_ev)
                  for i, nm in enumerate(names5)}
 
     # rows of the second pass: real (the kept groups' rows) and padded
@@ -996,11 +1038,11 @@ def run_shortlist(args, world, rank, local):
     peaks = measured_peaks()
     d, V = w.shape.hidden, w.shape.vocab
     flops = 2.0 * d * V * real_rows
-    achieved = flops / (stages_ms["head"] / 1e3) / 1e12
+    achieved = flops / (head_ms / 1e3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"],
                 "traffic": recorded_traffic(sw.name, real_rows, "lm_head_gemm_shortlist_traffic.json"),
-                "kernel": "umma_gemm_kernel<EpiHead> (second pass)", "head_ms": stages_ms["head"],
+                "kernel": "umma_gemm_kernel<EpiHead> (second pass)", "head_ms": head_ms,
                 "real_rows": real_rows, "padded_rows": pad_rows,
                 "peak_kind": f"bf16 burst ({peaks['source']})",
                 "note": "FLOPs of the kept groups' rows; padding rows (copies of the root) are extra work"}

@@ -13,6 +13,7 @@
 #include <cfloat>
 
 #include "kernels.h"
+#include "launch.cuh"
 #include "quail_internal.h"
 #include "sm103.cuh"
 #include "attn_common.cuh"
@@ -57,6 +58,7 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
 constexpr int kTreeHeads = 4;
 
 __global__ void tree_part_kernel(AttnArgs a, RopeTable rt) {
+  grid_dependency_wait();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int G = a.hq / a.hkv;
@@ -175,6 +177,7 @@ __device__ __forceinline__ void store_o_split(bf16* out, int hq, size_t orow, in
 __global__ void __launch_bounds__(kAttnThreads, 3)
     attn_doc_kernel(AttnArgs a, RopeTable rt, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV) {
+  grid_dependency_wait();
   extern __shared__ uint8_t smem_raw[];
   const bool shared_rows = a.row_tile == 16;
   const int q_tiles = shared_rows ? 1 : kConsumerWarps;
@@ -539,6 +542,7 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
 // Block per output row (slot, node); warp per q head: merge the document
 // splits with the tree part, normalise, write bf16 O.
 __global__ void attn_combine_kernel(AttnArgs a) {
+  grid_dependency_wait();
   const int row = blockIdx.x;
   const int nq = a.map.nq;
   const int slot = row / nq, e = row % nq;
@@ -597,7 +601,7 @@ cudaError_t launch_tree_part(const AttnArgs& a, cudaStream_t st) {
   const long warps = static_cast<long>(a.n_nodes) * a.hkv * ((G + kTreeHeads - 1) / kTreeHeads);
   if (warps <= 0) return cudaSuccess;
   count_launch();
-  tree_part_kernel<<<static_cast<int>((warps * 32 + 255) / 256), 256, 0, st>>>(a, make_rope_table(a.theta));
+  { const cudaError_t le_ = launch_pdl(tree_part_kernel, dim3(static_cast<int>((warps * 32 + 255) / 256)), dim3(256), 0, st, a, make_rope_table(a.theta)); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 
@@ -618,7 +622,7 @@ cudaError_t launch_attn_doc(const AttnArgs& a, const CUtensorMap& tmK, const CUt
   if (grid.x == 0 || grid.z == 0) return cudaSuccess;
   const size_t smem = attn_smem_bytes(a.row_tile == 16 ? 1 : kConsumerWarps);
   count_launch();
-  attn_doc_kernel<<<grid, kAttnThreads, smem, st>>>(a, make_rope_table(a.theta), tmK, tmV);
+  { const cudaError_t le_ = launch_pdl(attn_doc_kernel, dim3(grid), dim3(kAttnThreads), smem, st, a, make_rope_table(a.theta), tmK, tmV); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 
@@ -627,7 +631,7 @@ cudaError_t launch_attn_combine(const AttnArgs& a, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   const int threads = (a.hq < 32 ? a.hq : 32) * 32;
   count_launch();
-  attn_combine_kernel<<<rows, threads, 0, st>>>(a);
+  { const cudaError_t le_ = launch_pdl(attn_combine_kernel, dim3(rows), dim3(threads), 0, st, a); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 

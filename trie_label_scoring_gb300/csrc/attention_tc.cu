@@ -24,6 +24,7 @@
 // softmax (lazy reference max, as in attention.cu), write P and finish rows.
 #include "attn_common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 #include "quail_internal.h"
 #include "sm103.cuh"
 
@@ -126,6 +127,7 @@ __device__ __forceinline__ void load_ring(uint8_t* ring, uint64_t* full, uint64_
 __global__ void __launch_bounds__(kTcThreads, 1)
     attn_doc_tc_kernel(AttnArgs a, RopeTable rt, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV) {
+  grid_dependency_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   TcBars* bars = reinterpret_cast<TcBars*>(base + kOffBar);
@@ -540,7 +542,7 @@ cudaError_t launch_attn_doc_tc(const AttnArgs& a, const CUtensorMap& tmK, const 
   dim3 grid(a.rows_pad / kTcRows, a.n_splits * a.hkv, a.n_slots);
   if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
   count_launch();
-  attn_doc_tc_kernel<<<grid, kTcThreads, kTcSmem, st>>>(a, make_rope_table(a.theta), tmK, tmV);
+  { const cudaError_t le_ = launch_pdl(attn_doc_tc_kernel, dim3(grid), dim3(kTcThreads), kTcSmem, st, a, make_rope_table(a.theta), tmK, tmV); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 

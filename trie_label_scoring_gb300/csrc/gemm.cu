@@ -141,21 +141,22 @@ cudaError_t launch_umma(const CUtensorMap& tmA, const BSet& bset, int M, int N, 
   if (grid <= 0) return cudaSuccess;
   if (CM == 1) {
     count_launch();
-    kern<<<grid, kGemmThreads, smem, st>>>(tmA, bset, M, N, nk, k_splits, epi, err, m_live);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kGemmThreads), smem, st, tmA, bset, M, N, nk, k_splits, epi, err, m_live);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = CM;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see launch.cuh
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   count_launch();
   return cudaLaunchKernelEx(&cfg, kern, tmA, bset, M, N, nk, k_splits, epi, err, m_live);
 }

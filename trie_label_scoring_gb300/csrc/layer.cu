@@ -5,6 +5,7 @@
 #include <cfloat>
 
 #include "kernels.h"
+#include "launch.cuh"
 #include "quail_internal.h"
 
 namespace quail {
@@ -57,6 +58,7 @@ __global__ void __launch_bounds__(kNormThreads) embed_rmsnorm_kernel(const bf16*
                                                                      const bf16* __restrict__ gain, float eps,
                                                                      bf16* __restrict__ out,
                                                                      const int* __restrict__ live) {
+  grid_dependency_wait();
   if (live != nullptr && static_cast<int>(blockIdx.x) >= *live) return;
   __shared__ float scratch[32];
   const int r = blockIdx.x;
@@ -92,6 +94,7 @@ __global__ void __launch_bounds__(kNormThreads) embed_rmsnorm_kernel(const bf16*
 __global__ void qk_head_norm_kernel(const float* __restrict__ part, int k_splits, size_t slab, float* qkv, int rows,
                                     int ld, int hq, int hkv, const bf16* __restrict__ gq,
                                     const bf16* __restrict__ gk, float eps, const int* __restrict__ live) {
+  grid_dependency_wait();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (live != nullptr) rows = min(rows, *live);
   const int lane = threadIdx.x & 31;
@@ -134,6 +137,7 @@ __global__ void __launch_bounds__(kNormThreads) final_norm_kernel(const float* _
                                                                   int d, const bf16* __restrict__ gain, float eps,
                                                                   bf16* __restrict__ z_bf16,
                                                                   float* __restrict__ z_f32) {
+  grid_dependency_wait();
   __shared__ float scratch[32];
   const int r = blockIdx.x;
   const int slot = r / map.nq;
@@ -187,6 +191,7 @@ __global__ void __launch_bounds__(kNormThreads) final_norm_kernel(const float* _
 // One warp per row: max over the tile partials, then the rescaled sum.
 __global__ void lse_reduce_kernel(const float2* __restrict__ part, int rows, int n_tiles, float* __restrict__ lse,
                                   const int* __restrict__ live) {
+  grid_dependency_wait();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= rows || (live != nullptr && warp >= *live)) return;
@@ -211,6 +216,7 @@ __global__ void lse_reduce_kernel(const float2* __restrict__ part, int rows, int
 //              + [prefix label] log(1 - sum_c exp(logit(end, c) - LSE(end)))
 //   prob = softmax over labels; argmax = lowest index of the maximum.
 __global__ void label_score_kernel(LabelScoreArgs a) {
+  grid_dependency_wait();
   __shared__ float s_max[32];
   __shared__ int s_arg[32];
   __shared__ float s_sum[32];
@@ -293,6 +299,7 @@ __global__ void label_score_kernel(LabelScoreArgs a) {
 // label_softmax_kernel (CTA per document).
 constexpr int kLabelsPerCta = 64;
 __global__ void label_logscore_kernel(LabelScoreArgs a) {
+  grid_dependency_wait();
   const int doc = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const float* cl = a.child_logit + static_cast<size_t>(doc) * a.n_child;
@@ -317,6 +324,7 @@ __global__ void label_logscore_kernel(LabelScoreArgs a) {
 }
 
 __global__ void label_softmax_kernel(LabelScoreArgs a) {
+  grid_dependency_wait();
   __shared__ float s_max[32];
   __shared__ int s_arg[32];
   __shared__ float s_sum[32];
@@ -375,6 +383,7 @@ __global__ void label_softmax_kernel(LabelScoreArgs a) {
 __global__ void join_head_kernel(const float* __restrict__ z, const bf16* __restrict__ lm_head,
                                  const int* __restrict__ tokens, int n_true, int R, int M, int d,
                                  float* __restrict__ p_true) {
+  grid_dependency_wait();
   __shared__ float s_logit[kJoinMaxRows];
   const int row = blockIdx.x;  // anchor * M + partner
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -408,6 +417,7 @@ __global__ void join_head_kernel(const float* __restrict__ z, const bf16* __rest
 // 16-byte weight loads; 8 tokens per CTA, documents along y.
 __global__ void restricted_logits_kernel(const float* __restrict__ z, const bf16* __restrict__ lm_head,
                                          const int* __restrict__ tokens, int M, int d, float* __restrict__ logits) {
+  grid_dependency_wait();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int m = blockIdx.x * (blockDim.x >> 5) + warp;
   const int doc = blockIdx.y;
@@ -431,6 +441,7 @@ __global__ void restricted_logits_kernel(const float* __restrict__ z, const bf16
 // log-softmax and softmax over the M entries, argmax (lowest index of the max).
 __global__ void letters_softmax_kernel(int M, float* __restrict__ logprob, float* __restrict__ prob,
                                        int* __restrict__ argmax) {
+  grid_dependency_wait();
   extern __shared__ float s_logit[];
   __shared__ float s_red[32];
   const int doc = blockIdx.x;
@@ -478,6 +489,7 @@ __device__ __forceinline__ int settle(const DecodeTrie& t, int u) {
 // that still need the model into slots (in document order).
 __global__ void decode_prepare_kernel(DecodeTrie t, int num_docs, int* node_cursor, int* label_out, int* slot_doc,
                                       int* slot_node, int* n_slots, int* active_count) {
+  grid_dependency_wait();
   __shared__ int s_warp[32];
   __shared__ int s_base;
   if (threadIdx.x == 0) {
@@ -529,6 +541,7 @@ __global__ void decode_prepare_kernel(DecodeTrie t, int num_docs, int* node_curs
 __global__ void decode_select_kernel(DecodeTrie t, const float* __restrict__ z, const bf16* __restrict__ lm_head,
                                      int d, const int* __restrict__ slot_doc, const int* __restrict__ n_slots,
                                      int* node_cursor, int* label_out, int* active_count, uint8_t* touched) {
+  grid_dependency_wait();
   __shared__ float scratch[32];
   const int slot = blockIdx.x;
   if (slot >= *n_slots) return;
@@ -566,7 +579,7 @@ cudaError_t launch_embed_rmsnorm(const bf16* embed, const int* tokens, int n, in
                                  bf16* out, cudaStream_t st, const int* live) {
   if (n <= 0) return cudaSuccess;
   count_launch();
-  embed_rmsnorm_kernel<<<n, kNormThreads, 0, st>>>(embed, tokens, d, gain, eps, out, live);
+  { const cudaError_t le_ = launch_pdl(embed_rmsnorm_kernel, dim3(n), dim3(kNormThreads), 0, st, embed, tokens, d, gain, eps, out, live); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 
@@ -577,7 +590,7 @@ cudaError_t launch_qk_head_norm(const float* part, int k_splits, size_t slab, fl
   if (k_splits < 1 || k_splits > 8) return cudaErrorInvalidValue;  // the kernel sums at most 8 slabs
   const int blocks = static_cast<int>((warps * 32 + 255) / 256);
   count_launch();
-  qk_head_norm_kernel<<<blocks, 256, 0, st>>>(part, k_splits, slab, qkv, rows, ld, hq, hkv, gq, gk, eps, live);
+  { const cudaError_t le_ = launch_pdl(qk_head_norm_kernel, dim3(blocks), dim3(256), 0, st, part, k_splits, slab, qkv, rows, ld, hq, hkv, gq, gk, eps, live); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 
@@ -589,8 +602,8 @@ cudaError_t launch_final_norm(const float* h_part, int k_splits, size_t slab, co
 #define QUAIL_FINAL_NORM(KS)                                                                                    \
   case KS:                                                                                                      \
     count_launch();                                                                                          \
-    final_norm_kernel<KS><<<rows, kNormThreads, 0, st>>>(h_part, slab, embed, node_token, map, d, gain, eps, \
-                                                         z_bf16, z_f32);                                       \
+    { const cudaError_t le_ = launch_pdl(final_norm_kernel<KS>, dim3(rows), dim3(kNormThreads), 0, st, h_part, slab, embed, node_token, map, d, gain, eps, \
+                                                         z_bf16, z_f32); if (le_ != cudaSuccess) return le_; }                                       \
     break;
     QUAIL_FINAL_NORM(1)
     QUAIL_FINAL_NORM(2)
@@ -611,7 +624,7 @@ cudaError_t launch_lse_reduce(const float2* lse_part, int rows, int n_tiles, flo
                               const int* live) {
   if (rows <= 0) return cudaSuccess;
   count_launch();
-  lse_reduce_kernel<<<(rows * 32 + 255) / 256, 256, 0, st>>>(lse_part, rows, n_tiles, lse, live);
+  { const cudaError_t le_ = launch_pdl(lse_reduce_kernel, dim3((rows * 32 + 255) / 256), dim3(256), 0, st, lse_part, rows, n_tiles, lse, live); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 
@@ -619,17 +632,17 @@ cudaError_t launch_label_score(const LabelScoreArgs& args, int num_docs, int num
   if (num_docs <= 0) return cudaSuccess;
   if (num_docs >= num_sms) {  // enough documents to fill the GPU with one CTA each
     count_launch();
-    label_score_kernel<<<num_docs, 256, 0, st>>>(args);
+    { const cudaError_t le_ = launch_pdl(label_score_kernel, dim3(num_docs), dim3(256), 0, st, args); if (le_ != cudaSuccess) return le_; }
     return cudaGetLastError();
   }
   cudaError_t e = launch_lse_reduce(args.lse_part, num_docs * args.a, args.n_tiles, args.lse, st);
   if (e != cudaSuccess) return e;
   count_launch();
-  label_logscore_kernel<<<dim3(num_docs, (args.M + kLabelsPerCta - 1) / kLabelsPerCta), 256, 0, st>>>(args);
+  { const cudaError_t le_ = launch_pdl(label_logscore_kernel, dim3(dim3(num_docs, (args.M + kLabelsPerCta - 1) / kLabelsPerCta)), dim3(256), 0, st, args); if (le_ != cudaSuccess) return le_; }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   count_launch();
-  label_softmax_kernel<<<num_docs, 512, 0, st>>>(args);
+  { const cudaError_t le_ = launch_pdl(label_softmax_kernel, dim3(num_docs), dim3(512), 0, st, args); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 
@@ -638,7 +651,7 @@ cudaError_t launch_join_head(const float* z, const bf16* lm_head, const int* tok
   if (rows <= 0) return cudaSuccess;
   if (R < 1 || R > kJoinMaxRows || n_true < 0 || n_true > R) return cudaErrorInvalidValue;
   count_launch();
-  join_head_kernel<<<rows, 256, 0, st>>>(z, lm_head, tokens, n_true, R, M, d, p_true);
+  { const cudaError_t le_ = launch_pdl(join_head_kernel, dim3(rows), dim3(256), 0, st, z, lm_head, tokens, n_true, R, M, d, p_true); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 
@@ -647,7 +660,7 @@ cudaError_t launch_restricted_logits(const float* z, const bf16* lm_head, const 
   if (num_docs <= 0 || M <= 0) return cudaSuccess;
   if (d % 8 != 0 || num_docs > 65535) return cudaErrorInvalidValue;
   count_launch();
-  restricted_logits_kernel<<<dim3((M + 7) / 8, num_docs), 256, 0, st>>>(z, lm_head, tokens, M, d, logits);
+  { const cudaError_t le_ = launch_pdl(restricted_logits_kernel, dim3(dim3((M + 7) / 8, num_docs)), dim3(256), 0, st, z, lm_head, tokens, M, d, logits); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 
@@ -657,15 +670,15 @@ cudaError_t launch_letters_head(const float* z, const bf16* lm_head, const int* 
   cudaError_t e = launch_restricted_logits(z, lm_head, letter_tokens, M, num_docs, d, logprob, st);
   if (e != cudaSuccess) return e;
   count_launch();
-  letters_softmax_kernel<<<num_docs, 256, M * sizeof(float), st>>>(M, logprob, prob, argmax);
+  { const cudaError_t le_ = launch_pdl(letters_softmax_kernel, dim3(num_docs), dim3(256), M * sizeof(float), st, M, logprob, prob, argmax); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 
 cudaError_t launch_decode_prepare(DecodeTrie t, int num_docs, int* node_cursor, int* label_out, int* slot_doc,
                                   int* slot_node, int* n_slots, int* active_count, cudaStream_t st) {
   count_launch();
-  decode_prepare_kernel<<<1, 1024, 0, st>>>(t, num_docs, node_cursor, label_out, slot_doc, slot_node, n_slots,
-                                            active_count);
+  { const cudaError_t le_ = launch_pdl(decode_prepare_kernel, dim3(1), dim3(1024), 0, st, t, num_docs, node_cursor, label_out, slot_doc, slot_node, n_slots,
+                                            active_count); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 
@@ -674,8 +687,8 @@ cudaError_t launch_decode_select(DecodeTrie t, const float* z, const bf16* lm_he
                                  int* active_count, uint8_t* touched, cudaStream_t st) {
   if (num_docs <= 0) return cudaSuccess;
   count_launch();
-  decode_select_kernel<<<num_docs, 256, 0, st>>>(t, z, lm_head, d, slot_doc, n_slots, node_cursor, label_out,
-                                                 active_count, touched);
+  { const cudaError_t le_ = launch_pdl(decode_select_kernel, dim3(num_docs), dim3(256), 0, st, t, z, lm_head, d, slot_doc, n_slots, node_cursor, label_out,
+                                                 active_count, touched); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 

@@ -9,6 +9,7 @@
 #include <algorithm>
 
 #include "kernels.h"
+#include "launch.cuh"
 #include "quail_internal.h"
 
 namespace quail {
@@ -52,6 +53,7 @@ __device__ __forceinline__ void split4(float4 y, uint2* hi, uint2* lo) {
 // h[r] = E[tokens[r]] (fp32).
 __global__ void gather_embed_kernel(const bf16* __restrict__ embed, const int* __restrict__ tokens, int d,
                                     float* __restrict__ h) {
+  grid_dependency_wait();
   const int r = blockIdx.x;
   const uint2* e = reinterpret_cast<const uint2*>(embed + static_cast<size_t>(__ldg(tokens + r)) * d);
   float4* out = reinterpret_cast<float4*>(h + static_cast<size_t>(r) * d);
@@ -66,6 +68,7 @@ __global__ void __launch_bounds__(kRowThreads) residual_norm_kernel(float* __res
                                                                      const float* __restrict__ part, size_t slab,
                                                                      int d, const bf16* __restrict__ gain, float eps,
                                                                      bf16* __restrict__ out) {
+  grid_dependency_wait();
   __shared__ float scratch[32];
   const int r = blockIdx.x;
   float4* hr = reinterpret_cast<float4*>(h + static_cast<size_t>(r) * d);
@@ -116,6 +119,7 @@ __device__ __forceinline__ float silu(float g) { return g / (1.f + expf(-g)); }
 template <int KS>
 __global__ void silu_mul_split_kernel(const float* __restrict__ part, size_t slab, int rows, int I,
                                       bf16* __restrict__ act) {
+  grid_dependency_wait();
   const int iv = I >> 2;
   const size_t n = static_cast<size_t>(rows) * iv;
   const size_t slab4 = slab >> 2;
@@ -151,6 +155,7 @@ __global__ void silu_mul_split_kernel(const float* __restrict__ part, size_t sla
 __global__ void __launch_bounds__(kRowThreads) norm_out_kernel(const float* __restrict__ h, int d,
                                                                 const bf16* __restrict__ gain, float eps,
                                                                 bf16* __restrict__ z, float* __restrict__ z_f32) {
+  grid_dependency_wait();
   __shared__ float scratch[32];
   const int r = blockIdx.x;
   const float4* hr = reinterpret_cast<const float4*>(h + static_cast<size_t>(r) * d);
@@ -183,7 +188,7 @@ __global__ void __launch_bounds__(kRowThreads) norm_out_kernel(const float* __re
 cudaError_t launch_gather_embed(const bf16* embed, const int* tokens, int rows, int d, float* h, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   count_launch();
-  gather_embed_kernel<<<rows, kRowThreads, 0, st>>>(embed, tokens, d, h);
+  { const cudaError_t le_ = launch_pdl(gather_embed_kernel, dim3(rows), dim3(kRowThreads), 0, st, embed, tokens, d, h); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 
@@ -195,7 +200,7 @@ cudaError_t launch_residual_norm(float* h, const float* part, int ks, size_t sla
 #define QUAIL_RESIDUAL_NORM(KS)                                                                   \
   case KS:                                                                                        \
     count_launch();                                                                               \
-    residual_norm_kernel<KS><<<rows, kRowThreads, 0, st>>>(h, part, slab, d, gain, eps, out);     \
+    { const cudaError_t le_ = launch_pdl(residual_norm_kernel<KS>, dim3(rows), dim3(kRowThreads), 0, st, h, part, slab, d, gain, eps, out); if (le_ != cudaSuccess) return le_; }     \
     break;
     QUAIL_RESIDUAL_NORM(0)
     QUAIL_RESIDUAL_NORM(1)
@@ -223,7 +228,7 @@ cudaError_t launch_silu_mul_split(const float* part, int ks, size_t slab, int ro
 #define QUAIL_SILU_MUL(KS)                                                                 \
   case KS:                                                                                 \
     count_launch();                                                                        \
-    silu_mul_split_kernel<KS><<<blocks, kRowThreads, 0, st>>>(part, slab, rows, I, act);   \
+    { const cudaError_t le_ = launch_pdl(silu_mul_split_kernel<KS>, dim3(blocks), dim3(kRowThreads), 0, st, part, slab, rows, I, act); if (le_ != cudaSuccess) return le_; }   \
     break;
     QUAIL_SILU_MUL(1)
     QUAIL_SILU_MUL(2)
@@ -244,7 +249,7 @@ cudaError_t launch_norm_out(const float* h, int rows, int d, const bf16* gain, f
                             cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   count_launch();
-  norm_out_kernel<<<rows, kRowThreads, 0, st>>>(h, d, gain, eps, z, z_f32);
+  { const cudaError_t le_ = launch_pdl(norm_out_kernel, dim3(rows), dim3(kRowThreads), 0, st, h, d, gain, eps, z, z_f32); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 

@@ -10,6 +10,7 @@
 #include <cfloat>
 
 #include "kernels.h"
+#include "launch.cuh"
 #include "quail_internal.h"
 
 namespace quail {
@@ -74,6 +75,7 @@ __device__ float block_sum_f(float v, float* s) {
 // previous pick (so no group is taken twice and no mark table is needed).
 __global__ void __launch_bounds__(kSelectThreads) shortlist_select_kernel(const float* __restrict__ ls, int G, int B,
                                                                           int* __restrict__ sel) {
+  grid_dependency_wait();
   __shared__ float s_v[32];
   __shared__ int s_i[32];
   const int doc = blockIdx.x;
@@ -105,6 +107,7 @@ __global__ void shortlist_child_logprob_kernel(ShortlistTables T, const int* __r
                                                const int* __restrict__ block_base, const float* __restrict__ z32,
                                                const bf16* __restrict__ lm_head, int d, const float* __restrict__ lse,
                                                float* __restrict__ clp) {
+  grid_dependency_wait();
   const int lane = threadIdx.x & 31;
   const long long total = static_cast<long long>(n_blocks) * T.max_children;
   for (long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < total;
@@ -141,6 +144,7 @@ __global__ void __launch_bounds__(1024) shortlist_scan_kernel(ShortlistTables T,
                                                               int num_docs, int B, int* __restrict__ block_base,
                                                               int* __restrict__ doc_base, int* __restrict__ doc_rows,
                                                               int* __restrict__ count) {
+  grid_dependency_wait();
   __shared__ int s_part[1024];
   __shared__ int s_total;
   const int n_blocks = num_docs * B;
@@ -183,6 +187,7 @@ __global__ void shortlist_expand_kernel(ShortlistTables T, const int* __restrict
                                         const int* __restrict__ eval_depth, int* __restrict__ row_token,
                                         int* __restrict__ row_depth, int* __restrict__ row_parent,
                                         int* __restrict__ padded_of) {
+  grid_dependency_wait();
   const int blk = blockIdx.x;
   if (blk == static_cast<int>(gridDim.x) - 1) {
     for (int c = *count + threadIdx.x; c < R; c += blockDim.x) {
@@ -212,6 +217,7 @@ __global__ void shortlist_expand_kernel(ShortlistTables T, const int* __restrict
 // Block per compact row c < *count: 16-byte copies of row padded_of[c].
 __global__ void gather_rows_kernel(const uint4* __restrict__ src, const int* __restrict__ padded_of,
                                    const int* __restrict__ count, int vec_per_row, uint4* __restrict__ dst) {
+  grid_dependency_wait();
   const int c = blockIdx.x;
   if (c >= *count) return;
   const uint4* s = src + static_cast<size_t>(padded_of[c]) * vec_per_row;
@@ -221,6 +227,7 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ src, const int* __r
 
 // Every label's score -inf and probability 0 (the kept ones are overwritten next).
 __global__ void shortlist_clear_kernel(float* __restrict__ logscore, float* __restrict__ prob, size_t n) {
+  grid_dependency_wait();
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
     logscore[i] = -INFINITY;
@@ -233,6 +240,7 @@ __global__ void shortlist_clear_kernel(float* __restrict__ logscore, float* __re
 __global__ void __launch_bounds__(kScoreThreads) shortlist_label_score_kernel(
     ShortlistTables T, const int* __restrict__ sel, int B, int M, const float* __restrict__ clp,
     float* __restrict__ logscore) {
+  grid_dependency_wait();
   const int doc = blockIdx.x, b = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int blk = doc * B + b;
@@ -262,6 +270,7 @@ __global__ void __launch_bounds__(kScoreThreads) shortlist_softmax_kernel(Shortl
                                                                           const float* __restrict__ logscore,
                                                                           float* __restrict__ prob,
                                                                           int* __restrict__ argmax) {
+  grid_dependency_wait();
   __shared__ float s_v[32];
   __shared__ int s_i[32];
   const int doc = blockIdx.x;
@@ -305,7 +314,7 @@ cudaError_t launch_shortlist_select(const float* prefix_logscore, int num_docs, 
   if (num_docs <= 0) return cudaSuccess;
   if (B < 1 || B > G) return cudaErrorInvalidValue;
   count_launch();
-  shortlist_select_kernel<<<num_docs, kSelectThreads, 0, st>>>(prefix_logscore, G, B, sel);
+  { const cudaError_t le_ = launch_pdl(shortlist_select_kernel, dim3(num_docs), dim3(kSelectThreads), 0, st, prefix_logscore, G, B, sel); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 
@@ -313,7 +322,7 @@ cudaError_t launch_shortlist_scan(const ShortlistTables& T, const int* sel, int 
                                   int* doc_base, int* doc_rows, int* count, cudaStream_t st) {
   if (num_docs <= 0) return cudaSuccess;
   count_launch();
-  shortlist_scan_kernel<<<1, 1024, 0, st>>>(T, sel, num_docs, B, block_base, doc_base, doc_rows, count);
+  { const cudaError_t le_ = launch_pdl(shortlist_scan_kernel, dim3(1), dim3(1024), 0, st, T, sel, num_docs, B, block_base, doc_base, doc_rows, count); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 
@@ -323,9 +332,9 @@ cudaError_t launch_shortlist_expand(const ShortlistTables& T, const int* sel, in
                                     int* row_parent, int* padded_of, cudaStream_t st) {
   if (num_docs <= 0) return cudaSuccess;
   count_launch();
-  shortlist_expand_kernel<<<num_docs * B + 1, 128, 0, st>>>(T, sel, B, Bq, R, block_base, doc_base, count,
+  { const cudaError_t le_ = launch_pdl(shortlist_expand_kernel, dim3(num_docs * B + 1), dim3(128), 0, st, T, sel, B, Bq, R, block_base, doc_base, count,
                                                             eval_token, eval_depth, row_token, row_depth, row_parent,
-                                                            padded_of);
+                                                            padded_of); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 
@@ -334,8 +343,8 @@ cudaError_t launch_gather_rows(const void* src, const int* padded_of, const int*
   if (max_rows <= 0) return cudaSuccess;
   if (row_bytes % 16 != 0) return cudaErrorInvalidValue;
   count_launch();
-  gather_rows_kernel<<<max_rows, 256, 0, st>>>(static_cast<const uint4*>(src), padded_of, count,
-                                               static_cast<int>(row_bytes / 16), static_cast<uint4*>(dst));
+  { const cudaError_t le_ = launch_pdl(gather_rows_kernel, dim3(max_rows), dim3(256), 0, st, static_cast<const uint4*>(src), padded_of, count,
+                                               static_cast<int>(row_bytes / 16), static_cast<uint4*>(dst)); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 
@@ -347,8 +356,8 @@ cudaError_t launch_shortlist_child_logprob(const ShortlistTables& T, const int* 
   const long long warps = static_cast<long long>(num_docs) * B * T.max_children;
   const int blocks = static_cast<int>(std::min<long long>((warps + 7) / 8, 1 << 16));
   count_launch();
-  shortlist_child_logprob_kernel<<<blocks, 256, 0, st>>>(T, sel, num_docs * B, block_base, z32, lm_head, d, lse,
-                                                         clp);
+  { const cudaError_t le_ = launch_pdl(shortlist_child_logprob_kernel, dim3(blocks), dim3(256), 0, st, T, sel, num_docs * B, block_base, z32, lm_head, d, lse,
+                                                         clp); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 
@@ -359,15 +368,15 @@ cudaError_t launch_shortlist_label_score(const ShortlistTables& T, const int* se
   if (B > 65535) return cudaErrorInvalidValue;
   const size_t n = static_cast<size_t>(num_docs) * M;
   count_launch();
-  shortlist_clear_kernel<<<static_cast<int>(std::min<size_t>((n + 255) / 256, 4096)), 256, 0, st>>>(logscore, prob, n);
+  { const cudaError_t le_ = launch_pdl(shortlist_clear_kernel, dim3(static_cast<int>(std::min<size_t>((n + 255) / 256, 4096))), dim3(256), 0, st, logscore, prob, n); if (le_ != cudaSuccess) return le_; }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   count_launch();
-  shortlist_label_score_kernel<<<dim3(num_docs, B), kScoreThreads, 0, st>>>(T, sel, B, M, clp, logscore);
+  { const cudaError_t le_ = launch_pdl(shortlist_label_score_kernel, dim3(dim3(num_docs, B)), dim3(kScoreThreads), 0, st, T, sel, B, M, clp, logscore); if (le_ != cudaSuccess) return le_; }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   count_launch();
-  shortlist_softmax_kernel<<<num_docs, kScoreThreads, 0, st>>>(T, sel, B, M, logscore, prob, argmax);
+  { const cudaError_t le_ = launch_pdl(shortlist_softmax_kernel, dim3(num_docs), dim3(kScoreThreads), 0, st, T, sel, B, M, logscore, prob, argmax); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
 }
 

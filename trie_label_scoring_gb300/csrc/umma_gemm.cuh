@@ -31,6 +31,7 @@
 // from L2 for the other M tiles.
 #pragma once
 #include "sm103.cuh"
+#include "launch.cuh"
 #include "quail_internal.h"
 
 namespace quail {
@@ -136,11 +137,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int M_eff = m_live != nullptr ? min(M, max(*m_live, 0)) : M;
-  const int m_tiles = (M_eff + kGemmBM - 1) / kGemmBM;
-  const int m_tiles_s = (m_tiles + CM - 1) / CM * CM;  // scheduled M tiles: whole pairs
-  const int n_tiles = (N + BN - 1) / BN;
-  const int num_units = m_tiles_s * n_tiles * k_splits;
   const uint32_t crank = CM == 2 ? cluster_ctarank() : 0u;
 
   if (threadIdx.x == 0) {
@@ -166,6 +162,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (CM == 2) cluster_sync();  // the peer's barriers exist before any multicast reaches them
+  // Everything above touched shared memory, TMEM and the kernel parameters
+  // only; from here on the previous kernel's outputs are read.
+  grid_dependency_wait();
+  const int M_eff = m_live != nullptr ? min(M, max(*m_live, 0)) : M;
+  const int m_tiles = (M_eff + kGemmBM - 1) / kGemmBM;
+  const int m_tiles_s = (m_tiles + CM - 1) / CM * CM;  // scheduled M tiles: whole pairs
+  const int n_tiles = (N + BN - 1) / BN;
+  const int num_units = m_tiles_s * n_tiles * k_splits;
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
