@@ -575,9 +575,10 @@ def run_join(args, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ai = Q.STAGES.index("attention")  # only the roofline kernel's events inside the timed loop
     start.record(stream)
     for k in range(steps):
-        Q.set_stage_events(stage_ev[k])
+        Q.set_stage_events([None] * (2 * ai) + stage_ev[k][2 * ai: 2 * ai + 2])
         step()
     end.record(stream)
     torch.cuda.synchronize()
@@ -586,7 +587,14 @@ def run_join(args, world, rank, local):
     Q.set_stage_events(None)
     Q.device_status()
     elapsed_ms = max_over_ranks(world, start.elapsed_time(end))
-    stages_ms = {name: statistics.mean(ev[2 * i].elapsed_time(ev[2 * i + 1]) for ev in stage_ev)
+    attention_ms = statistics.mean(ev[2 * ai].elapsed_time(ev[2 * ai + 1]) for ev in stage_ev)
+    bd_ev = stage_ev[:min(steps, 20)]  # stage breakdown, after the timed region
+    for evs in bd_ev:
+        Q.set_stage_events(evs)
+        step()
+    torch.cuda.synchronize()
+    Q.set_stage_events(None)
+    stages_ms = {name: statistics.mean(ev[2 * i].elapsed_time(ev[2 * i + 1]) for ev in bd_ev)
                  for i, name in enumerate(Q.STAGES[:4])}
     ms_per_step = elapsed_ms / steps
     pairs = N * M
@@ -596,11 +604,11 @@ def run_join(args, world, rank, local):
     keys = float(docs.doc_len.sum())
     attn_flops = 4.0 * 128 * keys * w.shape.n_kv_heads * G * M
     peaks = measured_peaks()
-    achieved = attn_flops / (stages_ms["attention"] / 1e3) / 1e12
+    achieved = attn_flops / (attention_ms / 1e3) / 1e12
     kv_bytes = keys * w.shape.n_kv_heads * 128 * 2 * 2
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"], "traffic": None, "kernel": "attn_doc_tc_kernel",
-                "attention_ms": stages_ms["attention"], "peak_kind": f"bf16 burst ({peaks['source']})",
+                "attention_ms": attention_ms, "peak_kind": f"bf16 burst ({peaks['source']})",
                 "note": "FLOPs counted once per query row (the hi/lo splits double the issued work)"}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -1090,9 +1098,11 @@ def run_shortlist(args, world, rank, local):
         print(json.dumps(out), flush=True)
 
 
-def _timed_loop(stream, steps, world, call, n_stage_events=0):
+def _timed_loop(stream, steps, world, call, n_stage_events=0, keep=None):
     """K calls between CUDA events on `stream`, barrier + synchronize on both
-    sides; per-call stage events when n_stage_events > 0. Returns
+    sides; per-call stage events when n_stage_events > 0, of which only the
+    indices in `keep` are handed to the library when given (an event between
+    two kernels keeps the second from launching early). Returns
     (elapsed ms, stage events per call, clocks)."""
     import torch
 
@@ -1110,7 +1120,8 @@ def _timed_loop(stream, steps, world, call, n_stage_events=0):
     start.record(stream)
     for k in range(steps):
         if n_stage_events:
-            Q.set_stage_events(stage_ev[k])
+            evs = stage_ev[k]
+            Q.set_stage_events(evs if keep is None else [e if i in keep else None for i, e in enumerate(evs)])
         call()
     end.record(stream)
     torch.cuda.synchronize()
@@ -1157,13 +1168,21 @@ def run_letters(args, world, rank, local):
     Q.device_status()
     launches = Q.launch_count()
     steps = args.steps if args.steps is not None else 200
-    elapsed_ms, stage_ev, clk = _timed_loop(stream, steps, world, step, 10)
-    stages_ms = {name: statistics.mean(ev[2 * i].elapsed_time(ev[2 * i + 1]) for ev in stage_ev)
+    ai = Q.STAGES.index("attention")
+    elapsed_ms, stage_ev, clk = _timed_loop(stream, steps, world, step, 10, keep=(2 * ai, 2 * ai + 1))
+    attention_ms = statistics.mean(ev[2 * ai].elapsed_time(ev[2 * ai + 1]) for ev in stage_ev)
+    bd_ev = stage_ev[:min(steps, 20)]  # stage breakdown, after the timed region
+    for evs in bd_ev:
+        Q.set_stage_events(evs)
+        step()
+    torch.cuda.synchronize()
+    Q.set_stage_events(None)
+    stages_ms = {name: statistics.mean(ev[2 * i].elapsed_time(ev[2 * i + 1]) for ev in bd_ev)
                  for i, name in enumerate(Q.STAGES[:4])}
     ms = elapsed_ms / steps
     peaks = measured_peaks()
     kv_bytes = float(docs.doc_len.sum()) * w.shape.n_kv_heads * w.shape.head_dim * 2 * 2
-    att = kv_bytes / (stages_ms["attention"] / 1e3) / 1e9
+    att = kv_bytes / (attention_ms / 1e3) / 1e9
     t_kv = kv_bytes / (peaks["hbm_gbs"] * 1e9)
     if rank == 0:
         out = {
@@ -1176,7 +1195,7 @@ def run_letters(args, world, rank, local):
                        "parallelism": f"replicas x{world} (documents sharded, no collective)"},
             "roofline": {"bound": "hbm", "achieved": att, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": att / peaks["hbm_gbs"], "traffic": None, "kernel": "doc attention (one row per document)",
-                         "attention_ms": stages_ms["attention"], "peak_kind": f"HBM copy ({peaks['source']})"},
+                         "attention_ms": attention_ms, "peak_kind": f"HBM copy ({peaks['source']})"},
             "path_roofline": {"t_kv_us": t_kv * 1e6, "ms_per_step": ms, "frac": t_kv * 1e3 / ms},
             "stages_ms": stages_ms, "cpu_baseline": None, "e2e": None, "gpu_launches": launches * steps,
             "clocks": clk,
