@@ -189,7 +189,7 @@ AttnShape attn_shape(const quail_model_desc* m, int nq, int slots, int max_doc_l
     s.row_tile = 16;
     s.rows_pad = 16;
     const long items = static_cast<long>(slots) * m->n_kv_heads;
-    s.split_tokens = (items >= 6L * sms) ? std::min(whole, 4096) : std::min(whole, 512);
+    s.split_tokens = (items >= 3L * sms) ? std::min(whole, 4096) : std::min(whole, 512);
   } else {
     // Many rows: tcgen05 kernel on 128-row tiles, one CTA per SM. Split the
     // documents (in whole 128-key blocks) only as far as needed for about
