@@ -129,3 +129,47 @@ def test_workspace_size_positive_and_monotone():
     assert Q.workspace_size(m, t, 0, 32, 8192, Q.MODE_TRIE_DECODE) > 0
     with pytest.raises(Q.QuailError):
         Q.workspace_size(m, None, 0, 16, 1024, Q.MODE_TRIE_TREE)
+
+
+def _desc_only_model(sh):
+    desc = Q.ModelDesc(sh.hidden, sh.n_q_heads, sh.n_kv_heads, 128, sh.vocab, 1e-6, 1e6)
+    return type("M", (), {"desc": desc})()
+
+
+def test_shortlist_workspace_and_argument_errors():
+    """Host-side checks of the shortlist calls: workspace sizes grow with the
+    beam and the documents; a plan from another trie or a beam below 1 is
+    rejected before any device work."""
+    sh = S.QWEN3_4B
+    m = _desc_only_model(sh)
+    w = S.Workload("t", sh, 4, (64, 64), "tree", 300, (2, 6))
+    ls = S.make_labels(w, 0)
+    t = Q.Trie(ls.labels, ls.root_token, sh.vocab)
+    sl = Q.Shortlist(t, 1)
+    a = Q.workspace_size_shortlist(m, t, sl, 1, 16, 1024)
+    b = Q.workspace_size_shortlist(m, t, sl, 2, 16, 1024)
+    c = Q.workspace_size_shortlist(m, t, sl, 2, 64, 1024)
+    assert 0 < a < b < c
+    with pytest.raises(Q.QuailError):
+        Q.workspace_size_shortlist(m, t, sl, 0, 16, 1024)
+    other = Q.Trie(ls.labels[:-1], ls.root_token, sh.vocab)
+    with pytest.raises(Q.QuailError):
+        Q.workspace_size_shortlist(m, other, sl, 2, 16, 1024)
+    assert sl.num_groups == len(set(l[0] for l in ls.labels))
+
+
+def test_multilayer_workspace_grows_with_documents_and_layers():
+    sh = S.QWEN3_4B
+    ls = S.make_labels(S.WORKLOADS["qwen3-4b-support10-256docs"], 0)
+    t = Q.Trie(ls.labels, ls.root_token, sh.vocab, ls.continuation)
+
+    def model(n_layers):
+        lw = (Q.LayerWeights * n_layers)()
+        desc = Q.ModelMLDesc(sh.hidden, sh.n_q_heads, sh.n_kv_heads, 128, sh.vocab, 9728, n_layers, 1e-6, 1e6,
+                             None, None, None, lw)
+        return type("M", (), {"desc": desc})()
+
+    a = Q.workspace_size_ml(model(2), t, 16, 1024)
+    b = Q.workspace_size_ml(model(2), t, 64, 1024)
+    assert 0 < a < b
+    assert Q.workspace_size_ml(model(36), t, 64, 1024) == b  # activations are reused layer to layer
