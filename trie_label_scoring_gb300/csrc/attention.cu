@@ -138,9 +138,8 @@ __global__ void tree_part_kernel(AttnArgs a, RopeTable rt) {
 // ------------------------------------------------------------------ doc part
 // CTA = (split, kv head x row group, slot). Warp 4 streams the split's KV pages
 // (K and V of one KV head: 8 KB per page) into an 8-stage ring with TMA; warps
-// 0..3 run bf16 mma.sync on 16-row query tiles with an online softmax.
-// row_tile 16: all four warps share the 16 rows and take pages round-robin,
-// then merge; row_tile 64: each warp owns 16 rows and reads every page.
+// 0..3 run bf16 mma.sync on one 16-row query tile with an online softmax:
+// the four warps share the 16 rows, take pages round-robin, then merge.
 // The q fragments (RoPE at l_i + depth, two-term bf16 split) are built once
 // per CTA in shared memory in mma fragment order. With one split per
 // document the epilogue merges the tree part and writes O itself; otherwise
@@ -154,9 +153,7 @@ constexpr int kMaxSplitPagesV2 = 256;              // split_tokens <= 4096
 constexpr uint32_t kMergeBytes = kConsumerWarps * (16 * 128 + 32) * 4;
 constexpr uint32_t kRingBytes = kAttnStages * kPageBytes > kMergeBytes ? kAttnStages * kPageBytes : kMergeBytes;
 static_assert(kAttnStages % kConsumerWarps == 0, "each stage must belong to one consumer warp");
-__host__ __device__ constexpr size_t attn_smem_bytes(int q_tiles) {
-  return 1024 + kRingBytes + q_tiles * kQTileBytes + 2 * kAttnStages * 8 + 16 + kMaxSplitPagesV2 * 4;
-}
+constexpr size_t kAttnSmemBytes = 1024 + kRingBytes + kQTileBytes + 2 * kAttnStages * 8 + 16 + kMaxSplitPagesV2 * 4;
 
 __device__ __forceinline__ void mma_pair(float (&d0)[4], float (&d1)[4], const uint4& a, uint32_t b0, uint32_t b1,
                                          uint32_t b2, uint32_t b3) {
@@ -179,11 +176,9 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
                     const __grid_constant__ CUtensorMap tmV) {
   grid_dependency_wait();
   extern __shared__ uint8_t smem_raw[];
-  const bool shared_rows = a.row_tile == 16;
-  const int q_tiles = shared_rows ? 1 : kConsumerWarps;
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* s_q = base + kRingBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(s_q + q_tiles * kQTileBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(s_q + kQTileBytes);
   uint64_t* empty = full + kAttnStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kAttnStages);
   int* s_pages = reinterpret_cast<int*>(empty + kAttnStages) + 4;  // physical page of each split page
@@ -214,7 +209,7 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kAttnStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], shared_rows ? 1 : kConsumerWarps);
+      mbar_init(&empty[s], 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -271,63 +266,60 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
   const int t = threadIdx.x;  // 0..127
   const int gq = lane >> 2, tq = lane & 3;
 
-  // q fragments: item = (tile, row, pair j) -> rotated dims j and j + 64, split
+  // q fragments: item = (row, pair j) -> rotated dims j and j + 64, split
   // into hi/lo bf16 and scattered to their (ks, lane, register, half) slots.
   {
     uint16_t* sq16 = reinterpret_cast<uint16_t*>(s_q);
-    constexpr int kPer = 16 * 64 / (kConsumerWarps * 32);  // items per thread and q tile
-    for (int qt = 0; qt < q_tiles; ++qt) {
-      // all loads of this thread's items first (one memory round trip), then
-      // rotate, split and scatter
-      float x1[kPer], x2[kPer];
-      int pos[kPer];
+    constexpr int kPer = 16 * 64 / (kConsumerWarps * 32);  // items per thread
+    // all loads of this thread's items first (one memory round trip), then
+    // rotate, split and scatter
+    float x1[kPer], x2[kPer];
+    int pos[kPer];
 #pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        const int it = t + k * kConsumerWarps * 32;
-        const int r = it / 64, j = it % 64;
-        const int rr = rg * a.row_tile + qt * 16 + r;  // row within (slot, kv head)
-        x1[k] = x2[k] = 0.f;
-        pos[k] = -1;
-        if (rr < rows_per_kv) {
-          const int e = rr / G, hl = rr % G;
-          const int node = row_node(a.map, slot, e);
-          const float* q = a.qkv + static_cast<size_t>(node) * a.ldq + (g * G + hl) * 128;
-          x1[k] = q[j];
-          x2[k] = q[j + 64];
-          pos[k] = L + a.node_depth[node];
-        }
+    for (int k = 0; k < kPer; ++k) {
+      const int it = t + k * kConsumerWarps * 32;
+      const int r = it / 64, j = it % 64;
+      const int rr = rg * a.row_tile + r;  // row within (slot, kv head)
+      x1[k] = x2[k] = 0.f;
+      pos[k] = -1;
+      if (rr < rows_per_kv) {
+        const int e = rr / G, hl = rr % G;
+        const int node = row_node(a.map, slot, e);
+        const float* q = a.qkv + static_cast<size_t>(node) * a.ldq + (g * G + hl) * 128;
+        x1[k] = q[j];
+        x2[k] = q[j + 64];
+        pos[k] = L + a.node_depth[node];
       }
+    }
 #pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        const int it = t + k * kConsumerWarps * 32;
-        const int r = it / 64, j = it % 64;
-        float y0 = 0.f, y1 = 0.f;
-        if (pos[k] >= 0) {
-          float c, sn;
-          rope_cs(pos[k], rt.w[j], c, sn);
-          y0 = x1[k] * c - x2[k] * sn;
-          y1 = x2[k] * c + x1[k] * sn;
-        }
-        const int col = j % 16;
-        const int reg = (r >= 8 ? 1 : 0) + (col >= 8 ? 2 : 0);
-        const int ln = (r % 8) * 4 + (col % 8) / 2;
-        const int half = col & 1;
+    for (int k = 0; k < kPer; ++k) {
+      const int it = t + k * kConsumerWarps * 32;
+      const int r = it / 64, j = it % 64;
+      float y0 = 0.f, y1 = 0.f;
+      if (pos[k] >= 0) {
+        float c, sn;
+        rope_cs(pos[k], rt.w[j], c, sn);
+        y0 = x1[k] * c - x2[k] * sn;
+        y1 = x2[k] * c + x1[k] * sn;
+      }
+      const int col = j % 16;
+      const int reg = (r >= 8 ? 1 : 0) + (col >= 8 ? 2 : 0);
+      const int ln = (r % 8) * 4 + (col % 8) / 2;
+      const int half = col & 1;
 #pragma unroll
-        for (int w = 0; w < 2; ++w) {  // dims j (ks = j / 16) and j + 64 (ks + 4)
-          const float y = w ? y1 : y0;
-          const int ks = j / 16 + 4 * w;
-          const __nv_bfloat16 hb = __float2bfloat16(y);
-          const __nv_bfloat16 lb = __float2bfloat16(y - __bfloat162float(hb));
-          const int idx = (((qt * 8 + ks) * 2 + 0) * 32 + ln) * 8 + reg * 2 + half;  // in bf16 units
-          sq16[idx] = *reinterpret_cast<const uint16_t*>(&hb);
-          sq16[idx + 32 * 8] = *reinterpret_cast<const uint16_t*>(&lb);
-        }
+      for (int w = 0; w < 2; ++w) {  // dims j (ks = j / 16) and j + 64 (ks + 4)
+        const float y = w ? y1 : y0;
+        const int ks = j / 16 + 4 * w;
+        const __nv_bfloat16 hb = __float2bfloat16(y);
+        const __nv_bfloat16 lb = __float2bfloat16(y - __bfloat162float(hb));
+        const int idx = ((ks * 2 + 0) * 32 + ln) * 8 + reg * 2 + half;  // in bf16 units
+        sq16[idx] = *reinterpret_cast<const uint16_t*>(&hb);
+        sq16[idx + 32 * 8] = *reinterpret_cast<const uint16_t*>(&lb);
       }
     }
   }
   asm volatile("bar.sync 1, 128;" ::: "memory");
-  const int qtile = shared_rows ? 0 : warp;
-  const uint4* qf = reinterpret_cast<const uint4*>(s_q + qtile * kQTileBytes) + lane;  // [ks][hi/lo][lane]
+  const uint4* qf = reinterpret_cast<const uint4*>(s_q) + lane;  // [ks][hi/lo][lane]
 
   const float scale = kAttnLog2e * 0.08838834764831845f;
   float o[16][4];
@@ -335,9 +327,7 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
   for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
   float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
 
-  const int j0 = shared_rows ? warp : 0;
-  const int jstep = shared_rows ? kConsumerWarps : 1;
-  for (int j = j0; j < n_pages; j += jstep) {
+  for (int j = warp; j < n_pages; j += kConsumerWarps) {  // pages round-robin over the warps
     const int s = j % kAttnStages;
     // warp-uniform wait: the shuffles and __any_sync below need every lane
     if (!__all_sync(0xffffffffu, mbar_wait(&full[s], static_cast<uint32_t>((j / kAttnStages) & 1), abort_flag)))
@@ -448,36 +438,7 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
   const bool fused = a.n_splits == 1;
   const size_t part_row0 =
       ((static_cast<size_t>(slot) * a.hkv + g) * a.n_splits + split) * static_cast<size_t>(a.rows_pad);
-  if (!shared_rows) {
-    const int row_base = rg * a.row_tile + warp * 16;
-#pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-      const int r = row_base + gq + hr * 8;
-      if (!fused) {
-        float* dst = a.part_o + (part_row0 + r) * 128;
-#pragma unroll
-        for (int n = 0; n < 16; ++n)
-          *reinterpret_cast<float2*>(dst + n * 8 + tq * 2) = make_float2(o[n][hr * 2], o[n][hr * 2 + 1]);
-        if (tq == 0) a.part_ml[part_row0 + r] = make_float2(m_r[hr], l_r[hr]);
-      } else if (r < rows_per_kv) {
-        const int e = r / G, h = g * G + r % G;
-        const int node = row_node(a.map, slot, e);
-        const float2 tml = a.tree_ml[static_cast<size_t>(node) * a.hq + h];
-        const float M = fmaxf(m_r[hr], tml.x);
-        const float f1 = exp2f(m_r[hr] - M), f2 = exp2f(tml.x - M);
-        const float inv = 1.f / (f1 * l_r[hr] + f2 * tml.y);
-        const float* to = a.tree_o + (static_cast<size_t>(node) * a.hq + h) * 128;
-        const size_t orow = static_cast<size_t>(slot) * a.map.nq + e;
-#pragma unroll
-        for (int n = 0; n < 16; ++n) {
-          const int col = n * 8 + tq * 2;
-          const float2 tv = *reinterpret_cast<const float2*>(to + col);
-          store_o_split(a.out, a.hq, orow, h * 128 + col, (f1 * o[n][hr * 2] + f2 * tv.x) * inv,
-                        (f1 * o[n][hr * 2 + 1] + f2 * tv.y) * inv);
-        }
-      }
-    }
-  } else {
+  {
     // Merge the four warps' partial softmax states through the (now idle) page ring.
     asm volatile("bar.sync 1, 128;" ::: "memory");
     float* so = reinterpret_cast<float*>(base) + warp * (16 * 128 + 32);
@@ -612,7 +573,7 @@ cudaError_t launch_attn_doc(const AttnArgs& a, const CUtensorMap& tmK, const CUt
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
     e = cudaFuncSetAttribute(attn_doc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(attn_smem_bytes(kConsumerWarps)));
+                             static_cast<int>(kAttnSmemBytes));
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(attn_doc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
@@ -620,7 +581,8 @@ cudaError_t launch_attn_doc(const AttnArgs& a, const CUtensorMap& tmK, const CUt
   }
   dim3 grid(a.n_splits, a.hkv * (a.rows_pad / a.row_tile), a.n_slots);
   if (grid.x == 0 || grid.z == 0) return cudaSuccess;
-  const size_t smem = attn_smem_bytes(a.row_tile == 16 ? 1 : kConsumerWarps);
+  if (a.row_tile != 16 || a.rows_pad != 16) return cudaErrorInvalidValue;  // one shared 16-row tile
+  const size_t smem = kAttnSmemBytes;
   count_launch();
   { const cudaError_t le_ = launch_pdl(attn_doc_kernel, dim3(grid), dim3(kAttnThreads), smem, st, a, make_rope_table(a.theta), tmK, tmV); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();

@@ -224,7 +224,7 @@ struct AttnArgs {
   int split_tokens;
   int n_splits;
   int rows_pad;            // rows per (slot, kv head), padded to the row tile
-  int row_tile;            // 16 (one row tile shared by 4 warps) or 64 (4 warps x 16 rows)
+  int row_tile;            // 16 (mma.sync kernel: one tile shared by its 4 warps) or 128 (tcgen05 kernel)
   float* part_o;           // [n_slots, hkv, n_splits, rows_pad, 128]
   float2* part_ml;         // [n_slots, hkv, n_splits, rows_pad]
   float* tree_o;           // [n_nodes, hq, 128]
