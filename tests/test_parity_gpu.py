@@ -314,3 +314,48 @@ def test_workspace_too_small_is_rejected():
     with pytest.raises(Q.QuailError) as e:
         Q.classify_trie_tree(model, kv, trie, 4, ws, out, out, am)
     assert e.value.name == "QUAIL_ERR_WORKSPACE"
+
+
+def test_zero_documents_is_a_no_op():
+    """N = 0: the call succeeds and leaves the outputs untouched."""
+    import trie_label_scoring_gb300 as Q
+    from trie_label_scoring_gb300.torch_inputs import kv_from_docs
+    w = S.WORKLOADS["tiny-support10-4x128"]
+    model = C.device_model(w.shape)
+    ls = S.make_labels(w, 0)
+    docs = S.make_docs(w, 0)
+    kv = kv_from_docs(docs)
+    trie = Q.Trie(ls.labels, ls.root_token, w.shape.vocab, ls.continuation)
+    ws = torch.empty(Q.workspace_size(model, trie, 0, 1, docs.max_doc_len, Q.MODE_TRIE_TREE), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.full((1, len(ls.labels)), float("nan"), device="cuda")
+    am = torch.full((1,), -7, dtype=torch.int32, device="cuda")
+    Q.classify_trie_tree(model, kv, trie, 0, ws, out, out, am)
+    Q.device_status()
+    assert torch.isnan(out).all() and int(am[0]) == -7
+
+
+@pytest.mark.parametrize("labels", ["support10", "tree60"])
+def test_long_documents_past_the_split_cap(labels):
+    """Enough (document, KV head) items for whole-document splits, which are
+    capped at 4096 keys: documents of 4095..8192 tokens take one or two
+    splits (and the combine kernel) on the mma.sync path (16 rows per KV head)
+    and on the tcgen05 path (more than 128)."""
+    if labels == "support10":
+        w = S.with_docs(S.WORKLOADS["tiny-support10-4x128"], 232, (16, 8192))
+        ls = S.make_labels(w, 0)
+        assert _rows_per_kv(w, ls) <= 16
+    else:
+        w = _tiny_tree(232, (16, 8192))
+        ls = S.make_labels(w, 5)
+        assert _rows_per_kv(w, ls) > 128
+    long_lens = [4095, 4096, 4097, 5000, 8192]
+    rng = np.random.default_rng(11)
+    lens = np.concatenate([np.array(long_lens), rng.integers(16, 64, size=w.num_docs - len(long_lens))])
+    lens = lens.astype(np.int32)
+    docs = _resize_docs(None, lens, w)
+    ls, docs, lsc, prob, am = _run_trie_tree(w, seed=5 if labels == "tree60" else 0, labels=ls, docs=docs)
+    assert np.all(np.abs(prob.sum(axis=1) - 1) < 1e-4)
+    for i in [0, 2, 4, w.num_docs - 1]:  # 4095, 4097, 8192 tokens and a short one
+        r = _oracle_full(w, ls, docs, i, seed=5 if labels == "tree60" else 0)
+        C.check_scores(lsc[i], prob[i], am[i], r["logscore"], r["prob"], r["argmax"], f"len {lens[i]}")
