@@ -337,10 +337,10 @@ def test_zero_documents_is_a_no_op():
 
 @pytest.mark.parametrize("labels", ["support10", "tree60"])
 def test_long_documents_past_the_split_cap(labels):
-    """Enough (document, KV head) items for whole-document splits, which are
-    capped at 4096 keys: documents of 4095..8192 tokens take one or two
-    splits (and the combine kernel) on the mma.sync path (16 rows per KV head)
-    and on the tcgen05 path (more than 128)."""
+    """Enough (document, KV head) items for whole-document splits: capped at
+    4096 keys on the mma.sync path (16 rows per KV head), where documents of
+    4095..8192 tokens take one or two splits (and the combine kernel), and at
+    8192 on the tcgen05 path (more than 128 rows), where each is one tile."""
     if labels == "support10":
         w = S.with_docs(S.WORKLOADS["tiny-support10-4x128"], 232, (16, 8192))
         ls = S.make_labels(w, 0)

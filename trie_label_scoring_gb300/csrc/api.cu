@@ -191,19 +191,30 @@ AttnShape attn_shape(const quail_model_desc* m, int nq, int slots, int max_doc_l
     const long items = static_cast<long>(slots) * m->n_kv_heads;
     s.split_tokens = (items >= 3L * sms) ? std::min(whole, 4096) : std::min(whole, 512);
   } else {
-    // Many rows: tcgen05 kernel on 128-row tiles, one CTA per SM. Split the
-    // documents (in whole 128-key blocks) only as far as needed for about
-    // three waves of CTAs.
+    // Many rows: tcgen05 kernel on 128-row tiles, one CTA per SM. Besides
+    // its 128-key blocks a tile carries fixed work (pipeline fill, Q build,
+    // the epilogue) measured at about ten blocks' time, so the key split (in
+    // whole blocks, at most 8192 keys) minimises waves x (blocks per tile +
+    // 10): long documents on few (document, KV head) items are split only
+    // when that fills the SMs better than it costs in tiles.
     s.tc = true;
     s.row_tile = 128;
     s.rows_pad = static_cast<int>(round_up(s.rows_per_kv, 128));
     const long items = static_cast<long>(slots) * m->n_kv_heads * (s.rows_pad / 128);
-    const long want = 3L * sms;
-    int split = std::min(whole, 4096);
-    if (items < want) {
-      const long parts = (want + items - 1) / items;
-      split = static_cast<int>(round_up((max_doc_len + parts - 1) / parts, 128));
-      split = std::max(256, std::min(split, 4096));
+    const int nb = (max_doc_len + 127) / 128;
+    long best = -1;
+    int split = 128;
+    for (int p = 1; p <= nb; ++p) {
+      const int blocks = (nb + p - 1) / p;
+      if (blocks * 128 > 8192) continue;
+      const long splits = (nb + blocks - 1) / blocks;
+      const long waves = (items * splits + sms - 1) / sms;
+      const long cost = waves * (blocks + 10);
+      if (best < 0 || cost < best) {
+        best = cost;
+        split = blocks * 128;
+      }
+      if (blocks == 1) break;
     }
     s.split_tokens = split;
   }

@@ -38,7 +38,7 @@ constexpr int kTcRows = 128;
 constexpr int kTcBlkKeys = 128;                // keys per block = 8 pages
 constexpr int kTcBlkPages = kTcBlkKeys / 16;
 constexpr int kTcStages = 3;                   // per ring
-constexpr int kTcMaxPages = 256;               // split_tokens <= 4096
+constexpr int kTcMaxPages = 512;               // split_tokens <= 8192
 constexpr uint32_t kTcHalf = kTcBlkKeys * 128;  // 16 KB: 128 keys x 64 dims (128 B rows, 128B swizzle)
 constexpr uint32_t kTcStage = 2 * kTcHalf;      // dims 0..63 | dims 64..127
 constexpr uint32_t kOffK = 0;
@@ -47,6 +47,8 @@ constexpr uint32_t kOffBar = kOffV + kTcStages * kTcStage;
 constexpr uint32_t kOffPages = kOffBar + 256;
 constexpr uint32_t kOffX = kOffPages + kTcMaxPages * 4;  // softmax exchange: 3 KB
 constexpr size_t kTcSmem = 1024 + kOffX + 3 * 1024;
+constexpr uint32_t kStageRow = 528;  // bytes per row of the epilogue's shared-memory staging
+static_assert(128 * kStageRow <= kTcStages * kTcStage, "a ring holds a 128-row staging block");
 constexpr uint32_t kTmemCols = 512;  // S/P buffers 0..127, 128..255 | O 256..383 | Q hi 384..447, lo 448..511
 constexpr uint32_t kTmemO = 256;
 constexpr uint32_t kTmemQ = 384;  // column c of lane r: (q[r][2c], q[r][2c+1]) as bf16x2
@@ -57,6 +59,7 @@ struct TcBars {
   uint64_t p_full[2];   // P_b written over S_b (256 softmax threads)
   uint64_t pv_done[2];  // O += P_b V complete (MMA commit): P_b's columns and V's stage are free
   uint64_t q_full, drain, xbar[2], lbar;
+  uint64_t ebar[3];  // row epilogue steps (256 softmax threads each)
   uint32_t tmem_slot;
   int abort_flag;
 };
@@ -176,6 +179,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(&bars->q_full, 256);
     mbar_init(&bars->drain, 1);
     mbar_init(&bars->lbar, 256);
+    for (int i = 0; i < 3; ++i) mbar_init(&bars->ebar[i], 256);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -302,6 +306,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       e = rr / G;
       h = g * G + rr % G;
       node = row_node(a.map, slot, e);
+    }
+    if (row_ok && a.n_splits == 1) {
+      // the epilogue's tree-part inputs: start them towards L2 now, so the
+      // reads after the last block do not wait on HBM (this warpgroup's two
+      // 128-byte lines of the row, and the row's max / sum)
+      const float* to = a.tree_o + (static_cast<size_t>(node) * a.hq + h) * 128 + wg * 64;
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(to));
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(to + 32));
+      if (wg == 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.tree_ml + static_cast<size_t>(node) * a.hq + h));
     }
     // Q row into TMEM: RoPE at l_i + depth, two-term bf16 split; warpgroup 0
     // builds dims 0..63, warpgroup 1 dims 64..127 (the two outputs of each
@@ -460,53 +473,100 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else {
       ok = false;
     }
+    // Rows out through shared memory. Every page has been consumed, so the K
+    // ring stages tree_o rows in and the V ring stages output rows out: both
+    // cross global memory as whole rows, one row per warp instruction, while
+    // each thread works on its own row in shared memory. Rows are 528 bytes
+    // apart, so 8 consecutive rows fall in 8 different 16-byte bank groups.
+    uint8_t* tstage = base + kOffK;
+    uint8_t* ostage = base + kOffV;
+    long long* tab = reinterpret_cast<long long*>(xmax);  // [128 rows][tree_o row offset, output offset] (-1: none)
+    const bool fused = a.n_splits == 1;
+    const int cw = warp - 3;  // copy warp 0..7: rows 16 cw .. 16 cw + 15
+    if (ok) {
+      // the exchange buffer is free: the last block's maxima were read before lbar
+      if (wg == 0) {
+        long long src = -1, dstoff = -1;
+        if (row_ok && fused) {
+          src = (static_cast<long long>(node) * a.hq + h) * 128;
+          dstoff = (static_cast<long long>(slot) * a.map.nq + e) * 2 * a.hq * 128 + h * 128;
+        } else if (row_ok) {
+          dstoff = (((static_cast<long long>(slot) * a.hkv + g) * a.n_splits + split) * a.rows_pad + rr) * 128;
+        }
+        tab[2 * row] = src;
+        tab[2 * row + 1] = dstoff;
+      }
+      mbar_arrive(&bars->ebar[0]);
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->ebar[0], 0u, abort_flag));
+    }
+    if (ok && fused) {  // tree_o rows in (all loads first)
+      float4 tv[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const long long src = tab[2 * (cw * 16 + i)];
+        tv[i] = src >= 0 ? reinterpret_cast<const float4*>(a.tree_o + src)[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) reinterpret_cast<float4*>(tstage + (cw * 16 + i) * kStageRow)[lane] = tv[i];
+    }
+    if (ok) {
+      mbar_arrive(&bars->ebar[1]);
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->ebar[1], 0u, abort_flag));
+    }
     if (ok) {
       const float l_sum = l_part + xl[(wg ^ 1) * 128 + row];
-      const bool fused = a.n_splits == 1;
       float f1 = 1.f, f2 = 0.f, inv = 1.f;
-      const float* to = nullptr;
-      bf16* dst = nullptr;
-      float* pdst = nullptr;
       if (row_ok && fused) {
         const float2 tml = a.tree_ml[static_cast<size_t>(node) * a.hq + h];
         const float M = fmaxf(m_ref, tml.x);
         f1 = exp2f(m_ref - M);
         f2 = exp2f(tml.x - M);
         inv = 1.f / (f1 * l_sum + f2 * tml.y);
-        to = a.tree_o + (static_cast<size_t>(node) * a.hq + h) * 128;
-        dst = a.out + (static_cast<size_t>(slot) * a.map.nq + e) * 2 * a.hq * 128 + h * 128;
-      } else if (row_ok) {
-        const size_t pr =
-            ((static_cast<size_t>(slot) * a.hkv + g) * a.n_splits + split) * static_cast<size_t>(a.rows_pad) + rr;
-        pdst = a.part_o + pr * 128;
-        if (wg == 0) a.part_ml[pr] = make_float2(m_ref, l_sum);
+      } else if (row_ok && wg == 0) {
+        a.part_ml[tab[2 * row + 1] / 128] = make_float2(m_ref, l_sum);
       }
+      uint8_t* orow = ostage + row * kStageRow;
+      const float* trow = reinterpret_cast<const float*>(tstage + row * kStageRow);
 #pragma unroll 1
       for (int c = wg * 2; c < wg * 2 + 2; ++c) {  // this warpgroup's 64 columns of O, 32 at a time
-        float4 t4[8];
-        if (dst != nullptr) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) t4[i] = reinterpret_cast<const float4*>(to + c * 32)[i];
-        }
         float o[32];
         tmem_ld_32cols(lane_addr + kTmemO + c * 32, o);
-        if (dst != nullptr) {
-          const float* tv = reinterpret_cast<const float*>(t4);
+        if (fused) {
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {
+            const float4 ta = reinterpret_cast<const float4*>(trow + c * 32 + i)[0];
+            const float4 tb = reinterpret_cast<const float4*>(trow + c * 32 + i)[1];
+            const float tv[8] = {ta.x, ta.y, ta.z, ta.w, tb.x, tb.y, tb.z, tb.w};
             uint32_t hv[4], lv[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               const int k = i + 2 * u;
-              split_bf16((f1 * o[k] + f2 * tv[k]) * inv, (f1 * o[k + 1] + f2 * tv[k + 1]) * inv, hv[u], lv[u]);
+              split_bf16((f1 * o[k] + f2 * tv[2 * u]) * inv, (f1 * o[k + 1] + f2 * tv[2 * u + 1]) * inv, hv[u], lv[u]);
             }
-            *reinterpret_cast<uint4*>(dst + c * 32 + i) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-            *reinterpret_cast<uint4*>(dst + a.hq * 128 + c * 32 + i) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+            *reinterpret_cast<uint4*>(orow + (c * 32 + i) * 2) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+            *reinterpret_cast<uint4*>(orow + 256 + (c * 32 + i) * 2) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
           }
-        } else if (pdst != nullptr) {
+        } else {
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(pdst + c * 32 + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+            *reinterpret_cast<float4*>(orow + (c * 32 + i) * 4) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+        }
+      }
+      mbar_arrive(&bars->ebar[2]);
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->ebar[2], 0u, abort_flag));
+    }
+    if (ok) {  // output rows out: [hi | lo] bf16 halves to their two places, or fp32 partials
+#pragma unroll 4
+      for (int i = 0; i < 16; ++i) {
+        const int r = cw * 16 + i;
+        const long long dstoff = tab[2 * r + 1];
+        if (dstoff < 0) continue;
+        const uint4 v = reinterpret_cast<const uint4*>(ostage + r * kStageRow)[lane];
+        if (fused) {
+          bf16* dst = a.out + dstoff + (lane < 16 ? lane * 8 : a.hq * 128 + (lane - 16) * 8);
+          *reinterpret_cast<uint4*>(dst) = v;
+        } else {
+          reinterpret_cast<uint4*>(a.part_o + dstoff)[lane] = v;
         }
       }
     }
