@@ -162,15 +162,6 @@ __device__ __forceinline__ void mma_pair(float (&d0)[4], float (&d1)[4], const u
   mma_bf16(d1, av, b2, b3);
 }
 
-// Writes o (fp32) as the two-term bf16 split [hi | lo] of output row `orow`.
-__device__ __forceinline__ void store_o_split(bf16* out, int hq, size_t orow, int col, float x0, float x1) {
-  uint32_t hi, lo;
-  split_bf16(x0, x1, hi, lo);
-  bf16* dst = out + orow * 2 * hq * 128 + col;
-  *reinterpret_cast<uint32_t*>(dst) = hi;
-  *reinterpret_cast<uint32_t*>(dst + hq * 128) = lo;
-}
-
 __global__ void __launch_bounds__(kAttnThreads, 3)
     attn_doc_kernel(AttnArgs a, RopeTable rt, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV) {
@@ -454,7 +445,11 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
       }
     }
     asm volatile("bar.sync 1, 128;" ::: "memory");
-    const int r = t >> 3, d0 = (t & 7) * 16;  // row r, dims d0 .. d0 + 16
+    // Thread t: row r = t / 8 and dims 8k .. 8k + 7, 64 + 8k .. 64 + 8k + 7
+    // (k = t % 8), so the 8 threads of a row write each 128-byte half of a
+    // bf16 output row (or read each 256-byte run of a tree_o row) together.
+    const int r = t >> 3, k8 = t & 7;
+    auto dim = [&](int i) { return (i < 8 ? 8 * k8 : 64 + 8 * k8 - 8) + i; };  // dim of acc[i]
     const float* s0 = reinterpret_cast<const float*>(base);
     float M = -INFINITY;
 #pragma unroll
@@ -470,30 +465,43 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
       const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
       lsum += f * sw[16 * 128 + 16 + r];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) acc[i] += f * sw[r * 128 + d0 + i];
+      for (int i = 0; i < 16; i += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(sw + r * 128 + dim(i));
+        acc[i] += f * v.x;
+        acc[i + 1] += f * v.y;
+        acc[i + 2] += f * v.z;
+        acc[i + 3] += f * v.w;
+      }
     }
     if (!fused) {
-      float* dst = a.part_o + (part_row0 + r) * 128 + d0;
+      float* dst = a.part_o + (part_row0 + r) * 128;
 #pragma unroll
       for (int i = 0; i < 16; i += 4)
-        *reinterpret_cast<float4*>(dst + i) = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
-      if ((t & 7) == 0) a.part_ml[part_row0 + r] = make_float2(M, lsum);
+        *reinterpret_cast<float4*>(dst + dim(i)) = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+      if (k8 == 0) a.part_ml[part_row0 + r] = make_float2(M, lsum);
     } else if (r < rows_per_kv) {
       const int e = r / G, h = g * G + r % G;
       const int node = row_node(a.map, slot, e);
       const float2 tml = a.tree_ml[static_cast<size_t>(node) * a.hq + h];
+      const float* to = a.tree_o + (static_cast<size_t>(node) * a.hq + h) * 128;
       float tv[16];  // this thread's 16 dims of the tree part, loaded before any store
-      const float4* to = reinterpret_cast<const float4*>(a.tree_o + (static_cast<size_t>(node) * a.hq + h) * 128 + d0);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) *reinterpret_cast<float4*>(tv + 4 * i) = to[i];
+      for (int i = 0; i < 16; i += 4) *reinterpret_cast<float4*>(tv + i) = *reinterpret_cast<const float4*>(to + dim(i));
       const float M2 = fmaxf(M, tml.x);
       const float f1 = exp2f(M - M2), f2 = exp2f(tml.x - M2);
       const float inv = 1.f / (f1 * lsum + f2 * tml.y);
-      const size_t orow = static_cast<size_t>(slot) * a.map.nq + e;
+      bf16* orow = a.out + (static_cast<size_t>(slot) * a.map.nq + e) * 2 * a.hq * 128 + h * 128;
 #pragma unroll
-      for (int i = 0; i < 16; i += 2)
-        store_o_split(a.out, a.hq, orow, h * 128 + d0 + i, (f1 * acc[i] + f2 * tv[i]) * inv,
-                      (f1 * acc[i + 1] + f2 * tv[i + 1]) * inv);
+      for (int hf = 0; hf < 2; ++hf) {  // dims 8k.. and 64 + 8k..: one 16-byte hi and lo store each
+        uint32_t hv[4], lv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = hf * 8 + 2 * u;
+          split_bf16((f1 * acc[i] + f2 * tv[i]) * inv, (f1 * acc[i + 1] + f2 * tv[i + 1]) * inv, hv[u], lv[u]);
+        }
+        *reinterpret_cast<uint4*>(orow + dim(hf * 8)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        *reinterpret_cast<uint4*>(orow + a.hq * 128 + dim(hf * 8)) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+      }
     }
   }
   if (threadIdx.x == 0 && *abort_flag) raise_device_error(a.err, QUAIL_ERR_DEVICE_TIMEOUT, 2000 + slot);
