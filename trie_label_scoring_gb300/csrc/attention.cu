@@ -197,6 +197,35 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
   const int nq_rows = (a.map.slot_node ? 1 : a.map.nq);
   const int rows_per_kv = nq_rows * G;
 
+  // q items of this consumer thread: item = (row r, pair j) -> dims j and
+  // j + 64 (j = t % 64 for every item, since 128 threads step 128 items). The
+  // loads go out before the barrier setup so their latency overlaps it.
+  constexpr int kPer = 16 * 64 / (kConsumerWarps * 32);  // items per thread
+  const int t = threadIdx.x;
+  float x1[kPer], x2[kPer];
+  int pos[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    x1[k] = x2[k] = 0.f;
+    pos[k] = -1;
+  }
+  if (warp < kConsumerWarps) {
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int it = t + k * kConsumerWarps * 32;
+      const int r = it / 64, j = it % 64;
+      const int rr = rg * a.row_tile + r;  // row within (slot, kv head)
+      if (rr < rows_per_kv) {
+        const int e = rr / G, hl = rr % G;
+        const int node = row_node(a.map, slot, e);
+        const float* q = a.qkv + static_cast<size_t>(node) * a.ldq + (g * G + hl) * 128;
+        x1[k] = q[j];
+        x2[k] = q[j + 64];
+        pos[k] = L + a.node_depth[node];
+      }
+    }
+  }
+
   if (threadIdx.x == 0) {
     for (int s = 0; s < kAttnStages; ++s) {
       mbar_init(&full[s], 1);
@@ -254,34 +283,13 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
   }
 
   // -------------------------------------------------- consumers
-  const int t = threadIdx.x;  // 0..127
   const int gq = lane >> 2, tq = lane & 3;
 
   // q fragments: item = (row, pair j) -> rotated dims j and j + 64, split
   // into hi/lo bf16 and scattered to their (ks, lane, register, half) slots.
   {
     uint16_t* sq16 = reinterpret_cast<uint16_t*>(s_q);
-    constexpr int kPer = 16 * 64 / (kConsumerWarps * 32);  // items per thread
-    // all loads of this thread's items first (one memory round trip), then
-    // rotate, split and scatter
-    float x1[kPer], x2[kPer];
-    int pos[kPer];
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int it = t + k * kConsumerWarps * 32;
-      const int r = it / 64, j = it % 64;
-      const int rr = rg * a.row_tile + r;  // row within (slot, kv head)
-      x1[k] = x2[k] = 0.f;
-      pos[k] = -1;
-      if (rr < rows_per_kv) {
-        const int e = rr / G, hl = rr % G;
-        const int node = row_node(a.map, slot, e);
-        const float* q = a.qkv + static_cast<size_t>(node) * a.ldq + (g * G + hl) * 128;
-        x1[k] = q[j];
-        x2[k] = q[j + 64];
-        pos[k] = L + a.node_depth[node];
-      }
-    }
+    const float2 wj = rt.w[t & 63];  // the one frequency this thread needs
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
       const int it = t + k * kConsumerWarps * 32;
@@ -289,7 +297,7 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
       float y0 = 0.f, y1 = 0.f;
       if (pos[k] >= 0) {
         float c, sn;
-        rope_cs(pos[k], rt.w[j], c, sn);
+        rope_cs(pos[k], wj, c, sn);
         y0 = x1[k] * c - x2[k] * sn;
         y1 = x2[k] * c + x1[k] * sn;
       }
