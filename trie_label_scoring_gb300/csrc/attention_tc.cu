@@ -138,13 +138,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   int* s_pages = reinterpret_cast<int*>(base + kOffPages);
 
   // grid: x = row tile (fastest, so the tiles that share a document's KV run
-  // together and re-read it from L2), y = split + n_splits * kv head, z = slot
-  const int slot = blockIdx.z;
+  // together and re-read it from L2), y = slot, z = split + n_splits * kv
+  // head: the documents of one KV head come next, so their tiles re-read the
+  // same q and tree-part rows from L2 as well
+  const int slot = blockIdx.y;
   if (a.map.n_slots_dev != nullptr && slot >= *a.map.n_slots_dev) return;
   if (rows_past_end(a.map, slot, static_cast<int>(blockIdx.x) * kTcRows / (a.hq / a.hkv))) return;  // padding tile
   const int rt_idx = blockIdx.x;
-  const int split = blockIdx.y % a.n_splits;
-  const int g = blockIdx.y / a.n_splits;
+  const int split = blockIdx.z % a.n_splits;
+  const int g = blockIdx.z / a.n_splits;
   const int doc = row_doc(a.map, slot);
   const int L = a.doc_len[doc];
   if (L < 1 || L > a.max_doc_len) {
@@ -599,7 +601,7 @@ cudaError_t launch_attn_doc_tc(const AttnArgs& a, const CUtensorMap& tmK, const 
   if (a.row_tile != kTcRows || a.rows_pad % kTcRows != 0 || a.split_tokens > 16 * kTcMaxPages ||
       a.split_tokens % 16 != 0)
     return cudaErrorInvalidValue;
-  dim3 grid(a.rows_pad / kTcRows, a.n_splits * a.hkv, a.n_slots);
+  dim3 grid(a.rows_pad / kTcRows, a.n_slots, a.n_splits * a.hkv);
   if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
   count_launch();
   { const cudaError_t le_ = launch_pdl(attn_doc_tc_kernel, dim3(grid), dim3(kTcThreads), kTcSmem, st, a, make_rope_table(a.theta), tmK, tmV); if (le_ != cudaSuccess) return le_; }
