@@ -359,3 +359,27 @@ def test_long_documents_past_the_split_cap(labels):
     for i in [0, 2, 4, w.num_docs - 1]:  # 4095, 4097, 8192 tokens and a short one
         r = _oracle_full(w, ls, docs, i, seed=5 if labels == "tree60" else 0)
         C.check_scores(lsc[i], prob[i], am[i], r["logscore"], r["prob"], r["argmax"], f"len {lens[i]}")
+
+
+def test_prefix_labels_on_the_tcgen05_path():
+    """Labels that are prefixes of other labels, on a trie with more than 128
+    query rows per KV head: the prefix correction log(1 - sum of the end
+    node's child probabilities) over rows from the tcgen05 attention."""
+    w = _tiny_tree(6, (40, 400))
+    base = S.make_labels(w, 8)
+    labels = [list(l) for l in base.labels]
+    seen = {tuple(l) for l in labels}
+    for l in list(labels):  # add every proper prefix of length >= 1 of the longer labels once
+        for k in range(1, len(l)):
+            p = tuple(l[:k])
+            if p not in seen and len(labels) < 90:
+                seen.add(p)
+                labels.append(list(p))
+    ls = S.LabelSet(labels, base.root_token, None)
+    assert _rows_per_kv(w, ls) > 128
+    assert any(tuple(m[:len(l)]) == tuple(l) for l in labels for m in labels if len(m) > len(l))
+    ls_, docs, lsc, prob, am = _run_trie_tree(w, seed=8, labels=ls)
+    assert np.all(np.abs(prob.sum(axis=1) - 1) < 1e-4)
+    for i in range(w.num_docs):
+        r = _oracle_full(w, ls, docs, i, seed=8)
+        C.check_scores(lsc[i], prob[i], am[i], r["logscore"], r["prob"], r["argmax"], f"doc {i}")
