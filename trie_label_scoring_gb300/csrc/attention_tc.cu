@@ -66,6 +66,22 @@ struct TcBars {
 static_assert(sizeof(TcBars) <= 256, "barrier block");
 static_assert(kTcSmem <= 227 * 1024, "shared memory");
 
+// Stores 16 consecutive fp32 columns of this thread's TMEM lane without
+// waiting; tmem_st_wait() completes every store issued before it.
+__device__ __forceinline__ void tmem_st_16cols_nowait(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
+      "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
+      "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // D (+)= A * B^T with A in TMEM (M rows = lanes, K packed two bf16 per column)
 // and the B shared-memory descriptor given as its two 32-bit words.
 __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
@@ -318,42 +334,48 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       asm volatile("prefetch.global.L2 [%0];" ::"l"(to + 32));
       if (wg == 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.tree_ml + static_cast<size_t>(node) * a.hq + h));
     }
-    // Q row into TMEM: RoPE at l_i + depth, two-term bf16 split; warpgroup 0
-    // builds dims 0..63, warpgroup 1 dims 64..127 (the two outputs of each
-    // rotate-half pair), column c of a half holding dims (2c, 2c + 1). The
-    // row is read with 16-byte loads, issued together per 32 dims.
+    // Q row into TMEM: RoPE at l_i + depth, two-term bf16 split. Warpgroup w
+    // takes the rotate-half pairs (j, j + 64) for j = 32w .. 32w + 31 and
+    // writes both outputs of each pair, so it reads only those 64 dims (one
+    // round of 16-byte loads) and evaluates each angle once. TMEM column c
+    // holds dims (2c, 2c + 1): this thread fills columns 16w .. 16w + 15 and
+    // 32 + 16w .. 32 + 16w + 15 of the hi and of the lo half.
     {
       const float4* q4 =
           row_ok ? reinterpret_cast<const float4*>(a.qkv + static_cast<size_t>(node) * a.ldq + h * 128) : nullptr;
       const int pos = row_ok ? L + a.node_depth[node] : 0;
-      float hi[32], lo[32];
+      float4 x1[8], x2[8];  // dims 32w .. 32w + 31 and 64 + 32w .. 64 + 32w + 31
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {  // dims j = 32 half .. 32 half + 31 and j + 64
-        float4 x1[8], x2[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          x1[i] = row_ok ? q4[half * 8 + i] : make_float4(0.f, 0.f, 0.f, 0.f);
-          x2[i] = row_ok ? q4[16 + half * 8 + i] : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float* p1 = reinterpret_cast<const float*>(x1) + 2 * c;
-          const float* p2 = reinterpret_cast<const float*>(x2) + 2 * c;
-          float y[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            float cs, sn;
-            rope_cs(pos, rt.w[half * 32 + 2 * c + u], cs, sn);
-            y[u] = wg == 0 ? p1[u] * cs - p2[u] * sn : p2[u] * cs + p1[u] * sn;
-          }
-          uint32_t hv, lv;
-          split_bf16(y[0], y[1], hv, lv);
-          hi[half * 16 + c] = __uint_as_float(hv);
-          lo[half * 16 + c] = __uint_as_float(lv);
-        }
+      for (int i = 0; i < 8; ++i) {
+        x1[i] = row_ok ? q4[wg * 8 + i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        x2[i] = row_ok ? q4[16 + wg * 8 + i] : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      tmem_st_32cols(lane_addr + kTmemQ + wg * 32, hi);
-      tmem_st_32cols(lane_addr + kTmemQ + 64 + wg * 32, lo);
+      float hi1[16], lo1[16], hi2[16], lo2[16];  // first outputs (dims j), second outputs (dims j + 64)
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const float* p1 = reinterpret_cast<const float*>(x1) + 2 * c;
+        const float* p2 = reinterpret_cast<const float*>(x2) + 2 * c;
+        float y1[2], y2[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          float cs, sn;
+          rope_cs(pos, rt.w[wg * 32 + 2 * c + u], cs, sn);
+          y1[u] = p1[u] * cs - p2[u] * sn;
+          y2[u] = p2[u] * cs + p1[u] * sn;
+        }
+        uint32_t hv, lv;
+        split_bf16(y1[0], y1[1], hv, lv);
+        hi1[c] = __uint_as_float(hv);
+        lo1[c] = __uint_as_float(lv);
+        split_bf16(y2[0], y2[1], hv, lv);
+        hi2[c] = __uint_as_float(hv);
+        lo2[c] = __uint_as_float(lv);
+      }
+      tmem_st_16cols_nowait(lane_addr + kTmemQ + wg * 16, hi1);
+      tmem_st_16cols_nowait(lane_addr + kTmemQ + 32 + wg * 16, hi2);
+      tmem_st_16cols_nowait(lane_addr + kTmemQ + 64 + wg * 16, lo1);
+      tmem_st_16cols_nowait(lane_addr + kTmemQ + 96 + wg * 16, lo2);
+      tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars->q_full);
     }
