@@ -9,8 +9,9 @@
 // per block of 128 keys (8 pages). Q and P are two-term bf16 splits (as in
 // the mma.sync path) and both live in TMEM as the A operand: Q once per CTA,
 // P written by the softmax over the S block it was computed from. K and V come
-// from two TMA page rings (K-major K, MN-major V), so shared memory holds
-// nothing but keys and values.
+// from two TMA page rings (K-major K, MN-major V), so while the blocks run
+// shared memory holds nothing but keys and values; the epilogue then stages
+// the tile's tree-part rows in and output rows out through the idle rings.
 //
 // An M=128, K=16 MMA costs max(64, N/2) cycles on this part, so both products
 // use N = 128; per 128-key block the tensor pipe is busy 2 x 16 x 64 cycles.
@@ -20,8 +21,9 @@
 //
 // Roles (352 threads): warp 0 loads K pages, warp 1 owns TMEM and issues the
 // MMAs, warp 2 loads V pages, warps 3..10 (two warpgroups; each thread one
-// query row and half of every key block / of O's columns) build Q, run the
-// softmax (lazy reference max, as in attention.cu), write P and finish rows.
+// query row and half of every key block / of O's columns) build Q (each
+// warpgroup half of the rotate-half pairs), run the softmax (lazy reference
+// max, as in attention.cu), write P and finish rows.
 #include "attn_common.cuh"
 #include "kernels.h"
 #include "launch.cuh"
