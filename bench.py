@@ -10,8 +10,10 @@ head with fused log-sum-exp and child gather, label scoring).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-Prints one JSON line (rank 0). With torchrun (N > 1) every rank scores its own
-256 documents (weak scaling, no collective on the data path).
+Prints one JSON line. The method shards by document with no exchange step,
+so N GPUs would be N independent replicas; this benchmark runs one and
+refuses --gpus > 1 or a torchrun launch of several ranks. The reference arm
+(--impl reference, the CPU oracle) under torchrun runs on rank 0 only.
 """
 from __future__ import annotations
 
@@ -138,38 +140,21 @@ def recorded_traffic(workload: str, rows: int, record: str = "lm_head_gemm_traff
     return d["dram_bytes_per_launch"] * rows / d["rows"]
 
 
-def dist_setup():
-    import torch
+def gpu_setup(args) -> None:
+    """One process on one GPU. The path shards by document with no exchange
+    step (replicas only), and this benchmark runs one replica: a launch on
+    several GPUs (torchrun, WORLD_SIZE > 1, or --gpus > 1) is refused."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        import torch.distributed as dist
-        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    else:
-        torch.cuda.set_device(local)
-    return world, rank, local
-
-
-def barrier(world):
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
-
-
-def max_over_ranks(world, x: float) -> float:
-    if world == 1:
-        return x
+    if world > 1 or args.gpus != 1:
+        sys.stderr.write("bench.py runs on one GPU only: the method shards by document with no exchange step, "
+                         "so N GPUs are N independent replicas (trie_label_scoring_gb300.replicas); "
+                         f"got --gpus {args.gpus}, WORLD_SIZE {world}\n")
+        sys.exit(2)
     import torch
-    import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    torch.cuda.set_device(0)
 
 
-def timed_e2e(stream, world, h_in, dev_sets, call, outs, k_steps) -> float:
+def timed_e2e(stream, h_in, dev_sets, call, outs, k_steps) -> float:
     """End-to-end steps through the public API with inputs two buffers deep:
     the host-to-device copy of step i+1's inputs (from pinned host memory, on
     a stream of its own) runs while step i computes on the other device
@@ -177,8 +162,8 @@ def timed_e2e(stream, world, h_in, dev_sets, call, outs, k_steps) -> float:
     compute stream. h_in: pinned host tensors; dev_sets: per buffer, the
     device tensors they are copied to (same order); call(b): the library call
     on buffer b, on `stream`; outs: (device, pinned host) result pairs.
-    Returns the ms of k_steps steps, max over ranks, from the start of the
-    first copy to the last result read back."""
+    Returns the ms of k_steps steps, from the start of the first copy to the
+    last result read back."""
     import torch
     copy_st = torch.cuda.Stream()
     ready = [torch.cuda.Event() for _ in dev_sets]
@@ -202,7 +187,6 @@ def timed_e2e(stream, world, h_in, dev_sets, call, outs, k_steps) -> float:
     for i in range(3):
         one(i)
     torch.cuda.synchronize()
-    barrier(world)
     s = torch.cuda.Event(enable_timing=True)
     e = torch.cuda.Event(enable_timing=True)
     s.record(stream)
@@ -211,7 +195,43 @@ def timed_e2e(stream, world, h_in, dev_sets, call, outs, k_steps) -> float:
         one(i)
     e.record(stream)
     torch.cuda.synchronize()
-    return max_over_ranks(world, s.elapsed_time(e))
+    return s.elapsed_time(e)
+
+
+# ------------------------------------------------------------------ inputs
+_MODELS: dict = {}
+
+
+def model_bits(shape, seed: int = 0) -> dict:
+    """The seeded synthetic weights of a layer shape (bf16 bits), drawn once."""
+    import synthetic as S
+    key = (shape, seed)
+    if key not in _MODELS:
+        _MODELS[key] = S.make_model(shape, seed)
+    return _MODELS[key]
+
+
+def device_model(shape, seed: int = 0):
+    """Those weights on the current GPU as the library's model descriptor."""
+    from trie_label_scoring_gb300.torch_inputs import model_from_bits
+    return model_from_bits(model_bits(shape, seed), shape)
+
+
+def oracle_layer(shape, seed: int = 0):
+    """The CPU oracle's layer over the same weights (cpu_baseline and the
+    reference arm only): fp64, with the head in fp32 beyond a 16,384-token
+    vocabulary."""
+    import numpy as np
+
+    import oracle.model as OM
+    return OM.Layer(model_bits(shape, seed), shape, head_dtype=np.float64 if shape.vocab <= 16384 else np.float32)
+
+
+def oracle_doc_kv(docs, i: int):
+    """Document i's K and V widened exactly to float64 for the oracle."""
+    import oracle.model as OM
+    k, v = docs.doc_kv(i)
+    return OM.bf16_to_f64(k), OM.bf16_to_f64(v)
 
 
 # ------------------------------------------------------------------ oracle timing
@@ -220,14 +240,13 @@ def time_oracle(w, docs, labels, budget_s: float, max_docs: int | None = None) -
     time budget is spent (at least one document)."""
     from oracle import scoring as OS
     from oracle.trie import build_trie
-    from tests import gpu_cases as C
-    L = C.oracle_layer(w.shape)
+    L = oracle_layer(w.shape)
     L.lm_head()  # widen the head once (model load, not timed)
     t = build_trie(labels.labels, labels.root_token, w.shape.vocab, labels.continuation)
     n, t0 = 0, time.perf_counter()
     limit = max_docs or w.num_docs
     while n < limit:
-        dk, dv = C.oracle_doc_kv(docs, n % w.num_docs)
+        dk, dv = oracle_doc_kv(docs, n % w.num_docs)
         OS.trie_tree(L, dk, dv, t)
         n += 1
         if time.perf_counter() - t0 >= budget_s:
@@ -277,7 +296,6 @@ def run_reference(args, world, rank):
     import synthetic as S
     from oracle import scoring as OS
     from oracle.trie import build_trie
-    from tests import gpu_cases as C
     if args.workload in S.ML_WORKLOADS:
         run_reference_ml(args, world)
         return
@@ -289,13 +307,13 @@ def run_reference(args, world, rank):
         w = S.with_docs(w, args.docs)
     labels = S.make_labels(w, 0)
     docs = S.make_docs(w, 0)
-    L = C.oracle_layer(w.shape)
+    L = oracle_layer(w.shape)
     L.lm_head()
     t = build_trie(labels.labels, labels.root_token, w.shape.vocab, labels.continuation)
     steps = args.steps if args.steps is not None else 10
 
     def step(i):
-        dk, dv = C.oracle_doc_kv(docs, i % w.num_docs)
+        dk, dv = oracle_doc_kv(docs, i % w.num_docs)
         OS.trie_tree(L, dk, dv, t)
 
     for i in range(args.warmup):
@@ -347,7 +365,6 @@ def run_reference_shortlist(args, world):
     import synthetic as S
     from oracle import shortlist as OSL
     from oracle.trie import build_trie
-    from tests import gpu_cases as C
     sw = S.SHORTLIST_WORKLOADS[args.workload]
     w = S.with_docs(sw.base, args.docs) if args.docs else sw.base
     labels = S.make_labels(w, 0)
@@ -357,12 +374,12 @@ def run_reference_shortlist(args, world):
     rw = OSL.rewrite_grouped(labels.labels, names, OSL.group_labels(labels.labels, G))
     t = build_trie(rw, labels.root_token, w.shape.vocab)
     docs = S.make_docs(w, 0)
-    L = C.oracle_layer(w.shape)
+    L = oracle_layer(w.shape)
     L.lm_head()
     steps = args.steps if args.steps is not None else 3
 
     def step(i):
-        dk, dv = C.oracle_doc_kv(docs, i % w.num_docs)
+        dk, dv = oracle_doc_kv(docs, i % w.num_docs)
         OSL.shortlist(L, dk, dv, t, 1, sw.beam)
 
     for i in range(args.warmup):
@@ -386,22 +403,21 @@ def run_reference_shortlist(args, world):
 
 
 # ------------------------------------------------------------------ our arm
-def run_ours(args, world, rank, local):
+def run_ours(args):
     import numpy as np
     import torch
 
     import synthetic as S
     import trie_label_scoring_gb300 as Q
-    from tests import gpu_cases as C
     from trie_label_scoring_gb300.torch_inputs import bf16_tensor, kv_from_docs
 
     Q.build()
     w = S.WORKLOADS[args.workload]
     if args.docs:
         w = S.with_docs(w, args.docs)
-    model = C.device_model(w.shape, 0)
+    model = device_model(w.shape, 0)
     labels = S.make_labels(w, 0)
-    docs = S.make_docs(w, rank)  # each rank scores its own documents
+    docs = S.make_docs(w, 0)
     kv = kv_from_docs(docs)
     tb0 = time.perf_counter()
     trie = Q.Trie(labels.labels, labels.root_token, w.shape.vocab, labels.continuation)
@@ -446,13 +462,12 @@ def run_ours(args, world, rank, local):
             e.record(stream)
     bus = None
     try:
-        bus = torch.cuda.get_device_properties(local).pci_bus_id
+        bus = torch.cuda.get_device_properties(0).pci_bus_id
     except Exception:
         pass
     clocks = ClockSampler(str(bus) if bus is not None else None)
     clocks.start()
     time.sleep(0.3)
-    barrier(world)
     torch.cuda.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
@@ -467,15 +482,13 @@ def run_ours(args, world, rank, local):
         step()
     end.record(stream)
     torch.cuda.synchronize()
-    barrier(world)
     clk = clocks.stop()
     Q.set_stage_events(None)
     Q.device_status()
     elapsed_ms = start.elapsed_time(end)
-    elapsed_ms = max_over_ranks(world, elapsed_ms)
     head_ms = statistics.mean(ev[2 * hs].elapsed_time(ev[2 * hs + 1]) for ev in stage_ev)
     ms_per_step = elapsed_ms / steps
-    value = N * world * steps / (elapsed_ms / 1e3)
+    value = N * steps / (elapsed_ms / 1e3)
     # stage breakdown (every boundary marked), after the timed region
     n_bd = min(steps, 50)
     bd_ev = stage_ev[:n_bd]
@@ -507,9 +520,9 @@ def run_ours(args, world, rank, local):
             Q.classify_trie_tree(model, kvs[b], trie, N, ws, lsc, prob, am, stream)
 
         k_e2e = max(3, min(steps, int(3000.0 / max(est_ms + 3.0, 1e-3))))
-        e2e_ms = timed_e2e(stream, world, [hk, hv, hpt, hdl], [list(x.tensors) for x in kvs], e2e_call,
+        e2e_ms = timed_e2e(stream, [hk, hv, hpt, hdl], [list(x.tensors) for x in kvs], e2e_call,
                            [(lsc, o_ls), (prob, o_pr), (am, o_am)], k_e2e)
-        e2e = {"value": N * world * k_e2e / (e2e_ms / 1e3), "unit": "docs/s", "h2d_bytes_per_step": h2d,
+        e2e = {"value": N * k_e2e / (e2e_ms / 1e3), "unit": "docs/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": k_e2e, "input_buffers": 2}
 
     # ---- roofline of the dominant kernel (the output-head GEMM)
@@ -530,10 +543,10 @@ def run_ours(args, world, rank, local):
     path = {"t_kv_us": t_kv * 1e6, "t_head_us": t_head * 1e6, "t_star_us": t_star * 1e6,
             "ms_per_step": ms_per_step, "frac": t_star * 1e3 / ms_per_step}
 
-    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only),
+    # ---- CPU baseline: the oracle on a bounded sample,
     # on all host cores and, in a subprocess with single-threaded BLAS, on one
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if not args.no_cpu_baseline:
         r = time_oracle(w, docs, labels, budget_s=15.0)
         cpu = {"value": r["docs_per_s"], "unit": "docs/s", "cores": cores(), "kind": "oracle",
                "sample": f"first {r['docs']} documents of {w.name} ({r['seconds']:.1f} s); numpy BLAS threads "
@@ -542,42 +555,40 @@ def run_ours(args, world, rank, local):
         if one is not None:
             cpu["one_core"] = one
 
-    if rank == 0:
-        out = {
-            "metric": METRIC, "value": value, "unit": "docs/s", "n_gpus": world, "steps": steps,
-            "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, random-init weights)",
-            "config": {"workload": w.name, "docs_per_gpu": N, "labels": M, "eval_positions_per_doc": a,
-                       "trie_nodes": trie.n_nodes, "trie": trie_stats, "hidden": d, "vocab": V,
-                       "q_heads": w.shape.n_q_heads,
-                       "kv_heads": w.shape.n_kv_heads, "doc_tokens_per_gpu": int(docs.doc_len.sum()),
-                       "l2": "inputs larger than L2 (doc KV %.2f GB + output head %.2f GB per step)" % (
-                           kv_bytes / 1e9, 2.0 * d * V / 1e9),
-                       "parallelism": f"replicas x{world} (documents sharded, no collective)"},
-            "roofline": roofline, "path_roofline": path, "stages_ms": stages_ms, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches_per_step * steps, "clocks": clk,
-        }
-        print(json.dumps(out), flush=True)
+    out = {
+        "metric": METRIC, "value": value, "unit": "docs/s", "n_gpus": 1, "steps": steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, random-init weights)",
+        "config": {"workload": w.name, "docs_per_gpu": N, "labels": M, "eval_positions_per_doc": a,
+                   "trie_nodes": trie.n_nodes, "trie": trie_stats, "hidden": d, "vocab": V,
+                   "q_heads": w.shape.n_q_heads,
+                   "kv_heads": w.shape.n_kv_heads, "doc_tokens_per_gpu": int(docs.doc_len.sum()),
+                   "l2": "inputs larger than L2 (doc KV %.2f GB + output head %.2f GB per step)" % (
+                       kv_bytes / 1e9, 2.0 * d * V / 1e9),
+                   "parallelism": "one replica (documents shard across GPUs with no collective)"},
+        "roofline": roofline, "path_roofline": path, "stages_ms": stages_ms, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches_per_step * steps, "clocks": clk,
+    }
+    print(json.dumps(out), flush=True)
 
 
-def run_join(args, world, rank, local):
+def run_join(args):
     """AI.IF over joined pairs: every anchor document against every partner
     (quail_join_if). One step = one call over all anchors; metric = pairs/s."""
     import torch
 
     import synthetic as S
     import trie_label_scoring_gb300 as Q
-    from tests import gpu_cases as C
     from trie_label_scoring_gb300.torch_inputs import kv_from_docs
 
     Q.build()
     w = S.WORKLOADS[args.workload]
     if args.docs:
         w = S.with_docs(w, args.docs)
-    model = C.device_model(w.shape, 0)
+    model = device_model(w.shape, 0)
     partners = S.make_labels(w, 0)
     yes, no = S.make_answers(0, w.shape.vocab)
-    docs = S.make_docs(w, rank)
+    docs = S.make_docs(w, 0)
     kv = kv_from_docs(docs)
     trie = Q.Trie(partners.labels, partners.root_token, w.shape.vocab, all_nodes=True)
     trie.upload()
@@ -599,9 +610,8 @@ def run_join(args, world, rank, local):
     for evs in stage_ev:
         for e in evs:
             e.record(stream)
-    clocks = ClockSampler(str(torch.cuda.get_device_properties(local).pci_bus_id))
+    clocks = ClockSampler(str(torch.cuda.get_device_properties(0).pci_bus_id))
     clocks.start()
-    barrier(world)
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ai = Q.STAGES.index("attention")  # only the roofline kernel's events inside the timed loop
@@ -611,11 +621,10 @@ def run_join(args, world, rank, local):
         step()
     end.record(stream)
     torch.cuda.synchronize()
-    barrier(world)
     clk = clocks.stop()
     Q.set_stage_events(None)
     Q.device_status()
-    elapsed_ms = max_over_ranks(world, start.elapsed_time(end))
+    elapsed_ms = start.elapsed_time(end)
     attention_ms = statistics.mean(ev[2 * ai].elapsed_time(ev[2 * ai + 1]) for ev in stage_ev)
     bd_ev = stage_ev[:min(steps, 20)]  # stage breakdown, after the timed region
     for evs in bd_ev:
@@ -640,32 +649,31 @@ def run_join(args, world, rank, local):
                 "attention_ms": attention_ms, "peak_kind": f"bf16 burst ({peaks['source']})",
                 "note": "FLOPs counted once per query row (the hi/lo splits double the issued work)"}
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if not args.no_cpu_baseline:
         from oracle import join as J
-        L = C.oracle_layer(w.shape, 0)
+        L = oracle_layer(w.shape, 0)
         t0 = time.time()
         done = 0
-        dk, dv = C.oracle_doc_kv(docs, 0)
+        dk, dv = oracle_doc_kv(docs, 0)
         while done < M and time.time() - t0 < 15.0:
             J.join_if(L, dk, dv, partners.root_token, [partners.labels[done]], yes, no)
             done += 1
         sec = time.time() - t0
         cpu = {"value": done / sec, "unit": "pairs/s", "cores": cores(), "kind": "oracle",
                "sample": f"anchor 0 with its first {done} partners ({sec:.1f} s)"}
-    if rank == 0:
-        out = {
-            "metric": "joined pairs scored/sec at 1 GB300 (AI.IF, TRUE/FALSE head)",
-            "value": pairs * world * steps / (elapsed_ms / 1e3), "unit": "pairs/s", "n_gpus": world,
-            "steps": steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, random-init weights)",
-            "config": {"workload": w.name, "anchors_per_gpu": N, "partners": M, "partner_trie_nodes": trie.n_nodes,
-                       "answer_spellings": len(yes) + len(no), "anchor_tokens_per_gpu": int(keys),
-                       "l2": "anchor KV %.2f GB per step" % (kv_bytes / 1e9),
-                       "parallelism": f"replicas x{world} (anchors sharded, no collective)"},
-            "roofline": roofline, "stages_ms": stages_ms, "cpu_baseline": cpu, "e2e": None,
-            "gpu_launches": launches_per_step * steps, "clocks": clk,
-        }
-        print(json.dumps(out), flush=True)
+    out = {
+        "metric": "joined pairs scored/sec at 1 GB300 (AI.IF, TRUE/FALSE head)",
+        "value": pairs * steps / (elapsed_ms / 1e3), "unit": "pairs/s", "n_gpus": 1,
+        "steps": steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, random-init weights)",
+        "config": {"workload": w.name, "anchors_per_gpu": N, "partners": M, "partner_trie_nodes": trie.n_nodes,
+                   "answer_spellings": len(yes) + len(no), "anchor_tokens_per_gpu": int(keys),
+                   "l2": "anchor KV %.2f GB per step" % (kv_bytes / 1e9),
+                   "parallelism": "one replica (anchors shard across GPUs with no collective)"},
+        "roofline": roofline, "stages_ms": stages_ms, "cpu_baseline": cpu, "e2e": None,
+        "gpu_launches": launches_per_step * steps, "clocks": clk,
+    }
+    print(json.dumps(out), flush=True)
 
 
 def time_oracle_ml(mw, base, bits, docs_ml, labels, budget_s: float) -> dict:
@@ -706,7 +714,7 @@ def time_oracle_ml(mw, base, bits, docs_ml, labels, budget_s: float) -> dict:
     return {"docs_per_s": 1.0 / t_doc, "t1": t1, "t2": t2, "t_doc": t_doc}
 
 
-def run_ml(args, world, rank, local):
+def run_ml(args):
     """trie_tree through the whole decoder stack (quail_classify_trie_tree_ml).
     One step = one call over all documents; metric = documents/s."""
     import torch
@@ -725,7 +733,7 @@ def run_ml(args, world, rank, local):
     bits = S.make_model_ml(sh, L, I, 0)
     model = model_ml_from_bits(bits, sh, I)
     labels = S.make_labels(base, 0)
-    docs_ml = S.make_docs_ml(base, L, rank)
+    docs_ml = S.make_docs_ml(base, L, 0)
     d0 = docs_ml[0]
     kv = kv_ml_from_docs(*docs_ml)
     trie = Q.Trie(labels.labels, labels.root_token, sh.vocab, labels.continuation)
@@ -768,10 +776,9 @@ def run_ml(args, world, rank, local):
         for i in gu_idx:
             sel[i] = evs[i]
         return sel
-    clocks = ClockSampler(str(torch.cuda.get_device_properties(local).pci_bus_id))
+    clocks = ClockSampler(str(torch.cuda.get_device_properties(0).pci_bus_id))
     clocks.start()
     time.sleep(0.3)
-    barrier(world)
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
@@ -780,13 +787,12 @@ def run_ml(args, world, rank, local):
         step()
     end.record(stream)
     torch.cuda.synchronize()
-    barrier(world)
     clk = clocks.stop()
     Q.set_stage_events(None)
     Q.device_status()
-    elapsed_ms = max_over_ranks(world, start.elapsed_time(end))
+    elapsed_ms = start.elapsed_time(end)
     ms_per_step = elapsed_ms / steps
-    value = N * world * steps / (elapsed_ms / 1e3)
+    value = N * steps / (elapsed_ms / 1e3)
     gate_up_ms = statistics.mean(ev[i].elapsed_time(ev[i + 1]) for ev in stage_ev for i in gu_idx[::2])
     # breakdown with every stage and span marked, after the timed region
     bd_ev = stage_ev[:min(steps, 10)]
@@ -828,9 +834,9 @@ def run_ml(args, world, rank, local):
             return list(kd) + list(vd) + [pt, dl]
 
         k_e2e = max(3, min(steps, 10))
-        e2e_ms = timed_e2e(stream, world, hks + hvs + [hpt, hdl], [flat(x) for x in kvs], e2e_call,
+        e2e_ms = timed_e2e(stream, hks + hvs + [hpt, hdl], [flat(x) for x in kvs], e2e_call,
                            [(lsc, o_ls), (prob, o_pr), (am, o_am)], k_e2e)
-        e2e = {"value": N * world * k_e2e / (e2e_ms / 1e3), "unit": "docs/s", "h2d_bytes_per_step": h2d,
+        e2e = {"value": N * k_e2e / (e2e_ms / 1e3), "unit": "docs/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": k_e2e, "input_buffers": 2}
 
     # ---- roofline of the dominant kernel: the gate|up GEMM of a layer, with
@@ -869,27 +875,26 @@ def run_ml(args, world, rank, local):
             "bytes_per_step": path_bytes, "flops_per_step": path_flops}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if not args.no_cpu_baseline:
         r = time_oracle_ml(mw, base, bits, docs_ml, labels, budget_s=60.0)
         cpu = {"value": r["docs_per_s"], "unit": "docs/s", "cores": cores(), "kind": "oracle",
                "sample": f"document 0 of {base.name} through the first 1 and 2 layers ({r['t1']:.1f} s, "
                          f"{r['t2']:.1f} s); per-document time extrapolated to {L} layers = {r['t_doc']:.1f} s"}
-    if rank == 0:
-        out = {
-            "metric": f"documents classified/sec at 1 GB300 (trie_tree through {L} decoder layers)",
-            "value": value, "unit": "docs/s", "n_gpus": world, "steps": steps, "warmup": max(args.warmup, 3),
-            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16", "data": "synthetic (seeded, random-init weights)",
-            "config": {"workload": mw.name, "docs_per_gpu": N, "labels": M, "eval_positions_per_doc": a,
-                       "rows": rows, "layers": L, "intermediate": I, "hidden": d, "vocab": V,
-                       "doc_tokens_per_gpu": int(keys),
-                       "l2": "inputs larger than L2 (weights %.2f GB + document KV %.2f GB per step)" % (
-                           2.0 * layer_params * L / 1e9, kv_bytes / 1e9),
-                       "parallelism": f"replicas x{world} (documents sharded, no collective)"},
-            "roofline": roofline, "path_roofline": path, "stages_ms": stages_ms, "layer_spans_ms": span_ms,
-            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * steps, "clocks": clk,
-        }
-        print(json.dumps(out), flush=True)
+    out = {
+        "metric": f"documents classified/sec at 1 GB300 (trie_tree through {L} decoder layers)",
+        "value": value, "unit": "docs/s", "n_gpus": 1, "steps": steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded, random-init weights)",
+        "config": {"workload": mw.name, "docs_per_gpu": N, "labels": M, "eval_positions_per_doc": a,
+                   "rows": rows, "layers": L, "intermediate": I, "hidden": d, "vocab": V,
+                   "doc_tokens_per_gpu": int(keys),
+                   "l2": "inputs larger than L2 (weights %.2f GB + document KV %.2f GB per step)" % (
+                       2.0 * layer_params * L / 1e9, kv_bytes / 1e9),
+                   "parallelism": "one replica (documents shard across GPUs with no collective)"},
+        "roofline": roofline, "path_roofline": path, "stages_ms": stages_ms, "layer_spans_ms": span_ms,
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * steps, "clocks": clk,
+    }
+    print(json.dumps(out), flush=True)
 
 
 def _group_rows(view, D: int) -> dict:
@@ -910,7 +915,7 @@ def _group_rows(view, D: int) -> dict:
     return np.array(rows)
 
 
-def run_shortlist(args, world, rank, local):
+def run_shortlist(args):
     """Huge label sets: grouped labels scored through the shortlist
     (quail_classify_trie_tree_shortlist). One step = one call over all
     documents; metric = documents/s."""
@@ -919,13 +924,12 @@ def run_shortlist(args, world, rank, local):
 
     import synthetic as S
     import trie_label_scoring_gb300 as Q
-    from tests import gpu_cases as C
     from trie_label_scoring_gb300.torch_inputs import bf16_tensor, kv_from_docs
 
     Q.build()
     sw = S.SHORTLIST_WORKLOADS[args.workload]
     w = S.with_docs(sw.base, args.docs) if args.docs else sw.base
-    model = C.device_model(w.shape, 0)
+    model = device_model(w.shape, 0)
     labels = S.make_labels(w, 0)
     K = len(labels.labels)
     G = sw.groups or (math.isqrt(K - 1) + 1)  # ceil(sqrt K)
@@ -934,7 +938,7 @@ def run_shortlist(args, world, rank, local):
     trie.upload()
     sl = Q.Shortlist(trie, 1)
     beam = sw.beam
-    docs = S.make_docs(w, rank)
+    docs = S.make_docs(w, 0)
     kv = kv_from_docs(docs)
     N = w.num_docs
     ws = torch.empty(Q.workspace_size_shortlist(model, trie, sl, beam, N, docs.max_doc_len), dtype=torch.uint8,
@@ -963,10 +967,9 @@ def run_shortlist(args, world, rank, local):
     for evs in stage_ev:
         for e in evs:
             e.record(stream)
-    clocks = ClockSampler(str(torch.cuda.get_device_properties(local).pci_bus_id))
+    clocks = ClockSampler(str(torch.cuda.get_device_properties(0).pci_bus_id))
     clocks.start()
     time.sleep(0.3)
-    barrier(world)
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     hs = Q.STAGES.index("head")  # only the roofline kernel's events inside the timed loop
@@ -976,13 +979,12 @@ def run_shortlist(args, world, rank, local):
         step()
     end.record(stream)
     torch.cuda.synchronize()
-    barrier(world)
     clk = clocks.stop()
     Q.set_stage_events(None)
     Q.device_status()
-    elapsed_ms = max_over_ranks(world, start.elapsed_time(end))
+    elapsed_ms = start.elapsed_time(end)
     ms_per_step = elapsed_ms / steps
-    value = N * world * steps / (elapsed_ms / 1e3)
+    value = N * steps / (elapsed_ms / 1e3)
     head_ms = statistics.mean(ev[2 * hs].elapsed_time(ev[2 * hs + 1]) for ev in stage_ev)
     bd_ev = stage_ev[:min(steps, 50)]  # stage breakdown, after the timed region
     torch.cuda.synchronize()
@@ -1040,9 +1042,9 @@ def run_shortlist(args, world, rank, local):
             Q.classify_trie_tree_shortlist(model, kvs[b], trie, sl, beam, N, ws, lsc, prob, am, sel, stream)
 
         k_e2e = max(3, min(steps, int(3000.0 / max(est_ms + 3.0, 1e-3))))
-        e2e_ms = timed_e2e(stream, world, [hk, hv, hpt, hdl], [list(x.tensors) for x in kvs], e2e_call,
+        e2e_ms = timed_e2e(stream, [hk, hv, hpt, hdl], [list(x.tensors) for x in kvs], e2e_call,
                            [(lsc, o_ls), (prob, o_pr), (am, o_am)], k_e2e)
-        e2e = {"value": N * world * k_e2e / (e2e_ms / 1e3), "unit": "docs/s", "h2d_bytes_per_step": h2d,
+        e2e = {"value": N * k_e2e / (e2e_ms / 1e3), "unit": "docs/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": k_e2e, "input_buffers": 2}
 
     # roofline: the second pass's output-head GEMM, FLOPs of the real rows
@@ -1066,43 +1068,42 @@ def run_shortlist(args, world, rank, local):
             "ms_per_step": ms_per_step, "frac": max(t_b, t_f) * 1e3 / ms_per_step}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if not args.no_cpu_baseline:
         from oracle import shortlist as OSL
         from oracle.trie import build_trie
         rw = OSL.rewrite_grouped(labels.labels, names, OSL.group_labels(labels.labels, G))
         ref_t = build_trie(rw, labels.root_token, V)
-        L = C.oracle_layer(w.shape, 0)
+        L = oracle_layer(w.shape, 0)
         L.lm_head()
         c0 = time.perf_counter()
         done = 0
         while done < N and (done == 0 or time.perf_counter() - c0 < 15.0):
-            dk_, dv_ = C.oracle_doc_kv(docs, done)
+            dk_, dv_ = oracle_doc_kv(docs, done)
             OSL.shortlist(L, dk_, dv_, ref_t, 1, beam)
             done += 1
         sec = time.perf_counter() - c0
         cpu = {"value": done / sec, "unit": "docs/s", "cores": cores(), "kind": "oracle",
                "sample": f"first {done} documents of {w.name} ({sec:.1f} s, oracle shortlist with the same "
                          f"groups and beam)"}
-    if rank == 0:
-        out = {
-            "metric": "documents classified/sec at 1 GB300 (shortlisted trie_tree over grouped labels)",
-            "value": value, "unit": "docs/s", "n_gpus": world, "steps": steps, "warmup": max(args.warmup, 3),
-            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16", "data": "synthetic (seeded, random-init weights)",
-            "config": {"workload": sw.name, "docs_per_gpu": N, "labels": K, "groups": G, "beam": beam,
-                       "trie_nodes": trie.n_nodes, "eval_positions_flat": a, "second_pass_rows": real_rows,
-                       "second_pass_rows_padded": pad_rows, "hidden": d, "vocab": V,
-                       "l2": "inputs larger than L2 (output head 0.78 GB read twice per step)",
-                       "parallelism": f"replicas x{world} (documents sharded, no collective)"},
-            "roofline": roofline, "path_roofline": path, "stages_ms": stages_ms,
-            "flat_trie_tree_ms": flat_ms, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches_per_step * steps, "clocks": clk,
-        }
-        print(json.dumps(out), flush=True)
+    out = {
+        "metric": "documents classified/sec at 1 GB300 (shortlisted trie_tree over grouped labels)",
+        "value": value, "unit": "docs/s", "n_gpus": 1, "steps": steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded, random-init weights)",
+        "config": {"workload": sw.name, "docs_per_gpu": N, "labels": K, "groups": G, "beam": beam,
+                   "trie_nodes": trie.n_nodes, "eval_positions_flat": a, "second_pass_rows": real_rows,
+                   "second_pass_rows_padded": pad_rows, "hidden": d, "vocab": V,
+                   "l2": "inputs larger than L2 (output head 0.78 GB read twice per step)",
+                   "parallelism": "one replica (documents shard across GPUs with no collective)"},
+        "roofline": roofline, "path_roofline": path, "stages_ms": stages_ms,
+        "flat_trie_tree_ms": flat_ms, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches_per_step * steps, "clocks": clk,
+    }
+    print(json.dumps(out), flush=True)
 
 
-def _timed_loop(stream, steps, world, call, n_stage_events=0, keep=None):
-    """K calls between CUDA events on `stream`, barrier + synchronize on both
+def _timed_loop(stream, steps, call, n_stage_events=0, keep=None):
+    """K calls between CUDA events on `stream`, synchronize on both
     sides; per-call stage events when n_stage_events > 0, of which only the
     indices in `keep` are handed to the library when given (an event between
     two kernels keeps the second from launching early). Returns
@@ -1117,7 +1118,6 @@ def _timed_loop(stream, steps, world, call, n_stage_events=0, keep=None):
     clocks = ClockSampler(str(torch.cuda.get_device_properties(torch.cuda.current_device()).pci_bus_id))
     clocks.start()
     time.sleep(0.3)
-    barrier(world)
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
@@ -1128,14 +1128,13 @@ def _timed_loop(stream, steps, world, call, n_stage_events=0, keep=None):
         call()
     end.record(stream)
     torch.cuda.synchronize()
-    barrier(world)
     clk = clocks.stop()
     Q.set_stage_events(None)
     Q.device_status()
-    return max_over_ranks(world, start.elapsed_time(end)), stage_ev, clk
+    return start.elapsed_time(end), stage_ev, clk
 
 
-def run_letters(args, world, rank, local):
+def run_letters(args):
     """The letters variant ("To Classify, Try a Trie Tree", sec. 3.3): one
     answer position per document scored against the letter tokens
     (quail_classify_letters). One step = one call over all documents."""
@@ -1143,17 +1142,16 @@ def run_letters(args, world, rank, local):
 
     import synthetic as S
     import trie_label_scoring_gb300 as Q
-    from tests import gpu_cases as C
     from trie_label_scoring_gb300.torch_inputs import kv_from_docs
 
     Q.build()
     w = S.WORKLOADS[args.workload]
     if args.docs:
         w = S.with_docs(w, args.docs)
-    model = C.device_model(w.shape, 0)
+    model = device_model(w.shape, 0)
     letters = S.make_labels(w, 0)
     tokens = [l[0] for l in letters.labels]
-    docs = S.make_docs(w, rank)
+    docs = S.make_docs(w, 0)
     kv = kv_from_docs(docs)
     N, M = w.num_docs, len(tokens)
     ws = torch.empty(Q.workspace_size(model, None, M, N, docs.max_doc_len, Q.MODE_LETTERS), dtype=torch.uint8,
@@ -1172,7 +1170,7 @@ def run_letters(args, world, rank, local):
     launches = Q.launch_count()
     steps = args.steps if args.steps is not None else 200
     ai = Q.STAGES.index("attention")
-    elapsed_ms, stage_ev, clk = _timed_loop(stream, steps, world, step, 10, keep=(2 * ai, 2 * ai + 1))
+    elapsed_ms, stage_ev, clk = _timed_loop(stream, steps, step, 10, keep=(2 * ai, 2 * ai + 1))
     attention_ms = statistics.mean(ev[2 * ai].elapsed_time(ev[2 * ai + 1]) for ev in stage_ev)
     bd_ev = stage_ev[:min(steps, 20)]  # stage breakdown, after the timed region
     for evs in bd_ev:
@@ -1187,26 +1185,25 @@ def run_letters(args, world, rank, local):
     kv_bytes = float(docs.doc_len.sum()) * w.shape.n_kv_heads * w.shape.head_dim * 2 * 2
     att = kv_bytes / (attention_ms / 1e3) / 1e9
     t_kv = kv_bytes / (peaks["hbm_gbs"] * 1e9)
-    if rank == 0:
-        out = {
-            "metric": "documents classified/sec at 1 GB300 (letters)", "value": N * world * steps / (elapsed_ms / 1e3),
-            "unit": "docs/s", "n_gpus": world, "steps": steps, "warmup": max(args.warmup, 3), "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic (seeded, random-init weights)",
-            "config": {"workload": w.name, "docs_per_gpu": N, "letters": M, "doc_tokens_per_gpu": int(docs.doc_len.sum()),
-                       "l2": "doc KV %.2f GB per step" % (kv_bytes / 1e9),
-                       "parallelism": f"replicas x{world} (documents sharded, no collective)"},
-            "roofline": {"bound": "hbm", "achieved": att, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": att / peaks["hbm_gbs"], "traffic": None, "kernel": "doc attention (one row per document)",
-                         "attention_ms": attention_ms, "peak_kind": f"HBM copy ({peaks['source']})"},
-            "path_roofline": {"t_kv_us": t_kv * 1e6, "ms_per_step": ms, "frac": t_kv * 1e3 / ms},
-            "stages_ms": stages_ms, "cpu_baseline": None, "e2e": None, "gpu_launches": launches * steps,
-            "clocks": clk,
-        }
-        print(json.dumps(out), flush=True)
+    out = {
+        "metric": "documents classified/sec at 1 GB300 (letters)", "value": N * steps / (elapsed_ms / 1e3),
+        "unit": "docs/s", "n_gpus": 1, "steps": steps, "warmup": max(args.warmup, 3), "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded, random-init weights)",
+        "config": {"workload": w.name, "docs_per_gpu": N, "letters": M, "doc_tokens_per_gpu": int(docs.doc_len.sum()),
+                   "l2": "doc KV %.2f GB per step" % (kv_bytes / 1e9),
+                   "parallelism": "one replica (documents shard across GPUs with no collective)"},
+        "roofline": {"bound": "hbm", "achieved": att, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": att / peaks["hbm_gbs"], "traffic": None, "kernel": "doc attention (one row per document)",
+                     "attention_ms": attention_ms, "peak_kind": f"HBM copy ({peaks['source']})"},
+        "path_roofline": {"t_kv_us": t_kv * 1e6, "ms_per_step": ms, "frac": t_kv * 1e3 / ms},
+        "stages_ms": stages_ms, "cpu_baseline": None, "e2e": None, "gpu_launches": launches * steps,
+        "clocks": clk,
+    }
+    print(json.dumps(out), flush=True)
 
 
-def run_decode(args, world, rank, local):
+def run_decode(args):
     """Greedy trie_decode ("To Classify, Try a Trie Tree", sec. 3.1) over a
     tree workload: one step of the bench = the decode steps it takes for every
     document to reach a label (quail_classify_trie_decode_step, called that
@@ -1216,16 +1213,15 @@ def run_decode(args, world, rank, local):
 
     import synthetic as S
     import trie_label_scoring_gb300 as Q
-    from tests import gpu_cases as C
     from trie_label_scoring_gb300.torch_inputs import kv_from_docs
 
     Q.build()
     w = S.WORKLOADS[args.workload]
     if args.docs:
         w = S.with_docs(w, args.docs)
-    model = C.device_model(w.shape, 0)
+    model = device_model(w.shape, 0)
     labels = S.make_labels(w, 0)
-    docs = S.make_docs(w, rank)
+    docs = S.make_docs(w, 0)
     kv = kv_from_docs(docs)
     trie = Q.Trie(labels.labels, labels.root_token, w.shape.vocab, labels.continuation)
     trie.upload()
@@ -1254,29 +1250,28 @@ def run_decode(args, world, rank, local):
         decode()
     Q.device_status()
     steps = args.steps if args.steps is not None else 100
-    elapsed_ms, _, clk = _timed_loop(stream, steps, world, decode)
+    elapsed_ms, _, clk = _timed_loop(stream, steps, decode)
     ms = elapsed_ms / steps
     peaks = measured_peaks()
     kv_bytes = float(docs.doc_len.sum()) * w.shape.n_kv_heads * w.shape.head_dim * 2 * 2
-    if rank == 0:
-        out = {
-            "metric": "documents classified/sec at 1 GB300 (greedy trie_decode)",
-            "value": N * world * steps / (elapsed_ms / 1e3), "unit": "docs/s", "n_gpus": world, "steps": steps,
-            "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, random-init weights)",
-            "config": {"workload": w.name, "docs_per_gpu": N, "labels": len(labels.labels),
-                       "decode_steps": n_steps, "doc_tokens_per_gpu": int(docs.doc_len.sum()),
-                       "parallelism": f"replicas x{world} (documents sharded, no collective)"},
-            "roofline": {"bound": "hbm", "achieved": n_steps * kv_bytes / (ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
-                         "unit": "GB/s", "frac": n_steps * kv_bytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],
-                         "traffic": None, "kernel": "whole decode (document KV re-read at every step)",
-                         "peak_kind": f"HBM copy ({peaks['source']})",
-                         "note": "the bytes are those of all documents at every step; decided documents skip "
-                                 "their attention, so this overstates the work of the later steps"},
-            "cpu_baseline": None, "e2e": None,
-            "gpu_launches": launches_per_step_call * n_steps * steps, "clocks": clk,
-        }
-        print(json.dumps(out), flush=True)
+    out = {
+        "metric": "documents classified/sec at 1 GB300 (greedy trie_decode)",
+        "value": N * steps / (elapsed_ms / 1e3), "unit": "docs/s", "n_gpus": 1, "steps": steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, random-init weights)",
+        "config": {"workload": w.name, "docs_per_gpu": N, "labels": len(labels.labels),
+                   "decode_steps": n_steps, "doc_tokens_per_gpu": int(docs.doc_len.sum()),
+                   "parallelism": "one replica (documents shard across GPUs with no collective)"},
+        "roofline": {"bound": "hbm", "achieved": n_steps * kv_bytes / (ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": n_steps * kv_bytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                     "traffic": None, "kernel": "whole decode (document KV re-read at every step)",
+                     "peak_kind": f"HBM copy ({peaks['source']})",
+                     "note": "the bytes are those of all documents at every step; decided documents skip "
+                             "their attention, so this overstates the work of the later steps"},
+        "cpu_baseline": None, "e2e": None,
+        "gpu_launches": launches_per_step_call * n_steps * steps, "clocks": clk,
+    }
+    print(json.dumps(out), flush=True)
 
 
 def main():
@@ -1289,23 +1284,20 @@ def main():
     if args.impl == "reference":
         run_reference(args, world, rank)
         return
-    world, rank, local = dist_setup()
+    gpu_setup(args)
     import synthetic as S
     if args.workload in S.ML_WORKLOADS:  # the whole decoder stack
-        run_ml(args, world, rank, local)
+        run_ml(args)
     elif args.workload in S.SHORTLIST_WORKLOADS:  # grouped labels through the shortlist
-        run_shortlist(args, world, rank, local)
+        run_shortlist(args)
     elif "-join" in args.workload:  # AI.IF join workloads (synthetic labels kind "join")
-        run_join(args, world, rank, local)
+        run_join(args)
     elif "-letters" in args.workload:  # the letters variant
-        run_letters(args, world, rank, local)
+        run_letters(args)
     elif args.decode:  # greedy trie_decode on a tree workload
-        run_decode(args, world, rank, local)
+        run_decode(args)
     else:
-        run_ours(args, world, rank, local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+        run_ours(args)
 
 
 if __name__ == "__main__":

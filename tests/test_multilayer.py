@@ -89,6 +89,101 @@ def test_silu_is_x_times_sigmoid():
     np.testing.assert_allclose(ML.silu(x), x * expit(x), rtol=1e-15, atol=1e-300)
 
 
+# The Qwen3-style MLP of a layer (the reading of the layer for "To Classify,
+# Try a Trie Tree", sec. 4.2, "goes through the whole LLM"): SiLU on the gate
+# projection, times the up projection, then the down projection, all applied
+# to RMSNorm(h) * g_post where h is the state after the attention residual.
+# The cases below are worked by hand with integer weights, so a swapped
+# gate/up role, a missing post-norm gain or the MLP read from the wrong state
+# changes the result by far more than the tolerance.
+def _silu_by_hand(x: float) -> float:
+    import math
+    return x / (1.0 + math.exp(-x))
+
+
+def _bits(a):
+    return S.f32_to_bf16_bits(np.asarray(a, dtype=np.float32))
+
+
+def _tiny_mlp_weights():
+    # d = 2, width 2; every entry is exact in bf16
+    return {"post_norm": np.array([2.0, 3.0]), "w_gate": np.array([[1.0, 0.0], [0.0, -1.0]]),
+            "w_up": np.array([[0.0, 1.0], [1.0, 1.0]]), "w_down": np.array([[1.0, 0.0], [1.0, 1.0]])}
+
+
+def _mlp_by_hand(h0: float, h1: float, eps: float, swap: bool = False, no_gain: bool = False) -> tuple:
+    """down(SiLU(gate x) * up x), x = RMSNorm(h) * g_post, for the weights of
+    _tiny_mlp_weights, written out scalar by scalar."""
+    import math
+    r = 1.0 / math.sqrt((h0 * h0 + h1 * h1) / 2.0 + eps)
+    x0, x1 = h0 * r * (1.0 if no_gain else 2.0), h1 * r * (1.0 if no_gain else 3.0)
+    g0, g1 = x0, -x1              # gate rows [1, 0], [0, -1]
+    u0, u1 = x1, x0 + x1          # up rows   [0, 1], [1, 1]
+    if swap:
+        g0, g1, u0, u1 = u0, u1, g0, g1
+    a0, a1 = _silu_by_hand(g0) * u0, _silu_by_hand(g1) * u1
+    return a0, a0 + a1            # down rows [1, 0], [1, 1]
+
+
+def test_mlp_closed_form_on_a_hand_worked_case():
+    from oracle import multilayer as ML
+    lw = _tiny_mlp_weights()
+    h = np.array([[1.0, 1.0], [3.0, -4.0]])
+    got = ML.mlp(lw, h, 0.0)
+    # h = [1, 1]: RMSNorm gives [1, 1], times the gains [2, 3]: x = [2, 3];
+    # gate = [2, -3], up = [3, 5]; SiLU(2) * 3 and SiLU(-3) * 5; down sums them
+    a0 = 2.0 / (1.0 + np.exp(-2.0)) * 3.0
+    a1 = -3.0 / (1.0 + np.exp(3.0)) * 5.0
+    np.testing.assert_allclose(got[0], [a0, a0 + a1], rtol=1e-14, atol=0)
+    np.testing.assert_allclose(got[1], _mlp_by_hand(3.0, -4.0, 0.0), rtol=1e-14, atol=0)
+
+
+def test_mlp_pin_separates_the_plausible_mistakes():
+    """The hand-worked values are far from what a swapped gate/up or a dropped
+    post-norm gain would give, so the closed-form pin above catches both."""
+    from oracle import multilayer as ML
+    lw = _tiny_mlp_weights()
+    for h in ([1.0, 1.0], [3.0, -4.0]):
+        got = ML.mlp(lw, np.array([h]), 0.0)[0]
+        for wrong in (_mlp_by_hand(*h, 0.0, swap=True), _mlp_by_hand(*h, 0.0, no_gain=True)):
+            assert np.abs(got - np.array(wrong)).max() > 0.1
+
+
+def test_layer_applies_the_mlp_to_the_state_after_attention():
+    """One layer with d = 2, one head of 2 dims, W_q = W_v = 0: the query is
+    zero, so the position attends uniformly to the 3 document tokens (V = 4)
+    and to itself (V = 0), O = [3, 3]; with W_o = I and E[token] = [-2, -2]
+    the state after attention is h = [1, 1]. The MLP must read that state,
+    through its post-norm gain: H = h + mlp(h), z = RMSNorm(H)."""
+    import math
+    import types
+
+    from oracle import multilayer as ML
+    eps = 1e-6
+    shape = types.SimpleNamespace(hidden=2, n_q_heads=1, n_kv_heads=1, head_dim=2, vocab=4, rms_eps=eps,
+                                  rope_theta=1e6)
+    lw = _tiny_mlp_weights()
+    layer = {"w_q": _bits(np.zeros((2, 2))), "w_k": _bits([[1.0, 0.0], [0.0, 1.0]]), "w_v": _bits(np.zeros((2, 2))),
+             "w_o": _bits([[1.0, 0.0], [0.0, 1.0]]), "q_norm": _bits([1.0, 1.0]), "k_norm": _bits([1.0, 1.0]),
+             "in_norm": _bits([1.0, 1.0]), "post_norm": _bits(lw["post_norm"]), "w_gate": _bits(lw["w_gate"]),
+             "w_up": _bits(lw["w_up"]), "w_down": _bits(lw["w_down"])}
+    bits = {"embed": _bits([[-2.0, -2.0], [0.0, 0.0], [0.0, 0.0], [0.0, 0.0]]), "lm_head": _bits(np.eye(4, 2)),
+            "final_norm": _bits([1.0, 1.0]), "layers": [layer]}
+    md = ML.ModelML(bits, shape)
+    doc_k = np.zeros((3, 1, 2))
+    doc_v = np.full((3, 1, 2), 4.0)
+    z = ML.sequence_states(md, [(doc_k, doc_v)], [0])[0]
+    m0, m1 = _mlp_by_hand(1.0, 1.0, eps)
+    H0, H1 = 1.0 + m0, 1.0 + m1
+    r = 1.0 / math.sqrt((H0 * H0 + H1 * H1) / 2.0 + eps)
+    np.testing.assert_allclose(z, [H0 * r, H1 * r], rtol=1e-12, atol=0)
+    # the MLP read from the state before attention ([-2, -2]) gives another z
+    w0, w1 = _mlp_by_hand(-2.0, -2.0, eps)
+    W0, W1 = 1.0 + w0, 1.0 + w1
+    rw = 1.0 / math.sqrt((W0 * W0 + W1 * W1) / 2.0 + eps)
+    assert np.abs(z - np.array([W0 * rw, W1 * rw])).max() > 0.1
+
+
 # ------------------------------------------------------------------ GPU parity
 def _run_ml(mw, docs_ml, labels, n_layers=None, seed=0):
     import torch

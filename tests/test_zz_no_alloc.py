@@ -5,7 +5,8 @@ claimed nearly all of the GPU's memory for its own KV pool, or a code path
 where a cudaMalloc would synchronise the device mid-flight. For them the
 library keeps one fixed device scratch array and this entry point places
 every intermediate there. These tests call it through the C ABI and check
-that two calls in a row give what the workspace-based entry point gives.
+that two calls in a row give exactly (bit for bit) what the workspace-based
+entry point gives, and, on the tiny shape, what the oracle gives.
 
 This file is named so that pytest collects it last: if it fails, a run that
 stops at the first failure has already run every other test.
@@ -61,9 +62,18 @@ def test_noalloc_matches_workspace_entry_point_twice(name, ndocs):
         Q.classify_trie_tree_noalloc(model, kv, trie, N, out_ls, out_pr, out_am)
         Q.device_status()
         ls_, pr_, am_ = out_ls.cpu().numpy(), out_pr.cpu().numpy(), out_am.cpu().numpy()
+        # the same kernels in the same order on the same inputs: bit-identical
+        assert np.array_equal(ls_, ref_ls), f"call {call}: log scores differ from the workspace entry point"
+        assert np.array_equal(pr_, ref_pr), f"call {call}: probabilities differ from the workspace entry point"
+        assert np.array_equal(am_, ref_am), f"call {call}: argmax differs from the workspace entry point"
+    if name.startswith("tiny"):  # and both agree with the oracle
+        from oracle import scoring as OS
+        from oracle.trie import build_trie
+        t = build_trie(ls.labels, ls.root_token, w.shape.vocab, ls.continuation)
+        L = C.oracle_layer(w.shape)
         for i in range(N):
-            C.check_scores(ls_[i], pr_[i], am_[i], ref_ls[i].astype(np.float64), ref_pr[i].astype(np.float64),
-                           int(ref_am[i]), f"call {call} doc {i}")
+            r = OS.trie_tree(L, *C.oracle_doc_kv(docs, i), t)
+            C.check_scores(ls_[i], pr_[i], am_[i], r["logscore"], r["prob"], r["argmax"], f"doc {i} vs oracle")
 
 
 def test_noalloc_rejects_calls_larger_than_the_scratch():

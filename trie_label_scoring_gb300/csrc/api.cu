@@ -1375,31 +1375,7 @@ quail_status quail_classify_trie_tree_noalloc(const quail_model_desc* model, con
   if (s != QUAIL_OK) return s;
   Buffers b;
   plan(scratch + image, model, a, num_docs, a, kv->max_doc_len, true, n_child, false, 0, &b);
-  const NodeTables nt{img.eval_token, img.eval_depth, img.eval_parent, a};
-  const RowMap map{a, nullptr, nullptr, nullptr};
-  const int rows = num_docs * a;
-  s = run_prologue(model, nt, b, ds, st);
-  if (s != QUAIL_OK) return s;
-  s = run_attention(model, kv, nt, map, num_docs, b, ds, st);
-  if (s != QUAIL_OK) return s;
-  s = run_wo_norm(model, nt, map, rows, b, ds, st);
-  if (s != QUAIL_OK) return s;
-  const int d = model->hidden;
-  const int n_tiles = (model->vocab + kHeadBN - 1) / kHeadBN;
-  CUtensorMap tA, tB;
-  s = encode_2d_bf16(&tA, b.z, round_up(rows, 128), d, d, 64, 128);
-  if (s != QUAIL_OK) return s;
-  s = encode_2d_bf16(&tB, model->lm_head, model->vocab, d, d, 64, kHeadBBoxRows);
-  if (s != QUAIL_OK) return s;
-  HeadEpilogueArgs ha{b.lse_part, b.child_logit, img.eval_child_offsets, img.eval_child_tokens, b.z_f32,
-                      static_cast<const bf16*>(model->lm_head), d, a, n_child, n_tiles};
-  CUDA_TRY(launch_gemm_head(tA, tB, rows, model->vocab, d, ha, ds->num_sms, ds->err, st));
-  LabelScoreArgs la{b.child_logit,       b.lse_part,          n_tiles,        b.lse,
-                    img.label_term_offsets, img.label_term_eval, img.label_term_slot, img.label_prefix_eval,
-                    img.eval_child_offsets, a,                  n_child,        trie->num_labels,
-                    label_logscore,      label_prob,          label_argmax};
-  CUDA_TRY(launch_label_score(la, num_docs, ds->num_sms, st));
-  return QUAIL_OK;
+  return trie_tree_pass(model, kv, trie, &img, num_docs, b, ds, st, label_logscore, label_prob, label_argmax, false);
 }
 
 
