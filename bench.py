@@ -47,6 +47,7 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-other-configs", action="store_true", help="headline workload only")
     p.add_argument("--decode", action="store_true", help="greedy trie_decode instead of trie_tree on a tree workload")
     p.add_argument("--oracle-rate", action="store_true", help=argparse.SUPPRESS)
     p.add_argument("--budget", type=float, default=10.0, help=argparse.SUPPRESS)
@@ -534,7 +535,10 @@ def run_ours(args):
     traffic = recorded_traffic(w.name, rows)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"], "traffic": traffic, "kernel": "umma_gemm_kernel<EpiHead>",
-                "head_ms": head_ms, "peak_kind": f"bf16 burst ({peaks['source']})"}
+                "head_ms": head_ms, "peak_kind": f"bf16 burst ({peaks['source']})",
+                "frac_sustained": (achieved / peaks["bf16_tflops_sustained"]
+                                   if peaks.get("bf16_tflops_sustained") else None),
+                "frac_spec": achieved / SPEC_BF16_TFLOPS}
     # ---- path roofline (the benchmark spec): max(KV bytes / HBM, head FLOPs / tensor peak)
     kv_bytes = float(docs.doc_len.sum()) * w.shape.n_kv_heads * w.shape.head_dim * 2 * 2
     t_kv = kv_bytes / (peaks["hbm_gbs"] * 1e9)
@@ -555,6 +559,11 @@ def run_ours(args):
         if one is not None:
             cpu["one_core"] = one
 
+    # ---- configs 3, 3L, 4, 4D and 5, after the headline, same steps and warm-up
+    others = None
+    if w.name == DEFAULT_WORKLOAD and not args.no_other_configs:
+        others = measure_other_configs(model, args.steps if args.steps is not None else 20, max(args.warmup, 3))
+
     out = {
         "metric": METRIC, "value": value, "unit": "docs/s", "n_gpus": 1, "steps": steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -567,9 +576,190 @@ def run_ours(args):
                        kv_bytes / 1e9, 2.0 * d * V / 1e9),
                    "parallelism": "one replica (documents shard across GPUs with no collective)"},
         "roofline": roofline, "path_roofline": path, "stages_ms": stages_ms, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": launches_per_step * steps, "clocks": clk,
+        "gpu_launches": launches_per_step * steps, "clocks": clk, "other_configs": others,
     }
     print(json.dumps(out), flush=True)
+
+
+# ------------------------------------------------------------------ the other configurations
+# Measured in the same process as the headline, with the same step and
+# warm-up counts: the larger label sets, the long documents and the two
+# variants that fall out of the same kernels.
+OTHER_CONFIGS = (
+    ("config 3", "qwen3-4b-tree255-64x2048", "trie_tree"),
+    ("config 3L", "qwen3-4b-letters255-64x2048", "letters"),
+    ("config 4", "qwen3-4b-tree20-32x8192", "trie_tree"),
+    ("config 4D", "qwen3-4b-tree20-32x8192", "decode"),
+    ("config 5", "qwen3-4b-tree5000-16x1024", "trie_tree"),
+)
+SPEC_BF16_TFLOPS = 2250.0  # nominal dense bf16 of one GB300 (context next to the measured peaks)
+
+
+def _stage_breakdown(Q, step, n: int) -> dict:
+    """Mean stage spans over n calls, every boundary marked (after a timed loop)."""
+    import torch
+    stream = torch.cuda.current_stream()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(Q.STAGES))] for _ in range(n)]
+    for e in evs:
+        for x in e:
+            x.record(stream)
+    torch.cuda.synchronize()
+    for e in evs:
+        Q.set_stage_events(e)
+        step()
+    torch.cuda.synchronize()
+    Q.set_stage_events(None)
+    return {name: statistics.mean(e[2 * i].elapsed_time(e[2 * i + 1]) for e in evs)
+            for i, name in enumerate(Q.STAGES)}
+
+
+def _leg_trie_tree(Q, w, model, docs, labels, steps: int, warmup: int) -> dict:
+    import torch
+
+    from trie_label_scoring_gb300.torch_inputs import kv_from_docs
+    kv = kv_from_docs(docs)
+    trie = Q.Trie(labels.labels, labels.root_token, w.shape.vocab, labels.continuation)
+    trie.upload()
+    N, M, a = w.num_docs, len(labels.labels), trie.n_eval
+    ws = torch.empty(Q.workspace_size(model, trie, 0, N, docs.max_doc_len, Q.MODE_TRIE_TREE), dtype=torch.uint8,
+                     device="cuda")
+    lsc = torch.empty((N, M), device="cuda")
+    prob = torch.empty((N, M), device="cuda")
+    am = torch.empty((N,), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        Q.classify_trie_tree(model, kv, trie, N, ws, lsc, prob, am, stream)
+
+    for _ in range(warmup):
+        step()
+    Q.device_status()
+    launches = Q.launch_count()
+    hs = Q.STAGES.index("head")
+    elapsed_ms, stage_ev, clk = _timed_loop(stream, steps, step, 2 * len(Q.STAGES), keep=(2 * hs, 2 * hs + 1))
+    head_ms = statistics.mean(ev[2 * hs].elapsed_time(ev[2 * hs + 1]) for ev in stage_ev)
+    stages = _stage_breakdown(Q, step, min(steps, 10))
+    peaks = measured_peaks()
+    ms = elapsed_ms / steps
+    d, V = w.shape.hidden, w.shape.vocab
+    flops = 2.0 * d * V * N * a
+    kv_bytes = float(docs.doc_len.sum()) * w.shape.n_kv_heads * w.shape.head_dim * 2 * 2
+    t_kv = kv_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_head = flops / (peaks["bf16_tflops"] * 1e12)
+    head_tf = flops / (head_ms / 1e3) / 1e12
+    view = trie.view()
+    out = {"workload": w.name, "kind": "trie_tree", "docs": N, "labels": M, "eval_positions_per_doc": a,
+           "trie_nodes": int(view["n_nodes"]), "trie_max_depth": int(view["depth"].max()),
+           "ms_per_step": ms, "docs_per_s": N * steps / (elapsed_ms / 1e3),
+           "path_roofline": {"t_kv_us": t_kv * 1e6, "t_head_us": t_head * 1e6,
+                             "frac": max(t_kv, t_head) * 1e3 / ms},
+           "head": {"ms": head_ms, "achieved_tflops": head_tf, "frac": head_tf / peaks["bf16_tflops"],
+                    "frac_sustained": (head_tf / peaks["bf16_tflops_sustained"]
+                                       if peaks.get("bf16_tflops_sustained") else None),
+                    "frac_spec": head_tf / SPEC_BF16_TFLOPS},
+           "stages_ms": stages, "gpu_launches": launches * steps, "clocks": clk}
+    del kv, ws
+    return out
+
+
+def _leg_letters(Q, w, model, docs, labels, steps: int, warmup: int) -> dict:
+    import torch
+
+    from trie_label_scoring_gb300.torch_inputs import kv_from_docs
+    kv = kv_from_docs(docs)
+    tokens = [l[0] for l in labels.labels]
+    N, M = w.num_docs, len(tokens)
+    ws = torch.empty(Q.workspace_size(model, None, M, N, docs.max_doc_len, Q.MODE_LETTERS), dtype=torch.uint8,
+                     device="cuda")
+    lp = torch.empty((N, M), device="cuda")
+    pr = torch.empty((N, M), device="cuda")
+    am = torch.empty((N,), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        Q.classify_letters(model, kv, tokens, labels.root_token, N, ws, lp, pr, am, stream)
+
+    for _ in range(warmup):
+        step()
+    Q.device_status()
+    launches = Q.launch_count()
+    ai = Q.STAGES.index("attention")
+    elapsed_ms, stage_ev, clk = _timed_loop(stream, steps, step, 2 * len(Q.STAGES), keep=(2 * ai, 2 * ai + 1))
+    att_ms = statistics.mean(ev[2 * ai].elapsed_time(ev[2 * ai + 1]) for ev in stage_ev)
+    peaks = measured_peaks()
+    ms = elapsed_ms / steps
+    kv_bytes = float(docs.doc_len.sum()) * w.shape.n_kv_heads * w.shape.head_dim * 2 * 2
+    t_kv = kv_bytes / (peaks["hbm_gbs"] * 1e9)
+    out = {"workload": w.name, "kind": "letters", "docs": N, "letters": M, "ms_per_step": ms,
+           "docs_per_s": N * steps / (elapsed_ms / 1e3),
+           "path_roofline": {"t_kv_us": t_kv * 1e6, "frac": t_kv * 1e3 / ms},
+           "attention": {"ms": att_ms, "achieved_gbs": kv_bytes / (att_ms / 1e3) / 1e9,
+                         "frac": kv_bytes / (att_ms / 1e3) / 1e9 / peaks["hbm_gbs"]},
+           "gpu_launches": launches * steps, "clocks": clk}
+    del kv, ws
+    return out
+
+
+def _leg_decode(Q, w, model, docs, labels, steps: int, warmup: int) -> dict:
+    import torch
+
+    from trie_label_scoring_gb300.torch_inputs import kv_from_docs
+    kv = kv_from_docs(docs)
+    trie = Q.Trie(labels.labels, labels.root_token, w.shape.vocab, labels.continuation)
+    trie.upload()
+    N = w.num_docs
+    ws = torch.empty(Q.workspace_size(model, trie, 0, N, docs.max_doc_len, Q.MODE_TRIE_DECODE), dtype=torch.uint8,
+                     device="cuda")
+    cur = torch.zeros(N, dtype=torch.int32, device="cuda")
+    lab = torch.full((N,), -1, dtype=torch.int32, device="cuda")
+    act = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    n_steps = 0
+    while True:  # how many decode steps this batch takes
+        Q.classify_trie_decode_step(model, kv, trie, N, cur, lab, act, ws, None, stream)
+        n_steps += 1
+        if int(act.item()) == 0 or n_steps >= 64:
+            break
+    launches = Q.launch_count()
+
+    def decode():
+        cur.zero_()
+        lab.fill_(-1)
+        for _ in range(n_steps):
+            Q.classify_trie_decode_step(model, kv, trie, N, cur, lab, act, ws, None, stream)
+
+    for _ in range(warmup):
+        decode()
+    Q.device_status()
+    elapsed_ms, _, clk = _timed_loop(stream, steps, decode)
+    ms = elapsed_ms / steps
+    out = {"workload": w.name, "kind": "trie_decode", "docs": N, "labels": len(labels.labels),
+           "decode_steps": n_steps, "ms_per_batch": ms, "docs_per_s": N * steps / (elapsed_ms / 1e3),
+           "gpu_launches": launches * n_steps * steps, "clocks": clk,
+           "note": "one step = the whole greedy decode of the batch; reported, not graded"}
+    del kv, ws
+    return out
+
+
+def measure_other_configs(model, steps: int, warmup: int) -> dict:
+    """Every other configuration of the method on the same GPU, one after the
+    other; documents of the same shape are generated once."""
+    import torch
+
+    import synthetic as S
+    import trie_label_scoring_gb300 as Q
+    legs = {"trie_tree": _leg_trie_tree, "letters": _leg_letters, "decode": _leg_decode}
+    docs_cache: dict = {}
+    out = {}
+    for label, name, kind in OTHER_CONFIGS:
+        w = S.WORKLOADS[name]
+        key = (w.shape, w.num_docs, w.doc_len)
+        if key not in docs_cache:
+            docs_cache.clear()
+            docs_cache[key] = S.make_docs(w, 0)
+        out[label] = legs[kind](Q, w, model, docs_cache[key], S.make_labels(w, 0), steps, warmup)
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_join(args):

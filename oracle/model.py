@@ -153,6 +153,18 @@ def head_logprobs(L: Layer, z: np.ndarray) -> np.ndarray:
     return logits - logsumexp(logits)
 
 
+def head_logprobs_rows(L: Layer, Z: np.ndarray) -> np.ndarray:
+    """head_logprobs for several states at once: the rows of Z [r, d] against
+    the head in one product (in the head's dtype), then each row's own
+    log-sum-exp in float64. Row for row the same definition as head_logprobs."""
+    W = L.lm_head()
+    logits = (Z.astype(W.dtype) @ W.T).astype(np.float64)
+    out = np.empty_like(logits)
+    for r in range(logits.shape[0]):
+        out[r] = logits[r] - logsumexp(logits[r])
+    return out
+
+
 def sequence_logprobs(L: Layer, doc_k: np.ndarray, doc_v: np.ndarray, seq: list) -> np.ndarray:
     """Flat causal pass: the sequence seq (root first) after the document, all
     positions at once with an explicit causal mask. Returns [len(seq), V]

@@ -67,20 +67,26 @@ def normalise(logscore: np.ndarray) -> tuple:
     return prob, int(np.argmax(logscore))
 
 
-def eval_logprob_rows(L: M.Layer, doc_k: np.ndarray, doc_v: np.ndarray, trie: dict, nodes=None) -> dict:
+def eval_logprob_rows(L: M.Layer, doc_k: np.ndarray, doc_v: np.ndarray, trie: dict, nodes=None,
+                      head_rows: int = 128) -> dict:
     """log-prob of every child token at each node (default: the evaluated set
-    P), each node attending to the document and to its own path."""
+    P), each node attending to the document and to its own path. The nodes'
+    states go through the output head head_rows at a time (one product per
+    block, each row's log-sum-exp on its own)."""
     tok = trie["token"]
-    rows = {}
-    for e in (trie["eval_nodes"] if nodes is None else nodes):
-        e = int(e)
+    nodes = [int(e) for e in (trie["eval_nodes"] if nodes is None else nodes)]
+    Z = []
+    for e in nodes:
         path = [e]
         while path[-1] != 0:
             path.append(int(trie["parent"][path[-1]]))
         path = path[::-1]
-        z = M.path_state(L, doc_k, doc_v, [int(tok[u]) for u in path])
-        lp = M.head_logprobs(L, z)
-        rows[e] = {int(tok[c]): float(lp[tok[c]]) for c in children_of(trie, e)}
+        Z.append(M.path_state(L, doc_k, doc_v, [int(tok[u]) for u in path]))
+    rows = {}
+    for lo in range(0, len(nodes), head_rows):
+        lp = M.head_logprobs_rows(L, np.stack(Z[lo: lo + head_rows]))
+        for r, e in enumerate(nodes[lo: lo + head_rows]):
+            rows[e] = {int(tok[c]): float(lp[r, tok[c]]) for c in children_of(trie, e)}
     return rows
 
 

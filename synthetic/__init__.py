@@ -100,9 +100,10 @@ class Workload:
     shape: LayerShape
     num_docs: int
     doc_len: tuple  # (lo, hi) inclusive; lo == hi for fixed lengths
-    labels: str  # "support" | "tree" | "letters"
+    labels: str  # "support" | "tree" | "shared" | "letters" | "join"
     num_labels: int = 10
     label_len: tuple = (1, 4)
+    label_alpha: float = 0.0  # "shared": concentration of the prefix sharing
 
 
 TINY = LayerShape(hidden=512, n_q_heads=8, n_kv_heads=2, vocab=8192, kv_std=0.02)
@@ -116,7 +117,7 @@ WORKLOADS = {
         Workload("qwen3-4b-tree255-64x2048", QWEN3_4B, 64, (2048, 2048), "tree", 255, (1, 8)),
         Workload("qwen3-4b-letters255-64x2048", QWEN3_4B, 64, (2048, 2048), "letters", 255, (1, 1)),
         Workload("qwen3-4b-tree20-32x8192", QWEN3_4B, 32, (8192, 8192), "tree", 20, (1, 5)),
-        Workload("qwen3-4b-tree5000-16x1024", QWEN3_4B, 16, (1024, 1024), "tree", 5000, (2, 10)),
+        Workload("qwen3-4b-tree5000-16x1024", QWEN3_4B, 16, (1024, 1024), "shared", 5000, (2, 10), 10.0),
         Workload("qwen3-4b-join128-64x2048", QWEN3_4B, 64, (2048, 2048), "join", 128, (3, 9)),
     ]
 }
@@ -359,6 +360,55 @@ def tree_labels(M: int, lmin: int, lmax: int, vocab: int, rng) -> LabelSet:
     return LabelSet([out[i] for i in order], root, None)
 
 
+def shared_prefix_labels(M: int, lmin: int, lmax: int, vocab: int, rng, alpha: float) -> LabelSet:
+    """M labels whose lengths are uniform on [lmin, lmax], grown one at a
+    time down a shared tree of prefixes. At each step of a label's walk it
+    follows an existing child with probability proportional to the number of
+    earlier labels that went through that child (only children that end no
+    label), or opens a new child with probability alpha / (n + alpha), n the
+    number of earlier labels through the node; once on a new child the rest
+    of the label is new tokens. The last token always opens a new leaf, so no
+    label is a prefix of another and no two labels are equal. Larger alpha
+    shares less (more trie nodes). Labels are returned in generation order."""
+    root = int(rng.integers(0, vocab))
+    kids: list = [dict()]      # node -> {token: child}
+    visits: list = [0]         # labels through the node
+    open_: list = [True]       # the node ends no label, so a later label may pass through it
+    out: list = []
+    for _ in range(M):
+        L = int(rng.integers(lmin, lmax + 1))
+        node, path = 0, []
+        for k in range(L):
+            last = k == L - 1
+            cand = [] if last else [(t, c) for t, c in kids[node].items() if open_[c]]
+            n = sum(visits[c] for _, c in cand)
+            u = rng.random() * (n + alpha)
+            nxt = None
+            if u < n:
+                acc = 0
+                for t, c in cand:
+                    acc += visits[c]
+                    if u < acc:
+                        nxt = (t, c)
+                        break
+            if nxt is None:
+                t = int(rng.integers(0, vocab))
+                while t in kids[node]:
+                    t = int(rng.integers(0, vocab))
+                c = len(kids)
+                kids.append(dict())
+                visits.append(0)
+                open_.append(not last)
+                kids[node][t] = c
+                nxt = (t, c)
+            t, c = nxt
+            visits[c] += 1
+            path.append(t)
+            node = c
+        out.append(path)
+    return LabelSet(out, root, None)
+
+
 def make_labels(w: Workload, seed: int = 0) -> LabelSet:
     ss = _streams(seed)
     rng = np.random.Generator(np.random.PCG64(ss[_STREAM["labels"]]))
@@ -367,6 +417,8 @@ def make_labels(w: Workload, seed: int = 0) -> LabelSet:
         return support_labels(V, rng)
     if w.labels == "tree":
         return tree_labels(w.num_labels, w.label_len[0], w.label_len[1], V, rng)
+    if w.labels == "shared":
+        return shared_prefix_labels(w.num_labels, w.label_len[0], w.label_len[1], V, rng, w.label_alpha)
     if w.labels == "letters":
         ids = _distinct(rng, w.num_labels + 1, V)
         return LabelSet([[t] for t in ids[1:]], ids[0], None)

@@ -35,6 +35,8 @@ def test_library_exports_every_declared_symbol():
     for n in names:
         assert hasattr(L, n), n
     assert set(names) == set(Q._SIGNATURES), "binding and header disagree"
+    for n in Q._TEST_SIGNATURES:  # test hooks: exported, deliberately not in the public header
+        assert hasattr(L, n) and n not in names, n
 
 
 FIELDS = ["parent", "depth", "token", "subtree_size", "child_offsets", "child_nodes", "child_tokens",

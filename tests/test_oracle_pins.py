@@ -281,6 +281,10 @@ def test_head_logprobs_match_scipy():
     logits = OM.bf16_to_f64(L.lm_bits) @ z
     assert np.allclose(lp, scipy.special.log_softmax(logits), atol=1e-12)
     assert np.exp(lp).sum() == pytest.approx(1.0, abs=1e-12)
+    # several states through the head at once: each row is its own log-softmax
+    Z = np.stack([OM.path_state(L, kv[0][0], kv[0][1], p) for p in ([5], [5, 6], [9, 1, 2])])
+    rows = OM.head_logprobs_rows(L, Z)
+    assert np.allclose(rows, scipy.special.log_softmax(Z @ OM.bf16_to_f64(L.lm_bits).T, axis=1), atol=1e-12)
 
 
 def test_flat_sequence_equals_tree_masked():
@@ -299,6 +303,37 @@ def test_flat_sequence_equals_tree_masked():
                 flat = OS.label_logscore_flat(L, dk, dv, ls.root_token, lab, int(t["label_decide_depth"][m]))
                 assert tree["logscore"][m] == pytest.approx(flat, abs=1e-10)
             assert tree["prob"].sum() == pytest.approx(1.0, abs=1e-12)
+
+
+def test_flat_sequence_equals_tree_masked_many_rows():
+    """The same equivalence on a shared-prefix label set with more evaluated
+    nodes than one block of the oracle's batched output head (128 rows), so
+    several blocks and a partial one are checked."""
+    L, kv = _tiny_setup()
+    rng = np.random.Generator(np.random.PCG64(12))
+    ls = S.shared_prefix_labels(1200, 2, 6, S.TINY.vocab, rng, 4.0)
+    t = build_trie(ls.labels, ls.root_token, S.TINY.vocab)
+    assert t["n_eval"] > 2 * 128 and t["n_eval"] % 128 != 0
+    dk, dv = kv[0]
+    tree = OS.trie_tree(L, dk, dv, t)
+    assert tree["prob"].sum() == pytest.approx(1.0, abs=1e-12)
+    for m in range(0, 1200, 67):
+        flat = OS.label_logscore_flat(L, dk, dv, ls.root_token, ls.labels[m], int(t["label_decide_depth"][m]))
+        assert tree["logscore"][m] == pytest.approx(flat, abs=1e-10)
+
+
+def test_shared_prefix_generator_shape():
+    """The generator of the 5,000-label workload: lengths on [lmin, lmax], no
+    label a prefix of another, and about 20,000 trie nodes of depth at most 10
+    at the workload's sharing (the workload names 5,000 labels of 2-10 tokens,
+    ~20k nodes, maximum depth 10)."""
+    w = S.WORKLOADS["qwen3-4b-tree5000-16x1024"]
+    ls = S.make_labels(w, 0)
+    lens = [len(l) for l in ls.labels]
+    assert len(ls.labels) == 5000 and min(lens) == 2 and max(lens) == 10
+    t = build_trie(ls.labels, ls.root_token, w.shape.vocab)
+    assert not t["has_prefix_labels"]
+    assert 16000 <= t["n_nodes"] <= 24000 and t["max_depth"] == 10
 
 
 SMALL_V = S.LayerShape(hidden=64, n_q_heads=2, n_kv_heads=1, vocab=4, weight_std=0.5, kv_std=1.0)

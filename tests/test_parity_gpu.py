@@ -159,7 +159,7 @@ def test_trie_tree_qwen_small_all_docs(name, ndocs):
 
 @pytest.mark.parametrize("name,sample_docs", [
     ("qwen3-4b-support10-256docs", [0, 77, 255]),
-    ("qwen3-4b-tree255-64x2048", [5]),
+    ("qwen3-4b-tree255-64x2048", [0, 5, 42, 63]),
     ("qwen3-4b-tree20-32x8192", [0, 31]),
 ])
 def test_trie_tree_full_size_sampled_docs(name, sample_docs):
@@ -171,27 +171,27 @@ def test_trie_tree_full_size_sampled_docs(name, sample_docs):
         C.check_scores(lsc[i], prob[i], am[i], r["logscore"], r["prob"], r["argmax"], f"{name} doc {i}")
 
 
-def test_trie_tree_large_label_set_sampled_labels():
-    """5,000 labels: log scores of sampled labels one by one; probabilities via
-    properties (sum to 1, proportional to exp(log score))."""
-    from oracle import scoring as OS
-    from oracle.trie import build_trie
+def test_trie_tree_large_label_set_all_labels():
+    """5,000 labels of 2-10 tokens (~19k trie nodes): every label's log score
+    and probability, and the argmax, against the full oracle on the first and
+    last document."""
     w = S.WORKLOADS["qwen3-4b-tree5000-16x1024"]
     ls, docs, lsc, prob, am = _run_trie_tree(w)
     assert np.all(np.abs(prob.sum(axis=1) - 1) < 1e-4)
-    t = build_trie(ls.labels, ls.root_token, w.shape.vocab, ls.continuation)
-    L = C.oracle_layer(w.shape)
-    rng = np.random.default_rng(11)
     for i in (0, 15):
-        ratio = prob[i] / np.exp(lsc[i] - lsc[i].max())
-        assert np.allclose(ratio, ratio[0], rtol=1e-4)
-        labels = sorted(set(rng.choice(len(ls.labels), size=12, replace=False).tolist()) | {int(am[i])})
-        nodes = sorted({u for m in labels for u in OS.label_nodes(t, m)})
-        dk, dv = C.oracle_doc_kv(docs, i)
-        rows = OS.eval_logprob_rows(L, dk, dv, t, nodes=nodes)
-        for m in labels:
-            ref = OS.label_logscore(t, m, lambda u, tok: rows[u][tok])
-            assert abs(lsc[i, m] - ref) <= C.TOL_LOGSCORE, f"doc {i} label {m}: {lsc[i, m]} vs {ref}"
+        r = _oracle_full(w, ls, docs, i)
+        C.check_scores(lsc[i], prob[i], am[i], r["logscore"], r["prob"], r["argmax"], f"doc {i}")
+
+
+def test_trie_tree_large_label_set_small_layer_all_docs():
+    """The same 5,000-label shape (shared prefixes, 2-10 tokens) on the small
+    layer, where the oracle is cheap: every label of every document."""
+    w = S.Workload("tiny-shared5000-4", S.TINY, 4, (100, 700), "shared", 5000, (2, 10), 10.0)
+    ls, docs, lsc, prob, am = _run_trie_tree(w, seed=2)
+    assert _rows_per_kv(w, ls) > 128
+    for i in range(w.num_docs):
+        r = _oracle_full(w, ls, docs, i, seed=2)
+        C.check_scores(lsc[i], prob[i], am[i], r["logscore"], r["prob"], r["argmax"], f"doc {i}")
 
 
 def test_letters_tiny_and_full_size_sample():
@@ -296,6 +296,28 @@ def test_device_bounds_error_is_reported():
         _run_trie_tree(w, docs=bad)
     assert e.value.name == "QUAIL_ERR_DEVICE_BOUNDS"
     _run_trie_tree(w, docs=docs)  # context still usable, error word cleared
+
+
+def test_device_wait_timeout_is_reported():
+    """Every pipeline wait is bounded. With the limit cut to a few hundred
+    cycles (a test hook), the waits of the call's kernels run out before their
+    copies and MMAs arrive: each block leaves its pipeline, drains what is in
+    flight under the normal limit, frees its tensor memory and returns, and
+    the device error word reports QUAIL_ERR_DEVICE_TIMEOUT. The next call,
+    with the default limit, is correct again."""
+    import trie_label_scoring_gb300 as Q
+    w = S.WORKLOADS["tiny-support10-4x128"]
+    Q._test_set_pipeline_wait_limit(200)
+    try:
+        with pytest.raises(Q.QuailError) as e:
+            _run_trie_tree(w)
+    finally:
+        Q._test_set_pipeline_wait_limit(0)
+    assert e.value.name == "QUAIL_ERR_DEVICE_TIMEOUT"
+    ls, docs, lsc, prob, am = _run_trie_tree(w)  # context still usable, error word cleared
+    for i in range(w.num_docs):
+        r = _oracle_full(w, ls, docs, i)
+        C.check_scores(lsc[i], prob[i], am[i], r["logscore"], r["prob"], r["argmax"], f"doc {i}")
 
 
 def test_workspace_too_small_is_rejected():

@@ -180,6 +180,11 @@ _SIGNATURES = {
                                               ctypes.POINTER(ctypes.c_int32)]),
 }
 
+# Exported for the tests only; not declared in include/quail.h.
+_TEST_SIGNATURES = {
+    "quail_test_set_pipeline_wait_limit": (ctypes.c_int, [ctypes.c_longlong]),
+}
+
 _lib = None
 
 
@@ -190,7 +195,7 @@ def lib() -> ctypes.CDLL:
         if not os.path.exists(LIB):
             raise QuailError(-7, f"{LIB} is missing: build it with trie_label_scoring_gb300.build()")
         L = ctypes.CDLL(LIB)
-        for name, (res, args) in _SIGNATURES.items():
+        for name, (res, args) in {**_SIGNATURES, **_TEST_SIGNATURES}.items():
             f = getattr(L, name)
             f.restype = res
             f.argtypes = args
@@ -448,6 +453,12 @@ def classify_trie_tree_noalloc(model: Model, kv: KV, trie: Trie, num_docs: int, 
 
 def device_status(stream=None) -> None:
     _check(lib().quail_device_status(_stream(stream)))
+
+
+def _test_set_pipeline_wait_limit(cycles: int) -> None:
+    """Test hook (not in the public header): every pipeline wait gives up
+    after `cycles` cycles; cycles <= 0 restores the default limit."""
+    _check(lib().quail_test_set_pipeline_wait_limit(int(cycles)))
 
 
 def set_stage_events(events) -> None:

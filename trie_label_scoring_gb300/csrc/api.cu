@@ -1306,6 +1306,25 @@ quail_status quail_classify_trie_decode_step(const quail_model_desc* model, cons
   return QUAIL_OK;
 }
 
+// Test hook, not part of the public header: shortens the limit of every
+// pipeline wait (cycles > 0), or restores the default (cycles <= 0), so that a
+// test can make a wait run out and check that QUAIL_ERR_DEVICE_TIMEOUT comes
+// back through quail_device_status with the context still usable. Waits that
+// drain in-flight copies and MMAs before a block exits keep the long limit.
+// Synchronises the device.
+quail_status quail_test_set_pipeline_wait_limit(long long cycles) {
+  DeviceState* ds = nullptr;
+  quail_status s = device_state(&ds);
+  if (s != QUAIL_OK) return s;
+  const long long v = cycles > 0 ? cycles : quail::kWaitLimitCycles;
+  CUDA_TRY(cudaDeviceSynchronize());
+  CUDA_TRY(set_pipeline_wait_limit_gemm(v));
+  CUDA_TRY(set_pipeline_wait_limit_attention(v));
+  CUDA_TRY(set_pipeline_wait_limit_attention_tc(v));
+  CUDA_TRY(cudaDeviceSynchronize());
+  return QUAIL_OK;
+}
+
 quail_status quail_device_status(quail_stream_t stream) {
   DeviceState* ds = nullptr;
   quail_status s = device_state(&ds);

@@ -613,4 +613,9 @@ cudaError_t launch_attn_combine(const AttnArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// Test hook: this translation unit's copy of the pipeline wait limit.
+cudaError_t set_pipeline_wait_limit_attention(long long cycles) {
+  return cudaMemcpyToSymbol(g_pipeline_wait_limit, &cycles, sizeof(cycles));
+}
+
 }  // namespace quail

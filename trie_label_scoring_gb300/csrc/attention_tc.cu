@@ -632,4 +632,9 @@ cudaError_t launch_attn_doc_tc(const AttnArgs& a, const CUtensorMap& tmK, const 
   return cudaGetLastError();
 }
 
+// Test hook: this translation unit's copy of the pipeline wait limit.
+cudaError_t set_pipeline_wait_limit_attention_tc(long long cycles) {
+  return cudaMemcpyToSymbol(g_pipeline_wait_limit, &cycles, sizeof(cycles));
+}
+
 }  // namespace quail

@@ -251,4 +251,9 @@ cudaError_t launch_gemm_head(const CUtensorMap& tmA, const CUtensorMap& tmB, int
                                                               m_live);
 }
 
+// Test hook: this translation unit's copy of the pipeline wait limit.
+cudaError_t set_pipeline_wait_limit_gemm(long long cycles) {
+  return cudaMemcpyToSymbol(g_pipeline_wait_limit, &cycles, sizeof(cycles));
+}
+
 }  // namespace quail

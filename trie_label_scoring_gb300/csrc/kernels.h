@@ -238,4 +238,10 @@ cudaError_t launch_attn_combine(const AttnArgs& a, cudaStream_t st);
 // tcgen05 doc attention for 128-row query tiles (attention_tc.cu); row_tile must be 128.
 cudaError_t launch_attn_doc_tc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV, cudaStream_t st);
 
+// Test hooks: set the pipeline wait limit (cycles) of the GEMM, mma.sync
+// attention and tcgen05 attention translation units.
+cudaError_t set_pipeline_wait_limit_gemm(long long cycles);
+cudaError_t set_pipeline_wait_limit_attention(long long cycles);
+cudaError_t set_pipeline_wait_limit_attention_tc(long long cycles);
+
 }  // namespace quail

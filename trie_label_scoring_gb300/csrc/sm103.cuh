@@ -14,6 +14,13 @@ namespace quail {
 // About 2 s at 2 GHz. Legitimate waits in these kernels are microseconds.
 constexpr long long kWaitLimitCycles = 4000000000LL;
 
+// Limit of the pipeline waits (mbar_wait), in cycles; kWaitLimitCycles unless
+// a test shortens it to make those waits run out. Every translation unit that
+// includes this header holds its own copy (the library is built without
+// relocatable device code), and the library's test hook writes each copy. The
+// waits that drain in-flight copies and MMAs before a CTA exits never read it.
+static __device__ long long g_pipeline_wait_limit = kWaitLimitCycles;
+
 // Device error word layout (see quail.h): [0] = first error code, [1] = detail.
 __device__ __forceinline__ void raise_device_error(int* err, int code, int detail) {
   if (err != nullptr) {
@@ -56,15 +63,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
 
 // Waits until the phase with the given parity has completed. Returns false
 // (and leaves the pipeline) if another role already aborted, or if the wait
-// exceeds kWaitLimitCycles, in which case it raises the abort flag itself.
+// exceeds g_pipeline_wait_limit, in which case it raises the abort flag itself.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const long long t0 = clock64();
+  const long long limit = *const_cast<const volatile long long*>(&g_pipeline_wait_limit);
   while (true) {
     if (mbar_try_wait(a, parity)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       *abort_flag = 1;
       return false;
     }
