@@ -126,22 +126,50 @@ cudaError_t launch_umma(const CUtensorMap& tmA, const BSet& bset, int M, int N, 
   static_assert(smem <= 232448, "shared memory per CTA");
   auto kern = umma_gemm_kernel<BN, STAGES, SPLIT_A, Epi, CM>;
   static int configured_device = -1;  // the attribute is set per device
+  static int resident = 0;            // CTAs of this kernel that can be resident at once (whole clusters)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
+    resident = num_sms;
+    if (CM > 1) {
+      // Clusters are placed within one GPC, so a GPC with an odd number of
+      // free SMs leaves one idle: a persistent grid of num_sms CTAs could
+      // then hold clusters that only start when others finish.
+      cudaLaunchConfig_t q = {};
+      q.gridDim = dim3(num_sms / CM * CM, 1, 1);
+      q.blockDim = dim3(kGemmThreads, 1, 1);
+      q.dynamicSmemBytes = smem;
+      cudaLaunchAttribute qa[1];
+      qa[0].id = cudaLaunchAttributeClusterDimension;
+      qa[0].val.clusterDim.x = CM;
+      qa[0].val.clusterDim.y = 1;
+      qa[0].val.clusterDim.z = 1;
+      q.attrs = qa;
+      q.numAttrs = 1;
+      int clusters = 0;
+      e = cudaOccupancyMaxActiveClusters(&clusters, kern, &q);
+      if (e != cudaSuccess) return e;
+      if (clusters > 0 && clusters * CM < resident) resident = clusters * CM;
+    }
     configured_device = dev;
   }
   const int m_tiles = (M + kGemmBM - 1) / kGemmBM;
   const int units = ((m_tiles + CM - 1) / CM * CM) * ((N + BN - 1) / BN) * k_splits;
-  int grid = units < num_sms ? units : num_sms;
+  // Walk M-major when A is the larger operand (a W_o over many rows); pairs
+  // share B bands, so they always walk N bands.
+  const double a_bytes = static_cast<double>(M) * nk * kGemmBK * 2.0 * (SPLIT_A ? 2 : 1);
+  const double b_bytes = static_cast<double>(N) * nk * kGemmBK * 2.0;
+  const int m_major = (CM == 1 && a_bytes > b_bytes) ? 1 : 0;
+  int grid = units < resident ? units : resident;
   grid = grid / CM * CM;  // whole clusters; units is a multiple of CM
   if (grid <= 0) return cudaSuccess;
   if (CM == 1) {
     count_launch();
-    return launch_pdl(kern, dim3(grid), dim3(kGemmThreads), smem, st, tmA, bset, M, N, nk, k_splits, epi, err, m_live);
+    return launch_pdl(kern, dim3(grid), dim3(kGemmThreads), smem, st, tmA, bset, M, N, nk, k_splits, m_major, epi, err,
+                      m_live);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
@@ -158,7 +186,7 @@ cudaError_t launch_umma(const CUtensorMap& tmA, const BSet& bset, int M, int N, 
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   count_launch();
-  return cudaLaunchKernelEx(&cfg, kern, tmA, bset, M, N, nk, k_splits, epi, err, m_live);
+  return cudaLaunchKernelEx(&cfg, kern, tmA, bset, M, N, nk, k_splits, m_major, epi, err, m_live);
 }
 
 }  // namespace

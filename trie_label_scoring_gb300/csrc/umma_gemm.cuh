@@ -69,14 +69,23 @@ struct GemmUnit {
 };
 
 // unit -> (k-split, tile) with the k-split slowest, so the CTAs resident at
-// one time share B bands and A rows in L2; tile -> (n band, m tile), N-band-major.
-__device__ __forceinline__ GemmUnit gemm_unit(int u, int m_tiles, int n_tiles, int k_splits, int nk) {
+// one time share B bands and A rows in L2; tile -> (n band, m tile),
+// N-band-major (consecutive units share a B band), or M-major when A is the
+// larger operand (consecutive units share an A tile, so A streams from DRAM
+// once while the smaller B stays in L2).
+__device__ __forceinline__ GemmUnit gemm_unit(int u, int m_tiles, int n_tiles, int k_splits, int nk,
+                                              bool m_major) {
   GemmUnit g;
   const int tiles = m_tiles * n_tiles;
   g.ks = u / tiles;
   const int tile = u - g.ks * tiles;
-  g.n_blk = tile / m_tiles;
-  g.m_blk = tile - g.n_blk * m_tiles;
+  if (m_major) {
+    g.m_blk = tile / n_tiles;
+    g.n_blk = tile - g.m_blk * n_tiles;
+  } else {
+    g.n_blk = tile / m_tiles;
+    g.m_blk = tile - g.n_blk * m_tiles;
+  }
   g.kb0 = g.ks * nk / k_splits;
   g.kb1 = (g.ks + 1) * nk / k_splits;
   return g;
@@ -92,7 +101,7 @@ struct BPrefetch {
     while (kb >= kb1) {  // advance to this CTA's next unit
       u += gridDim.x;
       if (u >= num_units) return;
-      const GemmUnit h = gemm_unit(u, m_tiles_s, n_tiles, k_splits, nk);
+      const GemmUnit h = gemm_unit(u, m_tiles_s, n_tiles, k_splits, nk, false);
       int bi = 0;
       while (bi + 1 < bs.count && h.n_blk * bn >= bs.n_begin[bi + 1]) ++bi;
       map = &bs.map[bi];
@@ -119,7 +128,7 @@ struct BPrefetch {
 template <int BN, int STAGES, bool SPLIT_A, class Epi, int CM = 1>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ BSet bset, int M, int N,
-                     int nk, int k_splits, Epi epi, int* err, const int* m_live) {
+                     int nk, int k_splits, int m_major, Epi epi, int* err, const int* m_live) {
   static_assert(CM == 1 || (CM == 2 && !SPLIT_A && BN % 16 == 0), "pairs: plain A, B band split in two halves");
   using Cfg = GemmCfg<BN, STAGES, SPLIT_A>;
   constexpr uint32_t kBHalf = Cfg::kBBytes / CM;  // bytes of B each CTA of a pair loads
@@ -183,7 +192,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool ok = true;
       BPrefetch pf{static_cast<int>(blockIdx.x) - static_cast<int>(gridDim.x), 0, 0, 0, nullptr};
       for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-        const GemmUnit g = gemm_unit(u, m_tiles_s, n_tiles, k_splits, nk);
+        const GemmUnit g = gemm_unit(u, m_tiles_s, n_tiles, k_splits, nk, m_major != 0);
         const int n0 = g.n_blk * BN;
         int bi = 0;
         while (bi + 1 < bset.count && n0 >= bset.n_begin[bi + 1]) ++bi;
@@ -252,7 +261,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-        const GemmUnit g = gemm_unit(u, m_tiles_s, n_tiles, k_splits, nk);
+        const GemmUnit g = gemm_unit(u, m_tiles_s, n_tiles, k_splits, nk, m_major != 0);
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -307,7 +316,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
       if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) break;
       tc_fence_after();
-      const GemmUnit g = gemm_unit(u, m_tiles_s, n_tiles, k_splits, nk);
+      const GemmUnit g = gemm_unit(u, m_tiles_s, n_tiles, k_splits, nk, m_major != 0);
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
       epi(g.m_blk, g.n_blk, g.ks, lane_row, taddr,
           reinterpret_cast<float*>(epi_scratch) + quarter * (Epi::kScratchBytes / 16));
