@@ -25,7 +25,6 @@ namespace {
 constexpr int kPage = 16;
 constexpr int kConsumerWarps = 4;
 constexpr int kAttnThreads = 160;  // warps 0..3 consume, warp 4 loads pages
-constexpr int kAttnStages = 8;     // a multiple of kConsumerWarps: stage s is always read by warp s % 4
 constexpr uint32_t kHalfBytes = kPage * 64 * 2;   // 16 keys x 64 bf16, 128B-swizzled
 constexpr uint32_t kPageBytes = 4 * kHalfBytes;   // K[0:64) K[64:128) V[0:64) V[64:128)
 
@@ -151,9 +150,20 @@ constexpr int kMaxSplitPagesV2 = 256;              // split_tokens <= 4096
 // once every page has been consumed (16 rows x 128 dims + 32 floats each);
 // the ring region is sized to hold that merge too.
 constexpr uint32_t kMergeBytes = kConsumerWarps * (16 * 128 + 32) * 4;
-constexpr uint32_t kRingBytes = kAttnStages * kPageBytes > kMergeBytes ? kAttnStages * kPageBytes : kMergeBytes;
-static_assert(kAttnStages % kConsumerWarps == 0, "each stage must belong to one consumer warp");
-constexpr size_t kAttnSmemBytes = 1024 + kRingBytes + kQTileBytes + 2 * kAttnStages * 8 + 16 + kMaxSplitPagesV2 * 4;
+
+// The page ring: STAGES pages (a multiple of kConsumerWarps, so stage s is
+// always read by warp s % 4). Short splits run 8 stages at three CTAs per SM,
+// so one CTA's fixed work (Q build, merge, epilogue) overlaps two others'
+// pages; long splits run 12 stages at two CTAs per SM, so the loader keeps
+// streaming through the Q build of its own CTA.
+template <int STAGES>
+struct AttnRing {
+  static_assert(STAGES % kConsumerWarps == 0, "each stage must belong to one consumer warp");
+  static constexpr uint32_t kRingBytes = STAGES * kPageBytes > kMergeBytes ? STAGES * kPageBytes : kMergeBytes;
+  static constexpr size_t kSmemBytes = 1024 + kRingBytes + kQTileBytes + 2 * STAGES * 8 + 16 + kMaxSplitPagesV2 * 4;
+  static constexpr int kCtasPerSm = STAGES <= 8 ? 3 : 2;
+};
+constexpr int kLongSplitPages = 65;  // splits longer than 1,024 tokens take the 12-stage ring
 
 __device__ __forceinline__ void mma_pair(float (&d0)[4], float (&d1)[4], const uint4& a, uint32_t b0, uint32_t b1,
                                          uint32_t b2, uint32_t b3) {
@@ -162,12 +172,14 @@ __device__ __forceinline__ void mma_pair(float (&d0)[4], float (&d1)[4], const u
   mma_bf16(d1, av, b2, b3);
 }
 
-__global__ void __launch_bounds__(kAttnThreads, 3)
+template <int kAttnStages>
+__global__ void __launch_bounds__(kAttnThreads, AttnRing<kAttnStages>::kCtasPerSm)
     attn_doc_kernel(AttnArgs a, RopeTable rt, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV) {
   grid_dependency_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr uint32_t kRingBytes = AttnRing<kAttnStages>::kRingBytes;
   uint8_t* s_q = base + kRingBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(s_q + kQTileBytes);
   uint64_t* empty = full + kAttnStages;
@@ -582,26 +594,32 @@ cudaError_t launch_tree_part(const AttnArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_attn_doc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV, cudaStream_t st) {
+template <int STAGES>
+cudaError_t launch_attn_doc_ring(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV, cudaStream_t st) {
+  auto kern = attn_doc_kernel<STAGES>;
+  constexpr size_t smem = AttnRing<STAGES>::kSmemBytes;
   static int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(attn_doc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kAttnSmemBytes));
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_doc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
   dim3 grid(a.n_splits, a.hkv * (a.rows_pad / a.row_tile), a.n_slots);
   if (grid.x == 0 || grid.z == 0) return cudaSuccess;
-  if (a.row_tile != 16 || a.rows_pad != 16) return cudaErrorInvalidValue;  // one shared 16-row tile
-  const size_t smem = kAttnSmemBytes;
   count_launch();
-  { const cudaError_t le_ = launch_pdl(attn_doc_kernel, dim3(grid), dim3(kAttnThreads), smem, st, a, make_rope_table(a.theta), tmK, tmV); if (le_ != cudaSuccess) return le_; }
+  { const cudaError_t le_ = launch_pdl(kern, dim3(grid), dim3(kAttnThreads), smem, st, a, make_rope_table(a.theta), tmK, tmV); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
+}
+
+cudaError_t launch_attn_doc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV, cudaStream_t st) {
+  if (a.row_tile != 16 || a.rows_pad != 16) return cudaErrorInvalidValue;  // one shared 16-row tile
+  if (a.split_tokens / kPage >= kLongSplitPages) return launch_attn_doc_ring<12>(a, tmK, tmV, st);
+  return launch_attn_doc_ring<8>(a, tmK, tmV, st);
 }
 
 cudaError_t launch_attn_combine(const AttnArgs& a, cudaStream_t st) {
