@@ -194,32 +194,35 @@ __global__ void __launch_bounds__(kAttnThreads, AttnRing<kAttnStages>::kCtasPerS
   const int rg = blockIdx.y % n_row_groups;
   if (rows_past_end(a.map, slot, rg * a.row_tile / (a.hq / a.hkv))) return;  // a row group of padding only
   const int doc = row_doc(a.map, slot);
-  const int L = a.doc_len[doc];
-  if (L < 1 || L > a.max_doc_len) {
-    if (threadIdx.x == 0 && split == 0 && blockIdx.y == 0) raise_device_error(a.err, QUAIL_ERR_DEVICE_BOUNDS, doc);
-    return;
-  }
-  const int k_lo = split * a.split_tokens;
-  if (k_lo >= L) return;
-  const int k_hi = min(L, k_lo + a.split_tokens);
-  const int p0 = k_lo / kPage;
-  const int n_pages = (k_hi - k_lo + kPage - 1) / kPage;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.hq / a.hkv;
   const int nq_rows = (a.map.slot_node ? 1 : a.map.nq);
   const int rows_per_kv = nq_rows * G;
-
-  // q items of this consumer thread: item = (row r, pair j) -> dims j and
-  // j + 64 (j = t % 64 for every item, since 128 threads step 128 items). The
-  // loads go out before the barrier setup so their latency overlaps it.
-  constexpr int kPer = 16 * 64 / (kConsumerWarps * 32);  // items per thread
   const int t = threadIdx.x;
+  const int k_lo = split * a.split_tokens;
+  const int p0 = k_lo / kPage;
+
+  // Every load the CTA needs before its first copy goes out at once: the
+  // document length, the split's page ids (loader warp; up to a full split,
+  // trimmed to the document below) and the q items with their node depths
+  // (consumers). item = (row r, pair j) -> dims j and j + 64 (j = t % 64
+  // for every item, since 128 threads step 128 items).
+  const int L = a.doc_len[doc];
+  constexpr int kIdRegs = kMaxSplitPagesV2 / 32;
+  int ids[kIdRegs];
+  if (warp == kConsumerWarps) {
+    const int* pt = a.page_table + static_cast<size_t>(doc) * a.max_pages + p0;
+    const int avail = min(a.split_tokens / kPage, a.max_pages - p0);
+#pragma unroll
+    for (int k = 0; k < kIdRegs; ++k) ids[k] = (lane + 32 * k < avail) ? pt[lane + 32 * k] : 0;
+  }
+  constexpr int kPer = 16 * 64 / (kConsumerWarps * 32);  // items per thread
   float x1[kPer], x2[kPer];
-  int pos[kPer];
+  int dep[kPer];
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
     x1[k] = x2[k] = 0.f;
-    pos[k] = -1;
+    dep[k] = -1;
   }
   if (warp < kConsumerWarps) {
 #pragma unroll
@@ -233,10 +236,20 @@ __global__ void __launch_bounds__(kAttnThreads, AttnRing<kAttnStages>::kCtasPerS
         const float* q = a.qkv + static_cast<size_t>(node) * a.ldq + (g * G + hl) * 128;
         x1[k] = q[j];
         x2[k] = q[j + 64];
-        pos[k] = L + a.node_depth[node];
+        dep[k] = a.node_depth[node];
       }
     }
   }
+  if (L < 1 || L > a.max_doc_len) {
+    if (threadIdx.x == 0 && split == 0 && blockIdx.y == 0) raise_device_error(a.err, QUAIL_ERR_DEVICE_BOUNDS, doc);
+    return;
+  }
+  if (k_lo >= L) return;
+  const int k_hi = min(L, k_lo + a.split_tokens);
+  const int n_pages = (k_hi - k_lo + kPage - 1) / kPage;
+  int pos[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) pos[k] = dep[k] >= 0 ? L + dep[k] : -1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kAttnStages; ++s) {
@@ -250,10 +263,9 @@ __global__ void __launch_bounds__(kAttnThreads, AttnRing<kAttnStages>::kCtasPerS
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------ page loader
-    // All page ids of the split in one coalesced read, so no TMA issue waits
-    // on a dependent global load.
-    const int* pt = a.page_table + static_cast<size_t>(doc) * a.max_pages;
-    for (int j = lane; j < n_pages; j += 32) s_pages[j] = pt[p0 + j];
+#pragma unroll
+    for (int k = 0; k < kIdRegs; ++k)
+      if (lane + 32 * k < n_pages) s_pages[lane + 32 * k] = ids[k];
     __syncwarp();
     if (lane == 0) {
       int armed[kAttnStages];
@@ -449,6 +461,26 @@ __global__ void __launch_bounds__(kAttnThreads, AttnRing<kAttnStages>::kCtasPerS
   const bool fused = a.n_splits == 1;
   const size_t part_row0 =
       ((static_cast<size_t>(slot) * a.hkv + g) * a.n_splits + split) * static_cast<size_t>(a.rows_pad);
+  // Thread t of the epilogue: row r = t / 8 and dims 8k .. 8k + 7, 64 + 8k ..
+  // 64 + 8k + 7 (k = t % 8), so the 8 threads of a row write each 128-byte
+  // half of a bf16 output row (or read each 256-byte run of a tree_o row)
+  // together. Its tree-part values are requested before the merge, so their
+  // latency overlaps it.
+  const int r = t >> 3, k8 = t & 7;
+  auto dim = [&](int i) { return (i < 8 ? 8 * k8 : 64 + 8 * k8 - 8) + i; };  // dim of acc[i]
+  const bool out_row = fused && r < rows_per_kv;
+  float tv[16];
+  float2 tml = make_float2(-INFINITY, 0.f);
+  int e_out = 0, h_out = 0;
+  if (out_row) {
+    e_out = r / G;
+    h_out = g * G + r % G;
+    const int node = row_node(a.map, slot, e_out);
+    tml = a.tree_ml[static_cast<size_t>(node) * a.hq + h_out];
+    const float* to = a.tree_o + (static_cast<size_t>(node) * a.hq + h_out) * 128;
+#pragma unroll
+    for (int i = 0; i < 16; i += 4) *reinterpret_cast<float4*>(tv + i) = *reinterpret_cast<const float4*>(to + dim(i));
+  }
   {
     // Merge the four warps' partial softmax states through the (now idle) page ring.
     asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -465,11 +497,6 @@ __global__ void __launch_bounds__(kAttnThreads, AttnRing<kAttnStages>::kCtasPerS
       }
     }
     asm volatile("bar.sync 1, 128;" ::: "memory");
-    // Thread t: row r = t / 8 and dims 8k .. 8k + 7, 64 + 8k .. 64 + 8k + 7
-    // (k = t % 8), so the 8 threads of a row write each 128-byte half of a
-    // bf16 output row (or read each 256-byte run of a tree_o row) together.
-    const int r = t >> 3, k8 = t & 7;
-    auto dim = [&](int i) { return (i < 8 ? 8 * k8 : 64 + 8 * k8 - 8) + i; };  // dim of acc[i]
     const float* s0 = reinterpret_cast<const float*>(base);
     float M = -INFINITY;
 #pragma unroll
@@ -499,14 +526,8 @@ __global__ void __launch_bounds__(kAttnThreads, AttnRing<kAttnStages>::kCtasPerS
       for (int i = 0; i < 16; i += 4)
         *reinterpret_cast<float4*>(dst + dim(i)) = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
       if (k8 == 0) a.part_ml[part_row0 + r] = make_float2(M, lsum);
-    } else if (r < rows_per_kv) {
-      const int e = r / G, h = g * G + r % G;
-      const int node = row_node(a.map, slot, e);
-      const float2 tml = a.tree_ml[static_cast<size_t>(node) * a.hq + h];
-      const float* to = a.tree_o + (static_cast<size_t>(node) * a.hq + h) * 128;
-      float tv[16];  // this thread's 16 dims of the tree part, loaded before any store
-#pragma unroll
-      for (int i = 0; i < 16; i += 4) *reinterpret_cast<float4*>(tv + i) = *reinterpret_cast<const float4*>(to + dim(i));
+    } else if (out_row) {
+      const int e = e_out, h = h_out;
       const float M2 = fmaxf(M, tml.x);
       const float f1 = exp2f(M - M2), f2 = exp2f(tml.x - M2);
       const float inv = 1.f / (f1 * lsum + f2 * tml.y);
