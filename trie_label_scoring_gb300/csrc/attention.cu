@@ -58,6 +58,10 @@ constexpr int kTreeHeads = 4;
 
 __global__ void tree_part_kernel(AttnArgs a, RopeTable rt) {
   grid_dependency_wait();
+  // Everything before this kernel is complete now, so the doc-part kernel may
+  // launch: it streams its KV pages and builds its Q tiles meanwhile, and
+  // waits for this kernel only before it reads the tree part.
+  grid_launch_dependents();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int G = a.hq / a.hkv;
@@ -176,7 +180,10 @@ template <int kAttnStages>
 __global__ void __launch_bounds__(kAttnThreads, AttnRing<kAttnStages>::kCtasPerSm)
     attn_doc_kernel(AttnArgs a, RopeTable rt, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV) {
-  grid_dependency_wait();
+  // No grid_dependency_wait here: tree_part_kernel, the kernel before this
+  // one, lets it launch only after its own wait, so the document KV, page
+  // table and lengths (inputs) and q and the row maps (written before
+  // tree_part) are complete. Only the tree part itself is waited for, below.
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr uint32_t kRingBytes = AttnRing<kAttnStages>::kRingBytes;
@@ -187,12 +194,13 @@ __global__ void __launch_bounds__(kAttnThreads, AttnRing<kAttnStages>::kCtasPerS
   int* s_pages = reinterpret_cast<int*>(empty + kAttnStages) + 4;  // physical page of each split page
 
   const int slot = blockIdx.z;
-  if (a.map.n_slots_dev != nullptr && slot >= *a.map.n_slots_dev) return;
+  if (a.map.n_slots_dev != nullptr && slot >= *a.map.n_slots_dev) return grid_dependency_wait();
   const int split = blockIdx.x;
   const int n_row_groups = a.rows_pad / a.row_tile;
   const int g = blockIdx.y / n_row_groups;
   const int rg = blockIdx.y % n_row_groups;
-  if (rows_past_end(a.map, slot, rg * a.row_tile / (a.hq / a.hkv))) return;  // a row group of padding only
+  if (rows_past_end(a.map, slot, rg * a.row_tile / (a.hq / a.hkv)))  // a row group of padding only
+    return grid_dependency_wait();
   const int doc = row_doc(a.map, slot);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.hq / a.hkv;
@@ -242,9 +250,9 @@ __global__ void __launch_bounds__(kAttnThreads, AttnRing<kAttnStages>::kCtasPerS
   }
   if (L < 1 || L > a.max_doc_len) {
     if (threadIdx.x == 0 && split == 0 && blockIdx.y == 0) raise_device_error(a.err, QUAIL_ERR_DEVICE_BOUNDS, doc);
-    return;
+    return grid_dependency_wait();  // every exit waits, so this grid ends after the ones before it
   }
-  if (k_lo >= L) return;
+  if (k_lo >= L) return grid_dependency_wait();
   const int k_hi = min(L, k_lo + a.split_tokens);
   const int n_pages = (k_hi - k_lo + kPage - 1) / kPage;
   int pos[kPer];
@@ -303,6 +311,7 @@ __global__ void __launch_bounds__(kAttnThreads, AttnRing<kAttnStages>::kCtasPerS
         }
       }
     }
+    grid_dependency_wait();
     return;  // the loader warp takes no part in the consumers' named barrier
   }
 
@@ -469,6 +478,7 @@ __global__ void __launch_bounds__(kAttnThreads, AttnRing<kAttnStages>::kCtasPerS
   const int r = t >> 3, k8 = t & 7;
   auto dim = [&](int i) { return (i < 8 ? 8 * k8 : 64 + 8 * k8 - 8) + i; };  // dim of acc[i]
   const bool out_row = fused && r < rows_per_kv;
+  grid_dependency_wait();  // tree_part_kernel's outputs (and, by this wait, everything before this kernel)
   float tv[16];
   float2 tml = make_float2(-INFINITY, 0.f);
   int e_out = 0, h_out = 0;
