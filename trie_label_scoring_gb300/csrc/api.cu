@@ -691,7 +691,7 @@ quail_status trie_tree_pass(const quail_model_desc* model, const quail_paged_kv*
     CUtensorMap tA, tB;
     s = encode_2d_bf16(&tA, b.z, round_up(rows, 128), d, d, 64, 128);
     if (s != QUAIL_OK) return s;
-    s = encode_2d_bf16(&tB, model->lm_head, model->vocab, d, d, 64, kHeadBBoxRows);
+    s = encode_2d_bf16(&tB, model->lm_head, model->vocab, d, d, 64, head_b_box_rows(rows));
     if (s != QUAIL_OK) return s;
     HeadEpilogueArgs ha{b.lse_part, b.child_logit, img->eval_child_offsets, img->eval_child_tokens, b.z_f32,
                         static_cast<const bf16*>(model->lm_head), d, a, n_child, n_tiles};
@@ -1153,7 +1153,7 @@ quail_status quail_classify_trie_tree_ml(const quail_model_ml_desc* model, const
     CUtensorMap tA, tB;
     s = encode_2d_bf16(&tA, b.z, round_up(rows, 128), d, d, 64, 128);
     if (s != QUAIL_OK) return s;
-    s = encode_2d_bf16(&tB, model->lm_head, model->vocab, d, d, 64, kHeadBBoxRows);
+    s = encode_2d_bf16(&tB, model->lm_head, model->vocab, d, d, 64, head_b_box_rows(rows));
     if (s != QUAIL_OK) return s;
     HeadEpilogueArgs ha{b.lse_part, b.child_logit, img->eval_child_offsets, img->eval_child_tokens, b.z_f32,
                         static_cast<const bf16*>(model->lm_head), d, a, n_child, n_tiles};
@@ -1626,7 +1626,7 @@ quail_status quail_classify_trie_tree_shortlist(const quail_model_desc* model, c
     CUtensorMap tA, tB;
     s = encode_2d_bf16(&tA, b.z, round_up(R, 128), d, d, 64, 128);
     if (s != QUAIL_OK) return s;
-    s = encode_2d_bf16(&tB, model->lm_head, model->vocab, d, d, 64, kHeadBBoxRows);
+    s = encode_2d_bf16(&tB, model->lm_head, model->vocab, d, d, 64, head_b_box_rows(R));
     if (s != QUAIL_OK) return s;
     // log-sum-exp partials only: one row per slot and an empty child list
     HeadEpilogueArgs ha{b.lse_part, reinterpret_cast<float*>(zeros), zeros, zeros, b.z_f32,

@@ -266,6 +266,8 @@ cudaError_t launch_gemm_swiglu(const CUtensorMap& tmA, const BSet& bset, int M, 
   return launch_umma<kProjBN, kProjStages, true>(tmA, bset, M, 2 * I, K / kGemmBK, 1, epi, num_sms, err, st);
 }
 
+int head_cluster_ctas(int M) { return (M + kGemmBM - 1) / kGemmBM <= kHeadWideClusterMaxTiles ? 4 : 2; }
+
 cudaError_t launch_gemm_head(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int V, int K,
                              const HeadEpilogueArgs& args, int num_sms, int* err, cudaStream_t st,
                              const int* m_live) {
@@ -275,6 +277,9 @@ cudaError_t launch_gemm_head(const CUtensorMap& tmA, const CUtensorMap& tmB, int
   b.n_begin[0] = 0;
   b.n_begin[1] = V;
   b.count = 1;
+  if (head_cluster_ctas(M) == 4)
+    return launch_umma<kHeadBN, kHeadStages, false, EpiHead, 4>(tmA, b, M, V, K / kGemmBK, 1, epi, num_sms, err, st,
+                                                                m_live);
   return launch_umma<kHeadBN, kHeadStages, false, EpiHead, 2>(tmA, b, M, V, K / kGemmBK, 1, epi, num_sms, err, st,
                                                               m_live);
 }

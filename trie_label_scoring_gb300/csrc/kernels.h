@@ -50,9 +50,15 @@ struct HeadEpilogueArgs {
   int n_tiles;
 };
 constexpr int kHeadBN = 256;
-// The head runs on CTA pairs that share each 256-row band of W_lm: tmB's box is
-// 64 columns x kHeadBBoxRows rows (half a band, one per CTA, multicast to both).
-constexpr int kHeadBBoxRows = kHeadBN / 2;
+// The head runs on clusters of CTAs along M that share each 256-row band of
+// W_lm: every CTA loads 1/C of the band (tmB's box: 64 columns x 256/C rows)
+// and multicasts it to the others. C = 4 when the rows span at most
+// kHeadWideClusterMaxTiles 128-row tiles (A is small and B's L2 reads dominate:
+// four CTAs share each band), else C = 2 (A's re-reads dominate, and four
+// CTAs in lockstep cost more than the B they share).
+constexpr int kHeadWideClusterMaxTiles = 8;
+int head_cluster_ctas(int M);
+inline int head_b_box_rows(int M) { return kHeadBN / head_cluster_ctas(M); }
 cudaError_t launch_gemm_head(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int V, int K,
                              const HeadEpilogueArgs& args, int num_sms, int* err, cudaStream_t st,
                              const int* m_live = nullptr);

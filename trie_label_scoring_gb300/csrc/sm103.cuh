@@ -101,7 +101,7 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* tm, ui
       : "memory");
 }
 
-// Cluster helpers (CTA pairs sharing one operand through TMA multicast).
+// Cluster helpers (CTAs of a cluster sharing one operand through TMA multicast).
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));

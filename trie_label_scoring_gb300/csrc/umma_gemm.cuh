@@ -16,13 +16,13 @@
 //  * Split-K over CTAs: work unit = (tile, k-split); the epilogue receives the
 //    split index and writes its partial tile to its own slab (no atomics); the
 //    next kernel sums the slabs.
-//  * CM = 2: CTA pairs (clusters of two along M) share each B tile. The two
-//    CTAs of a cluster always work on M tiles 2i and 2i+1 of the same N band;
-//    each loads half of the B band with TMA multicast into both CTAs, so every
-//    byte of B crosses from L2 once per pair. A stage is refilled only after
-//    both CTAs' MMAs have released it (a multicast commit to both empty
-//    barriers). An odd M-tile count gets one all-padding tile per band (A
-//    reads past the end fill zeros; the epilogue skips rows >= M).
+//  * CM = 2 or 4: clusters of CM CTAs along M share each B tile. The CTAs of
+//    a cluster always work on M tiles CM i .. CM i + CM - 1 of the same N
+//    band; each loads 1/CM of the B band with TMA multicast into all of them,
+//    so every byte of B crosses from L2 once per cluster. A stage is refilled
+//    only after every CTA's MMAs have released it (a multicast commit to all
+//    empty barriers). M tiles are scheduled in whole clusters; the padding
+//    tiles read zeros past the end of A and the epilogue skips rows >= M.
 //
 // Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM owner + MMA
 // issuer, warps 2..5 = epilogue (warp w reads TMEM lanes 32*(w%4) .. +31).
@@ -39,7 +39,7 @@ namespace quail {
 constexpr int kGemmBM = 128;
 constexpr int kGemmBK = 64;  // 64 bf16 = one 128-byte swizzle row
 constexpr int kGemmThreads = 192;
-constexpr int kPrefetchKb = 8;  // k-blocks of B requested into L2 ahead of their loads (CTA pairs)
+constexpr int kPrefetchKb = 8;  // k-blocks of B requested into L2 ahead of their loads (clusters)
 
 // Up to three B operands covering output columns [n_begin[i], n_begin[i+1]).
 // glu != 0: two operands of equal shape whose rows pair up (gate and up
@@ -92,11 +92,11 @@ __device__ __forceinline__ GemmUnit gemm_unit(int u, int m_tiles, int n_tiles, i
 }
 
 // L2 prefetch cursor over one CTA's sequence of (unit, k-block) B loads:
-// step() requests the next B tile of that sequence (this CTA's half band).
+// step() requests the next B tile of that sequence (this CTA's part of the band).
 struct BPrefetch {
   int u, kb, kb1, nb;
   const CUtensorMap* map;
-  __device__ __forceinline__ void step(const BSet& bs, int bn, uint32_t crank, int m_tiles_s, int n_tiles,
+  __device__ __forceinline__ void step(const BSet& bs, int bn, int cm, uint32_t crank, int m_tiles_s, int n_tiles,
                                        int k_splits, int nk, int num_units) {
     while (kb >= kb1) {  // advance to this CTA's next unit
       u += gridDim.x;
@@ -105,7 +105,7 @@ struct BPrefetch {
       int bi = 0;
       while (bi + 1 < bs.count && h.n_blk * bn >= bs.n_begin[bi + 1]) ++bi;
       map = &bs.map[bi];
-      nb = h.n_blk * bn - bs.n_begin[bi] + static_cast<int>(crank) * (bn / 2);
+      nb = h.n_blk * bn - bs.n_begin[bi] + static_cast<int>(crank) * (bn / cm);
       kb = h.kb0;
       kb1 = h.kb1;
     }
@@ -129,9 +129,11 @@ template <int BN, int STAGES, bool SPLIT_A, class Epi, int CM = 1>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ BSet bset, int M, int N,
                      int nk, int k_splits, int m_major, Epi epi, int* err, const int* m_live) {
-  static_assert(CM == 1 || (CM == 2 && !SPLIT_A && BN % 16 == 0), "pairs: plain A, B band split in two halves");
+  static_assert(CM == 1 || ((CM == 2 || CM == 4) && !SPLIT_A && BN % (8 * CM) == 0),
+                "clusters: plain A, B band split in CM parts of whole 8-row swizzle atoms");
   using Cfg = GemmCfg<BN, STAGES, SPLIT_A>;
-  constexpr uint32_t kBHalf = Cfg::kBBytes / CM;  // bytes of B each CTA of a pair loads
+  constexpr uint32_t kBPart = Cfg::kBBytes / CM;  // bytes of B each CTA of a cluster loads
+  constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << CM) - 1u);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // the epilogue's scratch (Epi::kScratchBytes) follows the ring, then the barriers
@@ -146,7 +148,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t crank = CM == 2 ? cluster_ctarank() : 0u;
+  const uint32_t crank = CM > 1 ? cluster_ctarank() : 0u;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -170,13 +172,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (CM == 2) cluster_sync();  // the peer's barriers exist before any multicast reaches them
+  if (CM > 1) cluster_sync();  // the peers' barriers exist before any multicast reaches them
   // Everything above touched shared memory, TMEM and the kernel parameters
   // only; from here on the previous kernel's outputs are read.
   grid_dependency_wait();
   const int M_eff = m_live != nullptr ? min(M, max(*m_live, 0)) : M;
   const int m_tiles = (M_eff + kGemmBM - 1) / kGemmBM;
-  const int m_tiles_s = (m_tiles + CM - 1) / CM * CM;  // scheduled M tiles: whole pairs
+  const int m_tiles_s = (m_tiles + CM - 1) / CM * CM;  // scheduled M tiles: whole clusters
   const int n_tiles = (N + BN - 1) / BN;
   const int num_units = m_tiles_s * n_tiles * k_splits;
   const uint32_t tmem_base = *tmem_slot;
@@ -198,15 +200,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         while (bi + 1 < bset.count && n0 >= bset.n_begin[bi + 1]) ++bi;
         const CUtensorMap* tmB = &bset.map[bi];
         const int nb = n0 - bset.n_begin[bi];
-        const int nb_own = nb + static_cast<int>(crank) * (BN / 2);
+        const int nb_own = nb + static_cast<int>(crank) * (BN / CM);
         for (int kb = g.kb0; kb < g.kb1; ++kb) {
-          // Pairs stream each B band once from DRAM into L2 and then share it:
-          // this CTA's half-band k-blocks are requested kPrefetchKb loads ahead
-          // (running on into its next unit), so the first pair on a band does
-          // not wait on DRAM at every k-block.
-          if (CM == 2) {
+          // Clusters stream each B band once from DRAM into L2 and then share
+          // it: this CTA's part-band k-blocks are requested kPrefetchKb loads
+          // ahead (running on into its next unit), so the first cluster on a
+          // band does not wait on DRAM at every k-block.
+          if (CM > 1) {
             const int n = (u == static_cast<int>(blockIdx.x) && kb == g.kb0) ? kPrefetchKb + 1 : 1;
-            for (int p = 0; p < n; ++p) pf.step(bset, BN, crank, m_tiles_s, n_tiles, k_splits, nk, num_units);
+            for (int p = 0; p < n; ++p) pf.step(bset, BN, CM, crank, m_tiles_s, n_tiles, k_splits, nk, num_units);
           }
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
@@ -216,9 +218,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
           tma_load_2d(st, &tmA, &full[stage], kb * kGemmBK, g.m_blk * kGemmBM);
           if (SPLIT_A) tma_load_2d(st + Cfg::kABytes, &tmA, &full[stage], (nk + kb) * kGemmBK, g.m_blk * kGemmBM);
-          if (CM == 2) {
-            tma_load_2d_mcast(st + Cfg::kABytes + crank * kBHalf, tmB, &full[stage], kb * kGemmBK, nb_own,
-                              static_cast<uint16_t>(0x3));
+          if (CM > 1) {
+            tma_load_2d_mcast(st + Cfg::kABytes + crank * kBPart, tmB, &full[stage], kb * kGemmBK, nb_own,
+                              kClusterMask);
           } else if (bset.glu) {
             uint8_t* b_st = st + (SPLIT_A ? 2 : 1) * Cfg::kABytes;
             tma_load_2d(b_st, &bset.map[0], &full[stage], kb * kGemmBK, g.n_blk * (BN / 2));
@@ -234,12 +236,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
       // Never leave with copies in flight: every armed stage must have landed.
-      // In a pair, also wait until the last fill of every stage has been
-      // released by both CTAs, so that no commit from the peer is still on its
-      // way to this CTA's barriers when the pair synchronises and exits.
+      // In a cluster, also wait until the last fill of every stage has been
+      // released by all CTAs, so that no commit from a peer is still on its
+      // way to this CTA's barriers when the cluster synchronises and exits.
       for (int s = 0; s < STAGES; ++s) {
         if (armed_parity[s] < 0) continue;
-        for (int which = 0; which < CM; ++which) {
+        for (int which = 0; which < (CM > 1 ? 2 : 1); ++which) {
           const uint32_t a = smem_u32(which == 0 ? &full[s] : &empty[s]);
           const long long t0 = clock64();
           while (!mbar_try_wait(a, static_cast<uint32_t>(armed_parity[s]))) {
@@ -282,8 +284,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         (kb > g.kb0 || half > 0 || k > 0) ? 1u : 0u);
             }
           }
-          if (CM == 2)
-            umma_commit_mcast(&empty[stage], static_cast<uint16_t>(0x3));
+          if (CM > 1)
+            umma_commit_mcast(&empty[stage], kClusterMask);
           else
             umma_commit(&empty[stage]);
           if (++stage == STAGES) {
@@ -334,10 +336,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tmem_dealloc(tmem_base, Cfg::kTmemCols);
   }
   if (threadIdx.x == 0 && *abort_flag) raise_device_error(err, QUAIL_ERR_DEVICE_TIMEOUT, 1000 + blockIdx.x);
-  // Neither CTA of a pair leaves while the other may still multicast into its
-  // shared memory or arrive on its barriers: both producers have drained their
-  // copies and both MMA threads their commits before reaching this point.
-  if (CM == 2) cluster_sync();
+  // No CTA of a cluster leaves while another may still multicast into its
+  // shared memory or arrive on its barriers: every producer has drained its
+  // copies and every MMA thread its commits before reaching this point.
+  if (CM > 1) cluster_sync();
 }
 
 // ------------------------------------------------------------ epilogues
