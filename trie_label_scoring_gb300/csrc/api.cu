@@ -262,7 +262,8 @@ struct Buffers {
   float2* lse_part;
   float* lse;
   float* child_logit;
-  int* small;  // node tables / slot lists
+  int* slot_order;  // the doc attention's slot order
+  int* small;       // node tables / slot lists
 };
 
 // Carves (or sizes, when base is null) the workspace of one call.
@@ -293,6 +294,7 @@ size_t plan(uint8_t* base, const quail_model_desc* m, int nodes, int slots, int 
   t.lse_part = head ? c.take<float2>(rows * n_tiles) : nullptr;
   t.lse = head ? c.take<float>(rows) : nullptr;
   t.child_logit = head ? c.take<float>(static_cast<size_t>(slots) * n_child) : nullptr;
+  t.slot_order = c.take<int>(slots);
   t.small = c.take<int>(small_ints);
   if (b) *b = t;
   return c.off + 256;
@@ -391,12 +393,15 @@ quail_status run_attention(const quail_model_desc* m, const quail_paged_kv* kv, 
   a.tree_ml = b.tree_ml;
   a.out = b.attn_out;
   a.err = ds->err;
+  a.slot_order = nullptr;
+  if (!as.tc && attn_doc_wants_slot_order(a, ds->num_sms)) a.slot_order = b.slot_order;
   CUtensorMap tK, tV;
   const uint64_t pool_rows = static_cast<uint64_t>(kv->num_pages) * hkv * 16;
   quail_status s = encode_2d_bf16(&tK, kv->k_pool, pool_rows, 128, 128, 64, 16);
   if (s != QUAIL_OK) return s;
   s = encode_2d_bf16(&tV, kv->v_pool, pool_rows, 128, 128, 64, 16);
   if (s != QUAIL_OK) return s;
+  if (a.slot_order != nullptr) CUDA_TRY(launch_slot_order(a, st));
   CUDA_TRY(launch_tree_part(a, st));
   if (as.tc) {
     CUDA_TRY(launch_attn_doc_tc(a, tK, tV, st));

@@ -138,6 +138,56 @@ __global__ void tree_part_kernel(AttnArgs a, RopeTable rt) {
   }
 }
 
+// ------------------------------------------------------------------ slot order
+// One block: a counting sort of the slots by document pages, longest first.
+// Slots whose document length is out of range sort as empty documents; slots
+// past the live count go last. The order of equal keys is whatever the
+// shared-memory atomics give: it changes only which CTA runs when, never a
+// result.
+constexpr int kOrderBins = 1024;
+constexpr int kOrderThreads = 1024;
+
+__global__ void __launch_bounds__(kOrderThreads) slot_order_kernel(AttnArgs a) {
+  __shared__ int hist[kOrderBins];
+  __shared__ int warp_tot[kOrderThreads / 32];
+  grid_dependency_wait();
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  hist[t] = 0;  // kOrderBins == kOrderThreads
+  __syncthreads();
+  const int live = a.map.n_slots_dev != nullptr ? min(*a.map.n_slots_dev, a.n_slots) : a.n_slots;
+  auto bin_of = [&](int s) {
+    if (s >= live) return kOrderBins - 1;
+    const int L = a.doc_len[row_doc(a.map, s)];
+    const int pages = (L >= 1 && L <= a.max_doc_len) ? (L + 15) / 16 : 0;
+    return (kOrderBins - 2) - min(pages, kOrderBins - 2);
+  };
+  for (int s = t; s < a.n_slots; s += kOrderThreads) atomicAdd(&hist[bin_of(s)], 1);
+  __syncthreads();
+  // exclusive scan of hist (bin t) across the block
+  const int v = hist[t];
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_tot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_tot[lane] = w - warp_tot[lane];  // exclusive prefix of the warp totals
+  }
+  __syncthreads();
+  hist[t] = warp_tot[warp] + x - v;  // first position of bin t
+  __syncthreads();
+  for (int s = t; s < a.n_slots; s += kOrderThreads) a.slot_order[atomicAdd(&hist[bin_of(s)], 1)] = s;
+}
+
 // ------------------------------------------------------------------ doc part
 // CTA = (split, kv head x row group, slot). Warp 4 streams the split's KV pages
 // (K and V of one KV head: 8 KB per page) into an 8-stage ring with TMA; warps
@@ -193,7 +243,9 @@ __global__ void __launch_bounds__(kAttnThreads, AttnRing<kAttnStages>::kCtasPerS
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kAttnStages);
   int* s_pages = reinterpret_cast<int*>(empty + kAttnStages) + 4;  // physical page of each split page
 
-  const int slot = blockIdx.z;
+  // Slots run longest document first (slot_order_kernel, complete before
+  // tree_part_kernel passed its wait), so the last wave holds short CTAs.
+  const int slot = a.slot_order != nullptr ? a.slot_order[blockIdx.z] : static_cast<int>(blockIdx.z);
   if (a.map.n_slots_dev != nullptr && slot >= *a.map.n_slots_dev) return grid_dependency_wait();
   const int split = blockIdx.x;
   const int n_row_groups = a.rows_pad / a.row_tile;
@@ -625,6 +677,13 @@ cudaError_t launch_tree_part(const AttnArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+cudaError_t launch_slot_order(const AttnArgs& a, cudaStream_t st) {
+  if (a.n_slots <= 0 || a.slot_order == nullptr) return cudaSuccess;
+  count_launch();
+  { const cudaError_t le_ = launch_pdl(slot_order_kernel, dim3(1), dim3(kOrderThreads), 0, st, a); if (le_ != cudaSuccess) return le_; }
+  return cudaGetLastError();
+}
+
 template <int STAGES>
 cudaError_t launch_attn_doc_ring(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV, cudaStream_t st) {
   auto kern = attn_doc_kernel<STAGES>;
@@ -645,6 +704,16 @@ cudaError_t launch_attn_doc_ring(const AttnArgs& a, const CUtensorMap& tmK, cons
   count_launch();
   { const cudaError_t le_ = launch_pdl(kern, dim3(grid), dim3(kAttnThreads), smem, st, a, make_rope_table(a.theta), tmK, tmV); if (le_ != cudaSuccess) return le_; }
   return cudaGetLastError();
+}
+
+bool attn_doc_wants_slot_order(const AttnArgs& a, int num_sms) {
+  // Few waves: the last partial wave decides the kernel's end, and starting
+  // the long documents first leaves short CTAs for it. Over many waves the
+  // order is left alone: CTAs of equal length started together reach their
+  // setup and merge phases together, and an SM then streams less.
+  const int per_sm = a.split_tokens / kPage >= kLongSplitPages ? AttnRing<12>::kCtasPerSm : AttnRing<8>::kCtasPerSm;
+  const long ctas = static_cast<long>(a.n_slots) * a.hkv * a.n_splits;
+  return 2 * ctas <= 3L * per_sm * num_sms;
 }
 
 cudaError_t launch_attn_doc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV, cudaStream_t st) {

@@ -237,8 +237,16 @@ struct AttnArgs {
   float2* tree_ml;         // [n_nodes, hq]
   bf16* out;               // [n_slots * nq, 2 * hq * 128]: O as a two-term bf16 split [O_hi | O_lo]
   int* err;
+  int* slot_order;         // nullable: [n_slots] the mma.sync doc attention's slot order (longest document first)
 };
 cudaError_t launch_tree_part(const AttnArgs& a, cudaStream_t st);
+// slot_order = the slots sorted by document length, longest first (slots past
+// *map.n_slots_dev last), so the doc attention's long CTAs start in the first
+// waves and the last wave holds short ones.
+cudaError_t launch_slot_order(const AttnArgs& a, cudaStream_t st);
+// True when the mma.sync doc attention's grid spans at most 1.5 waves of
+// resident CTAs: there it runs its slots in slot_order.
+bool attn_doc_wants_slot_order(const AttnArgs& a, int num_sms);
 cudaError_t launch_attn_doc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV, cudaStream_t st);
 cudaError_t launch_attn_combine(const AttnArgs& a, cudaStream_t st);
 // tcgen05 doc attention for 128-row query tiles (attention_tc.cu); row_tile must be 128.
