@@ -23,8 +23,10 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// Per 128 x 256 accumulator tile and row: online max / sum of exp over the
-// valid columns (base-2 units: m2 = max * log2 e), from the tensor-core logits.
+// Per 128 x 256 accumulator tile and row: the max and the sum of exp over the
+// valid columns (base-2 units: m2 = max * log2 e), from the tensor-core
+// logits, in two passes over the TMEM accumulator (max, then one FFMA and one
+// exp2 per logit on four independent sums).
 // The child tokens of the row's node that fall inside the tile are gathered
 // here too; their logits are evaluated in fp32 from the unrounded hidden
 // state (z_f32 . W_lm[c], warp-cooperative, the tile's W rows being hot in
@@ -57,10 +59,13 @@ struct EpiHead {
       cur = lo;
       cl_out = a.child_logit + static_cast<size_t>(slot) * a.n_child;
     }
-    const bool full_tile = n0 + kHeadBN <= V;
-    float m2 = -INFINITY, s = 0.f;
+    const int n_valid = min(kHeadBN, V - n0);  // >= 1: column n0 of every tile is a real token
+    // Pass 1: the row's largest logit in the tile, and the child logits that
+    // fall in it. Four independent max chains per thread.
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
     for (int c = 0; c < kHeadBN / 32; ++c) {
+      if (c * 32 >= n_valid) break;  // warp-uniform
       float v[32];
       tmem_ld_32cols(taddr + c * 32, v);
       const int col_end = n0 + c * 32 + 32;
@@ -92,28 +97,35 @@ struct EpiHead {
         }
         hit = __ballot_sync(0xffffffffu, tok < col_end);
       }
-      const int col0 = n0 + c * 32;
-      float cm = -INFINITY;
-      if (full_tile) {
+      if (c * 32 + 32 <= n_valid) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          v[i] *= kLog2e;
-          cm = fmaxf(cm, v[i]);
-        }
+        for (int i = 0; i < 32; ++i) mx[i & 3] = fmaxf(mx[i & 3], v[i]);
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          v[i] = (col0 + i < V) ? v[i] * kLog2e : -INFINITY;
-          cm = fmaxf(cm, v[i]);
-        }
+        for (int i = 0; i < 32; ++i)
+          if (c * 32 + i < n_valid) mx[i & 3] = fmaxf(mx[i & 3], v[i]);
       }
-      const float nm = fmaxf(m2, cm);  // finite: column n0 of every tile is a real token
-      float acc = s * fast_exp2(m2 - nm);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) acc += fast_exp2(v[i] - nm);
-      m2 = nm;
-      s = acc;
     }
+    // Pass 2: sum of 2^(logit log2 e - m2) over the tile's tokens, one FFMA
+    // and one MUFU op per logit, four independent sums per thread (the TMEM
+    // accumulator is read a second time instead of being kept in registers).
+    const float m2 = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * kLog2e;
+    float sa[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+    for (int c = 0; c < kHeadBN / 32; ++c) {
+      if (c * 32 >= n_valid) break;
+      float v[32];
+      tmem_ld_32cols(taddr + c * 32, v);
+      if (c * 32 + 32 <= n_valid) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sa[i & 3] += fast_exp2(fmaf(v[i], kLog2e, -m2));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (c * 32 + i < n_valid) sa[i & 3] += fast_exp2(fmaf(v[i], kLog2e, -m2));
+      }
+    }
+    const float s = (sa[0] + sa[1]) + (sa[2] + sa[3]);
     if (valid) a.lse_part[static_cast<size_t>(row) * a.n_tiles + n_blk] = make_float2(m2, s);
   }
 };
@@ -163,13 +175,23 @@ cudaError_t launch_umma(const CUtensorMap& tmA, const BSet& bset, int M, int N, 
   const double a_bytes = static_cast<double>(M) * nk * kGemmBK * 2.0 * (SPLIT_A ? 2 : 1);
   const double b_bytes = static_cast<double>(N) * nk * kGemmBK * 2.0;
   const int m_major = (CM == 1 && a_bytes > b_bytes) ? 1 : 0;
+  // Walking N bands, the M tiles go in groups whose A rows (every k-block)
+  // fit in kGemmGroupABytes of L2: with thousands of rows (the head of a
+  // large label set) A would otherwise stream through L2 once per band.
+  const int m_tiles_s = (m_tiles + CM - 1) / CM * CM;
+  const double a_tile_bytes = static_cast<double>(kGemmBM) * nk * kGemmBK * 2.0 * (SPLIT_A ? 2 : 1);
+  int m_group = static_cast<int>(kGemmGroupABytes / a_tile_bytes) / CM * CM;
+  if (m_group < CM) m_group = CM;
+  if (m_group > m_tiles_s) m_group = m_tiles_s;
+  if (m_major) m_group = 0;
+  const int pf_depth = CM > 1 ? kPrefetchKb : 0;
   int grid = units < resident ? units : resident;
   grid = grid / CM * CM;  // whole clusters; units is a multiple of CM
   if (grid <= 0) return cudaSuccess;
   if (CM == 1) {
     count_launch();
-    return launch_pdl(kern, dim3(grid), dim3(kGemmThreads), smem, st, tmA, bset, M, N, nk, k_splits, m_major, epi, err,
-                      m_live);
+    return launch_pdl(kern, dim3(grid), dim3(kGemmThreads), smem, st, tmA, bset, M, N, nk, k_splits, m_group, pf_depth,
+                      epi, err, m_live);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
@@ -186,7 +208,7 @@ cudaError_t launch_umma(const CUtensorMap& tmA, const BSet& bset, int M, int N, 
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   count_launch();
-  return cudaLaunchKernelEx(&cfg, kern, tmA, bset, M, N, nk, k_splits, m_major, epi, err, m_live);
+  return cudaLaunchKernelEx(&cfg, kern, tmA, bset, M, N, nk, k_splits, m_group, pf_depth, epi, err, m_live);
 }
 
 }  // namespace

@@ -40,6 +40,7 @@ constexpr int kGemmBM = 128;
 constexpr int kGemmBK = 64;  // 64 bf16 = one 128-byte swizzle row
 constexpr int kGemmThreads = 192;
 constexpr int kPrefetchKb = 8;  // k-blocks of B requested into L2 ahead of their loads (clusters)
+constexpr double kGemmGroupABytes = 24.0 * 1024 * 1024;  // A rows in use at once, N-band-major walks
 
 // Up to three B operands covering output columns [n_begin[i], n_begin[i+1]).
 // glu != 0: two operands of equal shape whose rows pair up (gate and up
@@ -69,22 +70,29 @@ struct GemmUnit {
 };
 
 // unit -> (k-split, tile) with the k-split slowest, so the CTAs resident at
-// one time share B bands and A rows in L2; tile -> (n band, m tile),
-// N-band-major (consecutive units share a B band), or M-major when A is the
-// larger operand (consecutive units share an A tile, so A streams from DRAM
-// once while the smaller B stays in L2).
-__device__ __forceinline__ GemmUnit gemm_unit(int u, int m_tiles, int n_tiles, int k_splits, int nk,
-                                              bool m_major) {
+// one time share B bands and A rows in L2; tile -> (n band, m tile):
+//  * m_group > 0: N-band-major within groups of m_group M tiles (consecutive
+//    units share a B band; a group walks every band before the next group
+//    starts), so the A rows in use stay within one group's L2 footprint while
+//    each B band is read once per group;
+//  * m_group == 0: M-major, when A is the larger operand (consecutive units
+//    share an A tile, so A streams from DRAM once while the smaller B stays
+//    in L2).
+__device__ __forceinline__ GemmUnit gemm_unit(int u, int m_tiles, int n_tiles, int k_splits, int nk, int m_group) {
   GemmUnit g;
   const int tiles = m_tiles * n_tiles;
   g.ks = u / tiles;
   const int tile = u - g.ks * tiles;
-  if (m_major) {
+  if (m_group <= 0) {
     g.m_blk = tile / n_tiles;
     g.n_blk = tile - g.m_blk * n_tiles;
   } else {
-    g.n_blk = tile / m_tiles;
-    g.m_blk = tile - g.n_blk * m_tiles;
+    const int grp = tile / (m_group * n_tiles);
+    const int m0 = grp * m_group;
+    const int gm = min(m_group, m_tiles - m0);
+    const int t = tile - m0 * n_tiles;
+    g.n_blk = t / gm;
+    g.m_blk = m0 + (t - g.n_blk * gm);
   }
   g.kb0 = g.ks * nk / k_splits;
   g.kb1 = (g.ks + 1) * nk / k_splits;
@@ -97,11 +105,11 @@ struct BPrefetch {
   int u, kb, kb1, nb;
   const CUtensorMap* map;
   __device__ __forceinline__ void step(const BSet& bs, int bn, int cm, uint32_t crank, int m_tiles_s, int n_tiles,
-                                       int k_splits, int nk, int num_units) {
+                                       int k_splits, int nk, int num_units, int m_group) {
     while (kb >= kb1) {  // advance to this CTA's next unit
       u += gridDim.x;
       if (u >= num_units) return;
-      const GemmUnit h = gemm_unit(u, m_tiles_s, n_tiles, k_splits, nk, false);
+      const GemmUnit h = gemm_unit(u, m_tiles_s, n_tiles, k_splits, nk, m_group);
       int bi = 0;
       while (bi + 1 < bs.count && h.n_blk * bn >= bs.n_begin[bi + 1]) ++bi;
       map = &bs.map[bi];
@@ -128,7 +136,7 @@ struct BPrefetch {
 template <int BN, int STAGES, bool SPLIT_A, class Epi, int CM = 1>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ BSet bset, int M, int N,
-                     int nk, int k_splits, int m_major, Epi epi, int* err, const int* m_live) {
+                     int nk, int k_splits, int m_group, int pf_depth, Epi epi, int* err, const int* m_live) {
   static_assert(CM == 1 || ((CM == 2 || CM == 4) && !SPLIT_A && BN % (8 * CM) == 0),
                 "clusters: plain A, B band split in CM parts of whole 8-row swizzle atoms");
   using Cfg = GemmCfg<BN, STAGES, SPLIT_A>;
@@ -194,7 +202,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool ok = true;
       BPrefetch pf{static_cast<int>(blockIdx.x) - static_cast<int>(gridDim.x), 0, 0, 0, nullptr};
       for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-        const GemmUnit g = gemm_unit(u, m_tiles_s, n_tiles, k_splits, nk, m_major != 0);
+        const GemmUnit g = gemm_unit(u, m_tiles_s, n_tiles, k_splits, nk, m_group);
         const int n0 = g.n_blk * BN;
         int bi = 0;
         while (bi + 1 < bset.count && n0 >= bset.n_begin[bi + 1]) ++bi;
@@ -207,8 +215,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           // ahead (running on into its next unit), so the first cluster on a
           // band does not wait on DRAM at every k-block.
           if (CM > 1) {
-            const int n = (u == static_cast<int>(blockIdx.x) && kb == g.kb0) ? kPrefetchKb + 1 : 1;
-            for (int p = 0; p < n; ++p) pf.step(bset, BN, CM, crank, m_tiles_s, n_tiles, k_splits, nk, num_units);
+            const int n = (u == static_cast<int>(blockIdx.x) && kb == g.kb0) ? pf_depth + 1 : 1;
+            for (int p = 0; p < n; ++p)
+              pf.step(bset, BN, CM, crank, m_tiles_s, n_tiles, k_splits, nk, num_units, m_group);
           }
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
@@ -263,7 +272,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-        const GemmUnit g = gemm_unit(u, m_tiles_s, n_tiles, k_splits, nk, m_major != 0);
+        const GemmUnit g = gemm_unit(u, m_tiles_s, n_tiles, k_splits, nk, m_group);
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -318,7 +327,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
       if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) break;
       tc_fence_after();
-      const GemmUnit g = gemm_unit(u, m_tiles_s, n_tiles, k_splits, nk, m_major != 0);
+      const GemmUnit g = gemm_unit(u, m_tiles_s, n_tiles, k_splits, nk, m_group);
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
       epi(g.m_blk, g.n_blk, g.ks, lane_row, taddr,
           reinterpret_cast<float*>(epi_scratch) + quarter * (Epi::kScratchBytes / 16));
