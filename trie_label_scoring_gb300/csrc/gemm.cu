@@ -235,7 +235,11 @@ int choose_k_splits(int tiles, int nk, int num_sms) {
 
 cudaError_t launch_gemm_proj(const CUtensorMap& tmA, const BSet& bset, int M, int N, int K, int k_splits, float* C,
                              size_t slab, int ldc, int num_sms, int* err, cudaStream_t st, const int* m_live) {
-  EpiStoreF32<kProjBN> epi{C, slab, ldc, M, N};
+  EpiStoreF32<kProjBN> epi;
+  if (k_splits < 1 || ldc % 4 != 0 || slab % 4 != 0 ||
+      !encode_3d_f32_store(&epi.tm, C, static_cast<uint64_t>(N), static_cast<uint64_t>(M),
+                           static_cast<uint64_t>(k_splits), static_cast<uint64_t>(ldc), slab, 32, 32))
+    return cudaErrorInvalidValue;
   return launch_umma<kProjBN, kProjStages, true>(tmA, bset, M, N, K / kGemmBK, k_splits, epi, num_sms, err, st,
                                                  m_live);
 }

@@ -10,6 +10,12 @@ namespace quail {
 // call's start; read back through quail_launch_count).
 void count_launch();
 
+// fp32 tensor [planes, rows, cols] (cols contiguous; row stride ld, plane
+// stride plane_ld elements) for tile stores of box_cols x box_rows x 1, with
+// the 128-byte swizzle (box_cols * 4 must be 128). False if the encoding fails.
+bool encode_3d_f32_store(void* tm, void* ptr, uint64_t cols, uint64_t rows, uint64_t planes, uint64_t ld,
+                         uint64_t plane_ld, uint32_t box_cols, uint32_t box_rows);
+
 // Device error word indices.
 constexpr int kErrCode = 0;
 constexpr int kErrDetail = 1;

@@ -122,6 +122,19 @@ struct BPrefetch {
   }
 };
 
+// Calls epi.drain() where the epilogue functor defines one (stores still in
+// flight when its warps are done); nothing otherwise.
+template <class E>
+__device__ __forceinline__ auto epi_drain(const E& e, int) -> decltype(e.drain()) {
+  e.drain();
+}
+template <class E>
+__device__ __forceinline__ void epi_drain(const E&, long) {}
+template <class E>
+__device__ __forceinline__ void epi_drain(const E& e) {
+  epi_drain(e, 0);
+}
+
 // Epi must provide:
 //   static constexpr uint32_t kScratchBytes;   // shared memory it needs (a multiple of 64; 0 for none)
 //   __device__ void operator()(int m_blk, int n_blk, int ks, int lane_row, uint32_t taddr, float* warp_scratch) const;
@@ -136,7 +149,8 @@ struct BPrefetch {
 template <int BN, int STAGES, bool SPLIT_A, class Epi, int CM = 1>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ BSet bset, int M, int N,
-                     int nk, int k_splits, int m_group, int pf_depth, Epi epi, int* err, const int* m_live) {
+                     int nk, int k_splits, int m_group, int pf_depth, const __grid_constant__ Epi epi, int* err,
+                     const int* m_live) {
   static_assert(CM == 1 || ((CM == 2 || CM == 4) && !SPLIT_A && BN % (8 * CM) == 0),
                 "clusters: plain A, B band split in CM parts of whole 8-row swizzle atoms");
   using Cfg = GemmCfg<BN, STAGES, SPLIT_A>;
@@ -336,6 +350,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+    epi_drain(epi);
   }
 
   tc_fence_before();
@@ -355,38 +370,43 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 // fp32 store of the partial tile of k-split ks:
 //   C[ks * slab + row * ldc + col] = acc   (row < M, col < N)
-// Each warp passes its 32 rows x 32 columns through a padded shared-memory
-// block (stride 33: conflict-free both ways), so that every global store
-// instruction writes one row's 32 consecutive floats (128 bytes).
+// Each warp writes its 32 rows x 32 columns to shared memory in the 128-byte
+// swizzled layout of the tensor map tm (a [ks][M][N] view of C) and one lane
+// issues a bulk tile store, so a warp issues 8 stores per unit instead of
+// 256. Two buffers per warp: the next chunk is written while the previous
+// store still reads the other. The map clips rows >= M and columns >= N.
 template <int BN>
 struct EpiStoreF32 {
-  static constexpr uint32_t kScratchBytes = 4 * 32 * 33 * 4;
-  float* C;
-  size_t slab;
-  int ldc;
-  int M;
-  int N;
+  static constexpr uint32_t kScratchBytes = 4 * 2 * 4096;
+  CUtensorMap tm;
   __device__ __forceinline__ void operator()(int m_blk, int n_blk, int ks, int lane_row, uint32_t taddr,
                                              float* ws) const {
     const int lane = threadIdx.x & 31;
     const int row0 = m_blk * kGemmBM + lane_row - lane;  // this warp's first row
     const int n0 = n_blk * BN;
-    float* out = C + ks * slab;
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
+      float* buf = ws + (c & 1) * 1024;  // 4 KB: 32 rows x 128 bytes
       float v[32];
       tmem_ld_32cols(taddr + c * 32, v);
+      if (lane == 0) bulk_wait_group_read<1>();  // the store that last read this buffer is done with it
+      __syncwarp();
 #pragma unroll
-      for (int i = 0; i < 32; ++i) ws[lane * 33 + i] = v[i];
+      for (int q = 0; q < 8; ++q)  // 16-byte chunk q of row `lane` at chunk position q ^ (lane & 7)
+        *reinterpret_cast<float4*>(buf + lane * 32 + ((q ^ (lane & 7)) << 2)) =
+            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      fence_proxy_async_smem();  // the tile writes, visible to the bulk copy
       __syncwarp();
-      const int col = n0 + c * 32 + lane;
-      const int rows = min(32, M - row0);
-      if (col < N) {
-#pragma unroll 4
-        for (int j = 0; j < rows; ++j) out[static_cast<size_t>(row0 + j) * ldc + col] = ws[j * 33 + lane];
+      if (lane == 0) {
+        tma_store_3d(&tm, buf, n0 + c * 32, row0, ks);
+        bulk_commit_group();
       }
-      __syncwarp();
     }
+  }
+  // Before the CTA exits: every store of this warp has completed.
+  __device__ __forceinline__ void drain() const {
+    if ((threadIdx.x & 31) == 0) bulk_wait_group_all();
+    __syncwarp();
   }
 };
 
