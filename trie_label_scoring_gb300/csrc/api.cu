@@ -833,6 +833,18 @@ bool encode_3d_f32_store(void* tm, void* ptr, uint64_t cols, uint64_t rows, uint
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_3d_bf16_store(void* tm, void* ptr, uint64_t cols, uint64_t rows, uint64_t planes, uint64_t ld,
+                          uint64_t plane_ld, uint32_t box_cols, uint32_t box_rows) {
+  if (g_encode == nullptr) return false;
+  cuuint64_t dims[3] = {cols, rows, planes};
+  cuuint64_t strides[2] = {ld * 2, plane_ld * 2};
+  cuuint32_t box[3] = {box_cols, box_rows, static_cast<cuuint32_t>(planes)};
+  cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(static_cast<CUtensorMap*>(tm), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 quail_status estimate_methods_host(const quail_cost_model* md, const quail_cost_workload* w, const quail_trie* t,
                                    quail_method_cost* costs, int32_t* best, std::string* msg);
 }

@@ -246,49 +246,76 @@ cudaError_t launch_gemm_proj(const CUtensorMap& tmA, const BSet& bset, int M, in
 
 // SwiGLU epilogue of a gate|up GEMM in glu mode (one k-split): columns
 // [0, BN/2) of the tile are gate, [BN/2, BN) up, for outputs j0 = n_blk BN/2 ..
-// act[row][j] = split(SiLU(gate) * up) as [hi (I) | lo (I)] bf16, through a
-// padded shared-memory block per warp so each store covers one row's 32
-// consecutive outputs.
+// act[row][j] = split(SiLU(gate) * up) as [hi (I) | lo (I)] bf16. Each warp
+// builds its 32 rows x 32 outputs as two bf16 planes (hi, lo) in shared memory
+// and one lane issues a bulk tile store through tm, a [2][M][I] view of act
+// (plane stride I elements): 4 stores per warp and unit instead of 2 per
+// output. Lane r writes row r's 16-byte chunks in an order rotated by r / 2,
+// so the 32 lanes' chunk writes spread over all banks.
 template <int BN>
 struct EpiSwiGLU {
-  static constexpr uint32_t kScratchBytes = 4 * 32 * 33 * 4;
-  bf16* act;
-  int I;
-  int M;
+  static constexpr uint32_t kScratchBytes = 4 * 2 * 4096;
+  CUtensorMap tm;
   __device__ __forceinline__ void operator()(int m_blk, int n_blk, int /*ks*/, int lane_row, uint32_t taddr,
                                              float* ws) const {
     const int lane = threadIdx.x & 31;
     const int row0 = m_blk * kGemmBM + lane_row - lane;
     const int j0 = n_blk * (BN / 2);
-    const int rows = min(32, M - row0);
 #pragma unroll 1
     for (int c = 0; c < BN / 64; ++c) {
       float gv[32], uv[32];
       tmem_ld_32cols(taddr + c * 32, gv);
       tmem_ld_32cols(taddr + BN / 2 + c * 32, uv);
+      uint32_t hi[16], lo[16];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) ws[lane * 33 + i] = gv[i] / (1.f + expf(-gv[i])) * uv[i];
-      __syncwarp();
-      const int j = j0 + c * 32 + lane;
-      if (j < I) {
-#pragma unroll 4
-        for (int r = 0; r < rows; ++r) {
-          const float a = ws[r * 33 + lane];
-          const bf16 hi = __float2bfloat16(a);
-          bf16* o = act + static_cast<size_t>(row0 + r) * 2 * I;
-          o[j] = hi;
-          o[I + j] = __float2bfloat16(a - __bfloat162float(hi));
-        }
+      for (int i = 0; i < 16; ++i) {
+        const float a0 = gv[2 * i] / (1.f + expf(-gv[2 * i])) * uv[2 * i];
+        const float a1 = gv[2 * i + 1] / (1.f + expf(-gv[2 * i + 1])) * uv[2 * i + 1];
+        const __nv_bfloat162 h = __floats2bfloat162_rn(a0, a1);
+        const float2 hf = __bfloat1622float2(h);
+        const __nv_bfloat162 l = __floats2bfloat162_rn(a0 - hf.x, a1 - hf.y);
+        hi[i] = *reinterpret_cast<const uint32_t*>(&h);
+        lo[i] = *reinterpret_cast<const uint32_t*>(&l);
       }
+      uint4* buf = reinterpret_cast<uint4*>(ws + (c & 1) * 1024);  // 4 KB: planes hi, lo of 32 rows x 64 B
+      if (lane == 0) bulk_wait_group_read<1>();  // the store that last read this buffer is done with it
       __syncwarp();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int qq = (q + (lane >> 1)) & 3;
+        uint4 h, l;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          if (qq == k) {
+            h = make_uint4(hi[4 * k], hi[4 * k + 1], hi[4 * k + 2], hi[4 * k + 3]);
+            l = make_uint4(lo[4 * k], lo[4 * k + 1], lo[4 * k + 2], lo[4 * k + 3]);
+          }
+        }
+        buf[lane * 4 + qq] = h;
+        buf[128 + lane * 4 + qq] = l;
+      }
+      fence_proxy_async_smem();  // the tile writes, visible to the bulk copy
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(&tm, buf, j0 + c * 32, row0, 0);
+        bulk_commit_group();
+      }
     }
+  }
+  // Before the CTA exits: every store of this warp has completed.
+  __device__ __forceinline__ void drain() const {
+    if ((threadIdx.x & 31) == 0) bulk_wait_group_all();
+    __syncwarp();
   }
 };
 
 cudaError_t launch_gemm_swiglu(const CUtensorMap& tmA, const BSet& bset, int M, int I, int K, bf16* act,
                                int num_sms, int* err, cudaStream_t st) {
   if (!bset.glu || bset.count != 2 || I % (kProjBN / 2) != 0) return cudaErrorInvalidValue;
-  EpiSwiGLU<kProjBN> epi{act, I, M};
+  EpiSwiGLU<kProjBN> epi;
+  if (!encode_3d_bf16_store(&epi.tm, act, static_cast<uint64_t>(I), static_cast<uint64_t>(M), 2,
+                            2 * static_cast<uint64_t>(I), static_cast<uint64_t>(I), 32, 32))
+    return cudaErrorInvalidValue;
   return launch_umma<kProjBN, kProjStages, true>(tmA, bset, M, 2 * I, K / kGemmBK, 1, epi, num_sms, err, st);
 }
 

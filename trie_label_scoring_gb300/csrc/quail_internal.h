@@ -16,6 +16,11 @@ void count_launch();
 bool encode_3d_f32_store(void* tm, void* ptr, uint64_t cols, uint64_t rows, uint64_t planes, uint64_t ld,
                          uint64_t plane_ld, uint32_t box_cols, uint32_t box_rows);
 
+// bf16 tensor of the same shape for tile stores of box_cols x box_rows x
+// planes (every plane at once), without swizzle (box_cols * 2 a multiple of 16).
+bool encode_3d_bf16_store(void* tm, void* ptr, uint64_t cols, uint64_t rows, uint64_t planes, uint64_t ld,
+                          uint64_t plane_ld, uint32_t box_cols, uint32_t box_rows);
+
 // Device error word indices.
 constexpr int kErrCode = 0;
 constexpr int kErrDetail = 1;
