@@ -170,8 +170,8 @@ cudaError_t launch_umma(const CUtensorMap& tmA, const BSet& bset, int M, int N, 
   }
   const int m_tiles = (M + kGemmBM - 1) / kGemmBM;
   const int units = ((m_tiles + CM - 1) / CM * CM) * ((N + BN - 1) / BN) * k_splits;
-  // Walk M-major when A is the larger operand (a W_o over many rows); pairs
-  // share B bands, so they always walk N bands.
+  // Walk M-major when A is the larger operand (a W_o over many rows); the
+  // CTAs of a cluster share B bands, so clusters always walk N bands.
   const double a_bytes = static_cast<double>(M) * nk * kGemmBK * 2.0 * (SPLIT_A ? 2 : 1);
   const double b_bytes = static_cast<double>(N) * nk * kGemmBK * 2.0;
   const int m_major = (CM == 1 && a_bytes > b_bytes) ? 1 : 0;
