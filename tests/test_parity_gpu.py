@@ -157,6 +157,18 @@ def test_trie_tree_qwen_small_all_docs(name, ndocs):
         C.check_scores(lsc[i], prob[i], am[i], r["logscore"], r["prob"], r["argmax"], f"doc {i}")
 
 
+def test_output_head_partial_cluster_of_four():
+    """160 documents of the support-topic shape give 640 head rows, 5 tiles of
+    128: the head then runs on clusters of four CTAs whose second cluster holds
+    three all-padding tiles."""
+    w = S.with_docs(S.WORKLOADS["qwen3-4b-support10-256docs"], 160)
+    ls, docs, lsc, prob, am = _run_trie_tree(w)
+    assert np.all(np.abs(prob.sum(axis=1) - 1) < 1e-4)
+    for i in (0, 63, 127, 128, 159):  # rows in the first, middle and last tiles
+        r = _oracle_full(w, ls, docs, i)
+        C.check_scores(lsc[i], prob[i], am[i], r["logscore"], r["prob"], r["argmax"], f"doc {i}")
+
+
 @pytest.mark.parametrize("name,sample_docs", [
     ("qwen3-4b-support10-256docs", list(range(256))),  # every document of the bench workload
     ("qwen3-4b-tree255-64x2048", list(range(0, 64, 4)) + [63]),  # 17 of 64: the oracle takes seconds per document
