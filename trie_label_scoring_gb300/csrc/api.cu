@@ -361,9 +361,11 @@ quail_status run_qkv(const quail_model_desc* m, const NodeTables& nt, const Buff
 }
 
 // Attention (tree part, paged doc part, combine) for rows = slots x nq.
+// order_ready: b.slot_order already holds the slot order of these documents
+// (an earlier layer of the same call computed it), so it is not recomputed.
 quail_status run_attention(const quail_model_desc* m, const quail_paged_kv* kv, const NodeTables& nt, RowMap map,
                            int slots, const Buffers& b, DeviceState* ds, cudaStream_t st,
-                           const int* nodes_live = nullptr) {
+                           const int* nodes_live = nullptr, bool order_ready = false) {
   const int hq = m->n_q_heads, hkv = m->n_kv_heads;
   const AttnShape as = attn_shape(m, map.nq, slots, kv->max_doc_len, ds->num_sms);
   AttnArgs a{};
@@ -401,7 +403,7 @@ quail_status run_attention(const quail_model_desc* m, const quail_paged_kv* kv, 
   if (s != QUAIL_OK) return s;
   s = encode_2d_bf16(&tV, kv->v_pool, pool_rows, 128, 128, 64, 16);
   if (s != QUAIL_OK) return s;
-  if (a.slot_order != nullptr) CUDA_TRY(launch_slot_order(a, st));
+  if (a.slot_order != nullptr && !order_ready) CUDA_TRY(launch_slot_order(a, st));
   CUDA_TRY(launch_tree_part(a, st));
   if (as.tc) {
     CUDA_TRY(launch_attn_doc_tc(a, tK, tV, st));
@@ -1126,7 +1128,8 @@ quail_status quail_classify_trie_tree_ml(const quail_model_ml_desc* model, const
     if (s != QUAIL_OK) return s;
     span(QUAIL_SPAN_QKV, true);
     span(QUAIL_SPAN_ATTENTION, false);
-    s = run_attention(&ml, &kl, nt, map, num_docs, b, ds, st);
+    // every layer sees the same documents: the slot order is computed once
+    s = run_attention(&ml, &kl, nt, map, num_docs, b, ds, st, nullptr, l > 0);
     if (s != QUAIL_OK) return s;
     span(QUAIL_SPAN_ATTENTION, true);
     span(QUAIL_SPAN_WO_NORM, false);

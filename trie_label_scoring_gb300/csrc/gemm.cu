@@ -319,7 +319,10 @@ cudaError_t launch_gemm_swiglu(const CUtensorMap& tmA, const BSet& bset, int M, 
   return launch_umma<kProjBN, kProjStages, true>(tmA, bset, M, 2 * I, K / kGemmBK, 1, epi, num_sms, err, st);
 }
 
-int head_cluster_ctas(int M) { return (M + kGemmBM - 1) / kGemmBM <= kHeadWideClusterMaxTiles ? 4 : 2; }
+int head_cluster_ctas(int M) {
+  const int t = (M + kGemmBM - 1) / kGemmBM;
+  return t <= kHeadWideClusterMaxTiles && (t + 3) / 4 * 4 <= (t + 1) / 2 * 2 ? 4 : 2;
+}
 
 cudaError_t launch_gemm_head(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int V, int K,
                              const HeadEpilogueArgs& args, int num_sms, int* err, cudaStream_t st,

@@ -52,10 +52,12 @@ struct HeadEpilogueArgs {
 constexpr int kHeadBN = 256;
 // The head runs on clusters of CTAs along M that share each 256-row band of
 // W_lm: every CTA loads 1/C of the band (tmB's box: 64 columns x 256/C rows)
-// and multicasts it to the others. C = 4 when the rows span at most
-// kHeadWideClusterMaxTiles 128-row tiles (A is small and B's L2 reads dominate:
-// four CTAs share each band), else C = 2 (A's re-reads dominate, and four
-// CTAs in lockstep cost more than the B they share).
+// and multicasts it to the others. The M tiles are scheduled in whole
+// clusters, so a padding tile costs a full tile of MMAs. C = 4 when the rows
+// span at most kHeadWideClusterMaxTiles 128-row tiles (A is small and B's L2
+// reads dominate: four CTAs share each band) and clusters of four schedule no
+// more tiles than pairs do (3, 4, 7 or 8 tiles); else C = 2 (A's re-reads
+// dominate, and four CTAs in lockstep cost more than the B they share).
 constexpr int kHeadWideClusterMaxTiles = 8;
 int head_cluster_ctas(int M);
 inline int head_b_box_rows(int M) { return kHeadBN / head_cluster_ctas(M); }
