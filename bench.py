@@ -565,7 +565,7 @@ def run_ours(args):
                 "frac_sustained": (achieved / peaks["bf16_tflops_sustained"]
                                    if peaks.get("bf16_tflops_sustained") else None),
                 "frac_spec": achieved / SPEC_BF16_TFLOPS}
-    # ---- path roofline (the benchmark spec): max(KV bytes / HBM, head FLOPs / tensor peak)
+    # ---- path roofline: max(KV bytes / HBM, head FLOPs / tensor peak)
     kv_bytes = float(docs.doc_len.sum()) * w.shape.n_kv_heads * w.shape.head_dim * 2 * 2
     t_kv = kv_bytes / (peaks["hbm_gbs"] * 1e9)
     t_head = flops / (peaks["bf16_tflops"] * 1e12)
@@ -585,7 +585,7 @@ def run_ours(args):
         if one is not None:
             cpu["one_core"] = one
 
-    # ---- configs 3, 3L, 4, 4D and 5, after the headline, same steps and warm-up
+    # ---- the other workloads (larger label sets, long documents, letters, decode), after the headline, same steps and warm-up
     others = None
     if w.name == DEFAULT_WORKLOAD and not args.no_other_configs:
         others = measure_other_configs(model, args.steps if args.steps is not None else 20, max(args.warmup, 3))
@@ -612,11 +612,11 @@ def run_ours(args):
 # warm-up counts: the larger label sets, the long documents and the two
 # variants that fall out of the same kernels.
 OTHER_CONFIGS = (
-    ("config 3", "qwen3-4b-tree255-64x2048", "trie_tree"),
-    ("config 3L", "qwen3-4b-letters255-64x2048", "letters"),
-    ("config 4", "qwen3-4b-tree20-32x8192", "trie_tree"),
-    ("config 4D", "qwen3-4b-tree20-32x8192", "decode"),
-    ("config 5", "qwen3-4b-tree5000-16x1024", "trie_tree"),
+    ("tree255-64x2048", "qwen3-4b-tree255-64x2048", "trie_tree"),
+    ("letters255-64x2048", "qwen3-4b-letters255-64x2048", "letters"),
+    ("tree20-32x8192", "qwen3-4b-tree20-32x8192", "trie_tree"),
+    ("tree20-32x8192 decode", "qwen3-4b-tree20-32x8192", "decode"),
+    ("tree5000-16x1024", "qwen3-4b-tree5000-16x1024", "trie_tree"),
 )
 SPEC_BF16_TFLOPS = 2250.0  # nominal dense bf16 of one GB300 (context next to the measured peaks)
 
