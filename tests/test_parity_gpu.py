@@ -396,6 +396,30 @@ def test_long_documents_past_the_split_cap(labels):
         C.check_scores(lsc[i], prob[i], am[i], r["logscore"], r["prob"], r["argmax"], f"len {lens[i]}")
 
 
+@pytest.mark.parametrize("labels", ["support10", "tree60"])
+def test_very_long_documents_many_splits(labels):
+    """Three documents, one of 32,768 tokens: with so few (document, KV head)
+    items the long document is cut into many splits (up to the split caps of
+    4,096 and 8,192 keys), whose partials the combine kernel merges with the
+    tree part; every document against the oracle."""
+    lens = np.array([32768, 20001, 300], dtype=np.int32)
+    if labels == "support10":
+        w = S.with_docs(S.WORKLOADS["tiny-support10-4x128"], 3, (16, 32768))
+        ls = S.make_labels(w, 0)
+        assert _rows_per_kv(w, ls) <= 16
+    else:
+        w = _tiny_tree(3, (16, 32768))
+        ls = S.make_labels(w, 5)
+        assert _rows_per_kv(w, ls) > 128
+    seed = 5 if labels == "tree60" else 0
+    docs = _resize_docs(None, lens, w)
+    ls, docs, lsc, prob, am = _run_trie_tree(w, seed=seed, labels=ls, docs=docs)
+    assert np.all(np.abs(prob.sum(axis=1) - 1) < 1e-4)
+    for i in range(3):
+        r = _oracle_full(w, ls, docs, i, seed=seed)
+        C.check_scores(lsc[i], prob[i], am[i], r["logscore"], r["prob"], r["argmax"], f"len {lens[i]}")
+
+
 def test_prefix_labels_on_the_tcgen05_path():
     """Labels that are prefixes of other labels, on a trie with more than 128
     query rows per KV head: the prefix correction log(1 - sum of the end
