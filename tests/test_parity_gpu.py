@@ -157,14 +157,18 @@ def test_trie_tree_qwen_small_all_docs(name, ndocs):
         C.check_scores(lsc[i], prob[i], am[i], r["logscore"], r["prob"], r["argmax"], f"doc {i}")
 
 
-def test_output_head_partial_cluster_of_four():
-    """200 documents of the support-topic shape give 800 head rows, 7 tiles of
-    128 (the last holds 32 rows): the head then runs on clusters of four CTAs
-    whose second cluster holds one all-padding tile."""
-    w = S.with_docs(S.WORKLOADS["qwen3-4b-support10-256docs"], 200)
+@pytest.mark.parametrize("ndocs,check", [
+    (200, (0, 63, 127, 128, 191, 192, 199)),  # 800 rows, 7 tiles: two clusters of four, one padding tile
+    (96, (0, 31, 32, 64, 95)),                # 384 rows, 3 tiles: one cluster of four, one padding tile
+])
+def test_output_head_partial_cluster(ndocs, check):
+    """Documents of the support-topic shape (4 head rows each) whose head rows
+    fill 128-row tiles up to a partial cluster: the padding tile of the
+    cluster reads zeros and writes nothing."""
+    w = S.with_docs(S.WORKLOADS["qwen3-4b-support10-256docs"], ndocs)
     ls, docs, lsc, prob, am = _run_trie_tree(w)
     assert np.all(np.abs(prob.sum(axis=1) - 1) < 1e-4)
-    for i in (0, 63, 127, 128, 191, 192, 199):  # rows in the first, middle and last tiles
+    for i in check:  # rows in the first, middle and last tiles
         r = _oracle_full(w, ls, docs, i)
         C.check_scores(lsc[i], prob[i], am[i], r["logscore"], r["prob"], r["argmax"], f"doc {i}")
 
