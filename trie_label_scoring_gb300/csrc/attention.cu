@@ -710,10 +710,11 @@ bool attn_doc_wants_slot_order(const AttnArgs& a, int num_sms) {
   // Few waves: the last partial wave decides the kernel's end, and starting
   // the long documents first leaves short CTAs for it. Over many waves the
   // order is left alone: CTAs of equal length started together reach their
-  // setup and merge phases together, and an SM then streams less.
+  // setup and merge phases together, and an SM then streams less. Within one
+  // wave every CTA is resident at once and the order cannot matter.
   const int per_sm = a.split_tokens / kPage >= kLongSplitPages ? AttnRing<12>::kCtasPerSm : AttnRing<8>::kCtasPerSm;
   const long ctas = static_cast<long>(a.n_slots) * a.hkv * a.n_splits;
-  return 2 * ctas <= 3L * per_sm * num_sms;
+  return ctas > static_cast<long>(per_sm) * num_sms && 2 * ctas <= 3L * per_sm * num_sms;
 }
 
 cudaError_t launch_attn_doc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV, cudaStream_t st) {

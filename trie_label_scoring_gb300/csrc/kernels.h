@@ -246,8 +246,8 @@ cudaError_t launch_tree_part(const AttnArgs& a, cudaStream_t st);
 // *map.n_slots_dev last), so the doc attention's long CTAs start in the first
 // waves and the last wave holds short ones.
 cudaError_t launch_slot_order(const AttnArgs& a, cudaStream_t st);
-// True when the mma.sync doc attention's grid spans at most 1.5 waves of
-// resident CTAs: there it runs its slots in slot_order.
+// True when the mma.sync doc attention's grid spans more than one and at
+// most 1.5 waves of resident CTAs: there it runs its slots in slot_order.
 bool attn_doc_wants_slot_order(const AttnArgs& a, int num_sms);
 cudaError_t launch_attn_doc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV, cudaStream_t st);
 cudaError_t launch_attn_combine(const AttnArgs& a, cudaStream_t st);

@@ -292,12 +292,16 @@ __global__ void label_score_kernel(LabelScoreArgs a) {
   for (int m = threadIdx.x; m < a.M; m += blockDim.x) out_p[m] = expf(out_ls[m] - mx) / total;
 }
 
-// The same scoring split over many CTAs, for calls with few documents (the
-// fused kernel above runs one CTA per document): the LSE rows come from
-// lse_reduce_kernel (warp per row, every document at once); then
-// label_logscore_kernel (CTA per (document, 64 labels), warp per label) and
-// label_softmax_kernel (CTA per document).
+// The same scoring split over many CTAs, for calls with few documents whose
+// work is large (the fused kernel above runs one CTA per document): the LSE
+// rows come from lse_reduce_kernel (warp per row, every document at once);
+// then label_logscore_kernel (CTA per (document, 64 labels), warp per label)
+// and label_softmax_kernel (CTA per document).
 constexpr int kLabelsPerCta = 64;
+// A document is small work for one CTA of the fused kernel up to this many
+// tile partials (evaluated rows x vocabulary tiles) and labels.
+constexpr long kLabelScoreSmallPartials = 16384;
+constexpr int kLabelScoreSmallLabels = 1024;
 __global__ void label_logscore_kernel(LabelScoreArgs a) {
   grid_dependency_wait();
   const int doc = blockIdx.x;
@@ -630,7 +634,12 @@ cudaError_t launch_lse_reduce(const float2* lse_part, int rows, int n_tiles, flo
 
 cudaError_t launch_label_score(const LabelScoreArgs& args, int num_docs, int num_sms, cudaStream_t st) {
   if (num_docs <= 0) return cudaSuccess;
-  if (num_docs >= num_sms) {  // enough documents to fill the GPU with one CTA each
+  // One CTA per document when there are enough documents to fill the GPU, or
+  // when a document's work is small enough for one CTA (its rows' tile
+  // partials and its labels): then one launch costs less than three.
+  const bool small_doc = static_cast<long>(args.a) * args.n_tiles <= kLabelScoreSmallPartials &&
+                         args.M <= kLabelScoreSmallLabels;
+  if (num_docs >= num_sms || small_doc) {
     count_launch();
     { const cudaError_t le_ = launch_pdl(label_score_kernel, dim3(num_docs), dim3(256), 0, st, args); if (le_ != cudaSuccess) return le_; }
     return cudaGetLastError();
