@@ -424,6 +424,28 @@ def test_very_long_documents_many_splits(labels):
         C.check_scores(lsc[i], prob[i], am[i], r["logscore"], r["prob"], r["argmax"], f"len {lens[i]}")
 
 
+@pytest.mark.parametrize("shape", ["deep_chain", "one_token", "single_root_child", "twenty_deep"])
+def test_degenerate_label_shapes(shape):
+    """Label sets at the edges of the trie's shape, every document against
+    the oracle: two labels sharing nine tokens (ten evaluated nodes on one
+    chain), one-token labels (only the root is evaluated), a root with a
+    single child, and labels twenty tokens deep."""
+    w = S.WORKLOADS["tiny-support10-4x128"]
+    base = S.make_labels(w, 0)
+    labels = {
+        "deep_chain": [[5, 6, 7, 8, 9, 10, 11, 12, 13, 14], [5, 6, 7, 8, 9, 10, 11, 12, 13, 15]],
+        "one_token": [[100], [200], [300], [400], [8191]],
+        "single_root_child": [[7, 1], [7, 2], [7, 3, 4], [7, 3, 5]],
+        "twenty_deep": [list(range(1, 21)), list(range(1, 20)) + [99], list(range(40, 60))],
+    }[shape]
+    ls = S.LabelSet(labels, base.root_token, None)
+    ls_, docs, lsc, prob, am = _run_trie_tree(w, labels=ls)
+    assert np.all(np.abs(prob.sum(axis=1) - 1) < 1e-4)
+    for i in range(w.num_docs):
+        r = _oracle_full(w, ls, docs, i)
+        C.check_scores(lsc[i], prob[i], am[i], r["logscore"], r["prob"], r["argmax"], f"{shape} doc {i}")
+
+
 def test_prefix_labels_on_the_tcgen05_path():
     """Labels that are prefixes of other labels, on a trie with more than 128
     query rows per KV head: the prefix correction log(1 - sum of the end
